@@ -1,0 +1,445 @@
+#!/usr/bin/env python
+"""Benchmark of batched tree attention on GB300.
+
+One step = one ``tree_attn`` call = the plan kernel (work enumeration, tile
+classification, RoPE table) plus the persistent attention kernel, over one
+batch of the named synthetic workload.  Prints one JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                  [--impl gb300|reference]
+
+Under torchrun each rank runs its own copy of the workload on its own GPU
+(weak scaling, no data-path collective); the step time is the max over ranks.
+``--impl reference`` times the CPU oracle on bounded samples of the same
+workload (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import workloads as wl  # noqa: E402
+
+METRIC = "tree-attn TFLOP/s (unmasked pairs) + % of roofline, 1 GB300"
+UNIT = "TFLOP/s"
+WORKLOADS = {name: i + 1 for i, name in enumerate(wl.CONFIG_NAMES)}
+L2_BYTES = 129 * 2 ** 20
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# --------------------------------------------------------------------------
+# multi-rank helpers (host logic; covered by gloo tests on CPU)
+# --------------------------------------------------------------------------
+
+def dist_info():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, local, world
+
+
+def init_dist(world: int, backend: str):
+    if world > 1 and not torch.distributed.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        torch.distributed.init_process_group(backend=backend)
+
+
+def barrier(world: int):
+    if world > 1:
+        torch.distributed.barrier()
+
+
+def max_over_ranks(x: float, world: int, device="cpu") -> float:
+    if world == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def weak_scaling_value(units_per_rank: float, world: int, max_seconds: float) -> float:
+    """Whole-job throughput: every rank processed ``units_per_rank``."""
+    return units_per_rank * world / max_seconds
+
+
+# --------------------------------------------------------------------------
+# measurement helpers
+# --------------------------------------------------------------------------
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+    except (OSError, KeyError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in ("ta_attn.cu", "ta_device.cuh", "ta_layout.h"):
+        with open(os.path.join(ROOT, "tree_attention_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per attention launch from the committed ncu summary, if it
+    was taken on the current kernel source."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        e = d[workload]
+        if e.get("kernel_hash") == kernel_source_hash():
+            return float(e["dram_bytes_per_launch"])
+    except (OSError, KeyError, ValueError):
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.file = None
+
+    def start(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.file, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.file.flush()
+        self.file.seek(0)
+        rows = [r.strip().split(", ") for r in self.file.read().splitlines() if r.strip()]
+        os.unlink(self.file.name)
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[1]))
+                mx = max(mx, float(r[2]))
+                for n, v in zip(names, r[5:9]):
+                    if v.strip().lower() == "active":
+                        reasons.add(n)
+            except (ValueError, IndexError):
+                continue
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def set_bytes(w) -> int:
+    es = 2
+    return (2 * w.total_q * w.h_q * w.head_dim * es + 2 * w.total_kv * w.h_kv * w.head_dim * es
+            + 4 * w.total_q * w.h_q)
+
+
+# --------------------------------------------------------------------------
+# CPU oracle timing (baseline leg and the reference arm)
+# --------------------------------------------------------------------------
+
+def oracle_sample(w, budget_s: float):
+    """Pick a prefix of the sequences whose oracle time fits ``budget_s``
+    (estimated from visible pairs after timing one sequence)."""
+    import oracle
+    t0 = time.perf_counter()
+    oracle.tree_attention_workload(w, seqs=[0])
+    t1 = max(time.perf_counter() - t0, 1e-4)
+    per_pair = t1 / max(1, _pairs(w, [0]))
+    seqs, acc = [], 0.0
+    for b in range(w.batch_size):
+        est = per_pair * _pairs(w, [b])
+        if seqs and acc + est > budget_s:
+            break
+        seqs.append(b)
+        acc += est
+    return seqs
+
+
+def _pairs(w, seqs) -> int:
+    tot = 0
+    for b in seqs:
+        n = len(w.parents[b])
+        dep = wl.tree_depths(w.parents[b])
+        rows = np.arange(n - w.qo_lens[b], n)
+        tot += int(np.sum(dep[rows] + 1)) + w.prefix_lens[b] * len(rows)
+    return tot
+
+
+def time_oracle(w, seqs):
+    import oracle
+    t0 = time.perf_counter()
+    oracle.tree_attention_workload(w, seqs=seqs)
+    dt = time.perf_counter() - t0
+    flops = 4.0 * w.head_dim * w.h_q * _pairs(w, seqs)
+    return flops, dt
+
+
+def cpu_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def cpu_baseline(w, budget_s=15.0):
+    seqs = oracle_sample(w, budget_s)
+    flops, dt = time_oracle(w, seqs)
+    return {"value": flops / dt / 1e12, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+            "sample": f"{len(seqs)} of {w.batch_size} sequences of the {w.name} workload, "
+                      f"one pass, {dt:.1f} s (numpy float64, BLAS threads = host cores)"}
+
+
+# --------------------------------------------------------------------------
+# arms
+# --------------------------------------------------------------------------
+
+def run_reference(args):
+    rank, _, world = dist_info()
+    if rank != 0:
+        return 0
+    w = wl.config(WORKLOADS[args.workload])
+    per_step_budget = max(0.5, 150.0 / (args.steps + args.warmup))
+    seqs = oracle_sample(w, per_step_budget)
+    for _ in range(args.warmup):
+        time_oracle(w, seqs)
+    t0 = time.perf_counter()
+    flops = 0.0
+    for _ in range(args.steps):
+        f, _dt = time_oracle(w, seqs)
+        flops += f
+    total = time.perf_counter() - t0
+    value = flops / total / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": total / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": _config_dict(w, None),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+                         "sample": f"{len(seqs)} of {w.batch_size} sequences per step"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def _config_dict(w, l2_note):
+    d = {"workload": w.name, "batch": w.batch_size, "total_q": w.total_q,
+         "total_kv": w.total_kv, "h_q": w.h_q, "h_kv": w.h_kv, "head_dim": w.head_dim,
+         "rotary": bool(w.rotary_mode), "visible_pairs_per_head": wl.visible_pairs(w)}
+    if l2_note:
+        d["l2"] = l2_note
+    return d
+
+
+def run_gb300(args):
+    import tree_attention_gb300 as ta
+    from tree_attention_gb300 import build as ta_build
+
+    rank, local, world = dist_info()
+    init_dist(world, "nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    ta_build.build()
+    ta.lib()
+    w = wl.config(WORKLOADS[args.workload])
+    flops = wl.algorithmic_flops(w)
+    nbytes = wl.algorithmic_bytes(w)
+    sb = set_bytes(w)
+    n_sets = args.sets or max(1, min(16, math.ceil(2.2 * L2_BYTES / sb)))
+    l2_note = (f"rotating {n_sets} input/output sets ({n_sets * sb / 1e6:.0f} MB > 2x L2)"
+               if n_sets > 1 else f"inputs larger than L2 ({sb / 1e6:.0f} MB)")
+    base = wl.device_inputs(w, dev)
+    sets = []
+    for i in range(n_sets):
+        d = {k: (v.clone() if v is not None else None) for k, v in base.items()}
+        d["out"] = torch.empty_like(d["q"])
+        d["lse"] = torch.empty(d["q"].shape[:2], dtype=torch.float32, device=dev)
+        dims = ta.make_dims(d["q"], d["k"], d["q_indptr"], d["tree_order"])
+        d["ws"] = torch.zeros(ta.workspace_size(dims), dtype=torch.uint8, device=dev)
+        sets.append(d)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(d, ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        ta.plan(d["q"], d["q_indptr"], d["k"], d["kv_indptr"], d["q_rope_position"],
+                d["mn_indptr"], d["tree_order"], w.rotary_mode, w.rope_scale, w.rope_theta,
+                d["ws"], stream)
+        if ev is not None:
+            ev[1].record(stream)
+        ta.run(d["q"], d["k"], d["v"], d["q_indptr"], d["kv_indptr"], d["mn_indptr"],
+               d["tree_order"], d["out"], d["lse"], w.rotary_mode, w.sm_scale, d["ws"], stream)
+        if ev is not None:
+            ev[2].record(stream)
+
+    for i in range(args.warmup):
+        step(sets[i % n_sets])
+    torch.cuda.synchronize(dev)
+    for d in sets:
+        st = ta.device_status(d["ws"], stream)
+        if st != ta.TA_OK:
+            raise RuntimeError(f"device status after warm-up: {ta.status_string(st)}")
+
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    t_start.record(stream)
+    for i in range(K):
+        step(sets[i % n_sets], evs[i])
+    t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    clk = clocks.stop()
+    total_ms = t_start.elapsed_time(t_end)
+    attn_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
+    plan_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+    max_ms = max_over_ranks(total_ms, world, dev)
+    for d in sets:
+        st = ta.device_status(d["ws"], stream)
+        if st != ta.TA_OK:
+            raise RuntimeError(f"device status after timing: {ta.status_string(st)}")
+
+    # end to end through the public call with host buffers
+    keys_in = ["q", "k", "v", "q_indptr", "kv_indptr", "mn_indptr", "tree_order",
+               "q_rope_position"]
+    host = {k: (base[k].cpu().pin_memory() if base[k] is not None else None) for k in keys_in}
+    host_out = torch.empty(base["q"].shape, dtype=base["q"].dtype).pin_memory()
+    host_lse = torch.empty(base["q"].shape[:2], dtype=torch.float32).pin_memory()
+    h2d = sum(host[k].numel() * host[k].element_size() for k in keys_in if host[k] is not None)
+    d2h = host_out.numel() * host_out.element_size() + host_lse.numel() * 4
+    for i in range(min(args.warmup, 3)):
+        d = sets[i % n_sets]
+        for k in keys_in:
+            if host[k] is not None:
+                d[k].copy_(host[k], non_blocking=True)
+        ta.tree_attn(d["q"], d["q_indptr"], d["k"], d["v"], d["kv_indptr"],
+                     d["q_rope_position"], d["mn_indptr"], d["tree_order"], d["out"], d["lse"],
+                     w.rotary_mode, w.rope_scale, w.rope_theta, w.sm_scale, d["ws"], stream)
+        host_out.copy_(d["out"], non_blocking=True)
+        host_lse.copy_(d["lse"], non_blocking=True)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(K):
+        d = sets[i % n_sets]
+        for k in keys_in:
+            if host[k] is not None:
+                d[k].copy_(host[k], non_blocking=True)
+        ta.tree_attn(d["q"], d["q_indptr"], d["k"], d["v"], d["kv_indptr"],
+                     d["q_rope_position"], d["mn_indptr"], d["tree_order"], d["out"], d["lse"],
+                     w.rotary_mode, w.rope_scale, w.rope_theta, w.sm_scale, d["ws"], stream)
+        host_out.copy_(d["out"], non_blocking=True)
+        host_lse.copy_(d["lse"], non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
+    for d in sets:
+        if ta.device_status(d["ws"], stream) != ta.TA_OK:
+            raise RuntimeError("device status after the end-to-end pass")
+
+    peaks, peak_src = measured_peaks()
+    t_hbm = nbytes / (peaks["hbm_gbs"] * 1e9)
+    t_tc = flops / (peaks["bf16_tflops"] * 1e12)
+    attn_s = attn_ms / 1e3
+    if t_hbm >= t_tc:
+        roof = {"bound": "hbm", "achieved": nbytes / attn_s / 1e9, "peak": peaks["hbm_gbs"],
+                "unit": "GB/s"}
+    else:
+        roof = {"bound": "tensor", "achieved": flops / attn_s / 1e12,
+                "peak": peaks["bf16_tflops"], "unit": "TFLOP/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["traffic"] = recorded_traffic(w.name)
+    roof["peak_source"] = peak_src
+    roof["kernel"] = "attn_kernel (persistent tcgen05 tree attention)"
+    roof["kernel_ms"] = attn_ms
+    roof["plan_kernel_ms"] = plan_ms
+    roof["t_roof_8tbs_us"] = max(nbytes / 8e12, flops / (peaks["bf16_tflops"] * 1e12)) * 1e6
+    roof["step_frac_of_t_roof"] = roof["t_roof_8tbs_us"] / (max_ms / K * 1e3)
+
+    line = {
+        "metric": METRIC,
+        "value": weak_scaling_value(flops * K, world, max_ms / 1e3) / 1e12,
+        "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": max_ms / K, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+        "config": _config_dict(w, l2_note),
+        "tokens_per_s": weak_scaling_value(w.total_q * K, world, max_ms / 1e3),
+        "roofline": roof,
+        "e2e": {"value": weak_scaling_value(flops * K, world, e2e_ms / 1e3) / 1e12, "unit": UNIT,
+                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
+        "gpu_launches": 2 * K,
+        "clocks": clk,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default="spec-decode", choices=list(WORKLOADS))
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--sets", type=int, default=0, help="input/output buffer sets to rotate")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    args.warmup = max(3, args.warmup)   # at least three untimed warm-up steps
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gb300(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

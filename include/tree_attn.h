@@ -1,0 +1,175 @@
+/*
+ * tree_attn.h -- C ABI of the GB300 (sm_103a) batched tree-attention library
+ * (libtreeattn.so).
+ *
+ * The operation is the one the page "tree_attn.py"
+ * (python/tvm/relax/frontend/nn/llm/tree_attn.py) generates as
+ * ``batch_tree_attn`` (``tree_attn`` for GPUs, ``tree_attn_cpu`` for CPUs):
+ * ragged, multi-sequence grouped-query attention in which q row r of
+ * sequence b attends kv column c iff c lies in the sequence's causal prefix
+ * or c's tree node is an ancestor-or-self of r's tree node, decided from the
+ * DFS [enter, exit) intervals of ``_check_tree_order`` on that page.  RoPE
+ * (``_rope`` on the page "_kernel_common.py",
+ * python/tvm/relax/frontend/nn/llm/_kernel_common.py) is optionally applied
+ * to q and k as they are loaded.  The outputs are the attention output and
+ * the base-2 log-sum-exp (``m + log2(d)``, the ``lse_store`` epilogue).
+ *
+ * Conventions shared by every entry point:
+ *   - Pointers named "device" are CUDA device pointers owned by the caller;
+ *     the library never frees them and keeps no reference after returning.
+ *   - ``stream`` is a ``cudaStream_t`` passed as ``void*`` (NULL = the
+ *     legacy default stream).  Launching entry points are asynchronous on it
+ *     and never synchronise the host.
+ *   - Errors detectable from the arguments alone are returned synchronously
+ *     before anything is launched.  The contents of device index arrays are
+ *     not read on the host in the launching calls (see
+ *     ``tree_attn_check_inputs``).
+ *   - Only the current CUDA device is used.
+ */
+#ifndef TREE_ATTN_H_
+#define TREE_ATTN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  TA_OK = 0,
+  TA_ERR_INVALID_ARGUMENT = 1, /* null pointer, bad size, bad scalar         */
+  TA_ERR_UNSUPPORTED = 2,      /* valid but not built: head_dim, group size  */
+  TA_ERR_CUDA = 3,             /* a CUDA runtime/driver call failed          */
+  TA_ERR_DEVICE_TIMEOUT = 4    /* a bounded device-side wait expired         */
+} ta_status;
+
+typedef enum { TA_FP16 = 0, TA_BF16 = 1 } ta_dtype;
+
+/* Problem sizes.  The page's PrimFunc takes these from buffer shapes and
+ * generator constants (h_kv, h_q, d, dtype); a C ABI passes them explicitly.
+ *   batch_size  B, number of sequences (>= 1)
+ *   total_q     rows of q / out / lse           (q_indptr[B])
+ *   total_kv    rows of k / v                   (kv_indptr[B])
+ *   total_tree  rows of tree_order              (mn_indptr[B])
+ *   h_q, h_kv   heads; h_q % h_kv == 0, group size g = h_q / h_kv <= 128
+ *   head_dim    64 or 128
+ *   dtype       element type of q, k, v and out                            */
+typedef struct {
+  int32_t batch_size;
+  int32_t total_q;
+  int32_t total_kv;
+  int32_t total_tree;
+  int32_t h_q;
+  int32_t h_kv;
+  int32_t head_dim;
+  ta_dtype dtype;
+} ta_dims;
+
+/* Bytes of device workspace ``tree_attn`` needs for these sizes (a multiple
+ * of 256; 0 on invalid dims).  The workspace holds the per-launch work plan
+ * (tile classes, the cost-ordered work queue), the RoPE cos/sin table and a
+ * device status word.  It depends on the sizes only, so one allocation
+ * serves every call with the same dims. */
+size_t tree_attn_workspace_size(const ta_dims* dims);
+
+/* Batched tree attention.  Layouts (all row-major, contiguous, device):
+ *   q               [total_q, h_q, head_dim]   dtype
+ *   q_indptr        [B+1] int32, q rows of sequence b are
+ *                   q_indptr[b] .. q_indptr[b+1]-1
+ *   k, v            [total_kv, h_kv, head_dim] dtype
+ *   kv_indptr       [B+1] int32, kv rows of sequence b
+ *   q_rope_position [total_kv] int32, the RoPE position of every kv token;
+ *                   q row r of sequence b takes the position of its own tree
+ *                   node's kv slot.  May be NULL iff rotary_mode == 0.
+ *   mn_indptr       [B+1] int32, tree nodes of sequence b are tree_order
+ *                   rows mn_indptr[b] .. mn_indptr[b+1]-1
+ *   tree_order      [total_tree][2] int32, (enter, exit) DFS interval of each
+ *                   node, exit exclusive
+ *   out             [total_q, h_q, head_dim] dtype   (written)
+ *   lse             [total_q, h_q] float32, base-2 log-sum-exp (written);
+ *                   natural-log LSE = lse * ln 2
+ * For sequence b let qo = q rows, kv = kv rows, T = tree nodes; the last T kv
+ * rows are the tree nodes in node order, the first kv - T the prefix, and the
+ * q rows are the last qo tree nodes (0 <= qo <= T <= kv).  A q row none of
+ * whose columns is visible gets out = 0 and lse = -inf.
+ *   rotary_mode     0: no RoPE; 1: rotate-half RoPE on q and k at load time
+ *                   (any other value is TA_ERR_INVALID_ARGUMENT)
+ *   rope_scale      position multiplier (finite)
+ *   rope_theta      RoPE base (finite, > 0)
+ *   sm_scale        score scale (finite), typically 1/sqrt(head_dim)
+ *   workspace       device buffer of >= tree_attn_workspace_size(dims) bytes,
+ *                   256-byte aligned, zero-filled once before its first use
+ *                   (e.g. cudaMemset); every call leaves it ready for the
+ *                   next one.  Calls that may overlap on the GPU must use
+ *                   distinct workspaces.
+ * q, k, v and out must be 16-byte aligned.  Returns TA_OK once the work is
+ * enqueued; device-side failures are reported by tree_attn_device_status. */
+ta_status tree_attn(const void* q, const int32_t* q_indptr, const void* k, const void* v,
+                    const int32_t* kv_indptr, const int32_t* q_rope_position,
+                    const int32_t* mn_indptr, const int32_t* tree_order, void* out,
+                    float* lse, int32_t rotary_mode, float rope_scale, float rope_theta,
+                    float sm_scale, const ta_dims* dims, void* workspace,
+                    size_t workspace_bytes, void* stream);
+
+/* The two launches of tree_attn, for callers that reuse one tree layout
+ * across calls (every layer of a model verifies the same draft tree):
+ *   tree_attn_plan  enumerates the (sequence, q tile) work items, classifies
+ *                   every (q tile, kv tile) pair as empty / partial / full
+ *                   from the DFS intervals, orders the items longest-first
+ *                   and, if rotary_mode == 1, fills the RoPE cos/sin table of
+ *                   every kv token; it reads only the index arrays and
+ *                   positions.
+ *   tree_attn_run   the attention kernel proper, consuming the plan that the
+ *                   last tree_attn_plan (or tree_attn) left in ``workspace``.
+ * tree_attn_run must follow a plan made on the same workspace with the same
+ * dims, index-array contents, positions, rotary_mode, rope_scale and
+ * rope_theta; q, k, v, out, lse and sm_scale may change between runs.
+ * Arguments mean what they mean for tree_attn; both are asynchronous. */
+ta_status tree_attn_plan(const int32_t* q_indptr, const int32_t* kv_indptr,
+                         const int32_t* q_rope_position, const int32_t* mn_indptr,
+                         const int32_t* tree_order, int32_t rotary_mode, float rope_scale,
+                         float rope_theta, const ta_dims* dims, void* workspace,
+                         size_t workspace_bytes, void* stream);
+
+ta_status tree_attn_run(const void* q, const void* k, const void* v, const int32_t* q_indptr,
+                        const int32_t* kv_indptr, const int32_t* mn_indptr,
+                        const int32_t* tree_order, void* out, float* lse, int32_t rotary_mode,
+                        float sm_scale, const ta_dims* dims, void* workspace,
+                        size_t workspace_bytes, void* stream);
+
+/* Synchronises ``stream``, reads and clears the device status word that the
+ * kernels of earlier calls left in ``workspace`` (TA_ERR_DEVICE_TIMEOUT if a
+ * bounded wait expired, TA_ERR_CUDA on a CUDA error, else TA_OK). */
+ta_status tree_attn_device_status(void* workspace, void* stream);
+
+/* Human-readable name of a status code (static storage). */
+const char* tree_attn_status_string(ta_status s);
+
+/* Test helper: dense visibility of every (q row, kv column) pair, evaluated
+ * by the same device mask code the attention kernel uses.  Writes
+ * vis[total_q][max_kv] bytes (1 = visible) where column c of q row
+ * q_indptr[b] + r is kv column c of sequence b; columns >= kv_len are 0.
+ * Index arrays and vis are device pointers.  max_kv must be >= every
+ * sequence's kv length.  Asynchronous on stream. */
+ta_status tree_attn_mask_dense(const int32_t* q_indptr, const int32_t* kv_indptr,
+                               const int32_t* mn_indptr, const int32_t* tree_order,
+                               int32_t batch_size, int32_t total_q, int32_t max_kv,
+                               uint8_t* vis, void* stream);
+
+/* Host-side validation of HOST copies of the index arrays, for callers and
+ * tests: indptr arrays start at 0, are non-decreasing and end at the dims'
+ * totals; per sequence 0 <= qo <= T <= kv; every interval has
+ * 0 <= enter < exit <= T and the intervals of a sequence nest (any two are
+ * disjoint or one contains the other).  ``q_rope_position`` is accepted for
+ * symmetry with tree_attn and not inspected (every int32 position is valid).
+ * Returns TA_OK or TA_ERR_INVALID_ARGUMENT. */
+ta_status tree_attn_check_inputs(const int32_t* q_indptr, const int32_t* kv_indptr,
+                                 const int32_t* mn_indptr, const int32_t* tree_order,
+                                 const int32_t* q_rope_position, const ta_dims* dims);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TREE_ATTN_H_ */

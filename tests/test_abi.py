@@ -1,0 +1,142 @@
+"""CPU tests of the C-ABI library: it builds for sm_103a, loads without a
+GPU, exports every symbol include/tree_attn.h declares, and rejects bad
+arguments on the host before launching anything."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import tree_attention_gb300 as ta
+import workloads as wl
+from tree_attention_gb300 import build as ta_build
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include",
+                      "tree_attn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    ta_build.build()
+    return ta.lib()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(tree_attn\w*)\s*\(", src)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ("tree_attn", "tree_attn_workspace_size", "tree_attn_device_status",
+              "tree_attn_status_string", "tree_attn_mask_dense", "tree_attn_check_inputs"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+        assert ctypes.cast(getattr(lib, name), ctypes.c_void_p).value
+
+
+def test_status_strings(lib):
+    assert ta.status_string(ta.TA_OK) == "TA_OK"
+    assert ta.status_string(ta.TA_ERR_DEVICE_TIMEOUT) == "TA_ERR_DEVICE_TIMEOUT"
+
+
+def _dims(**kw):
+    d = dict(batch_size=2, total_q=19, total_kv=19, total_tree=19, h_q=4, h_kv=2, head_dim=64,
+             dtype=ta.TA_FP16)
+    d.update(kw)
+    return ta.Dims(**d)
+
+
+def test_workspace_size(lib):
+    n = ta.workspace_size(_dims())
+    assert n > 0 and n % 256 == 0
+    # grows with the problem, rejects what is not supported
+    assert ta.workspace_size(_dims(total_q=4096, total_kv=4096, total_tree=4096)) > n
+    assert ta.workspace_size(_dims(head_dim=96)) == 0
+    assert ta.workspace_size(_dims(h_q=5)) == 0
+    assert ta.workspace_size(_dims(h_q=256, h_kv=1)) == 0      # group size > 128
+    assert ta.workspace_size(_dims(batch_size=0)) == 0
+
+
+def _call(lib, dims, ptrs=None, **kw):
+    """tree_attn with fake (never dereferenced) device pointers."""
+    fake = ctypes.c_void_p(0x10000)
+    args = dict(q=fake, q_indptr=fake, k=fake, v=fake, kv_indptr=fake, pos=fake, mn=fake,
+                order=fake, out=fake, lse=fake, rotary=0, rs=1.0, rt=1e4, sm=0.125,
+                ws=ctypes.c_void_p(0x20000), wsb=1 << 30)
+    args.update(kw)
+    return lib.tree_attn(args["q"], args["q_indptr"], args["k"], args["v"], args["kv_indptr"],
+                         args["pos"], args["mn"], args["order"], args["out"], args["lse"],
+                         args["rotary"], args["rs"], args["rt"], args["sm"], ctypes.byref(dims),
+                         args["ws"], args["wsb"], None)
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(q=None), ta.TA_ERR_INVALID_ARGUMENT),
+    (dict(q_indptr=None), ta.TA_ERR_INVALID_ARGUMENT),
+    (dict(ws=None), ta.TA_ERR_INVALID_ARGUMENT),
+    (dict(rotary=2), ta.TA_ERR_INVALID_ARGUMENT),
+    (dict(rotary=1, pos=None), ta.TA_ERR_INVALID_ARGUMENT),
+    (dict(rotary=1, rt=0.0), ta.TA_ERR_INVALID_ARGUMENT),
+    (dict(sm=float("nan")), ta.TA_ERR_INVALID_ARGUMENT),
+    (dict(sm=float("inf")), ta.TA_ERR_INVALID_ARGUMENT),
+    (dict(wsb=16), ta.TA_ERR_INVALID_ARGUMENT),
+    (dict(ws=ctypes.c_void_p(0x20010)), ta.TA_ERR_INVALID_ARGUMENT),   # not 256-aligned
+    (dict(q=ctypes.c_void_p(0x10008)), ta.TA_ERR_INVALID_ARGUMENT),    # not 16-aligned
+])
+def test_host_validation_rejects_before_launch(lib, kw, expect):
+    assert _call(lib, _dims(), **kw) == expect
+
+
+def test_unsupported_shapes(lib):
+    assert _call(lib, _dims(head_dim=96)) == ta.TA_ERR_UNSUPPORTED
+    assert _call(lib, _dims(h_q=256, h_kv=1)) == ta.TA_ERR_UNSUPPORTED
+    assert _call(lib, _dims(h_q=5)) == ta.TA_ERR_INVALID_ARGUMENT
+    assert _call(lib, _dims(dtype=7)) == ta.TA_ERR_INVALID_ARGUMENT
+
+
+def test_empty_problem_is_a_no_op(lib):
+    assert _call(lib, _dims(total_q=0)) == ta.TA_OK
+
+
+def test_check_inputs_accepts_generated_workloads(lib):
+    for idx in (1, 2, 3):
+        w = wl.config(idx, batch_scale=0.25)
+        dims = ta.Dims(batch_size=w.batch_size, total_q=w.total_q, total_kv=w.total_kv,
+                       total_tree=w.total_tree, h_q=w.h_q, h_kv=w.h_kv, head_dim=w.head_dim,
+                       dtype=ta.TA_BF16)
+        assert ta.check_inputs(w.q_indptr, w.kv_indptr, w.mn_indptr, w.tree_order, dims) == ta.TA_OK
+
+
+def test_check_inputs_rejects_bad_tables(lib):
+    rng = np.random.default_rng(0)
+    w = wl.build_workload("t", [wl.random_tree(9, rng), wl.binary_tree(6)], h_q=2, h_kv=1,
+                          head_dim=64, dtype="fp16", tensor_seed=0, prefix_lens=[3, 0])
+    dims = ta.Dims(batch_size=2, total_q=w.total_q, total_kv=w.total_kv, total_tree=w.total_tree,
+                   h_q=2, h_kv=1, head_dim=64, dtype=ta.TA_FP16)
+    ok = ta.check_inputs(w.q_indptr, w.kv_indptr, w.mn_indptr, w.tree_order, dims)
+    assert ok == ta.TA_OK
+    bad = w.q_indptr.copy(); bad[-1] += 1
+    assert ta.check_inputs(bad, w.kv_indptr, w.mn_indptr, w.tree_order, dims) != ta.TA_OK
+    bad = w.kv_indptr.copy(); bad[1] -= 4          # kv < T in sequence 0
+    assert ta.check_inputs(w.q_indptr, bad, w.mn_indptr, w.tree_order, dims) != ta.TA_OK
+    order = w.tree_order.copy(); order[1, 1] = order[1, 0]   # empty interval
+    assert ta.check_inputs(w.q_indptr, w.kv_indptr, w.mn_indptr, order, dims) != ta.TA_OK
+    order = w.tree_order.copy(); order[1] = (1, 9); order[2] = (2, 11)  # crossing intervals
+    assert ta.check_inputs(w.q_indptr, w.kv_indptr, w.mn_indptr, order, dims) != ta.TA_OK
+
+
+def test_product_path_has_no_oracle_or_cpu_fallback():
+    """The binding never imports the oracle and has no CPU path."""
+    pkg = os.path.dirname(ta.__file__)
+    for root, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
+                src = open(os.path.join(root, f)).read()
+                assert "oracle" not in src.replace("oracle/", ""), f

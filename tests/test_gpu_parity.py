@@ -1,0 +1,231 @@
+"""GPU parity: the sm_103a library, called through its C ABI, against the CPU
+oracle on the same seeded inputs.
+
+Bars: the tree mask bit-exact; output max-abs error <= 1e-2 (fp16) and
+<= 2e-2 (bf16); LSE (base 2) abs error <= 1e-3; rows with nothing visible give
+out = 0 and lse = -inf on both sides.
+"""
+import zlib
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import tree_attention_gb300 as ta
+import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+TOL_OUT = {"fp16": 1e-2, "bf16": 2e-2}
+TOL_LSE = 1e-3
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _library():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    from tree_attention_gb300 import build
+    build.build()
+    ta.lib()
+
+
+def run_gpu(w):
+    d = wl.device_inputs(w)
+    attn = ta.TreeAttention(d["q"], d["k"], d["q_indptr"], d["tree_order"], w.rotary_mode,
+                            w.rope_scale, w.rope_theta, w.sm_scale)
+    out, lse = attn(**d)
+    st = ta.device_status(attn.workspace)
+    assert st == ta.TA_OK, ta.status_string(st)
+    return out.float().cpu().numpy(), lse.cpu().numpy()
+
+
+def assert_parity(w, out, lse, ref=None):
+    ro, rl = ref if ref is not None else oracle.tree_attention_workload(w)
+    assert out.shape == ro.shape and lse.shape == rl.shape
+    err_o = float(np.max(np.abs(out - ro))) if out.size else 0.0
+    assert err_o <= TOL_OUT[w.dtype], f"out max|err| {err_o}"
+    fin = np.isfinite(rl)
+    assert np.array_equal(fin, np.isfinite(lse)), "finite-ness of lse differs"
+    assert np.all(lse[~fin] == rl[~fin])
+    err_l = float(np.max(np.abs(lse[fin] - rl[fin]))) if fin.any() else 0.0
+    assert err_l <= TOL_LSE, f"lse max|err| {err_l}"
+    return err_o, err_l
+
+
+# --------------------------------------------------------------------------
+# mask
+# --------------------------------------------------------------------------
+
+def _mask_workloads():
+    rng = np.random.default_rng(77)
+    fams = [wl.chain_tree(150), wl.star_tree(40), wl.binary_tree(63), wl.random_tree(90, rng),
+            wl.main_chain_tree(70, rng), wl.spec_decode_tree(64, rng), np.array([-1])]
+    prefixes = [0, 5, 130, 0, 17, 0, 3]
+    qos = [150, 40, 20, 90, 1, 64, 1]
+    return [wl.build_workload("mask", fams, h_q=2, h_kv=1, head_dim=64, dtype="fp16",
+                              tensor_seed=1, prefix_lens=prefixes, qo_lens=qos),
+            wl.config(1), wl.config(2, batch_scale=0.25), wl.config(3, batch_scale=0.125)]
+
+
+@pytest.mark.parametrize("idx", range(4))
+def test_mask_bit_exact(idx):
+    w = _mask_workloads()[idx]
+    d = wl.device_inputs(w)
+    max_kv = int(np.max(np.diff(w.kv_indptr)))
+    vis = ta.mask_dense(d["q_indptr"], d["kv_indptr"], d["mn_indptr"], d["tree_order"],
+                        w.total_q, max_kv).cpu().numpy().astype(bool)
+    torch.cuda.synchronize()
+    for b in range(w.batch_size):
+        ref = oracle.visibility(w.q_indptr, w.kv_indptr, w.mn_indptr, w.tree_order, b)
+        q0, q1 = w.q_indptr[b], w.q_indptr[b + 1]
+        kv = w.kv_indptr[b + 1] - w.kv_indptr[b]
+        assert np.array_equal(vis[q0:q1, :kv], ref), b
+        assert not vis[q0:q1, kv:].any()
+
+
+# --------------------------------------------------------------------------
+# the five benchmark workloads at full size
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("idx", [1, 2, 3, 4, 5])
+def test_config_full_size(idx):
+    w = wl.config(idx)
+    out, lse = run_gpu(w)
+    assert_parity(w, out, lse)
+
+
+def test_degenerate_chain_equals_causal():
+    """The chain sequence of the degenerate workload is causal attention."""
+    w = wl.config(5)
+    out, lse = run_gpu(w)
+    n = len(w.parents[0])
+    q = w.q[:n].to(torch.float64).permute(1, 0, 2)
+    k = w.k[:n].to(torch.float64).permute(1, 0, 2)
+    v = w.v[:n].to(torch.float64).permute(1, 0, 2)
+    ref = torch.nn.functional.scaled_dot_product_attention(q, k, v, is_causal=True,
+                                                           scale=w.sm_scale)
+    err = np.max(np.abs(out[:n] - ref.permute(1, 0, 2).numpy()))
+    assert err <= TOL_OUT["fp16"]
+
+
+# --------------------------------------------------------------------------
+# edge cases: ragged tiles, group sizes, prefixes, partial q sets, empty rows
+# --------------------------------------------------------------------------
+
+def _pos(parents, prefixes, base=0):
+    return [np.concatenate([np.arange(pf), base + pf + wl.tree_depths(p)])
+            for p, pf in zip(parents, prefixes)]
+
+
+def _edge(name):
+    rng = np.random.default_rng(zlib.crc32(name.encode()))
+    if name == "mha_fp16_multi_tiles":
+        ps = [wl.chain_tree(300), wl.random_tree(50, rng)]
+        return wl.build_workload(name, ps, h_q=4, h_kv=4, head_dim=128, dtype="fp16",
+                                 tensor_seed=1, prefix_lens=[0, 70])
+    if name == "g2_d64_rope":
+        ps = [wl.random_tree(1, rng), wl.random_tree(7, rng), wl.random_tree(130, rng)]
+        pf = [5, 0, 200]
+        return wl.build_workload(name, ps, h_q=4, h_kv=2, head_dim=64, dtype="fp16",
+                                 tensor_seed=2, prefix_lens=pf, positions=_pos(ps, pf),
+                                 rotary_mode=1, rope_theta=1e4)
+    if name == "g4_bf16_rope":
+        ps = [wl.main_chain_tree(200, rng), wl.star_tree(33)]
+        pf = [150, 1]
+        return wl.build_workload(name, ps, h_q=8, h_kv=2, head_dim=128, dtype="bf16",
+                                 tensor_seed=3, prefix_lens=pf, positions=_pos(ps, pf, 7),
+                                 rotary_mode=1, rope_theta=5e5)
+    if name == "g8_bf16_rope":
+        ps = [wl.random_tree(90, rng), wl.spec_decode_tree(64, rng), wl.binary_tree(31)]
+        pf = [0, 0, 64]
+        return wl.build_workload(name, ps, h_q=16, h_kv=2, head_dim=128, dtype="bf16",
+                                 tensor_seed=4, prefix_lens=pf, positions=_pos(ps, pf),
+                                 rotary_mode=1)
+    if name == "g16_bf16":
+        ps = [wl.random_tree(45, rng), wl.chain_tree(17)]
+        return wl.build_workload(name, ps, h_q=32, h_kv=2, head_dim=128, dtype="bf16",
+                                 tensor_seed=5, prefix_lens=[9, 0])
+    if name == "g3_nonpow2":
+        ps = [wl.random_tree(100, rng), wl.random_tree(61, rng)]
+        pf = [11, 0]
+        return wl.build_workload(name, ps, h_q=6, h_kv=2, head_dim=128, dtype="bf16",
+                                 tensor_seed=6, prefix_lens=pf, positions=_pos(ps, pf),
+                                 rotary_mode=1)
+    if name == "g6_d64":
+        ps = [wl.random_tree(70, rng), wl.star_tree(25)]
+        return wl.build_workload(name, ps, h_q=12, h_kv=2, head_dim=64, dtype="fp16",
+                                 tensor_seed=7, prefix_lens=[0, 40])
+    if name == "g128_d64":
+        ps = [wl.random_tree(5, rng), wl.chain_tree(3)]
+        return wl.build_workload(name, ps, h_q=128, h_kv=1, head_dim=64, dtype="bf16",
+                                 tensor_seed=8, prefix_lens=[130, 2])
+    if name == "qo_less_than_tree":
+        ps = [wl.random_tree(10, rng), wl.random_tree(4, rng), wl.random_tree(150, rng)]
+        return wl.build_workload(name, ps, h_q=4, h_kv=1, head_dim=128, dtype="fp16",
+                                 tensor_seed=9, prefix_lens=[3, 6, 0], qo_lens=[3, 0, 140])
+    if name == "negative_scale":
+        ps = [wl.random_tree(40, rng)]
+        return wl.build_workload(name, ps, h_q=2, h_kv=1, head_dim=128, dtype="fp16",
+                                 tensor_seed=10, prefix_lens=[20], sm_scale=-0.05)
+    if name == "single_nodes":
+        ps = [np.array([-1])] * 5
+        pf = [0, 1, 63, 64, 129]
+        return wl.build_workload(name, ps, h_q=8, h_kv=2, head_dim=128, dtype="bf16",
+                                 tensor_seed=11, prefix_lens=pf, positions=_pos(ps, pf, 3),
+                                 rotary_mode=1)
+    if name == "large_positions":
+        ps = [wl.random_tree(64, rng)]
+        pf = [100]
+        return wl.build_workload(name, ps, h_q=4, h_kv=1, head_dim=128, dtype="bf16",
+                                 tensor_seed=12, prefix_lens=pf,
+                                 positions=_pos(ps, pf, 90000), rotary_mode=1,
+                                 rope_scale=0.75, rope_theta=5e5)
+    if name == "empty_rows":
+        ps = [wl.random_tree(12, rng), wl.random_tree(9, rng)]
+        w = wl.build_workload(name, ps, h_q=4, h_kv=2, head_dim=64, dtype="fp16",
+                              tensor_seed=13)
+        # every interval of the second sequence is empty: its rows see nothing
+        w.tree_order = w.tree_order.copy()
+        w.tree_order[12:, 1] = w.tree_order[12:, 0]
+        return w
+    raise KeyError(name)
+
+
+EDGE = ["mha_fp16_multi_tiles", "g2_d64_rope", "g4_bf16_rope", "g8_bf16_rope", "g16_bf16",
+        "g3_nonpow2", "g6_d64", "g128_d64", "qo_less_than_tree", "negative_scale",
+        "single_nodes", "large_positions", "empty_rows"]
+
+
+@pytest.mark.parametrize("name", EDGE)
+def test_edge_case(name):
+    w = _edge(name)
+    out, lse = run_gpu(w)
+    assert_parity(w, out, lse)
+
+
+def test_repeated_calls_are_bitwise_identical():
+    w = wl.config(2, batch_scale=0.5)
+    d = wl.device_inputs(w)
+    attn = ta.TreeAttention(d["q"], d["k"], d["q_indptr"], d["tree_order"], w.rotary_mode,
+                            w.rope_scale, w.rope_theta, w.sm_scale)
+    o1, l1 = attn(**d)
+    o1, l1 = o1.clone(), l1.clone()
+    o2, l2 = attn(**d)
+    assert ta.device_status(attn.workspace) == ta.TA_OK
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_bad_index_arrays_are_reported_not_computed():
+    w = wl.config(1)
+    d = wl.device_inputs(w)
+    d["q_indptr"][-1] += 1                         # no longer ends at total_q
+    attn = ta.TreeAttention(d["q"], d["k"], d["q_indptr"], d["tree_order"], 0, 1.0, 1e4,
+                            w.sm_scale)
+    out = torch.full_like(d["q"], 7.0)
+    lse = torch.full(d["q"].shape[:2], 7.0, device="cuda")
+    attn(**d, out=out, lse=lse)
+    assert ta.device_status(attn.workspace) == ta.TA_ERR_INVALID_ARGUMENT
+    assert torch.all(out == 7.0) and torch.all(lse == 7.0)
+    # the status word was cleared by the read
+    assert ta.device_status(attn.workspace) == ta.TA_OK

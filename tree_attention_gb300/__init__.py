@@ -1,0 +1,246 @@
+"""Python binding of ``libtreeattn.so``, the sm_103a batched tree-attention
+library (C ABI in ``include/tree_attn.h``).
+
+The binding only marshals arguments: tensors are passed to the C entry points
+as raw device pointers, every step of the computation runs in the library's
+CUDA kernels, and there is no CPU fallback.  If the library has not been
+built, importing works but every call raises ``RuntimeError``.
+
+The operation is ``batch_tree_attn`` of the page "tree_attn.py"
+(python/tvm/relax/frontend/nn/llm/tree_attn.py): ragged, multi-sequence GQA
+attention over a causal prefix plus each q row's tree ancestors (DFS
+``[enter, exit)`` intervals, ``_check_tree_order``), with optional inline
+rotate-half RoPE (``_rope`` of the page "_kernel_common.py"), emitting the
+output and the base-2 log-sum-exp.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+__all__ = [
+    "TA_OK", "TA_ERR_INVALID_ARGUMENT", "TA_ERR_UNSUPPORTED", "TA_ERR_CUDA",
+    "TA_ERR_DEVICE_TIMEOUT", "TreeAttnError", "Dims", "lib", "lib_path", "workspace_size",
+    "tree_attn", "plan", "run", "device_status", "status_string", "mask_dense", "check_inputs",
+    "TreeAttention",
+]
+
+TA_OK = 0
+TA_ERR_INVALID_ARGUMENT = 1
+TA_ERR_UNSUPPORTED = 2
+TA_ERR_CUDA = 3
+TA_ERR_DEVICE_TIMEOUT = 4
+TA_FP16 = 0
+TA_BF16 = 1
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+lib_path = os.path.join(_PKG, "libtreeattn.so")
+
+
+class TreeAttnError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: {status_string(status)} ({status})")
+        self.status = status
+
+
+class Dims(ctypes.Structure):
+    _fields_ = [("batch_size", ctypes.c_int32), ("total_q", ctypes.c_int32),
+                ("total_kv", ctypes.c_int32), ("total_tree", ctypes.c_int32),
+                ("h_q", ctypes.c_int32), ("h_kv", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("dtype", ctypes.c_int)]
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library; raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(lib_path):
+        raise RuntimeError(f"libtreeattn.so is not built ({lib_path}); run "
+                           "tree_attention_gb300.build.build() or __graft_entry__.build()")
+    L = ctypes.CDLL(lib_path)
+    vp, i32p, sz = ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t
+    L.tree_attn_workspace_size.argtypes = [ctypes.POINTER(Dims)]
+    L.tree_attn_workspace_size.restype = sz
+    L.tree_attn.argtypes = [vp, i32p, vp, vp, i32p, i32p, i32p, i32p, vp, vp, ctypes.c_int32,
+                            ctypes.c_float, ctypes.c_float, ctypes.c_float,
+                            ctypes.POINTER(Dims), vp, sz, vp]
+    L.tree_attn.restype = ctypes.c_int
+    L.tree_attn_plan.argtypes = [i32p, i32p, i32p, i32p, i32p, ctypes.c_int32, ctypes.c_float,
+                                 ctypes.c_float, ctypes.POINTER(Dims), vp, sz, vp]
+    L.tree_attn_plan.restype = ctypes.c_int
+    L.tree_attn_run.argtypes = [vp, vp, vp, i32p, i32p, i32p, i32p, vp, vp, ctypes.c_int32,
+                                ctypes.c_float, ctypes.POINTER(Dims), vp, sz, vp]
+    L.tree_attn_run.restype = ctypes.c_int
+    L.tree_attn_device_status.argtypes = [vp, vp]
+    L.tree_attn_device_status.restype = ctypes.c_int
+    L.tree_attn_status_string.argtypes = [ctypes.c_int]
+    L.tree_attn_status_string.restype = ctypes.c_char_p
+    L.tree_attn_mask_dense.argtypes = [i32p, i32p, i32p, i32p, ctypes.c_int32, ctypes.c_int32,
+                                       ctypes.c_int32, vp, vp]
+    L.tree_attn_mask_dense.restype = ctypes.c_int
+    L.tree_attn_check_inputs.argtypes = [i32p, i32p, i32p, i32p, i32p, ctypes.POINTER(Dims)]
+    L.tree_attn_check_inputs.restype = ctypes.c_int
+    _lib = L
+    return L
+
+
+def status_string(status: int) -> str:
+    try:
+        return lib().tree_attn_status_string(int(status)).decode()
+    except RuntimeError:
+        return f"status {status}"
+
+
+def _dtype_code(t: torch.dtype) -> int:
+    if t == torch.float16:
+        return TA_FP16
+    if t == torch.bfloat16:
+        return TA_BF16
+    raise TypeError(f"unsupported dtype {t}")
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_ptr(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def make_dims(q: torch.Tensor, k: torch.Tensor, q_indptr: torch.Tensor,
+              tree_order: torch.Tensor) -> Dims:
+    return Dims(batch_size=q_indptr.numel() - 1, total_q=q.shape[0], total_kv=k.shape[0],
+                total_tree=tree_order.shape[0], h_q=q.shape[1], h_kv=k.shape[1],
+                head_dim=q.shape[2], dtype=_dtype_code(q.dtype))
+
+
+def workspace_size(dims: Dims) -> int:
+    return int(lib().tree_attn_workspace_size(ctypes.byref(dims)))
+
+
+def _check_dev(name: str, t: Optional[torch.Tensor], dtype=None):
+    if t is None:
+        return
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+
+
+def tree_attn(q, q_indptr, k, v, kv_indptr, q_rope_position, mn_indptr, tree_order, out, lse,
+              rotary_mode: int, rope_scale: float, rope_theta: float, sm_scale: float,
+              workspace: torch.Tensor, stream=None) -> None:
+    """Enqueue one batched tree attention on ``stream`` (default: torch's
+    current stream).  All tensors are CUDA tensors with the layouts of
+    ``include/tree_attn.h``; ``out`` and ``lse`` are written."""
+    for name, t in (("q", q), ("k", k), ("v", v), ("out", out)):
+        _check_dev(name, t, q.dtype)
+    for name, t in (("q_indptr", q_indptr), ("kv_indptr", kv_indptr), ("mn_indptr", mn_indptr),
+                    ("tree_order", tree_order), ("q_rope_position", q_rope_position)):
+        _check_dev(name, t, torch.int32)
+    _check_dev("lse", lse, torch.float32)
+    _check_dev("workspace", workspace)
+    dims = make_dims(q, k, q_indptr, tree_order)
+    st = lib().tree_attn(_ptr(q), _ptr(q_indptr), _ptr(k), _ptr(v), _ptr(kv_indptr),
+                         _ptr(q_rope_position), _ptr(mn_indptr), _ptr(tree_order), _ptr(out),
+                         _ptr(lse), int(rotary_mode), float(rope_scale), float(rope_theta),
+                         float(sm_scale), ctypes.byref(dims), _ptr(workspace),
+                         workspace.numel() * workspace.element_size(), _stream_ptr(stream))
+    if st != TA_OK:
+        raise TreeAttnError(st, "tree_attn")
+
+
+def plan(q, q_indptr, k, kv_indptr, q_rope_position, mn_indptr, tree_order,
+         rotary_mode: int, rope_scale: float, rope_theta: float, workspace: torch.Tensor,
+         stream=None) -> None:
+    """Enqueue the plan kernel (work items, tile classes, RoPE table); q and
+    k are passed only for their shapes and dtype."""
+    dims = make_dims(q, k, q_indptr, tree_order)
+    st = lib().tree_attn_plan(_ptr(q_indptr), _ptr(kv_indptr), _ptr(q_rope_position),
+                              _ptr(mn_indptr), _ptr(tree_order), int(rotary_mode),
+                              float(rope_scale), float(rope_theta), ctypes.byref(dims),
+                              _ptr(workspace), workspace.numel() * workspace.element_size(),
+                              _stream_ptr(stream))
+    if st != TA_OK:
+        raise TreeAttnError(st, "tree_attn_plan")
+
+
+def run(q, k, v, q_indptr, kv_indptr, mn_indptr, tree_order, out, lse, rotary_mode: int,
+        sm_scale: float, workspace: torch.Tensor, stream=None) -> None:
+    """Enqueue the attention kernel on the plan held in ``workspace``."""
+    dims = make_dims(q, k, q_indptr, tree_order)
+    st = lib().tree_attn_run(_ptr(q), _ptr(k), _ptr(v), _ptr(q_indptr), _ptr(kv_indptr),
+                             _ptr(mn_indptr), _ptr(tree_order), _ptr(out), _ptr(lse),
+                             int(rotary_mode), float(sm_scale), ctypes.byref(dims),
+                             _ptr(workspace), workspace.numel() * workspace.element_size(),
+                             _stream_ptr(stream))
+    if st != TA_OK:
+        raise TreeAttnError(st, "tree_attn_run")
+
+
+def device_status(workspace: torch.Tensor, stream=None) -> int:
+    """Synchronise the stream and return (and clear) the device status."""
+    return int(lib().tree_attn_device_status(_ptr(workspace), _stream_ptr(stream)))
+
+
+def mask_dense(q_indptr, kv_indptr, mn_indptr, tree_order, total_q: int, max_kv: int,
+               stream=None) -> torch.Tensor:
+    """Dense visibility bytes ``[total_q, max_kv]`` from the device mask code."""
+    vis = torch.zeros((max(total_q, 1), max(max_kv, 1)), dtype=torch.uint8,
+                      device=q_indptr.device)
+    st = lib().tree_attn_mask_dense(_ptr(q_indptr), _ptr(kv_indptr), _ptr(mn_indptr),
+                                    _ptr(tree_order), q_indptr.numel() - 1, total_q, max_kv,
+                                    _ptr(vis), _stream_ptr(stream))
+    if st != TA_OK:
+        raise TreeAttnError(st, "tree_attn_mask_dense")
+    return vis[:total_q, :max_kv]
+
+
+def check_inputs(q_indptr, kv_indptr, mn_indptr, tree_order, dims: Dims) -> int:
+    """Host-side validation of host (CPU) int32 index arrays."""
+    import numpy as np
+    arrs = [np.ascontiguousarray(np.asarray(a, dtype=np.int32)) for a in
+            (q_indptr, kv_indptr, mn_indptr, tree_order)]
+    ptrs = [a.ctypes.data_as(ctypes.c_void_p) if a.size else None for a in arrs]
+    return int(lib().tree_attn_check_inputs(ptrs[0], ptrs[1], ptrs[2], ptrs[3], None,
+                                            ctypes.byref(dims)))
+
+
+class TreeAttention:
+    """Owns a workspace sized for one problem shape and runs the call.
+
+    ``inputs`` is a dict of CUDA tensors with keys ``q, q_indptr, k, v,
+    kv_indptr, q_rope_position (or None), mn_indptr, tree_order``."""
+
+    def __init__(self, q, k, q_indptr, tree_order, rotary_mode: int, rope_scale: float,
+                 rope_theta: float, sm_scale: float):
+        self.dims = make_dims(q, k, q_indptr, tree_order)
+        n = workspace_size(self.dims)
+        if n == 0:
+            raise TreeAttnError(TA_ERR_UNSUPPORTED, "tree_attn_workspace_size")
+        # zero-filled once: the library keeps its counters consistent afterwards
+        self.workspace = torch.zeros(n, dtype=torch.uint8, device=q.device)
+        self.rotary_mode, self.rope_scale = rotary_mode, rope_scale
+        self.rope_theta, self.sm_scale = rope_theta, sm_scale
+
+    def __call__(self, q, q_indptr, k, v, kv_indptr, q_rope_position, mn_indptr, tree_order,
+                 out=None, lse=None, stream=None):
+        if out is None:
+            out = torch.empty_like(q)
+        if lse is None:
+            lse = torch.empty(q.shape[:2], dtype=torch.float32, device=q.device)
+        tree_attn(q, q_indptr, k, v, kv_indptr, q_rope_position, mn_indptr, tree_order, out,
+                  lse, self.rotary_mode, self.rope_scale, self.rope_theta, self.sm_scale,
+                  self.workspace, stream)
+        return out, lse

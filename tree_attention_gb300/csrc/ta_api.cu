@@ -1,0 +1,373 @@
+// ta_api.cu -- host side of the C ABI declared in include/tree_attn.h:
+// argument validation, workspace layout, TMA tensor-map encoding and the two
+// launches (plan kernel, persistent attention kernel) of one tree_attn call.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "../../include/tree_attn.h"
+#include "ta_launch.h"
+
+using ta::WsHeader;
+using ta::WsLayout;
+
+namespace {
+
+constexpr unsigned long long kDeviceWaitLimitNs = 2000000000ull;  // 2 s per bounded wait
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                         cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return n;
+}
+
+bool dims_valid(const ta_dims* d) {
+  if (!d) return false;
+  if (d->batch_size < 1 || d->total_q < 0 || d->total_kv < 0 || d->total_tree < 0) return false;
+  if (d->h_q < 1 || d->h_kv < 1 || d->h_q % d->h_kv != 0) return false;
+  if (d->dtype != TA_FP16 && d->dtype != TA_BF16) return false;
+  if (d->head_dim < 1) return false;
+  return true;
+}
+
+ta_status dims_supported(const ta_dims* d) {
+  if (d->head_dim != 64 && d->head_dim != 128) return TA_ERR_UNSUPPORTED;
+  if (d->h_q / d->h_kv > ta::kMaxGroup) return TA_ERR_UNSUPPORTED;
+  return TA_OK;
+}
+
+WsLayout layout_of(const ta_dims* d) {
+  return ta::make_ws_layout(d->batch_size, d->total_q, d->total_kv, d->h_q / d->h_kv,
+                            d->head_dim);
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+// 3-D tensor map over [rows, heads, d] (d fastest) with a {64, box_heads,
+// box_rows} box and 128-byte swizzle.
+bool make_map(CUtensorMap* m, const void* base, ta_dtype dt, int rows, int heads, int d,
+              int box_heads, int box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t gdim[3] = {(cuuint64_t)d, (cuuint64_t)heads, (cuuint64_t)rows};
+  const cuuint64_t gstride[2] = {(cuuint64_t)d * 2, (cuuint64_t)heads * d * 2};
+  const cuuint32_t box[3] = {64u, (cuuint32_t)box_heads, (cuuint32_t)box_rows};
+  const cuuint32_t estride[3] = {1u, 1u, 1u};
+  const CUtensorMapDataType t =
+      dt == TA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  const CUresult r = fn(m, t, 3, const_cast<void*>(base), gdim, gstride, box, estride,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t tree_attn_workspace_size(const ta_dims* dims) {
+  if (!dims_valid(dims) || dims_supported(dims) != TA_OK) return 0;
+  const WsLayout L = layout_of(dims);
+  if (L.class_bytes >= (int64_t)INT32_MAX) return 0;
+  return L.total;
+}
+
+}  // extern "C"
+
+namespace {
+
+// Checks shared by the plan and run halves.
+ta_status check_common(const int32_t* q_indptr, const int32_t* kv_indptr,
+                       const int32_t* mn_indptr, const int32_t* tree_order, int32_t rotary_mode,
+                       const ta_dims* dims, const void* workspace, size_t workspace_bytes) {
+  if (!dims_valid(dims)) return TA_ERR_INVALID_ARGUMENT;
+  const ta_status sup = dims_supported(dims);
+  if (sup != TA_OK) return sup;
+  if (!q_indptr || !kv_indptr || !mn_indptr || !workspace) return TA_ERR_INVALID_ARGUMENT;
+  if (dims->total_tree > 0 && !tree_order) return TA_ERR_INVALID_ARGUMENT;
+  if (rotary_mode != 0 && rotary_mode != 1) return TA_ERR_INVALID_ARGUMENT;
+  if (!aligned(workspace, 256)) return TA_ERR_INVALID_ARGUMENT;
+  const size_t need = tree_attn_workspace_size(dims);
+  if (need == 0) return TA_ERR_UNSUPPORTED;
+  if (workspace_bytes < need) return TA_ERR_INVALID_ARGUMENT;
+  if (dims->total_q > 0 && dims->total_kv == 0) return TA_ERR_INVALID_ARGUMENT;  // qo <= T <= kv
+  return TA_OK;
+}
+
+ta_status check_plan_args(const int32_t* q_rope_position, int32_t rotary_mode, float rope_scale,
+                          float rope_theta, const ta_dims* dims) {
+  if (rotary_mode == 1 && !q_rope_position && dims->total_kv > 0) return TA_ERR_INVALID_ARGUMENT;
+  if (rotary_mode == 1 && (!std::isfinite(rope_scale) || !std::isfinite(rope_theta) ||
+                           !(rope_theta > 0.f)))
+    return TA_ERR_INVALID_ARGUMENT;
+  return TA_OK;
+}
+
+ta_status check_run_args(const void* q, const void* k, const void* v, const void* out,
+                         const float* lse, float sm_scale, const ta_dims* dims) {
+  if (dims->total_q > 0 && (!q || !out || !lse)) return TA_ERR_INVALID_ARGUMENT;
+  if (dims->total_kv > 0 && (!k || !v)) return TA_ERR_INVALID_ARGUMENT;
+  if (!std::isfinite(sm_scale)) return TA_ERR_INVALID_ARGUMENT;
+  if ((q && !aligned(q, 16)) || (k && !aligned(k, 16)) || (v && !aligned(v, 16)) ||
+      (out && !aligned(out, 16)))
+    return TA_ERR_INVALID_ARGUMENT;
+  return TA_OK;
+}
+
+struct WsPtrs {
+  WsHeader* hdr;
+  ta::PairInfo* pairs;
+  int32_t* sorted;
+  uint8_t* classes;
+  float2* rope_cs;
+};
+
+WsPtrs ws_ptrs(void* workspace, const WsLayout& L) {
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  return WsPtrs{reinterpret_cast<WsHeader*>(ws), reinterpret_cast<ta::PairInfo*>(ws + L.off_pairs),
+                reinterpret_cast<int32_t*>(ws + L.off_sorted), ws + L.off_classes,
+                reinterpret_cast<float2*>(ws + L.off_rope)};
+}
+
+ta_status launch_plan_checked(const int32_t* q_indptr, const int32_t* kv_indptr,
+                              const int32_t* q_rope_position, const int32_t* mn_indptr,
+                              const int32_t* tree_order, int32_t rotary_mode, float rope_scale,
+                              float rope_theta, const ta_dims* dims, void* workspace,
+                              cudaStream_t st) {
+  const int g = dims->h_q / dims->h_kv;
+  const WsLayout L = layout_of(dims);
+  const WsPtrs w = ws_ptrs(workspace, L);
+  const int nsm = sm_count();
+  if (nsm <= 0) return TA_ERR_CUDA;
+  ta::PlanParams pp{};
+  pp.q_indptr = q_indptr;
+  pp.kv_indptr = kv_indptr;
+  pp.mn_indptr = mn_indptr;
+  pp.tree_order = tree_order;
+  pp.rope_pos = q_rope_position;
+  pp.batch = dims->batch_size;
+  pp.g = g;
+  pp.R = ta::rows_per_item(g);
+  pp.h_kv = dims->h_kv;
+  pp.head_dim = dims->head_dim;
+  pp.total_q = dims->total_q;
+  pp.total_kv = dims->total_kv;
+  pp.total_tree = dims->total_tree;
+  pp.rotary = rotary_mode;
+  pp.max_pairs = L.max_pairs;
+  pp.rope_scale = rope_scale;
+  pp.rope_theta = rope_theta;
+  pp.hdr = w.hdr;
+  pp.pairs = w.pairs;
+  pp.sorted = w.sorted;
+  pp.classes = w.classes;
+  pp.rope_cs = w.rope_cs;
+  int plan_grid = (int)L.max_pairs;
+  if (rotary_mode == 1 && plan_grid < 2 * nsm) plan_grid = 2 * nsm;
+  return ta::launch_plan(pp, plan_grid, st) == cudaSuccess ? TA_OK : TA_ERR_CUDA;
+}
+
+ta_status launch_run_checked(const void* q, const void* k, const void* v, const int32_t* q_indptr,
+                             const int32_t* kv_indptr, const int32_t* mn_indptr,
+                             const int32_t* tree_order, void* out, float* lse,
+                             int32_t rotary_mode, float sm_scale, const ta_dims* dims,
+                             void* workspace, cudaStream_t st) {
+  const int g = dims->h_q / dims->h_kv;
+  const int R = ta::rows_per_item(g);
+  const int D = dims->head_dim;
+  const WsLayout L = layout_of(dims);
+  const WsPtrs w = ws_ptrs(workspace, L);
+  const int nsm = sm_count();
+  if (nsm <= 0) return TA_ERR_CUDA;
+  CUtensorMap tm_q, tm_k, tm_v;
+  if (!make_map(&tm_q, q, dims->dtype, dims->total_q, dims->h_q, D, g, R) ||
+      !make_map(&tm_k, k, dims->dtype, dims->total_kv, dims->h_kv, D, 1, ta::kKvBoxRows) ||
+      !make_map(&tm_v, v, dims->dtype, dims->total_kv, dims->h_kv, D, 1, ta::kKvBoxRows))
+    return TA_ERR_CUDA;
+  ta::AttnParams ap{};
+  ap.tree_order = tree_order;
+  ap.out = out;
+  ap.lse = lse;
+  ap.pairs = w.pairs;
+  ap.sorted = w.sorted;
+  ap.classes = w.classes;
+  ap.rope_cs = w.rope_cs;
+  ap.q_indptr = q_indptr;
+  ap.kv_indptr = kv_indptr;
+  ap.mn_indptr = mn_indptr;
+  ap.hdr = w.hdr;
+  ap.h_q = dims->h_q;
+  ap.h_kv = dims->h_kv;
+  ap.g = g;
+  ap.R = R;
+  ap.rotary = rotary_mode;
+  ap.max_pairs = L.max_pairs;
+  ap.scale_log2 = sm_scale * 1.4426950408889634f;
+  ap.timeout_ns = kDeviceWaitLimitNs;
+  const int64_t max_items = L.max_pairs * dims->h_kv;
+  const int grid = (int)(max_items < nsm ? max_items : nsm);
+  cudaError_t e;
+  const bool bf16 = dims->dtype == TA_BF16;
+  if (D == 64)
+    e = bf16 ? ta::launch_attn<64, true>(tm_q, tm_k, tm_v, ap, grid, st)
+             : ta::launch_attn<64, false>(tm_q, tm_k, tm_v, ap, grid, st);
+  else
+    e = bf16 ? ta::launch_attn<128, true>(tm_q, tm_k, tm_v, ap, grid, st)
+             : ta::launch_attn<128, false>(tm_q, tm_k, tm_v, ap, grid, st);
+  return e == cudaSuccess ? TA_OK : TA_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+ta_status tree_attn_plan(const int32_t* q_indptr, const int32_t* kv_indptr,
+                         const int32_t* q_rope_position, const int32_t* mn_indptr,
+                         const int32_t* tree_order, int32_t rotary_mode, float rope_scale,
+                         float rope_theta, const ta_dims* dims, void* workspace,
+                         size_t workspace_bytes, void* stream) {
+  ta_status s = check_common(q_indptr, kv_indptr, mn_indptr, tree_order, rotary_mode, dims,
+                             workspace, workspace_bytes);
+  if (s != TA_OK) return s;
+  s = check_plan_args(q_rope_position, rotary_mode, rope_scale, rope_theta, dims);
+  if (s != TA_OK) return s;
+  if (dims->total_q == 0) return TA_OK;
+  return launch_plan_checked(q_indptr, kv_indptr, q_rope_position, mn_indptr, tree_order,
+                             rotary_mode, rope_scale, rope_theta, dims, workspace,
+                             static_cast<cudaStream_t>(stream));
+}
+
+ta_status tree_attn_run(const void* q, const void* k, const void* v, const int32_t* q_indptr,
+                        const int32_t* kv_indptr, const int32_t* mn_indptr,
+                        const int32_t* tree_order, void* out, float* lse, int32_t rotary_mode,
+                        float sm_scale, const ta_dims* dims, void* workspace,
+                        size_t workspace_bytes, void* stream) {
+  ta_status s = check_common(q_indptr, kv_indptr, mn_indptr, tree_order, rotary_mode, dims,
+                             workspace, workspace_bytes);
+  if (s != TA_OK) return s;
+  s = check_run_args(q, k, v, out, lse, sm_scale, dims);
+  if (s != TA_OK) return s;
+  if (dims->total_q == 0) return TA_OK;
+  return launch_run_checked(q, k, v, q_indptr, kv_indptr, mn_indptr, tree_order, out, lse,
+                            rotary_mode, sm_scale, dims, workspace,
+                            static_cast<cudaStream_t>(stream));
+}
+
+ta_status tree_attn(const void* q, const int32_t* q_indptr, const void* k, const void* v,
+                    const int32_t* kv_indptr, const int32_t* q_rope_position,
+                    const int32_t* mn_indptr, const int32_t* tree_order, void* out, float* lse,
+                    int32_t rotary_mode, float rope_scale, float rope_theta, float sm_scale,
+                    const ta_dims* dims, void* workspace, size_t workspace_bytes, void* stream) {
+  ta_status s = check_common(q_indptr, kv_indptr, mn_indptr, tree_order, rotary_mode, dims,
+                             workspace, workspace_bytes);
+  if (s != TA_OK) return s;
+  s = check_plan_args(q_rope_position, rotary_mode, rope_scale, rope_theta, dims);
+  if (s != TA_OK) return s;
+  s = check_run_args(q, k, v, out, lse, sm_scale, dims);
+  if (s != TA_OK) return s;
+  if (dims->total_q == 0) return TA_OK;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  s = launch_plan_checked(q_indptr, kv_indptr, q_rope_position, mn_indptr, tree_order,
+                          rotary_mode, rope_scale, rope_theta, dims, workspace, st);
+  if (s != TA_OK) return s;
+  return launch_run_checked(q, k, v, q_indptr, kv_indptr, mn_indptr, tree_order, out, lse,
+                            rotary_mode, sm_scale, dims, workspace, st);
+}
+
+ta_status tree_attn_device_status(void* workspace, void* stream) {
+  if (!workspace) return TA_ERR_INVALID_ARGUMENT;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(st) != cudaSuccess) return TA_ERR_CUDA;
+  WsHeader* hdr = static_cast<WsHeader*>(workspace);
+  unsigned int err = 0;
+  if (cudaMemcpy(&err, &hdr->error, sizeof(err), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return TA_ERR_CUDA;
+  if (err != 0 && cudaMemset(&hdr->error, 0, sizeof(err)) != cudaSuccess) return TA_ERR_CUDA;
+  if (err & ta::DEVERR_TIMEOUT) return TA_ERR_DEVICE_TIMEOUT;
+  if (err & ta::DEVERR_BAD_INDPTR) return TA_ERR_INVALID_ARGUMENT;
+  return TA_OK;
+}
+
+const char* tree_attn_status_string(ta_status s) {
+  switch (s) {
+    case TA_OK: return "TA_OK";
+    case TA_ERR_INVALID_ARGUMENT: return "TA_ERR_INVALID_ARGUMENT";
+    case TA_ERR_UNSUPPORTED: return "TA_ERR_UNSUPPORTED";
+    case TA_ERR_CUDA: return "TA_ERR_CUDA";
+    case TA_ERR_DEVICE_TIMEOUT: return "TA_ERR_DEVICE_TIMEOUT";
+  }
+  return "TA_ERR_UNKNOWN";
+}
+
+ta_status tree_attn_mask_dense(const int32_t* q_indptr, const int32_t* kv_indptr,
+                               const int32_t* mn_indptr, const int32_t* tree_order,
+                               int32_t batch_size, int32_t total_q, int32_t max_kv, uint8_t* vis,
+                               void* stream) {
+  if (!q_indptr || !kv_indptr || !mn_indptr || !tree_order || !vis) return TA_ERR_INVALID_ARGUMENT;
+  if (batch_size < 1 || total_q < 0 || max_kv < 0) return TA_ERR_INVALID_ARGUMENT;
+  if (total_q == 0 || max_kv == 0) return TA_OK;
+  const cudaError_t e = ta::launch_mask_dense(q_indptr, kv_indptr, mn_indptr, tree_order,
+                                              batch_size, total_q, max_kv, vis,
+                                              static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? TA_OK : TA_ERR_CUDA;
+}
+
+ta_status tree_attn_check_inputs(const int32_t* q_indptr, const int32_t* kv_indptr,
+                                 const int32_t* mn_indptr, const int32_t* tree_order,
+                                 const int32_t* q_rope_position, const ta_dims* dims) {
+  (void)q_rope_position;
+  if (!dims_valid(dims) || !q_indptr || !kv_indptr || !mn_indptr) return TA_ERR_INVALID_ARGUMENT;
+  const int B = dims->batch_size;
+  if (q_indptr[0] != 0 || kv_indptr[0] != 0 || mn_indptr[0] != 0) return TA_ERR_INVALID_ARGUMENT;
+  if (q_indptr[B] != dims->total_q || kv_indptr[B] != dims->total_kv ||
+      mn_indptr[B] != dims->total_tree)
+    return TA_ERR_INVALID_ARGUMENT;
+  if (dims->total_tree > 0 && !tree_order) return TA_ERR_INVALID_ARGUMENT;
+  std::vector<int> stack;
+  for (int b = 0; b < B; ++b) {
+    const int qo = q_indptr[b + 1] - q_indptr[b];
+    const int kv = kv_indptr[b + 1] - kv_indptr[b];
+    const int T = mn_indptr[b + 1] - mn_indptr[b];
+    if (qo < 0 || T < qo || kv < T) return TA_ERR_INVALID_ARGUMENT;
+    // intervals: 0 <= enter < exit <= T and laminar (sort by enter, check nesting)
+    std::vector<std::pair<int, int>> iv(T);
+    for (int i = 0; i < T; ++i) {
+      const int e = tree_order[2 * (mn_indptr[b] + i)], x = tree_order[2 * (mn_indptr[b] + i) + 1];
+      if (e < 0 || x <= e || x > T) return TA_ERR_INVALID_ARGUMENT;
+      iv[i] = {e, -x};
+    }
+    std::sort(iv.begin(), iv.end());
+    stack.clear();
+    for (const auto& pr : iv) {
+      const int e = pr.first, x = -pr.second;
+      while (!stack.empty() && stack.back() <= e) stack.pop_back();
+      if (!stack.empty() && x > stack.back()) return TA_ERR_INVALID_ARGUMENT;  // overlaps
+      stack.push_back(x);
+    }
+  }
+  return TA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,60 @@
+// ta_launch.h -- internal interface between the C-ABI host code (ta_api.cu)
+// and the kernel translation units (ta_plan.cu, ta_attn.cu).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "ta_layout.h"
+
+namespace ta {
+
+struct PlanParams {
+  const int32_t* q_indptr;
+  const int32_t* kv_indptr;
+  const int32_t* mn_indptr;
+  const int32_t* tree_order;
+  const int32_t* rope_pos;  // may be null when rotary == 0
+  int batch, g, R, h_kv, head_dim, total_q, total_kv, total_tree, rotary;
+  int64_t max_pairs;
+  float rope_scale, rope_theta;
+  WsHeader* hdr;
+  PairInfo* pairs;
+  int32_t* sorted;
+  uint8_t* classes;
+  float2* rope_cs;
+};
+
+struct AttnParams {
+  const int32_t* tree_order;
+  void* out;
+  float* lse;
+  const PairInfo* pairs;
+  const int32_t* sorted;
+  const uint8_t* classes;
+  const float2* rope_cs;
+  const int32_t* q_indptr;
+  const int32_t* kv_indptr;
+  const int32_t* mn_indptr;
+  WsHeader* hdr;
+  int h_q, h_kv, g, R, rotary;
+  int64_t max_pairs;  // capacity of the pair table in the workspace
+  float scale_log2;   // sm_scale * log2(e)
+  unsigned long long timeout_ns;
+};
+
+// Plan kernel: sequence/tile enumeration, tile classification, LPT ordering
+// and the RoPE cos/sin table.  ``grid`` >= max_pairs.
+cudaError_t launch_plan(const PlanParams& p, int grid, cudaStream_t stream);
+
+// Dense mask export (test helper).
+cudaError_t launch_mask_dense(const int32_t* q_indptr, const int32_t* kv_indptr,
+                              const int32_t* mn_indptr, const int32_t* tree_order, int batch,
+                              int total_q, int max_kv, uint8_t* vis, cudaStream_t stream);
+
+// Persistent tree-attention kernel.
+template <int D, bool BF16>
+cudaError_t launch_attn(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
+                        const AttnParams& p, int grid, cudaStream_t stream);
+
+}  // namespace ta

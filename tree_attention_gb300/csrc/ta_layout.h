@@ -1,0 +1,83 @@
+// ta_layout.h -- definitions shared by the host launcher and the kernels:
+// tile sizes, the workspace layout and the records the plan kernel leaves
+// for the attention kernel.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+namespace ta {
+
+// One work item is a tile of kBlockM packed rows: floor(kBlockM / g) q rows
+// times the g q heads of one kv head (row index = q_row * g + head_in_group,
+// the packing of the "Q_load" block of the page "tree_attn.py"), attended
+// against kv tiles of kBlockN columns.
+constexpr int kBlockM = 128;
+constexpr int kBlockN = 128;
+constexpr int kKvBoxRows = 64;   // kv rows per TMA box (a kv tile is 1 or 2 boxes)
+constexpr int kMaxGroup = 128;   // largest supported h_q / h_kv
+
+// Tile classes computed by the plan kernel for each (q tile, kv tile).
+constexpr uint8_t kTileEmpty = 0;    // no (row, column) pair visible: skipped
+constexpr uint8_t kTilePartial = 1;  // some visible: the mask is evaluated per element
+constexpr uint8_t kTileFull = 2;     // every valid row sees every column: no mask
+
+// Device status bits (WsHeader::error).
+constexpr unsigned int DEVERR_TIMEOUT = 1u;     // a bounded wait expired
+constexpr unsigned int DEVERR_BAD_INDPTR = 2u;  // index arrays violate the layout rules
+
+constexpr int kCostBuckets = 4096;  // LPT ordering resolution (tiles per item)
+
+struct WsHeader {
+  unsigned int queue_head;  // next work item (attention kernel)
+  unsigned int queue_done;  // attention CTAs finished (the last one resets the queue)
+  unsigned int error;       // DEVERR_* bits, cleared by tree_attn_device_status
+  unsigned int num_pairs;   // (sequence, q tile) pairs found by the plan kernel
+  unsigned int num_items;   // num_pairs * h_kv, 0 if the index arrays are invalid
+  unsigned int plan_done;   // plan CTAs finished (the last one orders the work)
+  unsigned int pad[10];
+};
+static_assert(sizeof(WsHeader) == 64, "header size");
+
+struct PairInfo {
+  int32_t b;          // sequence
+  int32_t t;          // q tile within the sequence
+  int32_t class_off;  // byte offset of the tile's kv-tile classes (16-aligned)
+  int32_t n_tiles;    // number of non-empty kv tiles
+};
+
+inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+inline int64_t round_up(int64_t a, int64_t b) { return ceil_div(a, b) * b; }
+
+// q rows per work item for group size g.
+inline int rows_per_item(int g) { return kBlockM / g; }
+
+struct WsLayout {
+  int64_t max_pairs;    // upper bound on (sequence, q tile) pairs
+  int64_t class_bytes;  // bound on the class table
+  size_t off_pairs, off_sorted, off_classes, off_rope, total;
+};
+
+// Workspace layout for the given sizes (all offsets 256-byte aligned):
+//   header | PairInfo[max_pairs] | int32 sorted[max_pairs] | uint8 classes[]
+//   | float2 rope_cs[total_kv][head_dim / 2]
+inline WsLayout make_ws_layout(int64_t batch, int64_t total_q, int64_t total_kv, int g,
+                               int head_dim) {
+  WsLayout L{};
+  const int64_t R = rows_per_item(g);
+  L.max_pairs = ceil_div(total_q, R) + batch;
+  L.class_bytes = L.max_pairs * round_up(ceil_div(total_kv, kBlockN), 16);
+  size_t off = 256;
+  L.off_pairs = off;
+  off += round_up(L.max_pairs * (int64_t)sizeof(PairInfo), 256);
+  L.off_sorted = off;
+  off += round_up(L.max_pairs * 4, 256);
+  L.off_classes = off;
+  off += round_up(L.class_bytes, 256);
+  L.off_rope = off;
+  off += round_up(total_kv * (int64_t)(head_dim / 2) * 8, 256);
+  L.total = off;
+  return L;
+}
+
+}  // namespace ta

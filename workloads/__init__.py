@@ -367,3 +367,17 @@ def algorithmic_bytes(w: Workload) -> float:
     if w.rotary_mode == 1:
         b += 4 * w.total_kv
     return float(b)
+
+
+def device_inputs(w: Workload, device="cuda") -> dict:
+    """The workload's buffers as contiguous tensors on ``device`` (int32
+    index arrays, q/k/v in the storage dtype)."""
+    def i32(a):
+        return torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(device)
+    return {
+        "q": w.q.contiguous().to(device), "k": w.k.contiguous().to(device),
+        "v": w.v.contiguous().to(device),
+        "q_indptr": i32(w.q_indptr), "kv_indptr": i32(w.kv_indptr),
+        "mn_indptr": i32(w.mn_indptr), "tree_order": i32(w.tree_order.reshape(-1, 2)),
+        "q_rope_position": None if w.rope_position is None else i32(w.rope_position),
+    }
