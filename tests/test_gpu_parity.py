@@ -229,3 +229,30 @@ def test_bad_index_arrays_are_reported_not_computed():
     assert torch.all(out == 7.0) and torch.all(lse == 7.0)
     # the status word was cleared by the read
     assert ta.device_status(attn.workspace) == ta.TA_OK
+
+
+# --------------------------------------------------------------------------
+# RoPE table: float32 cos/sin rounded correctly (as the oracle takes them)
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("idx", [2, 3, 4])
+def test_rope_table_matches_correctly_rounded_cos_sin(idx):
+    """The plan kernel's per-token cos/sin table (the last region of the
+    workspace) equals float32-rounded cos/sin of the pages' float32 angle;
+    only rare near-ties (true value within ~1e-4 ulp of a rounding midpoint)
+    may differ by one ulp."""
+    w = wl.config(idx)
+    d = wl.device_inputs(w)
+    attn = ta.TreeAttention(d["q"], d["k"], d["q_indptr"], d["tree_order"], w.rotary_mode,
+                            w.rope_scale, w.rope_theta, w.sm_scale)
+    attn(**d)
+    assert ta.device_status(attn.workspace) == ta.TA_OK
+    half = w.head_dim // 2
+    nbytes = w.total_kv * half * 8
+    off = attn.workspace.numel() - ((nbytes + 255) // 256) * 256
+    tab = attn.workspace[off:off + nbytes].cpu().numpy().view(np.float32).reshape(-1, half, 2)
+    c, s = oracle.rope_cos_sin(w.rope_position, w.head_dim, w.rope_theta, w.rope_scale)
+    bad = int(np.sum(tab[..., 0] != c) + np.sum(tab[..., 1] != s))
+    assert bad <= max(2, c.size * 2 // 100000), f"{bad} of {2 * c.size} entries differ"
+    ulps = np.abs(tab[..., 0].view(np.int32).astype(np.int64) - c.view(np.int32))
+    assert ulps.max() <= 1

@@ -12,13 +12,16 @@
 //   3. orders the pairs longest-first (LPT) for the attention kernel's
 //      work queue (the last CTA to finish does a counting sort);
 //   4. fills the RoPE cos/sin table, one entry per (kv token, frequency), in
-//      the float32 steps of ``_rope`` (page "_kernel_common.py").
+//      the float32 steps of ``_rope`` (page "_kernel_common.py"): angle =
+//      fl32(fl32(pos * scale) / fl32(theta^(2i/d))), cos and sin of it
+//      rounded correctly to float32 (cr_sincosf).
 #include <cuda_runtime.h>
 
 #include <climits>
 #include <cstdint>
 
 #include "ta_device.cuh"
+#include "ta_sincos.cuh"
 #include "ta_launch.h"
 
 namespace ta {
@@ -233,7 +236,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanParams p) 
         const float s = __fmul_rn((float)p.rope_pos[tok], p.rope_scale);
         const float ang = __fdiv_rn(s, s_den[i]);
         float sn, cs;
-        sincosf(ang, &sn, &cs);
+        cr_sincosf(ang, &sn, &cs);
         p.rope_cs[tok * half + i] = make_float2(cs, sn);
       }
     }
