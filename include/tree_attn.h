@@ -138,6 +138,30 @@ ta_status tree_attn_run(const void* q, const void* k, const void* v, const int32
                         float sm_scale, const ta_dims* dims, void* workspace,
                         size_t workspace_bytes, void* stream);
 
+/* Allocation-free variant of tree_attn (the pages have no counterpart: it is
+ * a deployment convenience of this library).  Some callers cannot allocate
+ * device memory: a serving engine that has handed all free HBM to its own
+ * pool (typically the KV cache) and forbids further cudaMalloc, or a host
+ * framework whose plugins may not call allocation routines because they
+ * synchronise the device or escape the framework's memory accounting.  This
+ * entry point takes the same arguments as tree_attn minus the workspace and
+ * uses a static device array of 32 MiB (held by every GPU that loads the
+ * library until the process exits) as its workspace; it calls no cudaMalloc,
+ * cudaFree or other allocating routine.
+ *   - Problems whose tree_attn_workspace_size exceeds 32 MiB are rejected
+ *     with TA_ERR_UNSUPPORTED before anything is enqueued.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress); make that first call before any stream capture.
+ *   - Every call clears the array's work counters (two cudaMemsetAsync on
+ *     ``stream``) and then runs tree_attn on it.  All calls share the one
+ *     array, so calls that may overlap on the GPU (different streams without
+ *     ordering between them) race and must not be issued. */
+ta_status tree_attn_noalloc(const void* q, const int32_t* q_indptr, const void* k, const void* v,
+                            const int32_t* kv_indptr, const int32_t* q_rope_position,
+                            const int32_t* mn_indptr, const int32_t* tree_order, void* out,
+                            float* lse, int32_t rotary_mode, float rope_scale, float rope_theta,
+                            float sm_scale, const ta_dims* dims, void* stream);
+
 /* Synchronises ``stream``, reads and clears the device status word that the
  * kernels of earlier calls left in ``workspace`` (TA_ERR_DEVICE_TIMEOUT if a
  * bounded wait expired, TA_ERR_CUDA on a CUDA error, else TA_OK). */

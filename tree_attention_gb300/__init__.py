@@ -78,6 +78,10 @@ def lib() -> ctypes.CDLL:
     L.tree_attn_run.argtypes = [vp, vp, vp, i32p, i32p, i32p, i32p, vp, vp, ctypes.c_int32,
                                 ctypes.c_float, ctypes.POINTER(Dims), vp, sz, vp]
     L.tree_attn_run.restype = ctypes.c_int
+    L.tree_attn_noalloc.argtypes = [vp, i32p, vp, vp, i32p, i32p, i32p, i32p, vp, vp,
+                                    ctypes.c_int32, ctypes.c_float, ctypes.c_float,
+                                    ctypes.c_float, ctypes.POINTER(Dims), vp]
+    L.tree_attn_noalloc.restype = ctypes.c_int
     L.tree_attn_device_status.argtypes = [vp, vp]
     L.tree_attn_device_status.restype = ctypes.c_int
     L.tree_attn_status_string.argtypes = [ctypes.c_int]
@@ -159,6 +163,22 @@ def tree_attn(q, q_indptr, k, v, kv_indptr, q_rope_position, mn_indptr, tree_ord
                          workspace.numel() * workspace.element_size(), _stream_ptr(stream))
     if st != TA_OK:
         raise TreeAttnError(st, "tree_attn")
+
+
+def tree_attn_noalloc(q, q_indptr, k, v, kv_indptr, q_rope_position, mn_indptr, tree_order,
+                      out, lse, rotary_mode: int, rope_scale: float, rope_theta: float,
+                      sm_scale: float, stream=None) -> None:
+    """``tree_attn`` for callers that may not allocate device memory: the
+    library's static 32 MiB device scratch array serves as the workspace.
+    Calls share that array, so they must not overlap on the GPU."""
+    dims = make_dims(q, k, q_indptr, tree_order)
+    st = lib().tree_attn_noalloc(_ptr(q), _ptr(q_indptr), _ptr(k), _ptr(v), _ptr(kv_indptr),
+                                 _ptr(q_rope_position), _ptr(mn_indptr), _ptr(tree_order),
+                                 _ptr(out), _ptr(lse), int(rotary_mode), float(rope_scale),
+                                 float(rope_theta), float(sm_scale), ctypes.byref(dims),
+                                 _stream_ptr(stream))
+    if st != TA_OK:
+        raise TreeAttnError(st, "tree_attn_noalloc")
 
 
 def plan(q, q_indptr, k, kv_indptr, q_rope_position, mn_indptr, tree_order,

@@ -371,3 +371,63 @@ ta_status tree_attn_check_inputs(const int32_t* q_indptr, const int32_t* kv_indp
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Allocation-free entry point: tree_attn with its workspace in a static
+// device array instead of caller memory.
+// ---------------------------------------------------------------------------
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = size_t(32) << 20;  // 32 MiB on every device
+
+// Zero-initialised with the module; each GPU that loads the library holds one
+// copy until the process exits.  In host code this name is only a stand-in
+// for the symbol: the device address comes from cudaGetSymbolAddress.
+__device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+constexpr int kMaxDevices = 256;
+
+// Device address of the scratch array on the current device, looked up once
+// per device (the first call on a device does this set-up).
+void* noalloc_scratch_address() {
+  static std::mutex mu;
+  static void* addr[kMaxDevices] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (addr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) return nullptr;
+    addr[dev] = p;
+  }
+  return addr[dev];
+}
+
+}  // namespace
+
+extern "C" {
+
+ta_status tree_attn_noalloc(const void* q, const int32_t* q_indptr, const void* k, const void* v,
+                            const int32_t* kv_indptr, const int32_t* q_rope_position,
+                            const int32_t* mn_indptr, const int32_t* tree_order, void* out,
+                            float* lse, int32_t rotary_mode, float rope_scale, float rope_theta,
+                            float sm_scale, const ta_dims* dims, void* stream) {
+  if (!dims_valid(dims)) return TA_ERR_INVALID_ARGUMENT;
+  const size_t need = tree_attn_workspace_size(dims);
+  if (need == 0) return dims_supported(dims) != TA_OK ? TA_ERR_UNSUPPORTED : TA_ERR_INVALID_ARGUMENT;
+  if (need > kNoAllocScratchBytes) return TA_ERR_UNSUPPORTED;  // problem too large for the scratch
+  void* ws = noalloc_scratch_address();
+  if (ws == nullptr) return TA_ERR_CUDA;
+  // the work-queue and plan counters must start at zero (the status word at
+  // offset 8 is left as it is)
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint8_t* hdr = static_cast<uint8_t*>(ws);
+  if (cudaMemsetAsync(hdr, 0, 8, st) != cudaSuccess ||
+      cudaMemsetAsync(hdr + 12, 0, sizeof(WsHeader) - 12, st) != cudaSuccess)
+    return TA_ERR_CUDA;
+  return tree_attn(q, q_indptr, k, v, kv_indptr, q_rope_position, mn_indptr, tree_order, out,
+                   lse, rotary_mode, rope_scale, rope_theta, sm_scale, dims, ws,
+                   kNoAllocScratchBytes, stream);
+}
+
+}  // extern "C"
