@@ -293,7 +293,7 @@ def run_gb300(args):
         d = {k: (v.clone() if v is not None else None) for k, v in base.items()}
         d["out"] = torch.empty_like(d["q"])
         d["lse"] = torch.empty(d["q"].shape[:2], dtype=torch.float32, device=dev)
-        dims = ta.make_dims(d["q"], d["k"], d["q_indptr"], d["tree_order"])
+        dims = ta.make_dims(d["q"], d["k"], d["q_indptr"], d["tree_order"], w.rotary_mode)
         d["ws"] = torch.zeros(ta.workspace_size(dims), dtype=torch.uint8, device=dev)
         sets.append(d)
     stream = torch.cuda.current_stream(dev)

@@ -54,7 +54,9 @@ typedef enum { TA_FP16 = 0, TA_BF16 = 1 } ta_dtype;
  *   total_tree  rows of tree_order              (mn_indptr[B])
  *   h_q, h_kv   heads; h_q % h_kv == 0, group size g = h_q / h_kv <= 128
  *   head_dim    64 or 128
- *   dtype       element type of q, k, v and out                            */
+ *   dtype       element type of q, k, v and out
+ *   rotary_mode 0 or 1: whether the calls this workspace serves apply RoPE
+ *               (it sizes the workspace; it must match their rotary_mode) */
 typedef struct {
   int32_t batch_size;
   int32_t total_q;
@@ -64,13 +66,16 @@ typedef struct {
   int32_t h_kv;
   int32_t head_dim;
   ta_dtype dtype;
+  int32_t rotary_mode;
 } ta_dims;
 
 /* Bytes of device workspace ``tree_attn`` needs for these sizes (a multiple
  * of 256; 0 on invalid dims).  The workspace holds the per-launch work plan
- * (tile classes, the cost-ordered work queue), the RoPE cos/sin table and a
- * device status word.  It depends on the sizes only, so one allocation
- * serves every call with the same dims. */
+ * (tile classes, the cost-ordered work queue), a device status word and,
+ * with RoPE, the cos/sin table of the q tokens and the rotated k
+ * (total_kv * h_kv * head_dim elements, rotated once per call instead of
+ * once per q tile that reads it).  It depends on the dims only, so one
+ * allocation serves every call with the same dims. */
 size_t tree_attn_workspace_size(const ta_dims* dims);
 
 /* Batched tree attention.  Layouts (all row-major, contiguous, device):
@@ -94,7 +99,8 @@ size_t tree_attn_workspace_size(const ta_dims* dims);
  * q rows are the last qo tree nodes (0 <= qo <= T <= kv).  A q row none of
  * whose columns is visible gets out = 0 and lse = -inf.
  *   rotary_mode     0: no RoPE; 1: rotate-half RoPE on q and k at load time
- *                   (any other value is TA_ERR_INVALID_ARGUMENT)
+ *                   (any other value, or one that differs from
+ *                   dims->rotary_mode, is TA_ERR_INVALID_ARGUMENT)
  *   rope_scale      position multiplier (finite)
  *   rope_theta      RoPE base (finite, > 0)
  *   sm_scale        score scale (finite), typically 1/sqrt(head_dim)

@@ -216,6 +216,23 @@ def test_repeated_calls_are_bitwise_identical():
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
 
 
+@pytest.mark.parametrize("idx", [5, 2])
+def test_many_runs_bitwise_identical(idx):
+    """Each output row is computed by one CTA in a fixed order, so results
+    must not depend on scheduling: any race between the warps of a CTA shows
+    up as a difference (or a bounded-wait timeout) across repeated runs."""
+    w = wl.config(idx)
+    d = wl.device_inputs(w)
+    attn = ta.TreeAttention(d["q"], d["k"], d["q_indptr"], d["tree_order"], w.rotary_mode,
+                            w.rope_scale, w.rope_theta, w.sm_scale)
+    o0, l0 = attn(**d)
+    o0, l0 = o0.clone(), l0.clone()
+    for _ in range(12):
+        o, l = attn(**d)
+        assert ta.device_status(attn.workspace) == ta.TA_OK
+        assert torch.equal(o, o0) and torch.equal(l, l0)
+
+
 def test_bad_index_arrays_are_reported_not_computed():
     w = wl.config(1)
     d = wl.device_inputs(w)
@@ -237,8 +254,8 @@ def test_bad_index_arrays_are_reported_not_computed():
 
 @pytest.mark.parametrize("idx", [2, 3, 4])
 def test_rope_table_matches_correctly_rounded_cos_sin(idx):
-    """The plan kernel's per-token cos/sin table (the last region of the
-    workspace) equals float32-rounded cos/sin of the pages' float32 angle;
+    """The plan kernel's per-token cos/sin table (the workspace region
+    before the rotated keys) equals float32-rounded cos/sin of the pages' float32 angle;
     only rare near-ties (true value within ~1e-4 ulp of a rounding midpoint)
     may differ by one ulp."""
     w = wl.config(idx)
@@ -249,7 +266,8 @@ def test_rope_table_matches_correctly_rounded_cos_sin(idx):
     assert ta.device_status(attn.workspace) == ta.TA_OK
     half = w.head_dim // 2
     nbytes = w.total_kv * half * 8
-    off = attn.workspace.numel() - ((nbytes + 255) // 256) * 256
+    krot = w.total_kv * w.h_kv * w.head_dim * 2     # rotated keys follow the table
+    off = attn.workspace.numel() - ((krot + 255) // 256) * 256 - ((nbytes + 255) // 256) * 256
     tab = attn.workspace[off:off + nbytes].cpu().numpy().view(np.float32).reshape(-1, half, 2)
     c, s = oracle.rope_cos_sin(w.rope_position, w.head_dim, w.rope_theta, w.rope_scale)
     bad = int(np.sum(tab[..., 0] != c) + np.sum(tab[..., 1] != s))

@@ -28,11 +28,11 @@ def _library():
 def test_noalloc_rejects_problems_larger_than_its_scratch():
     """Checked on the host before anything is enqueued (no GPU needed)."""
     big = ta.Dims(batch_size=1, total_q=64, total_kv=200_000, total_tree=64, h_q=8, h_kv=8,
-                  head_dim=128, dtype=ta.TA_BF16)
+                  head_dim=128, dtype=ta.TA_BF16, rotary_mode=1)
     assert ta.workspace_size(big) > 32 << 20
     fake = ctypes.c_void_p(0x10000)
     st = ta.lib().tree_attn_noalloc(fake, fake, fake, fake, fake, fake, fake, fake, fake, fake,
-                                    0, 1.0, 1e4, 0.1, ctypes.byref(big), None)
+                                    1, 1.0, 1e4, 0.1, ctypes.byref(big), None)
     assert st == ta.TA_ERR_UNSUPPORTED
 
 

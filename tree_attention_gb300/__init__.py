@@ -50,7 +50,8 @@ class Dims(ctypes.Structure):
     _fields_ = [("batch_size", ctypes.c_int32), ("total_q", ctypes.c_int32),
                 ("total_kv", ctypes.c_int32), ("total_tree", ctypes.c_int32),
                 ("h_q", ctypes.c_int32), ("h_kv", ctypes.c_int32),
-                ("head_dim", ctypes.c_int32), ("dtype", ctypes.c_int)]
+                ("head_dim", ctypes.c_int32), ("dtype", ctypes.c_int),
+                ("rotary_mode", ctypes.c_int32)]
 
 
 _lib = None
@@ -121,10 +122,10 @@ def _stream_ptr(stream) -> ctypes.c_void_p:
 
 
 def make_dims(q: torch.Tensor, k: torch.Tensor, q_indptr: torch.Tensor,
-              tree_order: torch.Tensor) -> Dims:
+              tree_order: torch.Tensor, rotary_mode: int = 0) -> Dims:
     return Dims(batch_size=q_indptr.numel() - 1, total_q=q.shape[0], total_kv=k.shape[0],
                 total_tree=tree_order.shape[0], h_q=q.shape[1], h_kv=k.shape[1],
-                head_dim=q.shape[2], dtype=_dtype_code(q.dtype))
+                head_dim=q.shape[2], dtype=_dtype_code(q.dtype), rotary_mode=int(rotary_mode))
 
 
 def workspace_size(dims: Dims) -> int:
@@ -155,7 +156,7 @@ def tree_attn(q, q_indptr, k, v, kv_indptr, q_rope_position, mn_indptr, tree_ord
         _check_dev(name, t, torch.int32)
     _check_dev("lse", lse, torch.float32)
     _check_dev("workspace", workspace)
-    dims = make_dims(q, k, q_indptr, tree_order)
+    dims = make_dims(q, k, q_indptr, tree_order, rotary_mode)
     st = lib().tree_attn(_ptr(q), _ptr(q_indptr), _ptr(k), _ptr(v), _ptr(kv_indptr),
                          _ptr(q_rope_position), _ptr(mn_indptr), _ptr(tree_order), _ptr(out),
                          _ptr(lse), int(rotary_mode), float(rope_scale), float(rope_theta),
@@ -171,7 +172,7 @@ def tree_attn_noalloc(q, q_indptr, k, v, kv_indptr, q_rope_position, mn_indptr, 
     """``tree_attn`` for callers that may not allocate device memory: the
     library's static 32 MiB device scratch array serves as the workspace.
     Calls share that array, so they must not overlap on the GPU."""
-    dims = make_dims(q, k, q_indptr, tree_order)
+    dims = make_dims(q, k, q_indptr, tree_order, rotary_mode)
     st = lib().tree_attn_noalloc(_ptr(q), _ptr(q_indptr), _ptr(k), _ptr(v), _ptr(kv_indptr),
                                  _ptr(q_rope_position), _ptr(mn_indptr), _ptr(tree_order),
                                  _ptr(out), _ptr(lse), int(rotary_mode), float(rope_scale),
@@ -186,7 +187,7 @@ def plan(q, q_indptr, k, kv_indptr, q_rope_position, mn_indptr, tree_order,
          stream=None) -> None:
     """Enqueue the plan kernel (work items, tile classes, RoPE table); q and
     k are passed only for their shapes and dtype."""
-    dims = make_dims(q, k, q_indptr, tree_order)
+    dims = make_dims(q, k, q_indptr, tree_order, rotary_mode)
     st = lib().tree_attn_plan(_ptr(q_indptr), _ptr(kv_indptr), _ptr(q_rope_position),
                               _ptr(mn_indptr), _ptr(tree_order), int(rotary_mode),
                               float(rope_scale), float(rope_theta), ctypes.byref(dims),
@@ -199,7 +200,7 @@ def plan(q, q_indptr, k, kv_indptr, q_rope_position, mn_indptr, tree_order,
 def run(q, k, v, q_indptr, kv_indptr, mn_indptr, tree_order, out, lse, rotary_mode: int,
         sm_scale: float, workspace: torch.Tensor, stream=None) -> None:
     """Enqueue the attention kernel on the plan held in ``workspace``."""
-    dims = make_dims(q, k, q_indptr, tree_order)
+    dims = make_dims(q, k, q_indptr, tree_order, rotary_mode)
     st = lib().tree_attn_run(_ptr(q), _ptr(k), _ptr(v), _ptr(q_indptr), _ptr(kv_indptr),
                              _ptr(mn_indptr), _ptr(tree_order), _ptr(out), _ptr(lse),
                              int(rotary_mode), float(sm_scale), ctypes.byref(dims),
@@ -245,7 +246,7 @@ class TreeAttention:
 
     def __init__(self, q, k, q_indptr, tree_order, rotary_mode: int, rope_scale: float,
                  rope_theta: float, sm_scale: float):
-        self.dims = make_dims(q, k, q_indptr, tree_order)
+        self.dims = make_dims(q, k, q_indptr, tree_order, rotary_mode)
         n = workspace_size(self.dims)
         if n == 0:
             raise TreeAttnError(TA_ERR_UNSUPPORTED, "tree_attn_workspace_size")

@@ -49,6 +49,7 @@ bool dims_valid(const ta_dims* d) {
   if (d->h_q < 1 || d->h_kv < 1 || d->h_q % d->h_kv != 0) return false;
   if (d->dtype != TA_FP16 && d->dtype != TA_BF16) return false;
   if (d->head_dim < 1) return false;
+  if (d->rotary_mode != 0 && d->rotary_mode != 1) return false;
   return true;
 }
 
@@ -59,8 +60,8 @@ ta_status dims_supported(const ta_dims* d) {
 }
 
 WsLayout layout_of(const ta_dims* d) {
-  return ta::make_ws_layout(d->batch_size, d->total_q, d->total_kv, d->h_q / d->h_kv,
-                            d->head_dim);
+  return ta::make_ws_layout(d->batch_size, d->total_q, d->total_kv, d->h_q / d->h_kv, d->h_kv,
+                            d->head_dim, d->rotary_mode != 0);
 }
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
@@ -108,6 +109,7 @@ ta_status check_common(const int32_t* q_indptr, const int32_t* kv_indptr,
   if (!q_indptr || !kv_indptr || !mn_indptr || !workspace) return TA_ERR_INVALID_ARGUMENT;
   if (dims->total_tree > 0 && !tree_order) return TA_ERR_INVALID_ARGUMENT;
   if (rotary_mode != 0 && rotary_mode != 1) return TA_ERR_INVALID_ARGUMENT;
+  if (rotary_mode != dims->rotary_mode) return TA_ERR_INVALID_ARGUMENT;
   if (!aligned(workspace, 256)) return TA_ERR_INVALID_ARGUMENT;
   const size_t need = tree_attn_workspace_size(dims);
   if (need == 0) return TA_ERR_UNSUPPORTED;
@@ -138,16 +140,16 @@ ta_status check_run_args(const void* q, const void* k, const void* v, const void
 
 struct WsPtrs {
   WsHeader* hdr;
-  ta::PairInfo* pairs;
-  int32_t* sorted;
+  ta::ItemRec* recs;
+  ta::ItemRec* sorted;
   uint8_t* classes;
   float2* rope_cs;
 };
 
 WsPtrs ws_ptrs(void* workspace, const WsLayout& L) {
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  return WsPtrs{reinterpret_cast<WsHeader*>(ws), reinterpret_cast<ta::PairInfo*>(ws + L.off_pairs),
-                reinterpret_cast<int32_t*>(ws + L.off_sorted), ws + L.off_classes,
+  return WsPtrs{reinterpret_cast<WsHeader*>(ws), reinterpret_cast<ta::ItemRec*>(ws + L.off_pairs),
+                reinterpret_cast<ta::ItemRec*>(ws + L.off_sorted), ws + L.off_classes,
                 reinterpret_cast<float2*>(ws + L.off_rope)};
 }
 
@@ -180,7 +182,7 @@ ta_status launch_plan_checked(const int32_t* q_indptr, const int32_t* kv_indptr,
   pp.rope_scale = rope_scale;
   pp.rope_theta = rope_theta;
   pp.hdr = w.hdr;
-  pp.pairs = w.pairs;
+  pp.recs = w.recs;
   pp.sorted = w.sorted;
   pp.classes = w.classes;
   pp.rope_cs = w.rope_cs;
@@ -201,22 +203,28 @@ ta_status launch_run_checked(const void* q, const void* k, const void* v, const 
   const WsPtrs w = ws_ptrs(workspace, L);
   const int nsm = sm_count();
   if (nsm <= 0) return TA_ERR_CUDA;
+  // with RoPE the keys are rotated once per call (every q tile of a sequence
+  // reads them) and the attention kernel loads the rotated copy
+  const void* k_attn = k;
+  if (rotary_mode == 1) {
+    void* krot = static_cast<uint8_t*>(workspace) + L.off_krot;
+    if (ta::launch_krot(k, krot, w.rope_cs, dims->total_kv, dims->h_kv, D,
+                        dims->dtype == TA_BF16, 4 * nsm, st) != cudaSuccess)
+      return TA_ERR_CUDA;
+    k_attn = krot;
+  }
   CUtensorMap tm_q, tm_k, tm_v;
   if (!make_map(&tm_q, q, dims->dtype, dims->total_q, dims->h_q, D, g, R) ||
-      !make_map(&tm_k, k, dims->dtype, dims->total_kv, dims->h_kv, D, 1, ta::kKvBoxRows) ||
+      !make_map(&tm_k, k_attn, dims->dtype, dims->total_kv, dims->h_kv, D, 1, ta::kKvBoxRows) ||
       !make_map(&tm_v, v, dims->dtype, dims->total_kv, dims->h_kv, D, 1, ta::kKvBoxRows))
     return TA_ERR_CUDA;
   ta::AttnParams ap{};
   ap.tree_order = tree_order;
   ap.out = out;
   ap.lse = lse;
-  ap.pairs = w.pairs;
   ap.sorted = w.sorted;
   ap.classes = w.classes;
   ap.rope_cs = w.rope_cs;
-  ap.q_indptr = q_indptr;
-  ap.kv_indptr = kv_indptr;
-  ap.mn_indptr = mn_indptr;
   ap.hdr = w.hdr;
   ap.h_q = dims->h_q;
   ap.h_kv = dims->h_kv;

@@ -4,17 +4,21 @@
 // (per q row and head: masked online softmax of sm_scale * q.k in log2
 // units, output O / d and lse = m + log2(d)), re-designed for one GB300 SM:
 //
-//   warp 0      work queue + TMA producer: pops (sequence, q tile, kv head)
-//               items in longest-first order, loads the packed Q tile once
-//               and the non-empty K/V tiles of the item into a 2-stage ring
+//   warp 0      work queue + producer: pops (sequence, q tile, kv head) items
+//               in longest-first order, stages the item's per-row DFS enter
+//               indices, TMA-loads the packed Q tile into one of two Q
+//               buffers and the item's non-empty K/V tiles (64 kv rows each)
+//               into a 3-stage ring, with each partial tile's column
+//               intervals beside it; it runs up to a whole item ahead
 //   warp 1      TMEM owner and tcgen05 issuer: S = Q K^T into one of two TMEM
 //               score buffers, then O += P V into the TMEM accumulator
 //   warps 2-5   softmax / correction / epilogue, one TMEM lane (= packed row)
 //               per thread: tree mask, online softmax with a lazily moved
-//               reference max, P (fp16/bf16) to shared memory, O rescale,
-//               final O / l and lse stores
-//   warps 6-9   inline RoPE: rotate the staged Q and K tiles in shared memory
-//               (rotate-half, float32 products, rounded to the storage dtype)
+//               reference max, P (fp16/bf16) into one of two shared buffers,
+//               O rescale, final O / l and lse stores
+//   warps 6-9   inline RoPE on the staged Q tile (keys arrive rotated: the
+//               run rotates them once per call), rotate-half with float32
+//               products, rounded to the storage dtype
 //
 // Every cross-warp hand-off is an mbarrier with a bounded wait.
 #include <cuda_runtime.h>
@@ -29,59 +33,63 @@ namespace ta {
 namespace {
 
 constexpr int kThreads = 320;
-constexpr int kStages = 2;
+constexpr int kStages = 3;    // K/V ring depth
+constexpr int kQStages = 2;   // Q buffers
+constexpr int kSlots = 4;     // work-item slots
 
 enum Bar : int {
-  B_ITEM_FULL = 0,    // [2]
-  B_ITEM_EMPTY = 2,   // [2]
-  B_Q_FULL = 4,
-  B_Q_READY = 5,
-  B_Q_EMPTY = 6,
-  B_K_FULL = 7,       // [2]
-  B_V_FULL = 9,       // [2]
-  B_K_READY = 11,     // [2]
-  B_KV_EMPTY = 13,    // [2]
-  B_S_FULL = 15,      // [2]
-  B_S_FREE = 17,      // [2]
-  B_P_FULL = 19,
-  B_P_FREE = 20,
-  B_O_FREE = 21,
-  B_DRAIN = 22,
-  B_COUNT = 23
+  B_ITEM_FULL = 0,                       // [kSlots]
+  B_ITEM_EMPTY = B_ITEM_FULL + kSlots,   // [kSlots]
+  B_Q_FULL = B_ITEM_EMPTY + kSlots,      // [kQStages]
+  B_Q_READY = B_Q_FULL + kQStages,       // [kQStages]
+  B_Q_EMPTY = B_Q_READY + kQStages,      // [kQStages]
+  B_K_FULL = B_Q_EMPTY + kQStages,       // [kStages]
+  B_V_FULL = B_K_FULL + kStages,         // [kStages]
+  B_EX_FULL = B_V_FULL + kStages,        // [kStages]
+  B_KV_EMPTY = B_EX_FULL + kStages,      // [kStages]
+  B_S_FULL = B_KV_EMPTY + kStages,       // [2]
+  B_S_FREE = B_S_FULL + 2,               // [2]
+  B_P_FREE = B_S_FREE + 2,               // [2]
+  B_P_FULL = B_P_FREE + 2,               // [2] one per P buffer: a warp may run a tile ahead
+  B_O_FREE = B_P_FULL + 2,
+  B_DRAIN,
+  B_COUNT
 };
 
 struct Item {
-  int valid, b, t, kvh, n_tiles, class_off, q_row0, qo, kv, tl, ts, kv_base, tree_base, nq;
-  int pad[2];
+  ItemRec r;
+  int valid, kvh, pad[14];
+  int e_row[kBlockM];  // DFS enter index of every packed row's node (INT_MIN: none)
 };
+static_assert(sizeof(Item) == 128 + 4 * kBlockM, "item slot size");
 
 struct Misc {
   uint32_t tmem_base;
   int abort;
-  int pad[14];
-  Item items[2];
+  int pad[30];
+  Item items[kSlots];
 };
 
 template <int D>
 struct Cfg {
-  static constexpr int kAtoms = D / 64;           // 128-byte column blocks per row
-  static constexpr int kAtomBytes = 128 * 128;    // 128 rows x 128 bytes
-  static constexpr int kTileBytes = kAtoms * kAtomBytes;
+  static constexpr int kAtoms = D / 64;               // 128-byte column blocks per row
+  static constexpr int kQAtomBytes = kBlockM * 128;    // 128 rows x 128 bytes
+  static constexpr int kKVAtomBytes = kBlockN * 128;   // 64 rows x 128 bytes
+  static constexpr int kQBytes = kAtoms * kQAtomBytes;
+  static constexpr int kKVBytes = kAtoms * kKVAtomBytes;
+  static constexpr int kPBytes = kBlockM * 128;        // 128 x 64 elements = one atom
   static constexpr int kOffQ = 0;
-  static constexpr int kOffK = kOffQ + kTileBytes;
-  static constexpr int kOffV = kOffK + kStages * kTileBytes;
-  static constexpr int kOffP = kOffV + kStages * kTileBytes;
-  static constexpr int kOffEX = kOffP + 2 * kAtomBytes;   // P is 128 x 128 elements
-  static constexpr int kOffBar = kOffEX + 4 * kBlockN * 8;
-  static constexpr int kOffMisc = kOffBar + 32 * 8;
+  static constexpr int kOffK = kOffQ + kQStages * kQBytes;
+  static constexpr int kOffV = kOffK + kStages * kKVBytes;
+  static constexpr int kOffP = kOffV + kStages * kKVBytes;
+  static constexpr int kOffEX = kOffP + 2 * kPBytes;          // [kStages][kBlockN] int2
+  static constexpr int kOffBar = kOffEX + kStages * kBlockN * 8;
+  static constexpr int kOffMisc = kOffBar + 64 * 8;
   static constexpr int kSmemUsed = kOffMisc + (int)sizeof(Misc);
-  // request more than half of an SM's shared memory so that exactly one CTA
-  // (and one 512-column TMEM allocation) lives on each SM
-  static constexpr int kSmemAlloc =
-      (kSmemUsed + 1024) > 120 * 1024 ? (kSmemUsed + 1024) : 120 * 1024;
-  static constexpr uint32_t kTmemCols = 512;
+  static constexpr int kSmemAlloc = kSmemUsed + 1024;   // room to align the base to 1024
+  static constexpr uint32_t kTmemCols = 256;
   static constexpr uint32_t kTmemO = 0;
-  static constexpr uint32_t kTmemS = 128;  // S buffer sb at column 128 + 128 * sb
+  static constexpr uint32_t kTmemS = 128;  // score buffer sb at column 128 + 64 * sb
 };
 
 struct Ctx {
@@ -105,116 +113,148 @@ struct Ctx {
   }
 };
 
-// Iterates the non-empty kv tiles of a work item from the plan's class bytes.
+// Iterates the non-empty kv tiles of a work item: from the record's inline
+// 2-bit classes for short sequences, else from the plan's class bytes.
 struct TileIter {
   const uint8_t* cls;
   int kvt, j;
+  bool inl;
   uint32_t w[4];
-  __device__ TileIter(const uint8_t* c, int n) : cls(c), kvt(n), j(-1) {}
+  __device__ TileIter(const ItemRec& r, const uint8_t* classes)
+      : cls(classes + r.class_off), kvt(r.kvt), j(-1), inl(r.kvt <= kInlineTiles) {
+    if (inl) {
+      w[0] = r.cls2[0];
+      w[1] = r.cls2[1];
+      w[2] = r.cls2[2];
+      w[3] = 0;
+    }
+  }
   // advances to the next non-empty tile; returns its class (0 when done)
   __device__ int next() {
     while (true) {
       ++j;
       if (j >= kvt) return 0;
-      if ((j & 15) == 0) {
-        const uint4 v = __ldg(reinterpret_cast<const uint4*>(cls + j));
-        w[0] = v.x;
-        w[1] = v.y;
-        w[2] = v.z;
-        w[3] = v.w;
+      int c;
+      if (inl) {
+        c = (w[j >> 4] >> (2 * (j & 15))) & 3;
+      } else {
+        if ((j & 15) == 0) {
+          const uint4 v = __ldg(reinterpret_cast<const uint4*>(cls + j));
+          w[0] = v.x;
+          w[1] = v.y;
+          w[2] = v.z;
+          w[3] = v.w;
+        }
+        c = (w[(j & 15) >> 2] >> (8 * (j & 3))) & 0xff;
       }
-      const int c = (w[(j & 15) >> 2] >> (8 * (j & 3))) & 0xff;
       if (c != kTileEmpty) return c;
     }
   }
 };
 
-__device__ __forceinline__ int kv_tiles(int kv) { return (kv + kBlockN - 1) / kBlockN; }
-
 // ---------------------------------------------------------------------------
-// warp 0: work queue + TMA producer (one thread)
+// warp 0: work queue + producer (lane 0 issues; all lanes stage intervals)
 // ---------------------------------------------------------------------------
 template <int D>
 __device__ void run_producer(const Ctx& cx, const CUtensorMap* tm_q, const CUtensorMap* tm_k,
-                             const CUtensorMap* tm_v, const AttnParams& p) {
+                             const CUtensorMap* tm_v, const AttnParams& p, int lane) {
   using C = Cfg<D>;
   uint8_t* sQ = cx.smem + C::kOffQ;
   uint8_t* sK = cx.smem + C::kOffK;
   uint8_t* sV = cx.smem + C::kOffV;
+  int2* sEX = reinterpret_cast<int2*>(cx.smem + C::kOffEX);
   // the plan kernel wrote the item count; never trust it beyond the table size
   const unsigned long long cap = (unsigned long long)p.max_pairs * (unsigned long long)p.h_kv;
-  unsigned long long n_items = *(volatile unsigned int*)&p.hdr->num_items;
+  const unsigned long long n_items = *(volatile unsigned int*)&p.hdr->num_items;
   const unsigned int num_items = (unsigned int)(n_items < cap ? n_items : cap);
+  const int g = p.g, R = p.R;
   uint32_t it = 0, kv_it = 0, q_it = 0;
-  uint32_t issued[kStages] = {0, 0};
+  uint32_t issued[kStages] = {0, 0, 0};
   bool aborted = false;
+  unsigned int idx = 0;
+  if (lane == 0) idx = atomicAdd(&p.hdr->queue_head, 1u);
+  idx = __shfl_sync(0xffffffffu, idx, 0);
   for (;;) {
-    const int slot = it & 1;
-    if (!cx.wait(B_ITEM_EMPTY + slot, ((it >> 1) & 1) ^ 1)) { aborted = true; break; }
+    const int slot = it % kSlots;
+    if (!cx.warp_wait(B_ITEM_EMPTY + slot, ((it / kSlots) & 1) ^ 1)) { aborted = true; break; }
     Item& s = cx.misc->items[slot];
-    const unsigned int idx = atomicAdd(&p.hdr->queue_head, 1u);
     if (idx >= num_items) {
-      s.valid = 0;
-      mbar_arrive(&cx.bar[B_ITEM_FULL + slot]);
+      if (lane == 0) {
+        s.valid = 0;
+        mbar_arrive(&cx.bar[B_ITEM_FULL + slot]);
+      }
       break;
     }
-    const int pair = __ldg(&p.sorted[idx / p.h_kv]);
+    if (lane < 4)
+      reinterpret_cast<int4*>(&s.r)[lane] =
+          __ldg(reinterpret_cast<const int4*>(p.sorted + idx / p.h_kv) + lane);
     const int kvh = idx % p.h_kv;
-    if (pair < 0 || pair >= p.max_pairs) {   // a workspace that was never zero-filled
-      atomicOr(&p.hdr->error, DEVERR_BAD_INDPTR);
-      s.valid = 0;
-      mbar_arrive(&cx.bar[B_ITEM_FULL + slot]);
-      break;
-    }
-    const PairInfo pi = reinterpret_cast<const PairInfo*>(p.pairs)[pair];
-    const int b = pi.b;
-    const int q0 = __ldg(&p.q_indptr[b]), q1 = __ldg(&p.q_indptr[b + 1]);
-    const int k0 = __ldg(&p.kv_indptr[b]), k1 = __ldg(&p.kv_indptr[b + 1]);
-    const int m0 = __ldg(&p.mn_indptr[b]), m1 = __ldg(&p.mn_indptr[b + 1]);
-    s.valid = 1;
-    s.b = b;
-    s.t = pi.t;
-    s.kvh = kvh;
-    s.n_tiles = pi.n_tiles;
-    s.class_off = pi.class_off;
-    s.q_row0 = q0 + pi.t * p.R;
-    s.qo = q1 - q0;
-    s.kv = k1 - k0;
-    s.tl = m1 - m0;
-    s.ts = s.kv - s.tl;
-    s.kv_base = k0;
-    s.tree_base = m0;
-    s.nq = min(p.R, s.qo - pi.t * p.R);
-    mbar_arrive(&cx.bar[B_ITEM_FULL + slot]);
-    if (pi.n_tiles > 0) {
-      if (!cx.wait(B_Q_EMPTY, (q_it & 1) ^ 1)) { aborted = true; break; }
-      mbar_arrive_expect_tx(&cx.bar[B_Q_FULL], (uint32_t)(C::kAtoms * 128 * p.g * p.R));
+    // pop the next index now; its round trip overlaps this item's issue
+    unsigned int nidx = 0;
+    if (lane == 0) nidx = atomicAdd(&p.hdr->queue_head, 1u);
+    __syncwarp();
+    const ItemRec r = s.r;
+    if (r.n_tiles > 0) {
+      // the Q tile first: its load overlaps the staging below
+      const int qs = q_it % kQStages;
+      if (!cx.warp_wait(B_Q_EMPTY + qs, ((q_it / kQStages) & 1) ^ 1)) { aborted = true; break; }
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&cx.bar[B_Q_FULL + qs], (uint32_t)(C::kAtoms * 128 * g * R));
 #pragma unroll
-      for (int a = 0; a < C::kAtoms; ++a)
-        tma_load_3d(sQ + a * C::kAtomBytes, tm_q, &cx.bar[B_Q_FULL], a * 64, kvh * p.g,
-                    s.q_row0);
+        for (int a = 0; a < C::kAtoms; ++a)
+          tma_load_3d(sQ + qs * C::kQBytes + a * C::kQAtomBytes, tm_q, &cx.bar[B_Q_FULL + qs],
+                      a * 64, kvh * g, r.q_row0);
+      }
       ++q_it;
-      TileIter ti(p.classes + pi.class_off, kv_tiles(s.kv));
-      const int kv = s.kv;
-      for (int n = 0; n < pi.n_tiles; ++n) {
-        ti.next();
+    }
+    // DFS enter index of each packed row's tree node
+#pragma unroll
+    for (int k4 = 0; k4 < kBlockM / 32; ++k4) {
+      const int row = k4 * 32 + lane;
+      const int qr = row / g;
+      int e = INT_MIN;
+      if (row < g * R && qr < r.nq)
+        e = __ldg(&p.tree_order[2 * (r.tree_base + r.t * R + qr + r.tl - r.qo)]);
+      s.e_row[row] = e;
+    }
+    if (lane == 0) {
+      s.valid = 1;
+      s.kvh = kvh;
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&cx.bar[B_ITEM_FULL + slot]);
+    idx = __shfl_sync(0xffffffffu, nidx, 0);
+    if (r.n_tiles > 0) {
+      TileIter ti(r, p.classes);
+      for (int n = 0; n < r.n_tiles; ++n) {
+        const int cls = ti.next();
         const int j = ti.j;
-        const int stage = kv_it & 1;
-        if (!cx.wait(B_KV_EMPTY + stage, ((kv_it >> 1) & 1) ^ 1)) { aborted = true; break; }
-        const int nvalid = min(kBlockN, kv - j * kBlockN);
-        const int nbox = nvalid > kKvBoxRows ? 2 : 1;
-        const uint32_t bytes = (uint32_t)(C::kAtoms * nbox * kKvBoxRows * 128);
-        const int row0 = k0 + j * kBlockN;
-        mbar_arrive_expect_tx(&cx.bar[B_K_FULL + stage], bytes);
-        for (int a = 0; a < C::kAtoms; ++a)
-          for (int bx = 0; bx < nbox; ++bx)
-            tma_load_3d(sK + stage * C::kTileBytes + a * C::kAtomBytes + bx * kKvBoxRows * 128,
-                        tm_k, &cx.bar[B_K_FULL + stage], a * 64, kvh, row0 + bx * kKvBoxRows);
-        mbar_arrive_expect_tx(&cx.bar[B_V_FULL + stage], bytes);
-        for (int a = 0; a < C::kAtoms; ++a)
-          for (int bx = 0; bx < nbox; ++bx)
-            tma_load_3d(sV + stage * C::kTileBytes + a * C::kAtomBytes + bx * kKvBoxRows * 128,
-                        tm_v, &cx.bar[B_V_FULL + stage], a * 64, kvh, row0 + bx * kKvBoxRows);
+        const int row0 = r.kv_base + j * kBlockN;
+        const int stage = kv_it % kStages;
+        if (!cx.warp_wait(B_KV_EMPTY + stage, ((kv_it / kStages) & 1) ^ 1)) { aborted = true; break; }
+        if (lane == 0) {
+          const uint32_t bytes = (uint32_t)C::kKVBytes;
+          mbar_arrive_expect_tx(&cx.bar[B_K_FULL + stage], bytes);
+#pragma unroll
+          for (int a = 0; a < C::kAtoms; ++a)
+            tma_load_3d(sK + stage * C::kKVBytes + a * C::kKVAtomBytes, tm_k,
+                        &cx.bar[B_K_FULL + stage], a * 64, kvh, row0);
+          mbar_arrive_expect_tx(&cx.bar[B_V_FULL + stage], bytes);
+#pragma unroll
+          for (int a = 0; a < C::kAtoms; ++a)
+            tma_load_3d(sV + stage * C::kKVBytes + a * C::kKVAtomBytes, tm_v,
+                        &cx.bar[B_V_FULL + stage], a * 64, kvh, row0);
+        }
+        // column intervals of a partial tile for the mask (FULL tiles need none)
+        if (cls == kTilePartial) {
+          int2* ex = sEX + stage * kBlockN;
+#pragma unroll
+          for (int q = 0; q < kBlockN / 32; ++q)
+            ex[q * 32 + lane] =
+                column_interval(p.tree_order, r.tree_base, j * kBlockN + q * 32 + lane, r.kv, r.ts);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&cx.bar[B_EX_FULL + stage]);
         ++issued[stage];
         ++kv_it;
       }
@@ -222,9 +262,12 @@ __device__ void run_producer(const Ctx& cx, const CUtensorMap* tm_q, const CUten
     }
     ++it;
   }
-  if (aborted) {
+  if (aborted && lane == 0) {
     // let every copy already in flight land before the CTA's memory goes away
-    if (q_it > 0) cx.drain_wait(B_Q_FULL, (q_it - 1) & 1);
+    for (int qs = 0; qs < kQStages; ++qs) {
+      const uint32_t n = q_it / kQStages + (qs < (int)(q_it % kQStages) ? 1 : 0);
+      if (n > 0) cx.drain_wait(B_Q_FULL + qs, (n - 1) & 1);
+    }
     for (int st = 0; st < kStages; ++st) {
       if (issued[st] > 0) {
         cx.drain_wait(B_K_FULL + st, (issued[st] - 1) & 1);
@@ -246,77 +289,79 @@ __device__ void run_mma(const Ctx& cx, uint32_t tmem, const AttnParams& p) {
   const uint32_t sP = smem_u32(cx.smem + C::kOffP);
   constexpr uint32_t idesc_pv = umma_idesc_f16(BF16, 128, D, /*b_mn_major=*/true);
   const int q_bar = p.rotary ? B_Q_READY : B_Q_FULL;
-  const int k_bar = p.rotary ? B_K_READY : B_K_FULL;
-  uint32_t it = 0, kv_it = 0, s_it = 0, q_it = 0, o_it = 0, pf_it = 0;
+  uint32_t it = 0, kv_it = 0, q_it = 0, o_it = 0;
   bool issued_any = false;
   for (;;) {
-    const int slot = it & 1;
-    if (!cx.wait(B_ITEM_FULL + slot, (it >> 1) & 1)) break;
-    const Item s = cx.misc->items[slot];
+    const int slot = it % kSlots;
+    if (!cx.wait(B_ITEM_FULL + slot, (it / kSlots) & 1)) break;
+    const Item& s = cx.misc->items[slot];
     if (!s.valid) break;
-    if (s.n_tiles > 0) {
-      if (!cx.wait(q_bar, q_it & 1)) break;
+    const ItemRec r = s.r;
+    if (r.n_tiles > 0) {
+      const int qs = q_it % kQStages;
+      if (!cx.wait(q_bar + qs, (q_it / kQStages) & 1)) break;
       ++q_it;
       tc_fence_after();
-      TileIter ti(p.classes + s.class_off, kv_tiles(s.kv));
-      int nv_next = 0;
+      const uint32_t qst = sQ + qs * C::kQBytes;
+      TileIter ti(r, p.classes);
       bool ok = true;
-      // S(m) = Q K(m)^T into score buffer s_it & 1
+      // S(m) = Q K(m)^T into score buffer (kv_it + m) & 1
       auto issue_qk = [&](int m, int nvalid) -> bool {
         const uint32_t c = kv_it + m;
-        const int stage = c & 1;
-        if (!cx.wait(k_bar + stage, (c >> 1) & 1)) return false;
-        const int sb = s_it & 1;
-        if (!cx.wait(B_S_FREE + sb, ((s_it >> 1) & 1) ^ 1)) return false;
+        const int stage = c % kStages;
+        if (!cx.wait(B_K_FULL + stage, (c / kStages) & 1)) return false;
+        const int sb = c & 1;
+        if (!cx.wait(B_S_FREE + sb, ((c >> 1) & 1) ^ 1)) return false;
         tc_fence_after();
         const int n_eff = (nvalid + 15) & ~15;
         const uint32_t idesc = umma_idesc_f16(BF16, 128, n_eff, false);
-        const uint32_t kst = sK + stage * C::kTileBytes;
+        const uint32_t kst = sK + stage * C::kKVBytes;
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
-          const uint32_t koff = (k >> 2) * C::kAtomBytes + (k & 3) * 32;
-          umma_f16(tmem + C::kTmemS + 128 * sb, sw128_desc(sQ + koff, 0),
-                   sw128_desc(kst + koff, 0), idesc, k > 0 ? 1u : 0u);
+          umma_f16(tmem + C::kTmemS + 64 * sb,
+                   sw128_desc(qst + (k >> 2) * C::kQAtomBytes + (k & 3) * 32, 0),
+                   sw128_desc(kst + (k >> 2) * C::kKVAtomBytes + (k & 3) * 32, 0), idesc,
+                   k > 0 ? 1u : 0u);
         }
         umma_commit(&cx.bar[B_S_FULL + sb]);
         issued_any = true;
-        ++s_it;
-        if (m == s.n_tiles - 1) umma_commit(&cx.bar[B_Q_EMPTY]);
+        if (m == r.n_tiles - 1) umma_commit(&cx.bar[B_Q_EMPTY + qs]);
         return true;
       };
       ti.next();
-      int nv_cur = min(kBlockN, s.kv - ti.j * kBlockN);
+      int nv_cur = min(kBlockN, r.kv - ti.j * kBlockN);
+      int nv_next = 0;
       if (!issue_qk(0, nv_cur)) break;
-      for (int n = 0; n < s.n_tiles; ++n) {
-        if (n + 1 < s.n_tiles) {
+      for (int n = 0; n < r.n_tiles; ++n) {
+        if (n + 1 < r.n_tiles) {
           ti.next();
-          nv_next = min(kBlockN, s.kv - ti.j * kBlockN);
+          nv_next = min(kBlockN, r.kv - ti.j * kBlockN);
           if (!issue_qk(n + 1, nv_next)) { ok = false; break; }
         }
         const uint32_t c = kv_it + n;
-        const int stage = c & 1;
-        if (!cx.wait(B_P_FULL, pf_it & 1)) { ok = false; break; }
-        ++pf_it;
-        if (!cx.wait(B_V_FULL + stage, (c >> 1) & 1)) { ok = false; break; }
+        const int stage = c % kStages;
+        const int pb = c & 1;
+        if (!cx.wait(B_P_FULL + pb, (c >> 1) & 1)) { ok = false; break; }
+        if (!cx.wait(B_V_FULL + stage, (c / kStages) & 1)) { ok = false; break; }
         if (n == 0) {
           if (!cx.wait(B_O_FREE, (o_it & 1) ^ 1)) { ok = false; break; }
           ++o_it;
         }
         tc_fence_after();
         const int n_eff = (nv_cur + 15) & ~15;
-        const uint32_t vst = sV + stage * C::kTileBytes;
+        const uint32_t vst = sV + stage * C::kKVBytes;
+        const uint32_t pst = sP + pb * C::kPBytes;
         for (int k = 0; k < n_eff / 16; ++k) {
-          const uint32_t aoff = (k >> 2) * C::kAtomBytes + (k & 3) * 32;
-          umma_f16(tmem + C::kTmemO, sw128_desc(sP + aoff, 0),
-                   sw128_desc(vst + k * 16 * 128, C::kAtomBytes), idesc_pv,
+          umma_f16(tmem + C::kTmemO, sw128_desc(pst + k * 32, 0),
+                   sw128_desc(vst + k * 16 * 128, C::kKVAtomBytes), idesc_pv,
                    (n > 0 || k > 0) ? 1u : 0u);
         }
-        umma_commit(&cx.bar[B_P_FREE]);
+        umma_commit(&cx.bar[B_P_FREE + pb]);
         umma_commit(&cx.bar[B_KV_EMPTY + stage]);
         nv_cur = nv_next;
       }
       if (!ok) break;
-      kv_it += s.n_tiles;
+      kv_it += r.n_tiles;
     }
     mbar_arrive(&cx.bar[B_ITEM_EMPTY + slot]);
     ++it;
@@ -337,276 +382,296 @@ __device__ void run_softmax(const Ctx& cx, uint32_t tmem, const AttnParams& p, i
   const int wq = warp & 3;                     // TMEM lane quadrant of this warp
   const int row = wq * 32 + lane;              // packed row = TMEM lane
   const uint32_t t_row = tmem + ((uint32_t)(wq * 32) << 16);
-  int2* ex = reinterpret_cast<int2*>(cx.smem + C::kOffEX) + (warp - 2) * kBlockN;
-  uint8_t* sP = cx.smem + C::kOffP;
+  const int2* sEX = reinterpret_cast<const int2*>(cx.smem + C::kOffEX);
+  uint8_t* sP = cx.smem + C::kOffP + row * 128;
   const float c2 = p.scale_log2;
   const int g = p.g, R = p.R;
   const bool in_pack = row < g * R;
   const int qr = in_pack ? row / g : 0;
   const int hh = in_pack ? row - qr * g : 0;
-  uint32_t it = 0, s_it = 0, pf_it = 0;
+  uint32_t it = 0, gi = 0;  // gi: kv tiles processed by this CTA (S, P and stage index)
   for (;;) {
-    const int slot = it & 1;
-    if (!cx.warp_wait(B_ITEM_FULL + slot, (it >> 1) & 1)) return;
-    const Item s = cx.misc->items[slot];
+    const int slot = it % kSlots;
+    if (!cx.warp_wait(B_ITEM_FULL + slot, (it / kSlots) & 1)) return;
+    const Item& s = cx.misc->items[slot];
     if (!s.valid) return;
-    const bool valid = in_pack && qr < s.nq;
-    const int head = s.kvh * g + hh;
-    const size_t orow = (size_t)(s.q_row0 + qr) * p.h_q + head;
-    int e_row = INT_MIN;
-    if (valid) e_row = __ldg(&p.tree_order[2 * (s.tree_base + s.t * R + qr + s.tl - s.qo)]);
+    const ItemRec r = s.r;
+    const int kvh = s.kvh;
+    const int e_row = s.e_row[row];
+    const bool valid = in_pack && qr < r.nq;
+    const int head = kvh * g + hh;
+    const size_t orow = (size_t)(r.q_row0 + qr) * p.h_q + head;
     float m_ref = -INFINITY, l = 0.f;
-    if (s.n_tiles > 0) {
-      TileIter ti(p.classes + s.class_off, kv_tiles(s.kv));
-      for (int n = 0; n < s.n_tiles; ++n) {
+    if (r.n_tiles > 0) {
+      TileIter ti(r, p.classes);
+      for (int n = 0; n < r.n_tiles; ++n, ++gi) {
         const int cls = ti.next();
-        const int j = ti.j;
-        const int nvalid = min(kBlockN, s.kv - j * kBlockN);
-        const int nchunk = (nvalid + 31) >> 5;
-        const int sb = s_it & 1;
-        // visibility bits of this row for the tile's columns
-        uint32_t mw[4];
+        const int nvalid = min(kBlockN, r.kv - ti.j * kBlockN);
+        const int stage = gi % kStages;
+        const int sb = gi & 1;
+        // visibility bits of this row for the tile's 64 columns
+        uint32_t mw0, mw1;
         if (cls == kTilePartial) {
-          __syncwarp();
+          if (!cx.warp_wait(B_EX_FULL + stage, (gi / kStages) & 1)) return;
+          const int4* e4 = reinterpret_cast<const int4*>(sEX + stage * kBlockN);
+          mw0 = 0;
+          mw1 = 0;
 #pragma unroll
-          for (int q = 0; q < 4; ++q)
-            ex[q * 32 + lane] =
-                column_interval(p.tree_order, s.tree_base, j * kBlockN + q * 32 + lane, s.kv, s.ts);
-          __syncwarp();
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            uint32_t bits = 0;
-            const int4* e4 = reinterpret_cast<const int4*>(ex + q * 32);
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              const int4 v = e4[i];
-              bits |= (uint32_t)(v.x <= e_row && e_row < v.y) << (2 * i);
-              bits |= (uint32_t)(v.z <= e_row && e_row < v.w) << (2 * i + 1);
-            }
-            mw[q] = bits;
+          for (int i = 0; i < 16; ++i) {
+            const int4 a = e4[i], b = e4[16 + i];
+            mw0 |= (uint32_t)(a.x <= e_row && e_row < a.y) << (2 * i);
+            mw0 |= (uint32_t)(a.z <= e_row && e_row < a.w) << (2 * i + 1);
+            mw1 |= (uint32_t)(b.x <= e_row && e_row < b.y) << (2 * i);
+            mw1 |= (uint32_t)(b.z <= e_row && e_row < b.w) << (2 * i + 1);
           }
         } else {
+          mw0 = mw1 = 0xffffffffu;  // FULL tiles are never ragged
+        }
+        if (!cx.warp_wait(B_S_FULL + sb, (gi >> 1) & 1)) return;
+        tc_fence_after();
+        // the whole 64-column score row in registers: one TMEM round trip
+        float v[64];
+        {
+          float a[32], b[32];
+          const uint32_t t_s = t_row + C::kTmemS + 64 * sb;
+          tmem_ld32(t_s, a);
+          if (nvalid > 32) tmem_ld32(t_s + 32, b);
+          tmem_wait_ld();
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const int rem = nvalid - q * 32;
-            mw[q] = rem >= 32 ? 0xffffffffu : (rem > 0 ? ((1u << rem) - 1u) : 0u);
+          for (int i = 0; i < 32; ++i) {
+            v[i] = a[i];
+            v[32 + i] = nvalid > 32 ? b[i] : 0.f;
           }
         }
-        if (!cx.warp_wait(B_S_FULL + sb, (s_it >> 1) & 1)) return;
-        tc_fence_after();
-        const uint32_t t_s = t_row + C::kTmemS + 128 * sb;
-        // pass 1: masked row max in log2 units
-        float mx = -INFINITY;
-        for (int q = 0; q < nchunk; ++q) {
-          float v[32];
-          tmem_ld32(t_s + q * 32, v);
-          tmem_wait_ld();
-          const uint32_t bits = mw[q];
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&cx.bar[B_S_FREE + sb]);
+        // masked row max in log2 units (eight independent chains)
+        float mx8[8];
 #pragma unroll
-          for (int i = 0; i < 32; ++i)
-            if ((bits >> i) & 1u) mx = fmaxf(mx, v[i] * c2);
+        for (int k = 0; k < 8; ++k) mx8[k] = -INFINITY;
+        if (cls == kTileFull) {
+#pragma unroll
+          for (int i = 0; i < 64; ++i) mx8[i & 7] = fmaxf(mx8[i & 7], v[i] * c2);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 64; ++i) {
+            const uint32_t bit = i < 32 ? (mw0 >> i) & 1u : (mw1 >> (i - 32)) & 1u;
+            if (bit) mx8[i & 7] = fmaxf(mx8[i & 7], v[i] * c2);
+          }
         }
+        const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                               fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
         // move the reference max only when it grew by more than 2^8; the
         // final O / l and lse = m + log2(l) do not depend on the reference
         const float m_new = fmaxf(m_ref, mx);
         float ref = m_ref;
         if (m_new > m_ref + 8.f) ref = m_new;
         const float alpha = (ref == m_ref) ? 1.f : ex2_approx(m_ref - ref);
-        l *= alpha;
         m_ref = ref;
         const float m_use = (ref == -INFINITY) ? 0.f : ref;
-        if (n > 0) {
-          if (!cx.warp_wait(B_P_FREE, pf_it & 1)) return;
-          ++pf_it;
-          tc_fence_after();
-        }
-        // pass 2: P = exp2(s * c2 - m) on visible columns, row sum, P -> smem
-        for (int q = 0; q < nchunk; ++q) {
-          float v[32];
-          tmem_ld32(t_s + q * 32, v);
-          tmem_wait_ld();
-          const uint32_t bits = mw[q];
-          uint32_t pk[16];
+        // P = exp2(s * c2 - m) on visible columns, in registers
+        float l8[8];
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const float p0 = ((bits >> (2 * i)) & 1u) ? ex2_approx(fmaf(v[2 * i], c2, -m_use)) : 0.f;
-            const float p1 =
-                ((bits >> (2 * i + 1)) & 1u) ? ex2_approx(fmaf(v[2 * i + 1], c2, -m_use)) : 0.f;
-            l += p0 + p1;
+        for (int k = 0; k < 8; ++k) l8[k] = 0.f;
+        uint32_t pk[32];
+        if (cls == kTileFull) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const float p0 = ex2_approx(fmaf(v[2 * i], c2, -m_use));
+            const float p1 = ex2_approx(fmaf(v[2 * i + 1], c2, -m_use));
+            l8[i & 7] += p0 + p1;
             pk[i] = pack2<BF16>(p0, p1);
           }
-          // columns q*32 .. q*32+31 = 128-byte atom q/2, 16-byte chunks (q&1)*4 .. +3
-          uint8_t* prow = sP + (q >> 1) * C::kAtomBytes + row * 128;
+        } else {
 #pragma unroll
-          for (int cc = 0; cc < 4; ++cc) {
-            const int chunk = ((q & 1) * 4 + cc) ^ (row & 7);
-            *reinterpret_cast<uint4*>(prow + chunk * 16) =
-                make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
+          for (int i = 0; i < 32; ++i) {
+            const int i0 = 2 * i, i1 = 2 * i + 1;
+            const uint32_t b0 = i0 < 32 ? (mw0 >> i0) & 1u : (mw1 >> (i0 - 32)) & 1u;
+            const uint32_t b1 = i1 < 32 ? (mw0 >> i1) & 1u : (mw1 >> (i1 - 32)) & 1u;
+            const float p0 = b0 ? ex2_approx(fmaf(v[i0], c2, -m_use)) : 0.f;
+            const float p1 = b1 ? ex2_approx(fmaf(v[i1], c2, -m_use)) : 0.f;
+            l8[i & 7] += p0 + p1;
+            pk[i] = pack2<BF16>(p0, p1);
           }
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&cx.bar[B_S_FREE + sb]);
-        ++s_it;
-        // rescale the running O when the reference moved (PV of the previous
-        // tile is complete: P_FREE was awaited above)
+        l = l * alpha + (((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7])));
+        // P buffer gi & 1 is free once the PV of tile gi - 2 has completed
+        if (!cx.warp_wait(B_P_FREE + (gi & 1), ((gi >> 1) & 1) ^ 1)) return;
+#pragma unroll
+        for (int cc = 0; cc < 8; ++cc) {
+          const int chunk = cc ^ (row & 7);
+          *reinterpret_cast<uint4*>(sP + (gi & 1) * C::kPBytes + chunk * 16) =
+              make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
+        }
+        // rescale the running O when the reference moved (after the PV of
+        // tile gi - 1, which is the last one that wrote O)
         if (n > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+          const uint32_t pv = gi - 1;
+          if (!cx.warp_wait(B_P_FREE + (pv & 1), (pv >> 1) & 1)) return;
+          tc_fence_after();
 #pragma unroll
           for (int oc = 0; oc < D / 32; ++oc) {
-            float v[32];
-            tmem_ld32(t_row + C::kTmemO + oc * 32, v);
+            float o[32];
+            tmem_ld32(t_row + C::kTmemO + oc * 32, o);
             tmem_wait_ld();
 #pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] *= alpha;
-            tmem_st32(t_row + C::kTmemO + oc * 32, v);
+            for (int i = 0; i < 32; ++i) o[i] *= alpha;
+            tmem_st32(t_row + C::kTmemO + oc * 32, o);
           }
           tmem_wait_st();
         }
         fence_proxy_async_smem();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&cx.bar[B_P_FULL]);
+        if (lane == 0) mbar_arrive(&cx.bar[B_P_FULL + (gi & 1)]);
       }
-      // epilogue: wait for the last PV, then O / l and the base-2 lse
-      if (!cx.warp_wait(B_P_FREE, pf_it & 1)) return;
-      ++pf_it;
+      // epilogue: wait for the last PV (tile gi - 1), then O / l and lse
+      const uint32_t pv = gi - 1;
+      if (!cx.warp_wait(B_P_FREE + (pv & 1), (pv >> 1) & 1)) return;
       tc_fence_after();
     }
     const float inv = l > 0.f ? 1.f / l : 0.f;
     const float lse_v = l > 0.f ? m_ref + log2f(l) : -INFINITY;
-    using T = uint16_t;
-    T* orow_ptr = reinterpret_cast<T*>(p.out) + orow * D;
+    // O / l in the storage dtype goes to the P buffers first (both are free:
+    // the item's last PV has completed), as 128-byte swizzled rows; d in
+    // [64a, 64a + 64) lands in buffer a
+    uint8_t* ostage = cx.smem + C::kOffP;
 #pragma unroll
     for (int oc = 0; oc < D / 32; ++oc) {
-      float v[32];
-      if (s.n_tiles > 0) {
-        tmem_ld32(t_row + C::kTmemO + oc * 32, v);
+      float o[32];
+      if (r.n_tiles > 0) {
+        tmem_ld32(t_row + C::kTmemO + oc * 32, o);
         tmem_wait_ld();
       } else {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] = 0.f;
+        for (int i = 0; i < 32; ++i) o[i] = 0.f;
       }
-      if (valid) {
-        uint32_t pk[16];
+      uint32_t pk[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) pk[i] = pack2<BF16>(v[2 * i] * inv, v[2 * i + 1] * inv);
-        uint4* dst = reinterpret_cast<uint4*>(orow_ptr + oc * 32);
+      for (int i = 0; i < 16; ++i) pk[i] = pack2<BF16>(o[2 * i] * inv, o[2 * i + 1] * inv);
+      uint8_t* rowp = ostage + (oc >> 1) * C::kPBytes + row * 128;
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc)
-          dst[cc] = make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
-      }
+      for (int cc = 0; cc < 4; ++cc)
+        *reinterpret_cast<uint4*>(rowp + ((((oc & 1) * 4 + cc) ^ (row & 7)) * 16)) =
+            make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
     }
     if (valid) p.lse[orow] = lse_v;
     tc_fence_before();
     __syncwarp();
-    if (lane == 0) {
-      if (s.n_tiles > 0) mbar_arrive(&cx.bar[B_O_FREE]);
-      mbar_arrive(&cx.bar[B_ITEM_EMPTY + slot]);
+    if (lane == 0 && r.n_tiles > 0) mbar_arrive(&cx.bar[B_O_FREE]);  // O is out of TMEM
+    // each warp writes its own 32 rows with whole-warp coalesced 16-byte stores
+    {
+      constexpr int kChunks = D / 8;              // 16-byte chunks per row
+      constexpr int kRowsPerStep = 32 / kChunks;
+      const int ch = lane % kChunks;
+      uint16_t* outp = reinterpret_cast<uint16_t*>(p.out);
+#pragma unroll 4
+      for (int st = 0; st < 32 / kRowsPerStep; ++st) {
+        const int src = st * kRowsPerStep + lane / kChunks;  // row within the quadrant
+        const long long ro = __shfl_sync(0xffffffffu, (long long)orow, src);
+        const int ok = __shfl_sync(0xffffffffu, valid ? 1 : 0, src);
+        const int rr = wq * 32 + src;
+        const uint4 val = *reinterpret_cast<const uint4*>(
+            ostage + (ch >> 3) * C::kPBytes + rr * 128 + (((ch & 7) ^ (rr & 7)) * 16));
+        if (ok) *reinterpret_cast<uint4*>(outp + ro * D + ch * 8) = val;
+      }
     }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&cx.bar[B_ITEM_EMPTY + slot]);
     ++it;
   }
 }
 
 // ---------------------------------------------------------------------------
-// warps 6-9: inline RoPE on the staged Q and K tiles
+// warps 6-9: inline RoPE on the staged Q tile
 // ---------------------------------------------------------------------------
-// Rotate rows [0, nrows) of a 128-row tile in shared memory.  ``token_of``
-// maps a tile row to its kv-token index (or -1 to leave the row as is).
-template <int D, bool BF16, typename TokenOf>
-__device__ void rope_tile(uint8_t* tile, const float2* __restrict__ cs, int rw, int lane,
-                          TokenOf token_of) {
-  constexpr int kHalfChunks = D / 16;          // 16-byte chunks in half a row
-  constexpr int kRowsPerPass = 32 / kHalfChunks;
-  const int sub = lane / kHalfChunks;
-  const int c = lane % kHalfChunks;
-  for (int r0 = rw * 32; r0 < rw * 32 + 32; r0 += kRowsPerPass) {
-    const int row = r0 + sub;
-    const long long tok = token_of(row);
-    if (tok < 0) continue;
-    // element block [8c, 8c+8) of the first half and its partner block in the second
-    uint8_t *lo, *hi;
-    if constexpr (D == 128) {
-      lo = tile + row * 128 + ((c ^ (row & 7)) * 16);
-      hi = tile + 128 * 128 + row * 128 + ((c ^ (row & 7)) * 16);
-    } else {
-      lo = tile + row * 128 + ((c ^ (row & 7)) * 16);
-      hi = tile + row * 128 + (((c + 4) ^ (row & 7)) * 16);
-    }
-    const uint4 a = *reinterpret_cast<const uint4*>(lo);
-    const uint4 b = *reinterpret_cast<const uint4*>(hi);
-    const float4* csp = reinterpret_cast<const float4*>(cs + tok * (D / 2) + c * 8);
-    float cosv[8], sinv[8];
+// Task = (q row of the tile, 16-byte block c of the first half of the head
+// dimension): one load of the row's cos/sin for that block, applied to the
+// block and its partner block in the second half, for each of the row's g
+// heads (packed rows qr * g .. qr * g + g - 1).
+template <int D, bool BF16>
+__device__ void rope_q_tile(uint8_t* tile, const float2* __restrict__ cs, long long tok0, int nq,
+                            int g, int t) {
+  constexpr int kHalfChunks = D / 16;  // 16-byte blocks in half a row
+  constexpr int kBatch = 2;            // tasks whose loads are in flight together
+  const int ntask = nq * kHalfChunks;
+  for (int t0 = t; t0 < ntask; t0 += 128 * kBatch) {
+    float4 cv[kBatch][4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float4 t = __ldg(csp + i);
-      cosv[2 * i] = t.x;
-      sinv[2 * i] = t.y;
-      cosv[2 * i + 1] = t.z;
-      sinv[2 * i + 1] = t.w;
-    }
-    const uint32_t au[4] = {a.x, a.y, a.z, a.w};
-    const uint32_t bu[4] = {b.x, b.y, b.z, b.w};
-    uint32_t ao[4], bo[4];
+    for (int u = 0; u < kBatch; ++u) {
+      const int task = t0 + u * 128;
+      if (task < ntask) {
+        const int qr = task / kHalfChunks, c = task % kHalfChunks;
+        const float4* csp = reinterpret_cast<const float4*>(cs + (tok0 + qr) * (D / 2) + c * 8);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float2 x0 = unpack2<BF16>(au[i]);
-      const float2 x1 = unpack2<BF16>(bu[i]);
-      const float c0 = cosv[2 * i], s0 = sinv[2 * i], c1 = cosv[2 * i + 1], s1 = sinv[2 * i + 1];
-      // first half: cos*x[j] + sin*(-x[j+d/2]); second half: cos*x[j] + sin*x[j-d/2]
-      const float y0a = __fadd_rn(__fmul_rn(c0, x0.x), __fmul_rn(s0, -x1.x));
-      const float y0b = __fadd_rn(__fmul_rn(c1, x0.y), __fmul_rn(s1, -x1.y));
-      const float y1a = __fadd_rn(__fmul_rn(c0, x1.x), __fmul_rn(s0, x0.x));
-      const float y1b = __fadd_rn(__fmul_rn(c1, x1.y), __fmul_rn(s1, x0.y));
-      ao[i] = pack2<BF16>(y0a, y0b);
-      bo[i] = pack2<BF16>(y1a, y1b);
+        for (int i = 0; i < 4; ++i) cv[u][i] = __ldg(csp + i);
+      }
     }
-    *reinterpret_cast<uint4*>(lo) = make_uint4(ao[0], ao[1], ao[2], ao[3]);
-    *reinterpret_cast<uint4*>(hi) = make_uint4(bo[0], bo[1], bo[2], bo[3]);
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int task = t0 + u * 128;
+      if (task >= ntask) continue;
+      const int qr = task / kHalfChunks, c = task % kHalfChunks;
+      for (int h = 0; h < g; ++h) {
+        const int row = qr * g + h;
+        uint8_t* lo;
+        uint8_t* hi;
+        if constexpr (D == 128) {
+          lo = tile + row * 128 + ((c ^ (row & 7)) * 16);
+          hi = tile + kBlockM * 128 + row * 128 + ((c ^ (row & 7)) * 16);
+        } else {
+          lo = tile + row * 128 + ((c ^ (row & 7)) * 16);
+          hi = tile + row * 128 + (((c + 4) ^ (row & 7)) * 16);
+        }
+        const uint4 a = *reinterpret_cast<const uint4*>(lo);
+        const uint4 b = *reinterpret_cast<const uint4*>(hi);
+        const uint32_t au[4] = {a.x, a.y, a.z, a.w};
+        const uint32_t bu[4] = {b.x, b.y, b.z, b.w};
+        uint32_t ao[4], bo[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float2 x0 = unpack2<BF16>(au[i]);
+          const float2 x1 = unpack2<BF16>(bu[i]);
+          const float c0 = cv[u][i].x, s0 = cv[u][i].y, c1 = cv[u][i].z, s1 = cv[u][i].w;
+          // first half: cos*x[j] + sin*(-x[j+d/2]); second half: cos*x[j] + sin*x[j-d/2]
+          const float y0a = __fadd_rn(__fmul_rn(c0, x0.x), __fmul_rn(s0, -x1.x));
+          const float y0b = __fadd_rn(__fmul_rn(c1, x0.y), __fmul_rn(s1, -x1.y));
+          const float y1a = __fadd_rn(__fmul_rn(c0, x1.x), __fmul_rn(s0, x0.x));
+          const float y1b = __fadd_rn(__fmul_rn(c1, x1.y), __fmul_rn(s1, x0.y));
+          ao[i] = pack2<BF16>(y0a, y0b);
+          bo[i] = pack2<BF16>(y1a, y1b);
+        }
+        *reinterpret_cast<uint4*>(lo) = make_uint4(ao[0], ao[1], ao[2], ao[3]);
+        *reinterpret_cast<uint4*>(hi) = make_uint4(bo[0], bo[1], bo[2], bo[3]);
+      }
+    }
   }
 }
 
 template <int D, bool BF16>
 __device__ void run_rope(const Ctx& cx, const AttnParams& p, int warp, int lane) {
   using C = Cfg<D>;
-  const int rw = warp - 6;
+  const int t = (warp - 6) * 32 + lane;
   uint8_t* sQ = cx.smem + C::kOffQ;
-  uint8_t* sK = cx.smem + C::kOffK;
   const int g = p.g, R = p.R;
-  uint32_t it = 0, kv_it = 0, q_it = 0;
+  uint32_t it = 0, q_it = 0;
   for (;;) {
-    const int slot = it & 1;
-    if (!cx.warp_wait(B_ITEM_FULL + slot, (it >> 1) & 1)) return;
-    const Item s = cx.misc->items[slot];
+    const int slot = it % kSlots;
+    if (!cx.warp_wait(B_ITEM_FULL + slot, (it / kSlots) & 1)) return;
+    const Item& s = cx.misc->items[slot];
     if (!s.valid) return;
-    if (s.n_tiles > 0) {
-      if (!cx.warp_wait(B_Q_FULL, q_it & 1)) return;
+    const ItemRec r = s.r;
+    if (r.n_tiles > 0) {
+      const int qs = q_it % kQStages;
+      if (!cx.warp_wait(B_Q_FULL + qs, (q_it / kQStages) & 1)) return;
       ++q_it;
       // q row r of the tile takes the position of its own tree node's kv slot
-      const long long qtok0 = (long long)s.kv_base + s.ts + (s.tl - s.qo) + (long long)s.t * R;
-      rope_tile<D, BF16>(sQ, p.rope_cs, rw, lane, [&](int row) -> long long {
-        if (row >= g * R) return -1;
-        const int qr = row / g;
-        return qr < s.nq ? qtok0 + qr : -1;
-      });
+      const long long qtok0 = (long long)r.kv_base + r.ts + (r.tl - r.qo) + (long long)r.t * R;
+      rope_q_tile<D, BF16>(sQ + qs * C::kQBytes, p.rope_cs, qtok0, r.nq, g, t);
       fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&cx.bar[B_Q_READY]);
-      TileIter ti(p.classes + s.class_off, kv_tiles(s.kv));
-      for (int n = 0; n < s.n_tiles; ++n) {
-        ti.next();
-        const int j = ti.j;
-        const int nvalid = min(kBlockN, s.kv - j * kBlockN);
-        const uint32_t c = kv_it + n;
-        const int stage = c & 1;
-        if (!cx.warp_wait(B_K_FULL + stage, (c >> 1) & 1)) return;
-        const long long ktok0 = (long long)s.kv_base + (long long)j * kBlockN;
-        rope_tile<D, BF16>(sK + stage * C::kTileBytes, p.rope_cs, rw, lane,
-                           [&](int row) -> long long { return row < nvalid ? ktok0 + row : -1; });
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&cx.bar[B_K_READY + stage]);
-      }
-      kv_it += s.n_tiles;
+      if (lane == 0) mbar_arrive(&cx.bar[B_Q_READY + qs]);
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&cx.bar[B_ITEM_EMPTY + slot]);
@@ -633,21 +698,27 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     const uint32_t consumers = 5u + (p.rotary ? 4u : 0u);
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kSlots; ++i) {
       mbar_init(&cx.bar[B_ITEM_FULL + i], 1);
       mbar_init(&cx.bar[B_ITEM_EMPTY + i], consumers);
+    }
+    for (int i = 0; i < kQStages; ++i) {
+      mbar_init(&cx.bar[B_Q_FULL + i], 1);
+      mbar_init(&cx.bar[B_Q_READY + i], 4);
+      mbar_init(&cx.bar[B_Q_EMPTY + i], 1);
+    }
+    for (int i = 0; i < kStages; ++i) {
       mbar_init(&cx.bar[B_K_FULL + i], 1);
       mbar_init(&cx.bar[B_V_FULL + i], 1);
-      mbar_init(&cx.bar[B_K_READY + i], 4);
+      mbar_init(&cx.bar[B_EX_FULL + i], 1);
       mbar_init(&cx.bar[B_KV_EMPTY + i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
       mbar_init(&cx.bar[B_S_FULL + i], 1);
       mbar_init(&cx.bar[B_S_FREE + i], 4);
+      mbar_init(&cx.bar[B_P_FREE + i], 1);
+      mbar_init(&cx.bar[B_P_FULL + i], 4);
     }
-    mbar_init(&cx.bar[B_Q_FULL], 1);
-    mbar_init(&cx.bar[B_Q_READY], 4);
-    mbar_init(&cx.bar[B_Q_EMPTY], 1);
-    mbar_init(&cx.bar[B_P_FULL], 4);
-    mbar_init(&cx.bar[B_P_FREE], 1);
     mbar_init(&cx.bar[B_O_FREE], 4);
     mbar_init(&cx.bar[B_DRAIN], 1);
     cx.misc->abort = 0;
@@ -658,10 +729,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
   }
-  // rows of the Q tile that no TMA box covers (g * R < 128) must read as zero
+  // rows of the Q buffers that no TMA box covers (g * R < 128) must read as zero
   if (p.g * p.R < kBlockM) {
     uint4* q4 = reinterpret_cast<uint4*>(smem + C::kOffQ);
-    for (int i = threadIdx.x; i < C::kTileBytes / 16; i += kThreads) q4[i] = make_uint4(0, 0, 0, 0);
+    for (int i = threadIdx.x; i < kQStages * C::kQBytes / 16; i += kThreads)
+      q4[i] = make_uint4(0, 0, 0, 0);
     fence_proxy_async_smem();
   }
   if (warp == 1) tmem_alloc(&cx.misc->tmem_base, C::kTmemCols);
@@ -671,7 +743,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = cx.misc->tmem_base;
 
   if (warp == 0) {
-    if (lane == 0) run_producer<D>(cx, &tm_q, &tm_k, &tm_v, p);
+    run_producer<D>(cx, &tm_q, &tm_k, &tm_v, p, lane);
   } else if (warp == 1) {
     if (lane == 0) run_mma<D, BF16>(cx, tmem, p);
   } else if (warp < 6) {
@@ -706,6 +778,7 @@ cudaError_t launch_attn(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const 
                         const AttnParams& p, int grid, cudaStream_t stream) {
   using C = Cfg<D>;
   static_assert(C::kSmemAlloc <= 227 * 1024, "shared memory budget");
+  static_assert(B_COUNT <= 64, "barrier area");
   auto kern = attn_kernel<D, BF16>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemAlloc);

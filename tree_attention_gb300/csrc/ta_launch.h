@@ -19,8 +19,8 @@ struct PlanParams {
   int64_t max_pairs;
   float rope_scale, rope_theta;
   WsHeader* hdr;
-  PairInfo* pairs;
-  int32_t* sorted;
+  ItemRec* recs;     // one record per (sequence, q tile), enumeration order
+  ItemRec* sorted;   // the same records, longest first
   uint8_t* classes;
   float2* rope_cs;
 };
@@ -29,16 +29,12 @@ struct AttnParams {
   const int32_t* tree_order;
   void* out;
   float* lse;
-  const PairInfo* pairs;
-  const int32_t* sorted;
+  const ItemRec* sorted;
   const uint8_t* classes;
   const float2* rope_cs;
-  const int32_t* q_indptr;
-  const int32_t* kv_indptr;
-  const int32_t* mn_indptr;
   WsHeader* hdr;
   int h_q, h_kv, g, R, rotary;
-  int64_t max_pairs;  // capacity of the pair table in the workspace
+  int64_t max_pairs;  // capacity of the record tables in the workspace
   float scale_log2;   // sm_scale * log2(e)
   unsigned long long timeout_ns;
 };
@@ -46,6 +42,11 @@ struct AttnParams {
 // Plan kernel: sequence/tile enumeration, tile classification, LPT ordering
 // and the RoPE cos/sin table.  ``grid`` >= max_pairs.
 cudaError_t launch_plan(const PlanParams& p, int grid, cudaStream_t stream);
+
+// Rotates every key once: krot[t, h, :] = rope(k[t, h, :]) with the plan's
+// cos/sin table (rows of all kv tokens).
+cudaError_t launch_krot(const void* k, void* krot, const float2* rope_cs, int total_kv, int h_kv,
+                        int head_dim, bool bf16, int grid, cudaStream_t stream);
 
 // Dense mask export (test helper).
 cudaError_t launch_mask_dense(const int32_t* q_indptr, const int32_t* kv_indptr,

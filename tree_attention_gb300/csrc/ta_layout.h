@@ -13,8 +13,8 @@ namespace ta {
 // the packing of the "Q_load" block of the page "tree_attn.py"), attended
 // against kv tiles of kBlockN columns.
 constexpr int kBlockM = 128;
-constexpr int kBlockN = 128;
-constexpr int kKvBoxRows = 64;   // kv rows per TMA box (a kv tile is 1 or 2 boxes)
+constexpr int kBlockN = 64;
+constexpr int kKvBoxRows = 64;   // kv rows per TMA box (one box per kv tile)
 constexpr int kMaxGroup = 128;   // largest supported h_q / h_kv
 
 // Tile classes computed by the plan kernel for each (q tile, kv tile).
@@ -26,7 +26,7 @@ constexpr uint8_t kTileFull = 2;     // every valid row sees every column: no ma
 constexpr unsigned int DEVERR_TIMEOUT = 1u;     // a bounded wait expired
 constexpr unsigned int DEVERR_BAD_INDPTR = 2u;  // index arrays violate the layout rules
 
-constexpr int kCostBuckets = 4096;  // LPT ordering resolution (tiles per item)
+constexpr int kCostBuckets = 512;  // LPT ordering resolution (tiles per item)
 
 struct WsHeader {
   unsigned int queue_head;  // next work item (attention kernel)
@@ -39,12 +39,31 @@ struct WsHeader {
 };
 static_assert(sizeof(WsHeader) == 64, "header size");
 
-struct PairInfo {
+// Everything the attention kernel needs about one (sequence, q tile) pair,
+// written by the plan kernel so that a work item costs one 64-byte load.
+struct ItemRec {
   int32_t b;          // sequence
   int32_t t;          // q tile within the sequence
-  int32_t class_off;  // byte offset of the tile's kv-tile classes (16-aligned)
-  int32_t n_tiles;    // number of non-empty kv tiles
+  int32_t q_row0;     // global index of the tile's first q row
+  int32_t nq;         // q rows of the sequence inside this tile
+  int32_t qo, kv;     // q rows / kv rows of the sequence
+  int32_t tl, ts;     // tree nodes, tree start (= prefix length)
+  int32_t kv_base;    // kv_indptr[b]
+  int32_t tree_base;  // mn_indptr[b]
+  int32_t n_tiles;    // non-empty kv tiles
+  int32_t class_off;  // byte offset of the pair's kv-tile classes (16-aligned)
+  int32_t kvt;        // kv tiles of the sequence
+  uint32_t cls2[3];   // if kvt <= kInlineTiles: tile j's class in bits 2(j%16).. of word j/16
 };
+constexpr int kInlineTiles = 48;
+
+// Class of kv tile j of a record (inline bits for short sequences, else the
+// class table).
+__host__ __device__ inline int tile_class(const ItemRec& r, const uint8_t* classes, int j) {
+  if (r.kvt <= kInlineTiles) return (r.cls2[j >> 4] >> (2 * (j & 15))) & 3;
+  return classes[r.class_off + j];
+}
+static_assert(sizeof(ItemRec) == 64, "item record size");
 
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 inline int64_t round_up(int64_t a, int64_t b) { return ceil_div(a, b) * b; }
@@ -55,27 +74,31 @@ inline int rows_per_item(int g) { return kBlockM / g; }
 struct WsLayout {
   int64_t max_pairs;    // upper bound on (sequence, q tile) pairs
   int64_t class_bytes;  // bound on the class table
-  size_t off_pairs, off_sorted, off_classes, off_rope, total;
+  size_t off_pairs, off_sorted, off_classes, off_rope, off_krot, total;
 };
 
 // Workspace layout for the given sizes (all offsets 256-byte aligned):
-//   header | PairInfo[max_pairs] | int32 sorted[max_pairs] | uint8 classes[]
-//   | float2 rope_cs[total_kv][head_dim / 2]
+//   header | ItemRec recs[max_pairs] | ItemRec sorted[max_pairs] (LPT order)
+//   | uint8 classes[]
+//   and with RoPE: | float2 rope_cs[total_kv][head_dim / 2] (rows of q tokens)
+//                  | rotated k [total_kv][h_kv][head_dim] (storage dtype)
 inline WsLayout make_ws_layout(int64_t batch, int64_t total_q, int64_t total_kv, int g,
-                               int head_dim) {
+                               int h_kv, int head_dim, bool rotary) {
   WsLayout L{};
   const int64_t R = rows_per_item(g);
   L.max_pairs = ceil_div(total_q, R) + batch;
   L.class_bytes = L.max_pairs * round_up(ceil_div(total_kv, kBlockN), 16);
   size_t off = 256;
   L.off_pairs = off;
-  off += round_up(L.max_pairs * (int64_t)sizeof(PairInfo), 256);
+  off += round_up(L.max_pairs * (int64_t)sizeof(ItemRec), 256);
   L.off_sorted = off;
-  off += round_up(L.max_pairs * 4, 256);
+  off += round_up(L.max_pairs * (int64_t)sizeof(ItemRec), 256);
   L.off_classes = off;
   off += round_up(L.class_bytes, 256);
   L.off_rope = off;
-  off += round_up(total_kv * (int64_t)(head_dim / 2) * 8, 256);
+  if (rotary) off += round_up(total_kv * (int64_t)(head_dim / 2) * 8, 256);
+  L.off_krot = off;
+  if (rotary) off += round_up(total_kv * (int64_t)h_kv * head_dim * 2, 256);
   L.total = off;
   return L;
 }
