@@ -121,15 +121,13 @@ struct TileIter {
   const uint8_t* cls;
   int kvt, j;
   bool inl;
-  uint32_t w[4];
+  uint32_t w0, w1, w2, w3;   // inline classes, or the current 16 class bytes
   __device__ TileIter(const ItemRec& r, const uint8_t* classes)
       : cls(classes + r.class_off), kvt(r.kvt), j(-1), inl(r.kvt <= kInlineTiles) {
-    if (inl) {
-      w[0] = r.cls2[0];
-      w[1] = r.cls2[1];
-      w[2] = r.cls2[2];
-      w[3] = 0;
-    }
+    w0 = r.cls2[0];
+    w1 = r.cls2[1];
+    w2 = r.cls2[2];
+    w3 = 0;
   }
   // advances to the next non-empty tile; returns its class (0 when done)
   __device__ int next() {
@@ -138,16 +136,19 @@ struct TileIter {
       if (j >= kvt) return 0;
       int c;
       if (inl) {
-        c = (w[j >> 4] >> (2 * (j & 15))) & 3;
+        const uint32_t w = j < 16 ? w0 : (j < 32 ? w1 : w2);
+        c = (w >> (2 * (j & 15))) & 3;
       } else {
         if ((j & 15) == 0) {
           const uint4 v = __ldg(reinterpret_cast<const uint4*>(cls + j));
-          w[0] = v.x;
-          w[1] = v.y;
-          w[2] = v.z;
-          w[3] = v.w;
+          w0 = v.x;
+          w1 = v.y;
+          w2 = v.z;
+          w3 = v.w;
         }
-        c = (w[(j & 15) >> 2] >> (8 * (j & 3))) & 0xff;
+        const int q = (j & 15) >> 2;
+        const uint32_t w = q == 0 ? w0 : (q == 1 ? w1 : (q == 2 ? w2 : w3));
+        c = (w >> (8 * (j & 3))) & 0xff;
       }
       if (c != kTileEmpty) return c;
     }
@@ -171,11 +172,15 @@ __device__ void run_producer(const Pipe& pp, const CUtensorMap* tm_q, const CUte
   const unsigned int num_items = (unsigned int)(n_items < cap ? n_items : cap);
   const int g = p.g, R = p.R;
   uint32_t it = 0, kv_it = 0, q_it = 0;
-  uint32_t issued_k[kStages] = {0, 0}, issued_v[kStages] = {0, 0};
+  uint32_t issued_k = 0, issued_v = 0;   // loads issued (stage = count % kStages)
   bool aborted = false;
   unsigned int idx = 0;
   if (lane == 0) idx = atomicAdd(&p.hdr->queue_head, 1u);
   idx = __shfl_sync(0xffffffffu, idx, 0);
+  // lanes 0-3 hold the next record (16 bytes each), fetched one item ahead
+  int4 rec_next = make_int4(0, 0, 0, 0);
+  if (idx < num_items && lane < 4)
+    rec_next = __ldg(reinterpret_cast<const int4*>(p.sorted + idx / p.h_kv) + lane);
   for (;;) {
     const int slot = it % kSlots;
     if (!pp.warp_wait(B_ITEM_EMPTY + slot, ((it / kSlots) & 1) ^ 1)) { aborted = true; break; }
@@ -187,9 +192,7 @@ __device__ void run_producer(const Pipe& pp, const CUtensorMap* tm_q, const CUte
       }
       break;
     }
-    if (lane < 4)
-      reinterpret_cast<int4*>(&s.r)[lane] =
-          __ldg(reinterpret_cast<const int4*>(p.sorted + idx / p.h_kv) + lane);
+    if (lane < 4) reinterpret_cast<int4*>(&s.r)[lane] = rec_next;
     const int kvh = idx % p.h_kv;
     // pop the next index now; its round trip overlaps this item's issue
     unsigned int nidx = 0;
@@ -201,7 +204,6 @@ __device__ void run_producer(const Pipe& pp, const CUtensorMap* tm_q, const CUte
     __syncwarp();
     const ItemRec r = s.r;
     if (lane == 0) mbar_arrive(&pp.bar[B_ITEM_FULL + slot]);
-    idx = __shfl_sync(0xffffffffu, nidx, 0);
     if (r.n_tiles > 0) {
       if (!pp.warp_wait(B_Q_EMPTY, (q_it & 1) ^ 1)) { aborted = true; break; }
       if (lane == 0) {
@@ -228,7 +230,7 @@ __device__ void run_producer(const Pipe& pp, const CUtensorMap* tm_q, const CUte
             tma_load_3d(sK + stage * C::kKVBytes + a * C::kKVAtomBytes, tm_k,
                         &pp.bar[B_K_FULL + stage], a * 64, kvh, row0);
         }
-        ++issued_k[stage];
+        ++issued_k;
         if (!pp.warp_wait(B_V_EMPTY + stage, empty_par)) { aborted = true; break; }
         if (lane == 0) {
           mbar_arrive_expect_tx(&pp.bar[B_V_FULL + stage], bytes);
@@ -237,7 +239,7 @@ __device__ void run_producer(const Pipe& pp, const CUtensorMap* tm_q, const CUte
             tma_load_3d(sV + stage * C::kKVBytes + a * C::kKVAtomBytes, tm_v,
                         &pp.bar[B_V_FULL + stage], a * 64, kvh, row0);
         }
-        ++issued_v[stage];
+        ++issued_v;
         // column intervals of a partial tile for the mask (FULL tiles need none)
         if (cls == kTilePartial) {
           int2* ex = sEX + stage * kBlockN;
@@ -252,15 +254,20 @@ __device__ void run_producer(const Pipe& pp, const CUtensorMap* tm_q, const CUte
       }
       if (aborted) break;
     }
+    idx = __shfl_sync(0xffffffffu, nidx, 0);
+    if (idx < num_items && lane < 4)
+      rec_next = __ldg(reinterpret_cast<const int4*>(p.sorted + idx / p.h_kv) + lane);
     ++it;
   }
   if (aborted && lane == 0) {
     // let every copy already in flight land before the CTA's memory goes away
     if (q_it > 0) pp.drain_wait(B_Q_FULL, (q_it - 1) & 1);
-    for (int st = 0; st < kStages; ++st) {
-      if (issued_k[st] > 0) pp.drain_wait(B_K_FULL + st, (issued_k[st] - 1) & 1);
-      if (issued_v[st] > 0) pp.drain_wait(B_V_FULL + st, (issued_v[st] - 1) & 1);
-    }
+    // the last load issued into each stage: load i went to stage i % kStages
+    // and completes that stage's phase i / kStages
+    for (uint32_t i = issued_k > kStages ? issued_k - kStages : 0; i < issued_k; ++i)
+      pp.drain_wait(B_K_FULL + i % kStages, (i / kStages) & 1);
+    for (uint32_t i = issued_v > kStages ? issued_v - kStages : 0; i < issued_v; ++i)
+      pp.drain_wait(B_V_FULL + i % kStages, (i / kStages) & 1);
   }
 }
 
@@ -270,9 +277,14 @@ __device__ void run_producer(const Pipe& pp, const CUtensorMap* tm_q, const CUte
 template <int D, bool BF16>
 __device__ void run_mma(const Pipe& pp, const AttnParams& p) {
   using C = Cfg<D>;
-  const uint32_t sQ = smem_u32(pp.smem + C::kOffQ);
-  const uint32_t sK = smem_u32(pp.smem + C::kOffK);
-  const uint32_t sV = smem_u32(pp.smem + C::kOffV);
+  // descriptors of k-step 0; a k-step or stage offset is added to the
+  // descriptor's 14-bit start-address field (addresses stay below 256 KB)
+  static_assert(kStages == 2, "descriptor selection below assumes two stages");
+  const uint64_t dq0 = sw128_desc(smem_u32(pp.smem + C::kOffQ), 0);
+  const uint64_t dk_s0 = sw128_desc(smem_u32(pp.smem + C::kOffK), 0);
+  const uint64_t dk_s1 = dk_s0 + (uint64_t)(C::kKVBytes >> 4);
+  const uint64_t dv_s0 = sw128_desc(smem_u32(pp.smem + C::kOffV), C::kKVAtomBytes);
+  const uint64_t dv_s1 = dv_s0 + (uint64_t)(C::kKVBytes >> 4);
   constexpr uint32_t idesc_pv = umma_idesc_f16(BF16, 128, D, /*b_mn_major=*/true);
   const int q_bar = p.rotary ? B_Q_READY : B_Q_FULL;
   uint32_t it = 0, kv_it = 0, q_it = 0, o_it = 0;
@@ -300,13 +312,13 @@ __device__ void run_mma(const Pipe& pp, const AttnParams& p) {
         const int sb = c & 1;
         const int n_eff = (nvalid + 15) & ~15;
         const uint32_t idesc = umma_idesc_f16(BF16, 128, n_eff, false);
-        const uint32_t kst = sK + stage * C::kKVBytes;
+        const uint64_t dk = stage ? dk_s1 : dk_s0;
+        const uint32_t d_s = pp.tmem + C::kTmemS + 64 * sb;
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
-          umma_f16(pp.tmem + C::kTmemS + 64 * sb,
-                   sw128_desc(sQ + (k >> 2) * C::kQAtomBytes + (k & 3) * 32, 0),
-                   sw128_desc(kst + (k >> 2) * C::kKVAtomBytes + (k & 3) * 32, 0), idesc,
-                   k > 0 ? 1u : 0u);
+          const uint32_t qo = (uint32_t)(((k >> 2) * C::kQAtomBytes + (k & 3) * 32) >> 4);
+          const uint32_t ko = (uint32_t)(((k >> 2) * C::kKVAtomBytes + (k & 3) * 32) >> 4);
+          umma_f16(d_s, dq0 + qo, dk + ko, idesc, k > 0 ? 1u : 0u);
         }
         umma_commit(&pp.bar[B_S_FULL + sb]);
         umma_commit(&pp.bar[B_K_EMPTY + stage]);
@@ -334,13 +346,14 @@ __device__ void run_mma(const Pipe& pp, const AttnParams& p) {
           ++o_it;
         }
         tc_fence_after();
-        const int n_eff = (nv_cur + 15) & ~15;
-        const uint32_t vst = sV + stage * C::kKVBytes;
+        const int nk = (nv_cur + 15) >> 4;   // 16-row k-steps holding valid kv rows
+        const uint64_t dv = stage ? dv_s1 : dv_s0;
         const uint32_t pcol = pp.tmem + C::kTmemS + 64 * pb;   // P: two elements per column
-        for (int k = 0; k < n_eff / 16; ++k) {
-          umma_f16_tmem_a(pp.tmem + C::kTmemO, pcol + k * 8,
-                          sw128_desc(vst + k * 16 * 128, C::kKVAtomBytes), idesc_pv,
-                          (n > 0 || k > 0) ? 1u : 0u);
+#pragma unroll
+        for (int k = 0; k < kBlockN / 16; ++k) {
+          if (k < nk)
+            umma_f16_tmem_a(pp.tmem + C::kTmemO, pcol + k * 8, dv + (uint64_t)(k * 16 * 128 >> 4),
+                            idesc_pv, (n > 0 || k > 0) ? 1u : 0u);
         }
         umma_commit(&pp.bar[B_PV_DONE + pb]);
         umma_commit(&pp.bar[B_V_EMPTY + stage]);
@@ -365,32 +378,53 @@ __device__ void run_mma(const Pipe& pp, const AttnParams& p) {
 // 16-byte block c of the first half of the head dimension): one load of the
 // row's cos/sin for that block, applied to the block and its partner block in
 // the second half, for each of the q row's heads that lie in these 32 rows.
-template <int D, bool BF16>
-__device__ void rope_q_rows(uint8_t* tile, const float2* __restrict__ cs, long long tok0, int nq,
-                            int g, int wq, int lane) {
+// Tasks are taken 64 at a time (two per lane); rope_load issues the loads of
+// one batch so that the first batch can be fetched before the Q tile lands.
+struct RopeRange {
+  int row_lo, row_hi, qr_lo, ntask;
+};
+
+template <int D>
+__device__ __forceinline__ RopeRange rope_range(int nq, int g, int wq) {
   constexpr int kHalfChunks = D / 16;  // 16-byte blocks in half a row
-  const int row_lo = wq * 32, row_hi = row_lo + 32;
-  const int qr_lo = row_lo / g;
-  const int qr_hi = min(nq, (row_hi + g - 1) / g);   // q rows touching this quadrant
-  const int ntask = max(0, qr_hi - qr_lo) * kHalfChunks;
-  for (int t0 = 0; t0 < ntask; t0 += 64) {
-    float4 cv[2][4];
+  RopeRange rr;
+  rr.row_lo = wq * 32;
+  rr.row_hi = rr.row_lo + 32;
+  rr.qr_lo = rr.row_lo / g;
+  const int qr_hi = min(nq, (rr.row_hi + g - 1) / g);   // q rows touching this quadrant
+  rr.ntask = max(0, qr_hi - rr.qr_lo) * kHalfChunks;
+  return rr;
+}
+
+template <int D>
+__device__ __forceinline__ void rope_load(float4 (&cv)[2][4], const float2* __restrict__ cs,
+                                          long long tok0, const RopeRange& rr, int t0, int lane) {
+  constexpr int kHalfChunks = D / 16;
 #pragma unroll
-    for (int u = 0; u < 2; ++u) {
-      const int task = t0 + u * 32 + lane;
-      if (task < ntask) {
-        const int qr = qr_lo + task / kHalfChunks, c = task % kHalfChunks;
-        const float4* csp = reinterpret_cast<const float4*>(cs + (tok0 + qr) * (D / 2) + c * 8);
+  for (int u = 0; u < 2; ++u) {
+    const int task = t0 + u * 32 + lane;
+    if (task < rr.ntask) {
+      const int qr = rr.qr_lo + task / kHalfChunks, c = task % kHalfChunks;
+      const float4* csp = reinterpret_cast<const float4*>(cs + (tok0 + qr) * (D / 2) + c * 8);
 #pragma unroll
-        for (int i = 0; i < 4; ++i) cv[u][i] = __ldg(csp + i);
-      }
+      for (int i = 0; i < 4; ++i) cv[u][i] = __ldg(csp + i);
     }
+  }
+}
+
+// Applies the rotation with the first batch already in ``cv``.
+template <int D, bool BF16>
+__device__ void rope_q_rows(uint8_t* tile, const float2* __restrict__ cs, long long tok0,
+                            const RopeRange& rr, int g, int lane, float4 (&cv)[2][4]) {
+  constexpr int kHalfChunks = D / 16;
+  for (int t0 = 0; t0 < rr.ntask; t0 += 64) {
+    if (t0 > 0) rope_load<D>(cv, cs, tok0, rr, t0, lane);
 #pragma unroll
     for (int u = 0; u < 2; ++u) {
       const int task = t0 + u * 32 + lane;
-      if (task >= ntask) continue;
-      const int qr = qr_lo + task / kHalfChunks, c = task % kHalfChunks;
-      const int h_lo = max(0, row_lo - qr * g), h_hi = min(g, row_hi - qr * g);
+      if (task >= rr.ntask) continue;
+      const int qr = rr.qr_lo + task / kHalfChunks, c = task % kHalfChunks;
+      const int h_lo = max(0, rr.row_lo - qr * g), h_hi = min(g, rr.row_hi - qr * g);
       for (int h = h_lo; h < h_hi; ++h) {
         const int row = qr * g + h;
         uint8_t* lo;
@@ -457,9 +491,13 @@ __device__ void run_softmax(const Pipe& pp, const AttnParams& p, int sw, int lan
     if (r.n_tiles > 0) {
       if (p.rotary) {
         // q row r of the tile takes the position of its own tree node's kv slot
-        if (!pp.warp_wait(B_Q_FULL, q_it & 1)) return;
+        // (the first cos/sin batch is fetched while the Q tile lands)
         const long long qtok0 = (long long)r.kv_base + r.ts + (r.tl - r.qo) + (long long)r.t * R;
-        rope_q_rows<D, BF16>(pp.smem + C::kOffQ, p.rope_cs, qtok0, r.nq, g, wq, lane);
+        const RopeRange rr = rope_range<D>(r.nq, g, wq);
+        float4 cv[2][4];
+        rope_load<D>(cv, p.rope_cs, qtok0, rr, 0, lane);
+        if (!pp.warp_wait(B_Q_FULL, q_it & 1)) return;
+        rope_q_rows<D, BF16>(pp.smem + C::kOffQ, p.rope_cs, qtok0, rr, g, lane, cv);
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(&pp.bar[B_Q_READY]);
@@ -586,42 +624,59 @@ __device__ void run_softmax(const Pipe& pp, const AttnParams& p, int sw, int lan
     const float inv = l > 0.f ? 1.f / l : 0.f;
     const float lse_v = l > 0.f ? m_ref + log2f(l) : -INFINITY;
     if (valid) p.lse[orow] = lse_v;
-    // O / l in the storage dtype, 32 columns (64 bytes) at a time: through the
-    // warp's staging buffer, then whole-warp coalesced 16-byte stores
+    // O / l in the storage dtype: 64 columns per TMEM round trip, written 32
+    // columns (64 bytes per row) at a time through the warp's staging buffer,
+    // then as whole-warp 16-byte stores of 8 rows x 64 bytes
     uint16_t* outp = reinterpret_cast<uint16_t*>(p.out);
-    for (int oc = 0; oc < D / 32; ++oc) {
-      float o[32];
+    long long ro[4];
+    int ok[4];
+#pragma unroll
+    for (int st = 0; st < 4; ++st) {
+      const int src = st * 8 + (lane >> 2);   // row within the quadrant
+      ro[st] = __shfl_sync(0xffffffffu, (long long)orow, src);
+      ok[st] = __shfl_sync(0xffffffffu, valid ? 1 : 0, src);
+    }
+#pragma unroll
+    for (int oc2 = 0; oc2 < D / 64; ++oc2) {
+      float oa[32], ob[32];
       if (r.n_tiles > 0) {
-        tmem_ld32(t_row + C::kTmemO + oc * 32, o);
+        tmem_ld32(t_row + C::kTmemO + oc2 * 64, oa);
+        tmem_ld32(t_row + C::kTmemO + oc2 * 64 + 32, ob);
         tmem_wait_ld();
       } else {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) o[i] = 0.f;
+        for (int i = 0; i < 32; ++i) oa[i] = ob[i] = 0.f;
       }
-      if (oc == D / 32 - 1) {
+      if (oc2 == D / 64 - 1) {
         // O is out of TMEM: the next item's first PV may overwrite it
         tc_fence_before();
         __syncwarp();
         if (lane == 0 && r.n_tiles > 0) mbar_arrive(&pp.bar[B_O_FREE]);
       }
-      uint32_t pk[16];
 #pragma unroll
-      for (int i = 0; i < 16; ++i) pk[i] = pack2<BF16>(o[2 * i] * inv, o[2 * i + 1] * inv);
-      __syncwarp();   // the previous chunk's readers are done with the buffer
+      for (int hf = 0; hf < 2; ++hf) {
+        const int oc = oc2 * 2 + hf;
+        uint32_t pk[16];
 #pragma unroll
-      for (int cc = 0; cc < 4; ++cc)
-        *reinterpret_cast<uint4*>(ost + lane * 64 + ((cc ^ ((lane >> 1) & 3)) * 16)) =
-            make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
-      __syncwarp();
+        for (int i = 0; i < 16; ++i) {
+          const float x0 = hf ? ob[2 * i] : oa[2 * i];
+          const float x1 = hf ? ob[2 * i + 1] : oa[2 * i + 1];
+          pk[i] = pack2<BF16>(x0 * inv, x1 * inv);
+        }
+        __syncwarp();   // the previous chunk's readers are done with the buffer
 #pragma unroll
-      for (int st = 0; st < 4; ++st) {
-        const int src = st * 8 + (lane >> 2);   // row within the quadrant
-        const int cc = lane & 3;
-        const long long ro = __shfl_sync(0xffffffffu, (long long)orow, src);
-        const int ok = __shfl_sync(0xffffffffu, valid ? 1 : 0, src);
-        const uint4 val =
-            *reinterpret_cast<const uint4*>(ost + src * 64 + ((cc ^ ((src >> 1) & 3)) * 16));
-        if (ok) *reinterpret_cast<uint4*>(outp + ro * D + oc * 32 + cc * 8) = val;
+        for (int cc = 0; cc < 4; ++cc)
+          *reinterpret_cast<uint4*>(ost + lane * 64 + ((cc ^ ((lane >> 1) & 3)) * 16)) =
+              make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
+        __syncwarp();
+#pragma unroll
+        for (int st = 0; st < 4; ++st) {
+          const int src = st * 8 + (lane >> 2);
+          const int cc = lane & 3;
+          const uint4 val =
+              *reinterpret_cast<const uint4*>(ost + src * 64 + ((cc ^ ((src >> 1) & 3)) * 16));
+          if (ok[st]) *reinterpret_cast<uint4*>(outp + ro[st] * D + oc * 32 + cc * 8) = val;
+        }
       }
     }
     __syncwarp();
@@ -692,6 +747,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   pp.tmem = cta->tmem_base + pipe * C::kTmemPipe;
+  // everything above is private to the CTA; the plan, the rotated keys and
+  // the work queue belong to the kernels before this one on the stream
+  pdl_wait();
 
   if (pw == 0) {
     run_producer<D>(pp, &tm_q, &tm_k, &tm_v, p, lane);
@@ -733,8 +791,7 @@ cudaError_t launch_attn(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const 
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemAlloc);
   if (e != cudaSuccess) return e;
-  kern<<<grid, kThreads, C::kSmemAlloc, stream>>>(tm_q, tm_k, tm_v, p);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(grid), dim3(kThreads), C::kSmemAlloc, stream, tm_q, tm_k, tm_v, p);
 }
 
 template cudaError_t launch_attn<64, false>(const CUtensorMap&, const CUtensorMap&,

@@ -109,6 +109,17 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
 }
 
 // ---------------------------------------------------------------------------
+// programmatic dependent launch
+// ---------------------------------------------------------------------------
+// Blocks until the previous kernel on the stream has completed and its memory
+// operations are visible (returns at once for a normal launch).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Lets the next kernel on the stream be scheduled before this one finishes.
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// ---------------------------------------------------------------------------
 // fences
 // ---------------------------------------------------------------------------
 // Make this thread's generic-proxy shared-memory writes visible to the async

@@ -5,9 +5,32 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <utility>
+
 #include "ta_layout.h"
 
 namespace ta {
+
+// Launches a kernel of this library with programmatic dependent launch: its
+// CTAs may be scheduled while the previous kernel on the stream is still
+// running, and every kernel here executes pdl_wait() (griddepcontrol.wait)
+// before it reads or writes anything that kernel may touch, so stream order
+// is kept while launch latency and prologues overlap.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
 
 struct PlanParams {
   const int32_t* q_indptr;

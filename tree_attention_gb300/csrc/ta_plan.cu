@@ -113,9 +113,12 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanParams p) 
   __shared__ int s_count;
   __shared__ double s_log2_theta;
   __shared__ float s_den[64];
+  __shared__ float4 s_sct[27];
   __shared__ int s_last;
   __shared__ int s_hist[kCostBuckets];
 
+  pdl_wait();
+  pdl_trigger();
   const int tid = threadIdx.x;
   if (tid < kGroup) {
     // ======================= group A: enumerate and classify ================
@@ -262,6 +265,9 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanParams p) 
     const int wb = tb >> 5, lane = tb & 31;
     const int D = p.head_dim, half = D / 2;
     if (tb == 0) s_log2_theta = log2((double)p.rope_theta);
+    if (tb < 27)
+      s_sct[tb] = make_float4(kSinCosTable[tb][0], kSinCosTable[tb][1], kSinCosTable[tb][2],
+                              kSinCosTable[tb][3]);
     group_sync(kBarB);
     // fl32(theta^(2i/d)), through float64 so that the float32 rounding is right
     if (tb < half) s_den[tb] = (float)exp2(s_log2_theta * ((2.0 * tb) / (double)D));
@@ -280,15 +286,24 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanParams p) 
         const long long my_tok = base + lane;
         const int my_pos = my_tok < t1 ? p.rope_pos[my_tok] : 0;
         const int ntok = (int)min(32LL, t1 - base);
-        for (int u = 0; u < ntok; ++u) {
-          const long long tok = base + u;
-          const int pos = __shfl_sync(0xffffffffu, my_pos, u);
-          const float s = __fmul_rn((float)pos, p.rope_scale);
-          float s0, c0, s1, c1;
-          cr_sincosf(__fdiv_rn(s, s_den[i0]), &s0, &c0);
-          cr_sincosf(__fdiv_rn(s, s_den[i1]), &s1, &c1);
-          if (D == 128 || lane < 16)
-            reinterpret_cast<float4*>(p.rope_cs + tok * half)[pl] = make_float4(c0, s0, c1, s1);
+        const float den0 = s_den[i0], den1 = s_den[i1];
+        // two tokens per step: four independent sin/cos evaluations in flight
+        for (int u = 0; u < ntok; u += 2) {
+          const bool two = u + 1 < ntok;
+          const int pos_a = __shfl_sync(0xffffffffu, my_pos, u);
+          const int pos_b = __shfl_sync(0xffffffffu, my_pos, two ? u + 1 : u);
+          const float sa = __fmul_rn((float)pos_a, p.rope_scale);
+          const float sb = __fmul_rn((float)pos_b, p.rope_scale);
+          float s0a, c0a, s1a, c1a, s0b, c0b, s1b, c1b;
+          cr_sincosf(__fdiv_rn(sa, den0), &s0a, &c0a, s_sct);
+          cr_sincosf(__fdiv_rn(sa, den1), &s1a, &c1a, s_sct);
+          cr_sincosf(__fdiv_rn(sb, den0), &s0b, &c0b, s_sct);
+          cr_sincosf(__fdiv_rn(sb, den1), &s1b, &c1b, s_sct);
+          if (D == 128 || lane < 16) {
+            float4* row = reinterpret_cast<float4*>(p.rope_cs + (base + u) * half);
+            row[pl] = make_float4(c0a, s0a, c1a, s1a);
+            if (two) row[half / 2 + pl] = make_float4(c0b, s0b, c1b, s1b);
+          }
         }
       }
     }
@@ -361,6 +376,8 @@ __global__ void __launch_bounds__(256) krot_kernel(const uint32_t* __restrict__ 
   const int pl = (D == 128) ? lane : (lane & 15);
   const int h0 = (D == 128) ? 0 : (lane >> 4);
   constexpr int hstep = (D == 128) ? 1 : 2;
+  pdl_wait();
+  pdl_trigger();
   const long long warps = (long long)gridDim.x * (blockDim.x / 32);
   for (long long tok = (long long)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
        tok < total_kv; tok += warps) {
@@ -427,8 +444,7 @@ __global__ void mask_dense_kernel(const int32_t* __restrict__ q_indptr,
 }  // namespace
 
 cudaError_t launch_plan(const PlanParams& p, int grid, cudaStream_t stream) {
-  plan_kernel<<<grid, kPlanThreads, 0, stream>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(plan_kernel, dim3(grid), dim3(kPlanThreads), 0, stream, p);
 }
 
 cudaError_t launch_krot(const void* k, void* krot, const float2* rope_cs, int total_kv, int h_kv,
@@ -437,18 +453,23 @@ cudaError_t launch_krot(const void* k, void* krot, const float2* rope_cs, int to
   const uint32_t* kin = static_cast<const uint32_t*>(k);
   uint32_t* kout = static_cast<uint32_t*>(krot);
   const float4* cs = reinterpret_cast<const float4*>(rope_cs);
+  cudaError_t e;
   if (head_dim == 128) {
     if (bf16)
-      krot_kernel<true, 128><<<grid, 256, 0, stream>>>(kin, kout, cs, total_kv, h_kv);
+      e = launch_pdl(krot_kernel<true, 128>, dim3(grid), dim3(256), 0, stream, kin, kout,
+                     cs, total_kv, h_kv);
     else
-      krot_kernel<false, 128><<<grid, 256, 0, stream>>>(kin, kout, cs, total_kv, h_kv);
+      e = launch_pdl(krot_kernel<false, 128>, dim3(grid), dim3(256), 0, stream, kin, kout,
+                     cs, total_kv, h_kv);
   } else {
     if (bf16)
-      krot_kernel<true, 64><<<grid, 256, 0, stream>>>(kin, kout, cs, total_kv, h_kv);
+      e = launch_pdl(krot_kernel<true, 64>, dim3(grid), dim3(256), 0, stream, kin, kout,
+                     cs, total_kv, h_kv);
     else
-      krot_kernel<false, 64><<<grid, 256, 0, stream>>>(kin, kout, cs, total_kv, h_kv);
+      e = launch_pdl(krot_kernel<false, 64>, dim3(grid), dim3(256), 0, stream, kin, kout,
+                     cs, total_kv, h_kv);
   }
-  return cudaGetLastError();
+  return e;
 }
 
 cudaError_t launch_mask_dense(const int32_t* q_indptr, const int32_t* kv_indptr,

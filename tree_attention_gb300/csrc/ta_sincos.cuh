@@ -35,7 +35,11 @@ __device__ __forceinline__ void two_prod(float a, float b, float& p, float& e) {
   e = fmaf(a, b, -p);
 }
 
-__device__ __forceinline__ void cr_sincosf(float x, float* sin_out, float* cos_out) {
+// ``tab`` is kSinCosTable as float4 rows {sin_hi, sin_lo, cos_hi, cos_lo}, in
+// shared memory: lanes index it with different j, which the constant cache
+// would serve one address at a time.
+__device__ __forceinline__ void cr_sincosf(float x, float* sin_out, float* cos_out,
+                                           const float4* tab) {
   if (!(fabsf(x) < 8388608.0f)) {
     sincosf(x, sin_out, cos_out);
     return;
@@ -66,8 +70,9 @@ __device__ __forceinline__ void cr_sincosf(float x, float* sin_out, float* cos_o
   const float cmh = -0.5f * b2h;  // exact
   const float cml = fmaf(b2h * b2h, fmaf(b2h, -1.0f / 720.0f, 1.0f / 24.0f), -0.5f * b2l);
   const float sbl = fmaf(bh * b2h, fmaf(b2h, 1.0f / 120.0f, -1.0f / 6.0f), bl);  // sin b - bh
-  float Sh = kSinCosTable[ja][0], Sl = kSinCosTable[ja][1];
-  const float Ch = kSinCosTable[ja][2], Cl = kSinCosTable[ja][3];
+  const float4 e = tab[ja];
+  float Sh = e.x, Sl = e.y;
+  const float Ch = e.z, Cl = e.w;
   if (j < 0) {
     Sh = -Sh;
     Sl = -Sl;
