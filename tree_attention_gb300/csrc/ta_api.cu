@@ -140,7 +140,6 @@ ta_status check_run_args(const void* q, const void* k, const void* v, const void
 
 struct WsPtrs {
   WsHeader* hdr;
-  ta::ItemRec* recs;
   ta::ItemRec* sorted;
   uint8_t* classes;
   float2* rope_cs;
@@ -148,7 +147,7 @@ struct WsPtrs {
 
 WsPtrs ws_ptrs(void* workspace, const WsLayout& L) {
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  return WsPtrs{reinterpret_cast<WsHeader*>(ws), reinterpret_cast<ta::ItemRec*>(ws + L.off_pairs),
+  return WsPtrs{reinterpret_cast<WsHeader*>(ws),
                 reinterpret_cast<ta::ItemRec*>(ws + L.off_sorted), ws + L.off_classes,
                 reinterpret_cast<float2*>(ws + L.off_rope)};
 }
@@ -181,8 +180,13 @@ ta_status launch_plan_checked(const int32_t* q_indptr, const int32_t* kv_indptr,
   pp.max_pairs = L.max_pairs;
   pp.rope_scale = rope_scale;
   pp.rope_theta = rope_theta;
+  for (int i = 0; i < 64; ++i) pp.rope_den[i] = 1.f;
+  if (rotary_mode == 1) {
+    const double l2 = std::log2((double)rope_theta);
+    for (int i = 0; i < dims->head_dim / 2; ++i)
+      pp.rope_den[i] = (float)std::exp2(l2 * ((2.0 * i) / (double)dims->head_dim));
+  }
   pp.hdr = w.hdr;
-  pp.recs = w.recs;
   pp.sorted = w.sorted;
   pp.classes = w.classes;
   pp.rope_cs = w.rope_cs;

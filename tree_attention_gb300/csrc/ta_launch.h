@@ -41,9 +41,11 @@ struct PlanParams {
   int batch, g, R, h_kv, head_dim, total_q, total_kv, total_tree, rotary;
   int64_t max_pairs;
   float rope_scale, rope_theta;
+  // fl32(theta^(2i/d)) for i < d/2, the RoPE frequency denominators of
+  // ``_rope`` (page "_kernel_common.py"), rounded once from float64 on the host
+  float rope_den[64];
   WsHeader* hdr;
-  ItemRec* recs;     // one record per (sequence, q tile), enumeration order
-  ItemRec* sorted;   // the same records, longest first
+  ItemRec* sorted;   // one record per (sequence, q tile), longest first
   uint8_t* classes;
   float2* rope_cs;
 };

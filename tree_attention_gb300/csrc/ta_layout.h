@@ -34,7 +34,7 @@ struct WsHeader {
   unsigned int error;       // DEVERR_* bits, cleared by tree_attn_device_status
   unsigned int num_pairs;   // (sequence, q tile) pairs found by the plan kernel
   unsigned int num_items;   // num_pairs * h_kv, 0 if the index arrays are invalid
-  unsigned int plan_done;   // plan CTAs finished (the last one orders the work)
+  unsigned int reserved;    // unused (zero)
   unsigned int pad[10];
 };
 static_assert(sizeof(WsHeader) == 64, "header size");
@@ -74,11 +74,11 @@ inline int rows_per_item(int g) { return kBlockM / g; }
 struct WsLayout {
   int64_t max_pairs;    // upper bound on (sequence, q tile) pairs
   int64_t class_bytes;  // bound on the class table
-  size_t off_pairs, off_sorted, off_classes, off_rope, off_krot, total;
+  size_t off_sorted, off_classes, off_rope, off_krot, total;
 };
 
 // Workspace layout for the given sizes (all offsets 256-byte aligned):
-//   header | ItemRec recs[max_pairs] | ItemRec sorted[max_pairs] (LPT order)
+//   header | ItemRec sorted[max_pairs] (longest-first order)
 //   | uint8 classes[]
 //   and with RoPE: | float2 rope_cs[total_kv][head_dim / 2] (rows of q tokens)
 //                  | rotated k [total_kv][h_kv][head_dim] (storage dtype)
@@ -89,8 +89,6 @@ inline WsLayout make_ws_layout(int64_t batch, int64_t total_q, int64_t total_kv,
   L.max_pairs = ceil_div(total_q, R) + batch;
   L.class_bytes = L.max_pairs * round_up(ceil_div(total_kv, kBlockN), 16);
   size_t off = 256;
-  L.off_pairs = off;
-  off += round_up(L.max_pairs * (int64_t)sizeof(ItemRec), 256);
   L.off_sorted = off;
   off += round_up(L.max_pairs * (int64_t)sizeof(ItemRec), 256);
   L.off_classes = off;

@@ -1,26 +1,17 @@
 // ta_plan.cu -- the plan kernel of batched tree attention and the dense
 // mask export used by tests.
 //
-// One launch of the plan kernel does, per CTA, two independent jobs in two
-// warp groups (synchronised with named barriers, so neither waits for the
-// other):
-//   group A (warps 0-3)
-//     1. enumerates the (sequence, q tile) pairs of the ragged batch (the
-//        ``advance_tile_batch`` walk of the page "_kernel_common.py", done
-//        once up front instead of per CTA), validating the index arrays;
-//     2. classifies every (q tile, kv tile) of its pair as EMPTY / PARTIAL /
-//        FULL from the DFS intervals of ``_check_tree_order`` (page
-//        "tree_attn.py"), exactly: the q rows' enter indices are sorted and,
-//        for each kv column, two binary searches count the rows inside the
-//        column's [enter, exit) interval; then writes the pair's item record;
-//   group B (warps 4-7)
-//     4. fills a slice of the RoPE cos/sin table, one entry per (kv token,
-//        frequency), in the float32 steps of ``_rope`` (page
-//        "_kernel_common.py"): angle = fl32(fl32(pos * scale) /
-//        fl32(theta^(2i/d))), cos and sin of it rounded correctly to float32
-//        (cr_sincosf).
-// Finally (3.) the last CTA to finish orders the item records longest-first
-// (LPT) for the attention kernel's work queue with a counting sort.
+// One launch of the plan kernel, every CTA:
+//   1. walks the (sequence, q tile) pairs of the ragged batch (the
+//      ``advance_tile_batch`` walk of the page "_kernel_common.py", done once
+//      up front), validating the index arrays, and places its own pair in the
+//      longest-first (LPT) order of the attention kernel's work queue by an
+//      estimated cost -- no global barrier, no serial tail;
+//   2. (warps 0-3) classifies every kv tile of its pair as EMPTY / PARTIAL /
+//      FULL exactly from the DFS intervals of ``_check_tree_order`` (page
+//      "tree_attn.py") and writes the pair's item record;
+//   3. (all warps) fills its share of the RoPE cos/sin table, one entry per
+//      (kv token, frequency), in the float32 steps of ``_rope``.
 #include <cuda_runtime.h>
 
 #include <climits>
@@ -35,7 +26,7 @@ namespace {
 
 constexpr int kPlanThreads = 256;
 constexpr int kGroup = 128;  // threads per warp group
-constexpr int kBarA = 1, kBarB = 2;
+constexpr int kBarA = 1;
 constexpr int kPassTiles = 256;  // kv tiles classified per pass
 
 __device__ __forceinline__ void group_sync(int id) {
@@ -102,262 +93,280 @@ __device__ __forceinline__ long long seg_bytes(int kv) {
   return ((kv + kBlockN - 1) / kBlockN + 15) / 16 * 16;
 }
 
+// Estimated cost of q tile t of a sequence, in kv tiles, for the
+// longest-first order: the kv tiles up to the tile's last row's own slot
+// (exact for trees whose nodes come after their parents, as in a causal
+// prefix; only the order of the work depends on it).
+__device__ __forceinline__ int pair_cost(int qo, int kv, int R, int t) {
+  const long long end = (long long)kv - max(0LL, (long long)qo - (long long)(t + 1) * R);
+  return (int)min((long long)kCostBuckets - 1, (end + kBlockN - 1) / kBlockN);
+}
+
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanParams p) {
   __shared__ long long s_scan_a[9], s_scan_b[9];
   __shared__ int s_keys[kBlockM];
-  __shared__ int s_pair_b, s_pair_t;
-  __shared__ long long s_pair_off, s_total;
-  __shared__ int s_bad;
+  __shared__ int s_pair_b, s_pair_t, s_pair_cost;
+  __shared__ long long s_pair_off;
+  __shared__ int s_bad, s_rank;
   __shared__ int s_any[kPassTiles], s_notall[kPassTiles];
   __shared__ uint32_t s_cls2[3];
   __shared__ int s_count;
-  __shared__ double s_log2_theta;
   __shared__ float s_den[64];
   __shared__ float4 s_sct[27];
-  __shared__ int s_last;
   __shared__ int s_hist[kCostBuckets];
 
   pdl_wait();
   pdl_trigger();
-  const int tid = threadIdx.x;
-  if (tid < kGroup) {
-    // ======================= group A: enumerate and classify ================
-    const int B = p.batch, R = p.R;
-    if (tid == 0) {
-      s_bad = (p.q_indptr[0] != 0 || p.kv_indptr[0] != 0 || p.mn_indptr[0] != 0 ||
-               p.q_indptr[B] != p.total_q || p.kv_indptr[B] != p.total_kv ||
-               p.mn_indptr[B] != p.total_tree);
-      s_count = 0;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int B = p.batch, R = p.R;
+  // ---- 0. constants and counters of this CTA
+  if (p.rotary) {
+    if (tid < 64) s_den[tid] = p.rope_den[tid];
+    if (tid < 27)
+      s_sct[tid] = make_float4(kSinCosTable[tid][0], kSinCosTable[tid][1], kSinCosTable[tid][2],
+                               kSinCosTable[tid][3]);
+  }
+  for (int i = tid; i < kCostBuckets; i += kPlanThreads) s_hist[i] = 0;
+  if (tid == 0) {
+    s_bad = (p.q_indptr[0] != 0 || p.kv_indptr[0] != 0 || p.mn_indptr[0] != 0 ||
+             p.q_indptr[B] != p.total_q || p.kv_indptr[B] != p.total_kv ||
+             p.mn_indptr[B] != p.total_tree);
+    s_count = 0;
+    s_rank = 0;
+  }
+  __syncthreads();
+
+  // ---- 1. the (sequence, q tile) pairs: every CTA walks the whole batch
+  // (the ``advance_tile_batch`` walk of the page "_kernel_common.py", done up
+  // front), validating the index arrays and counting pairs per cost
+  const int per = (B + kPlanThreads - 1) / kPlanThreads;
+  const int b_lo = min(B, tid * per), b_hi = min(B, b_lo + per);
+  long long my_tiles = 0, my_seg = 0;
+  int bad = 0;
+  for (int b = b_lo; b < b_hi; ++b) {
+    const int qo = p.q_indptr[b + 1] - p.q_indptr[b];
+    const int kv = p.kv_indptr[b + 1] - p.kv_indptr[b];
+    const int tl = p.mn_indptr[b + 1] - p.mn_indptr[b];
+    if (qo < 0 || tl < qo || kv < tl) {
+      bad = 1;
+      continue;
     }
-    const int per = (B + kGroup - 1) / kGroup;
-    const int b_lo = min(B, tid * per), b_hi = min(B, b_lo + per);
-    long long my_tiles = 0, my_seg = 0;
-    int bad = 0;
-    for (int b = b_lo; b < b_hi; ++b) {
-      const int qo = p.q_indptr[b + 1] - p.q_indptr[b];
-      const int kv = p.kv_indptr[b + 1] - p.kv_indptr[b];
-      const int tl = p.mn_indptr[b + 1] - p.mn_indptr[b];
-      if (qo < 0 || tl < qo || kv < tl) {
-        bad = 1;
-        continue;
-      }
-      const long long tiles = (qo + R - 1) / R;
-      my_tiles += tiles;
-      my_seg += tiles * seg_bytes(kv);
-    }
-    long long ex_tiles = my_tiles, ex_seg = my_seg, total_tiles, total_seg;
-    exclusive_scan2(ex_tiles, ex_seg, total_tiles, total_seg, s_scan_a, s_scan_b, 0, kGroup,
-                    [] { group_sync(kBarA); });
-    if (bad) atomicOr(&s_bad, 1);
-    const long long pair = blockIdx.x;
-    if (pair >= ex_tiles && pair < ex_tiles + my_tiles) {
-      long long tcum = ex_tiles, scum = ex_seg;
-      for (int b = b_lo; b < b_hi; ++b) {
-        const int qo = p.q_indptr[b + 1] - p.q_indptr[b];
-        const int kv = p.kv_indptr[b + 1] - p.kv_indptr[b];
-        const long long tiles = (qo + R - 1) / R;
-        if (pair < tcum + tiles) {
-          s_pair_b = b;
-          s_pair_t = (int)(pair - tcum);
-          s_pair_off = scum + (pair - tcum) * seg_bytes(kv);
-          break;
-        }
-        tcum += tiles;
-        scum += tiles * seg_bytes(kv);
-      }
-    }
-    group_sync(kBarA);
-    const bool ok = !s_bad && total_tiles <= p.max_pairs;
-    if (tid == 0) {
-      s_total = total_tiles;
-      if (!ok) s_bad = 1;
-    }
-    if (ok && pair < total_tiles) {
-      const int b = s_pair_b, t = s_pair_t;
-      const long long off = s_pair_off;
-      const int q0 = p.q_indptr[b];
-      const int qo = p.q_indptr[b + 1] - q0;
-      const int kv_base = p.kv_indptr[b];
-      const int kv = p.kv_indptr[b + 1] - kv_base;
-      const int tree_base = p.mn_indptr[b];
-      const int tl = p.mn_indptr[b + 1] - tree_base;
-      const int ts = kv - tl;
-      const int r0 = t * R;
-      const int nrows = min(R, qo - r0);
-      s_keys[tid] =
-          tid < nrows ? p.tree_order[2 * (tree_base + r0 + tid + tl - qo)] : INT_MAX;
-      group_sync(kBarA);
-      // bitonic sort of the q rows' enter indices (128 keys, one per thread)
-      for (int k = 2; k <= kBlockM; k <<= 1) {
-        for (int j = k >> 1; j > 0; j >>= 1) {
-          const int ixj = tid ^ j;
-          if (ixj > tid) {
-            const int a = s_keys[tid], c = s_keys[ixj];
-            const bool up = (tid & k) == 0;
-            if ((a > c) == up) {
-              s_keys[tid] = c;
-              s_keys[ixj] = a;
-            }
-          }
-          group_sync(kBarA);
-        }
-      }
-      const int kvt = (kv + kBlockN - 1) / kBlockN;
-      if (tid < 3) s_cls2[tid] = 0;
-      // up to kPassTiles kv tiles per pass; every thread takes every 128th
-      // column of the pass and folds its verdict into per-tile flags
-      for (int j0 = 0; j0 < kvt; j0 += kPassTiles) {
-        const int nt = min(kPassTiles, kvt - j0);
-        for (int i = tid; i < nt; i += kGroup) {
-          s_any[i] = 0;
-          s_notall[i] = 0;
-        }
-        group_sync(kBarA);
-        const int c_end = min(kv, (j0 + nt) * kBlockN);
-        for (int c = j0 * kBlockN + tid; c < c_end; c += kGroup) {
-          int cnt;
-          if (c < ts) {
-            cnt = nrows;
-          } else {
-            const int2 iv = reinterpret_cast<const int2*>(p.tree_order)[tree_base + c - ts];
-            cnt = max(0, lower_bound(s_keys, nrows, iv.y) - lower_bound(s_keys, nrows, iv.x));
-          }
-          const int jt = c / kBlockN - j0;
-          if (cnt > 0 && !s_any[jt]) s_any[jt] = 1;
-          if (cnt != nrows && !s_notall[jt]) s_notall[jt] = 1;
-        }
-        group_sync(kBarA);
-        for (int i = tid; i < nt; i += kGroup) {
-          const int j = j0 + i;
-          const bool ragged = (j + 1) * kBlockN > kv;
-          const uint8_t cls =
-              !s_any[i] ? kTileEmpty : ((!s_notall[i] && !ragged) ? kTileFull : kTilePartial);
-          p.classes[off + j] = cls;
-          if (cls != kTileEmpty) atomicAdd(&s_count, 1);
-          if (kvt <= kInlineTiles) atomicOr(&s_cls2[j >> 4], (uint32_t)cls << (2 * (j & 15)));
-        }
-        group_sync(kBarA);
-      }
-      if (tid == 0) {
-        ItemRec r;
-        r.b = b;
-        r.t = t;
-        r.q_row0 = q0 + r0;
-        r.nq = nrows;
-        r.qo = qo;
-        r.kv = kv;
-        r.tl = tl;
-        r.ts = ts;
-        r.kv_base = kv_base;
-        r.tree_base = tree_base;
-        r.n_tiles = s_count;
-        r.class_off = (int32_t)off;
-        r.kvt = kvt;
-        r.cls2[0] = s_cls2[0];
-        r.cls2[1] = s_cls2[1];
-        r.cls2[2] = s_cls2[2];
-        p.recs[pair] = r;
-      }
-    }
-  } else if (p.rotary) {
-    // ======================= group B: RoPE ==================================
-    const int tb = tid - kGroup;
-    const int wb = tb >> 5, lane = tb & 31;
-    const int D = p.head_dim, half = D / 2;
-    if (tb == 0) s_log2_theta = log2((double)p.rope_theta);
-    if (tb < 27)
-      s_sct[tb] = make_float4(kSinCosTable[tb][0], kSinCosTable[tb][1], kSinCosTable[tb][2],
-                              kSinCosTable[tb][3]);
-    group_sync(kBarB);
-    // fl32(theta^(2i/d)), through float64 so that the float32 rounding is right
-    if (tb < half) s_den[tb] = (float)exp2(s_log2_theta * ((2.0 * tb) / (double)D));
-    group_sync(kBarB);
-    // every warp owns a contiguous run of kv tokens
-    const long long nwarps = (long long)gridDim.x * (kGroup / 32);
-    const long long per = ((long long)p.total_kv + nwarps - 1) / nwarps;
-    const long long t0 = ((long long)blockIdx.x * (kGroup / 32) + wb) * per;
-    const long long t1 = min((long long)p.total_kv, t0 + per);
-    if (t0 < t1) {
-      // lane l computes frequencies (2l, 2l+1) (d = 128) or, for d = 64, lanes
-      // 0..15 compute them and lanes 16..31 repeat the work of lanes 0..15
-      const int pl = (D == 128) ? lane : (lane & 15);
-      const int i0 = 2 * pl, i1 = 2 * pl + 1;
-      for (long long base = t0; base < t1; base += 32) {
-        const long long my_tok = base + lane;
-        const int my_pos = my_tok < t1 ? p.rope_pos[my_tok] : 0;
-        const int ntok = (int)min(32LL, t1 - base);
-        const float den0 = s_den[i0], den1 = s_den[i1];
-        // two tokens per step: four independent sin/cos evaluations in flight
-        for (int u = 0; u < ntok; u += 2) {
-          const bool two = u + 1 < ntok;
-          const int pos_a = __shfl_sync(0xffffffffu, my_pos, u);
-          const int pos_b = __shfl_sync(0xffffffffu, my_pos, two ? u + 1 : u);
-          const float sa = __fmul_rn((float)pos_a, p.rope_scale);
-          const float sb = __fmul_rn((float)pos_b, p.rope_scale);
-          float s0a, c0a, s1a, c1a, s0b, c0b, s1b, c1b;
-          cr_sincosf(__fdiv_rn(sa, den0), &s0a, &c0a, s_sct);
-          cr_sincosf(__fdiv_rn(sa, den1), &s1a, &c1a, s_sct);
-          cr_sincosf(__fdiv_rn(sb, den0), &s0b, &c0b, s_sct);
-          cr_sincosf(__fdiv_rn(sb, den1), &s1b, &c1b, s_sct);
-          if (D == 128 || lane < 16) {
-            float4* row = reinterpret_cast<float4*>(p.rope_cs + (base + u) * half);
-            row[pl] = make_float4(c0a, s0a, c1a, s1a);
-            if (two) row[half / 2 + pl] = make_float4(c0b, s0b, c1b, s1b);
-          }
-        }
-      }
-    }
+    const int tiles = (qo + R - 1) / R;
+    my_tiles += tiles;
+    my_seg += (long long)tiles * seg_bytes(kv);
+    for (int t = 0; t < tiles; ++t) atomicAdd(&s_hist[pair_cost(qo, kv, R, t)], 1);
+  }
+  if (bad) atomicOr(&s_bad, 1);
+  long long ex_tiles = my_tiles, ex_seg = my_seg, total_tiles, total_seg;
+  exclusive_scan2(ex_tiles, ex_seg, total_tiles, total_seg, s_scan_a, s_scan_b, 0, kPlanThreads,
+                  [] { __syncthreads(); });
+  const bool ok = !s_bad && total_tiles <= p.max_pairs;
+  const long long n_pairs = ok ? total_tiles : 0;
+  if (blockIdx.x == 0 && tid == 0) {
+    p.hdr->num_pairs = (unsigned int)n_pairs;
+    p.hdr->num_items = (unsigned int)(n_pairs * p.h_kv);
+    p.hdr->queue_head = 0;
+    p.hdr->queue_done = 0;
+    if (!ok) atomicOr(&p.hdr->error, DEVERR_BAD_INDPTR);
   }
 
-  // ======================= 3. the last CTA orders the records ===============
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) s_last = atomicAdd(&p.hdr->plan_done, 1u) == gridDim.x - 1;
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
-  const long long np = s_bad ? 0 : s_total;
-  for (int i = tid; i < kCostBuckets; i += kPlanThreads) s_hist[i] = 0;
-  __syncthreads();
-  for (long long i = tid; i < np; i += kPlanThreads) {
-    const int c = min(__ldcg(&p.recs[i].n_tiles), kCostBuckets - 1);
-    atomicAdd(&s_hist[kCostBuckets - 1 - c], 1);
-  }
-  __syncthreads();
+  // ---- 2. where each cost bucket starts in the longest-first order: the
+  // pairs of higher cost come first
   {
     constexpr int per_t = kCostBuckets / kPlanThreads;
     long long sum = 0;
-    for (int i = 0; i < per_t; ++i) sum += s_hist[tid * per_t + i];
-    long long excl = sum, dummy = 0, tot, tot2;
-    exclusive_scan2(excl, dummy, tot, tot2, s_scan_a, s_scan_b, 0, kPlanThreads,
+    for (int i = 0; i < per_t; ++i) sum += s_hist[kCostBuckets - 1 - (tid * per_t + i)];
+    long long start = sum, dummy = 0, tot, tot2;
+    exclusive_scan2(start, dummy, tot, tot2, s_scan_a, s_scan_b, 0, kPlanThreads,
                     [] { __syncthreads(); });
-    long long run = excl;
     for (int i = 0; i < per_t; ++i) {
-      const int v = s_hist[tid * per_t + i];
-      s_hist[tid * per_t + i] = (int)run;
-      run += v;
+      const int c = kCostBuckets - 1 - (tid * per_t + i);
+      const int v = s_hist[c];
+      s_hist[c] = (int)start;
+      start += v;
+    }
+  }
+
+  // ---- 3. this CTA's pair and its place: the bucket's start plus the pairs
+  // of the same cost earlier in (sequence, q tile) order
+  const long long pair = blockIdx.x;
+  if (ok && pair >= ex_tiles && pair < ex_tiles + my_tiles) {
+    long long tcum = ex_tiles, scum = ex_seg;
+    for (int b = b_lo; b < b_hi; ++b) {
+      const int qo = p.q_indptr[b + 1] - p.q_indptr[b];
+      const int kv = p.kv_indptr[b + 1] - p.kv_indptr[b];
+      const long long tiles = (qo + R - 1) / R;
+      if (pair < tcum + tiles) {
+        const int t = (int)(pair - tcum);
+        s_pair_b = b;
+        s_pair_t = t;
+        s_pair_off = scum + (long long)t * seg_bytes(kv);
+        s_pair_cost = pair_cost(qo, kv, R, t);
+        break;
+      }
+      tcum += tiles;
+      scum += tiles * seg_bytes(kv);
     }
   }
   __syncthreads();
-  for (long long i = tid; i < np; i += kPlanThreads) {
-    const int4* src = reinterpret_cast<const int4*>(&p.recs[i]);
-    int4 r[4];
-#pragma unroll
-    for (int w = 0; w < 4; ++w) r[w] = __ldcg(src + w);
-    const int c = min(r[2].z, kCostBuckets - 1);  // n_tiles is the 11th field
-    const int pos = atomicAdd(&s_hist[kCostBuckets - 1 - c], 1);
-    int4* dst = reinterpret_cast<int4*>(&p.sorted[pos]);
-#pragma unroll
-    for (int w = 0; w < 4; ++w) dst[w] = r[w];
+  const bool has_pair = ok && pair < total_tiles;
+  if (has_pair) {
+    const int pb = s_pair_b, pt = s_pair_t, pc = s_pair_cost;
+    int cnt = 0;
+    for (int b = b_lo; b < min(b_hi, pb + 1); ++b) {
+      const int qo = p.q_indptr[b + 1] - p.q_indptr[b];
+      const int kv = p.kv_indptr[b + 1] - p.kv_indptr[b];
+      const int tiles = (qo + R - 1) / R;
+      const int t_end = b < pb ? tiles : pt;
+      for (int t = 0; t < t_end; ++t) cnt += pair_cost(qo, kv, R, t) == pc;
+    }
+    if (cnt) atomicAdd(&s_rank, cnt);
   }
-  if (tid == 0) {
-    p.hdr->num_pairs = (unsigned int)np;
-    p.hdr->num_items = (unsigned int)(np * p.h_kv);
-    p.hdr->queue_head = 0;
-    p.hdr->queue_done = 0;
-    p.hdr->plan_done = 0;
-    if (s_bad) atomicOr(&p.hdr->error, DEVERR_BAD_INDPTR);
-    __threadfence();
+  __syncthreads();
+
+  // ---- 4. warps 0-3 classify the pair's kv tiles and write its record
+  if (tid < kGroup && has_pair) {
+    const int b = s_pair_b, t = s_pair_t;
+    const long long off = s_pair_off;
+    const long long pos = (long long)s_hist[s_pair_cost] + s_rank;
+    const int q0 = p.q_indptr[b];
+    const int qo = p.q_indptr[b + 1] - q0;
+    const int kv_base = p.kv_indptr[b];
+    const int kv = p.kv_indptr[b + 1] - kv_base;
+    const int tree_base = p.mn_indptr[b];
+    const int tl = p.mn_indptr[b + 1] - tree_base;
+    const int ts = kv - tl;
+    const int r0 = t * R;
+    const int nrows = min(R, qo - r0);
+    s_keys[tid] = tid < nrows ? p.tree_order[2 * (tree_base + r0 + tid + tl - qo)] : INT_MAX;
+    group_sync(kBarA);
+    // exact classification from the DFS intervals of ``_check_tree_order``
+    // (page "tree_attn.py"): the rows' enter indices are sorted (bitonic, one
+    // key per thread) and, for each kv column, two binary searches count the
+    // rows inside the column's [enter, exit) interval
+    for (int k = 2; k <= kBlockM; k <<= 1) {
+      for (int j = k >> 1; j > 0; j >>= 1) {
+        const int ixj = tid ^ j;
+        if (ixj > tid) {
+          const int a = s_keys[tid], c = s_keys[ixj];
+          const bool up = (tid & k) == 0;
+          if ((a > c) == up) {
+            s_keys[tid] = c;
+            s_keys[ixj] = a;
+          }
+        }
+        group_sync(kBarA);
+      }
+    }
+    const int kvt = (kv + kBlockN - 1) / kBlockN;
+    if (tid < 3) s_cls2[tid] = 0;
+    // up to kPassTiles kv tiles per pass; every thread takes every 128th
+    // column of the pass and folds its verdict into per-tile flags
+    for (int j0 = 0; j0 < kvt; j0 += kPassTiles) {
+      const int nt = min(kPassTiles, kvt - j0);
+      for (int i = tid; i < nt; i += kGroup) {
+        s_any[i] = 0;
+        s_notall[i] = 0;
+      }
+      group_sync(kBarA);
+      const int c_end = min(kv, (j0 + nt) * kBlockN);
+      for (int c = j0 * kBlockN + tid; c < c_end; c += kGroup) {
+        int cnt;
+        if (c < ts) {
+          cnt = nrows;
+        } else {
+          const int2 iv = reinterpret_cast<const int2*>(p.tree_order)[tree_base + c - ts];
+          cnt = max(0, lower_bound(s_keys, nrows, iv.y) - lower_bound(s_keys, nrows, iv.x));
+        }
+        const int jt = c / kBlockN - j0;
+        if (cnt > 0 && !s_any[jt]) s_any[jt] = 1;
+        if (cnt != nrows && !s_notall[jt]) s_notall[jt] = 1;
+      }
+      group_sync(kBarA);
+      for (int i = tid; i < nt; i += kGroup) {
+        const int j = j0 + i;
+        const bool ragged = (j + 1) * kBlockN > kv;
+        const uint8_t cls =
+            !s_any[i] ? kTileEmpty : ((!s_notall[i] && !ragged) ? kTileFull : kTilePartial);
+        p.classes[off + j] = cls;
+        if (cls != kTileEmpty) atomicAdd(&s_count, 1);
+        if (kvt <= kInlineTiles) atomicOr(&s_cls2[j >> 4], (uint32_t)cls << (2 * (j & 15)));
+      }
+      group_sync(kBarA);
+    }
+    if (tid == 0) {
+      ItemRec r;
+      r.b = b;
+      r.t = t;
+      r.q_row0 = q0 + r0;
+      r.nq = nrows;
+      r.qo = qo;
+      r.kv = kv;
+      r.tl = tl;
+      r.ts = ts;
+      r.kv_base = kv_base;
+      r.tree_base = tree_base;
+      r.n_tiles = s_count;
+      r.class_off = (int32_t)off;
+      r.kvt = kvt;
+      r.cls2[0] = s_cls2[0];
+      r.cls2[1] = s_cls2[1];
+      r.cls2[2] = s_cls2[2];
+      p.sorted[pos] = r;
+    }
+  }
+
+  // ---- 5. the RoPE cos/sin table, one entry per (kv token, frequency), in
+  // the float32 steps of ``_rope`` (page "_kernel_common.py"): angle =
+  // fl32(fl32(pos * scale) / fl32(theta^(2i/d))), cos and sin of it rounded
+  // correctly to float32 (cr_sincosf).  8-token chunks are dealt out over
+  // every warp of the grid, first to the warps with nothing else to do.
+  if (p.rotary) {
+    const int D = p.head_dim, half = D / 2;
+    // warp ranks: the CTAs without a pair first (all 8 warps), then warps
+    // 4-7 of the CTAs with one, then their warps 0-3 (busy classifying)
+    const long long grid = gridDim.x;
+    const long long n_busy = ok ? min(total_tiles, grid) : 0;   // CTAs with a pair: 0..n_busy-1
+    const long long idle_warps = (grid - n_busy) * 8;
+    long long rank;
+    if (!has_pair)
+      rank = ((long long)blockIdx.x - n_busy) * 8 + warp;
+    else if (warp >= 4)
+      rank = idle_warps + (long long)blockIdx.x * 4 + (warp - 4);
+    else
+      rank = idle_warps + n_busy * 4 + (long long)blockIdx.x * 4 + warp;
+    // tokens per chunk: enough to cover the table in about one chunk per
+    // warp, even (two tokens per step), at most 32 (one per lane)
+    const long long per_warp = ((long long)p.total_kv + grid * 8 - 1) / (grid * 8);
+    const int kChunk = (int)min(32LL, max(2LL, (per_warp + 1) & ~1LL));
+    const long long n_chunks = ((long long)p.total_kv + kChunk - 1) / kChunk;
+    // lane l computes frequencies (2l, 2l+1) (d = 128) or, for d = 64, lanes
+    // 0..15 compute them and lanes 16..31 repeat the work of lanes 0..15
+    const int pl = (D == 128) ? lane : (lane & 15);
+    const float den0 = s_den[2 * pl], den1 = s_den[2 * pl + 1];
+    for (long long ch = rank; ch < n_chunks; ch += grid * 8) {
+      const long long base = ch * kChunk;
+      const int ntok = (int)min((long long)kChunk, (long long)p.total_kv - base);
+      const int my_pos = lane < ntok ? p.rope_pos[base + lane] : 0;
+      // two tokens per step: four independent sin/cos evaluations in flight
+      for (int u = 0; u < ntok; u += 2) {
+        const bool two = u + 1 < ntok;
+        const int pos_a = __shfl_sync(0xffffffffu, my_pos, u);
+        const int pos_b = __shfl_sync(0xffffffffu, my_pos, two ? u + 1 : u);
+        const float sa = __fmul_rn((float)pos_a, p.rope_scale);
+        const float sb = __fmul_rn((float)pos_b, p.rope_scale);
+        float s0a, c0a, s1a, c1a, s0b, c0b, s1b, c1b;
+        cr_sincosf(__fdiv_rn(sa, den0), &s0a, &c0a, s_sct);
+        cr_sincosf(__fdiv_rn(sa, den1), &s1a, &c1a, s_sct);
+        cr_sincosf(__fdiv_rn(sb, den0), &s0b, &c0b, s_sct);
+        cr_sincosf(__fdiv_rn(sb, den1), &s1b, &c1b, s_sct);
+        if (D == 128 || lane < 16) {
+          float4* row = reinterpret_cast<float4*>(p.rope_cs + (base + u) * half);
+          row[pl] = make_float4(c0a, s0a, c1a, s1a);
+          if (two) row[half / 2 + pl] = make_float4(c0b, s0b, c1b, s1b);
+        }
+      }
+    }
   }
 }
 
