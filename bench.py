@@ -421,7 +421,8 @@ def run_gb300(args):
         "roofline": roof,
         "e2e": {"value": weak_scaling_value(flops * K, world, e2e_ms / 1e3) / 1e12, "unit": UNIT,
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
-        "gpu_launches": 2 * K,
+        # per step: plan kernel, key-rotation kernel (RoPE only), attention kernel
+        "gpu_launches": (3 if w.rotary_mode == 1 else 2) * K,
         "clocks": clk,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
