@@ -25,6 +25,11 @@ Functions and the passages they restate:
                          output the softmax-weighted sum of v and the
                          log-sum-exp in base 2 (``m + log2(d)`` with scores
                          pre-multiplied by log2(e)).
+* ``paged_kv_lengths``,
+  ``tree_attention_paged`` -- ``_get_kv_chunk_len`` (page "_kernel_common.py")
+                         and ``tree_attn_with_paged_kv_cache_cpu`` (page
+                         "tree_attn.py"): the same attention with K/V rows
+                         fetched through a page table of 16-slot pages.
 """
 from __future__ import annotations
 
@@ -178,28 +183,106 @@ def tree_attention(q: torch.Tensor, q_indptr, k: torch.Tensor, v: torch.Tensor, 
             kpos = pos[k0:k1]
             qb = apply_rope(qb, qpos, rope_theta, rope_scale)
             kb = apply_rope(kb, kpos, rope_theta, rope_scale)
-        q64 = qb.to(torch.float64).numpy()
-        k64 = kb.to(torch.float64).numpy()
-        v64 = vb.to(torch.float64).numpy()
-        any_vis = vis.any(axis=1)                                   # [qo]
-        for kh in range(h_kv):
-            heads = slice(kh * g, (kh + 1) * g)
-            qh = np.transpose(q64[:, heads, :], (1, 0, 2))          # [g, qo, d]
-            s = sm_scale * np.matmul(qh, k64[:, kh, :].T)            # [g, qo, kv]
-            s = np.where(vis[None], s, -np.inf)
-            m = np.max(s, axis=2, keepdims=True) if kv else np.full((g, qo, 1), -np.inf)
-            m = np.where(np.isfinite(m), m, 0.0)
-            e = np.exp(s - m)                                        # masked -> 0
-            z = np.sum(e, axis=2, keepdims=True)
-            with np.errstate(divide="ignore", invalid="ignore"):
-                L = m + np.log(z)                                    # natural log-sum-exp
-                w = np.where(z > 0, e / z, 0.0)
-            o = np.matmul(w, v64[:, kh, :])                          # [g, qo, d]
-            o[:, ~any_vis, :] = 0.0
-            Lr = L[..., 0]
-            Lr[:, ~any_vis] = -np.inf
-            out[q0:q1, heads, :] = np.transpose(o, (1, 0, 2))
-            lse[q0:q1, heads] = (Lr / LN2).T
+        _attend_sequence(qb, kb, vb, vis, sm_scale, g, out[q0:q1], lse[q0:q1])
+    return out, lse
+
+
+def _attend_sequence(qb: torch.Tensor, kb: torch.Tensor, vb: torch.Tensor, vis: np.ndarray,
+                     sm_scale: float, g: int, out: np.ndarray, lse: np.ndarray) -> None:
+    """One sequence of ``tree_attn_cpu`` (page "tree_attn.py") after the
+    q/k/v rows are fetched (and rotated): per kv head and q head, the masked
+    softmax over the visible columns of ``sm_scale * q.k`` in float64, the
+    softmax-weighted sum of v into ``out [qo, h_q, d]`` and the base-2
+    log-sum-exp into ``lse [qo, h_q]``.  A row with no visible column gets
+    ``out = 0`` and ``lse = -inf``."""
+    qo, kv = vis.shape
+    h_kv = kb.shape[1]
+    q64 = qb.to(torch.float64).numpy()
+    k64 = kb.to(torch.float64).numpy()
+    v64 = vb.to(torch.float64).numpy()
+    any_vis = vis.any(axis=1)                                   # [qo]
+    for kh in range(h_kv):
+        heads = slice(kh * g, (kh + 1) * g)
+        qh = np.transpose(q64[:, heads, :], (1, 0, 2))          # [g, qo, d]
+        s = sm_scale * np.matmul(qh, k64[:, kh, :].T)            # [g, qo, kv]
+        s = np.where(vis[None], s, -np.inf)
+        m = np.max(s, axis=2, keepdims=True) if kv else np.full((g, qo, 1), -np.inf)
+        m = np.where(np.isfinite(m), m, 0.0)
+        e = np.exp(s - m)                                        # masked -> 0
+        z = np.sum(e, axis=2, keepdims=True)
+        with np.errstate(divide="ignore", invalid="ignore"):
+            L = m + np.log(z)                                    # natural log-sum-exp
+            w = np.where(z > 0, e / z, 0.0)
+        o = np.matmul(w, v64[:, kh, :]) if kv else np.zeros((g, qo, v64.shape[2]))
+        o[:, ~any_vis, :] = 0.0
+        Lr = L[..., 0]
+        Lr[:, ~any_vis] = -np.inf
+        out[:, heads, :] = np.transpose(o, (1, 0, 2))
+        lse[:, heads] = (Lr / LN2).T
+
+
+# --------------------------------------------------------------------------
+# paged KV cache: tree_attn_with_paged_kv_cache_cpu
+# --------------------------------------------------------------------------
+
+PAGE_SIZE = 16
+
+
+def paged_kv_lengths(page_indptr, last_page_len) -> np.ndarray:
+    """kv length of every sequence of a paged cache, ``_get_kv_chunk_len``
+    (page "_kernel_common.py") without a sliding window:
+    ``(num_pages - 1) * page_size + last_page_len``, and 0 for a sequence that
+    owns no page (the guard of ``tree_attn_with_paged_kv_cache_cpu``)."""
+    page_indptr = _as_np(page_indptr).astype(np.int64)
+    last = _as_np(last_page_len).astype(np.int64)
+    n = page_indptr[1:] - page_indptr[:-1]
+    return np.where(n > 0, (n - 1) * PAGE_SIZE + last, 0)
+
+
+def tree_attention_paged(q: torch.Tensor, q_indptr, pages: torch.Tensor, page_indptr,
+                         page_values, last_page_len, mn_indptr, tree_order, rotary_mode: int,
+                         sm_scale: float,
+                         seqs: Optional[Iterable[int]] = None) -> Tuple[np.ndarray, np.ndarray]:
+    """Tree attention over a paged KV cache; ``(out, lse)`` as in
+    ``tree_attention``.
+
+    Restates ``tree_attn_with_paged_kv_cache_cpu`` (page "tree_attn.py"):
+    ``pages [max_num_pages, 2, h_kv, 16, d]`` holds K (index 0) and V (1);
+    kv row r of sequence b lives in page
+    ``page_values[page_indptr[b] + r // 16]`` at slot ``r % 16``; the kv length
+    comes from ``paged_kv_lengths``; the tree mask is ``_check_tree_order``
+    with that length.  The pages assert ``rotary_mode == 0`` for this kernel
+    (no RoPE), and so does this function.  Slots past a sequence's length are
+    never read.
+    """
+    if rotary_mode != 0:
+        raise ValueError("paged tree attention supports rotary_mode 0 only")
+    q_indptr = _as_np(q_indptr).astype(np.int64)
+    page_indptr = _as_np(page_indptr).astype(np.int64)
+    page_values = _as_np(page_values).astype(np.int64)
+    mn_indptr = _as_np(mn_indptr).astype(np.int64)
+    order = _as_np(tree_order).astype(np.int64).reshape(-1, 2)
+    kv_len = paged_kv_lengths(page_indptr, last_page_len)
+    kv_indptr = np.concatenate([[0], np.cumsum(kv_len)])
+    tq, h_q, d = q.shape
+    h_kv = pages.shape[2]
+    if h_q % h_kv != 0:
+        raise ValueError("h_q must be a multiple of h_kv")
+    g = h_q // h_kv
+    out = np.full((tq, h_q, d), np.nan, dtype=np.float64)
+    lse = np.full((tq, h_q), np.nan, dtype=np.float64)
+    B = len(q_indptr) - 1
+    for b in (range(B) if seqs is None else seqs):
+        q0, q1 = int(q_indptr[b]), int(q_indptr[b + 1])
+        if q1 == q0:
+            continue
+        rows = np.arange(int(kv_len[b]))
+        phys = page_values[page_indptr[b] + rows // PAGE_SIZE]
+        slot = rows % PAGE_SIZE
+        kb = pages[phys, 0, :, slot, :]                          # [kv, h_kv, d]
+        vb = pages[phys, 1, :, slot, :]
+        vis = visibility(q_indptr, kv_indptr, mn_indptr, order, b)
+        _attend_sequence(q[q0:q1], kb, vb, vis, sm_scale, g, out[q0:q1], lse[q0:q1])
     return out, lse
 
 

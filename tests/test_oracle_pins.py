@@ -406,3 +406,67 @@ def test_visible_pairs_counts_ancestors():
     ww = wl.build_workload("r", ps, h_q=1, h_kv=1, head_dim=8, dtype="fp16", tensor_seed=0,
                            prefix_lens=[4])
     assert wl.visible_pairs(ww) == int(ancestor_mask(ps[0], 4, 30).sum())
+
+
+# --------------------------------------------------------------------------
+# paged KV cache (tree_attn_with_paged_kv_cache_cpu, page "tree_attn.py")
+# --------------------------------------------------------------------------
+
+def _paged_workloads():
+    rng = np.random.default_rng(11)
+    ws = [wl.config(1)]
+    # prefix + tree, several pages per sequence, partial last pages, GQA
+    ws.append(wl.build_workload("pp", [wl.random_tree(23, rng), wl.random_tree(40, rng),
+                                       wl.random_tree(5, rng)],
+                                h_q=4, h_kv=2, head_dim=64, dtype="bf16", tensor_seed=5,
+                                prefix_lens=[37, 0, 16], qo_lens=[9, 40, 5]))
+    # chain, star and binary trees whose lengths are exact multiples of 16
+    ws.append(wl.build_workload("pd", [wl.chain_tree(32), wl.star_tree(48), wl.binary_tree(16)],
+                                h_q=2, h_kv=2, head_dim=64, dtype="fp16", tensor_seed=6))
+    return ws
+
+
+@pytest.mark.parametrize("i", range(3))
+def test_paged_equals_contiguous(i):
+    """Fetching K/V rows through the page table (scattered physical pages,
+    partial last pages, NaN in every slot no sequence owns) gives exactly the
+    contiguous-cache attention, which is pinned on its own above."""
+    w = _paged_workloads()[i]
+    pk = wl.paged_from(w, seed=100 + i)
+    assert not np.array_equal(pk.page_values, np.arange(len(pk.page_values)))
+    o1, l1 = oracle.tree_attention_workload(w)
+    o2, l2 = oracle.tree_attention_paged(w.q, w.q_indptr, pk.pages, pk.page_indptr,
+                                         pk.page_values, pk.last_page_len, w.mn_indptr,
+                                         w.tree_order, 0, w.sm_scale)
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+
+
+def test_paged_kv_lengths_follow_the_page_count():
+    # 3 pages with 5 rows in the last: 2*16 + 5; one full page: 16; no page: 0
+    lens = oracle.paged_kv_lengths(np.array([0, 3, 4, 4]), np.array([5, 16, 7]))
+    assert lens.tolist() == [37, 16, 0]
+    w = _paged_workloads()[1]
+    pk = wl.paged_from(w)
+    assert np.array_equal(oracle.paged_kv_lengths(pk.page_indptr, pk.last_page_len),
+                          np.diff(w.kv_indptr))
+
+
+def test_paged_never_reads_unowned_slots():
+    w = _paged_workloads()[1]
+    outs = []
+    for fill in (float("nan"), float("inf"), 0.0, 3.0):
+        pk = wl.paged_from(w, seed=3, fill=fill)
+        outs.append(oracle.tree_attention_paged(w.q, w.q_indptr, pk.pages, pk.page_indptr,
+                                                pk.page_values, pk.last_page_len, w.mn_indptr,
+                                                w.tree_order, 0, w.sm_scale))
+    for o, l in outs[1:]:
+        assert np.array_equal(o, outs[0][0]) and np.array_equal(l, outs[0][1])
+    assert np.isfinite(outs[0][0]).all()
+
+
+def test_paged_rejects_rope():
+    w = _paged_workloads()[0]
+    pk = wl.paged_from(w)
+    with pytest.raises(ValueError):
+        oracle.tree_attention_paged(w.q, w.q_indptr, pk.pages, pk.page_indptr, pk.page_values,
+                                    pk.last_page_len, w.mn_indptr, w.tree_order, 1, w.sm_scale)

@@ -381,3 +381,51 @@ def device_inputs(w: Workload, device="cuda") -> dict:
         "mn_indptr": i32(w.mn_indptr), "tree_order": i32(w.tree_order.reshape(-1, 2)),
         "q_rope_position": None if w.rope_position is None else i32(w.rope_position),
     }
+
+
+# --------------------------------------------------------------------------
+# paged KV cache layout of a workload (no arithmetic: a data layout only)
+# --------------------------------------------------------------------------
+
+PAGE_SIZE = 16
+
+
+@dataclasses.dataclass
+class PagedKV:
+    """A workload's K/V moved into a paged cache ``pages [n_pages, 2, h_kv,
+    16, d]`` (index 0 = K, 1 = V) with the page table of the paged tree
+    attention: sequence b owns pages ``page_values[page_indptr[b]:
+    page_indptr[b+1]]`` in order, its last page holding ``last_page_len[b]``
+    rows."""
+    pages: torch.Tensor          # [n_pages, 2, h_kv, 16, d]  CPU
+    page_indptr: np.ndarray      # [B+1] int32
+    page_values: np.ndarray      # [nnz_pages] int32 physical page ids
+    last_page_len: np.ndarray    # [B] int32 (the pages' ``length_info``)
+
+
+def paged_from(w: Workload, seed: int = 7, spare_pages: int = 3,
+               fill: float = float("nan")) -> PagedKV:
+    """Copies ``w.k``/``w.v`` into a paged cache: each sequence's kv rows fill
+    ceil(kv / 16) logical pages, mapped to physical pages in a seeded random
+    order within a pool that also has ``spare_pages`` unused pages.  Slots
+    that hold no row (the tail of a last page, the spare pages) are set to
+    ``fill`` -- NaN by default, so that any read of them shows."""
+    rng = np.random.default_rng(seed)
+    kv_lens = np.diff(w.kv_indptr.astype(np.int64))
+    n_log = (kv_lens + PAGE_SIZE - 1) // PAGE_SIZE
+    nnz = int(n_log.sum())
+    n_pages = nnz + spare_pages
+    perm = rng.permutation(n_pages)[:nnz]
+    page_indptr = np.concatenate([[0], np.cumsum(n_log)]).astype(np.int32)
+    last = np.where(n_log > 0, kv_lens - (n_log - 1) * PAGE_SIZE, 0).astype(np.int32)
+    pages = torch.full((n_pages, 2, w.h_kv, PAGE_SIZE, w.head_dim), fill, dtype=w.k.dtype)
+    for b in range(len(kv_lens)):
+        k0 = int(w.kv_indptr[b])
+        for lp in range(int(n_log[b])):
+            phys = int(perm[page_indptr[b] + lp])
+            r0 = lp * PAGE_SIZE
+            r1 = min(int(kv_lens[b]), r0 + PAGE_SIZE)
+            pages[phys, 0, :, : r1 - r0, :] = w.k[k0 + r0:k0 + r1].transpose(0, 1)
+            pages[phys, 1, :, : r1 - r0, :] = w.v[k0 + r0:k0 + r1].transpose(0, 1)
+    return PagedKV(pages=pages, page_indptr=page_indptr, page_values=perm.astype(np.int32),
+                   last_page_len=last)
