@@ -168,6 +168,62 @@ ta_status tree_attn_noalloc(const void* q, const int32_t* q_indptr, const void* 
                             float* lse, int32_t rotary_mode, float rope_scale, float rope_theta,
                             float sm_scale, const ta_dims* dims, void* stream);
 
+/* ---- Paged KV cache ------------------------------------------------------
+ * The same tree attention with K and V held in a paged cache, as the page
+ * "tree_attn.py" generates it in ``tree_attn_with_paged_kv_cache`` (GPU) and
+ * ``tree_attn_with_paged_kv_cache_cpu``; kv lengths follow
+ * ``_get_kv_chunk_len`` of the page "_kernel_common.py" without a sliding
+ * window (the pages disable it for tree attention).
+ *   batch_size, total_q, total_tree, h_q, h_kv, head_dim, dtype
+ *               as in ta_dims
+ *   num_pages   pages in the pool (>= 1): the pages buffer is
+ *               [num_pages, 2, h_kv, 16, head_dim]
+ *   nnz_pages   entries of page_values (= page_indptr[B]) */
+typedef struct {
+  int32_t batch_size;
+  int32_t total_q;
+  int32_t total_tree;
+  int32_t h_q;
+  int32_t h_kv;
+  int32_t head_dim;
+  ta_dtype dtype;
+  int32_t num_pages;
+  int32_t nnz_pages;
+} ta_paged_dims;
+
+/* Bytes of device workspace tree_attn_paged needs (0 on invalid dims); the
+ * same rules as tree_attn_workspace_size. */
+size_t tree_attn_paged_workspace_size(const ta_paged_dims* dims);
+
+/* Tree attention over a paged KV cache (one call: plan and run).  Layouts
+ * (device, contiguous):
+ *   q, out, lse, q_indptr, mn_indptr, tree_order   as for tree_attn
+ *   pages        [num_pages, 2, h_kv, 16, head_dim] dtype: plane 0 holds K,
+ *                plane 1 holds V, 16 kv slots per page
+ *   page_indptr  [B+1] int32: sequence b owns page_values[page_indptr[b] ..
+ *                page_indptr[b+1]-1], in kv order
+ *   page_values  [nnz_pages] int32 physical page indices (an index outside
+ *                [0, num_pages) reads zeros)
+ *   length_info  [B] int32, the number of slots used in each sequence's last
+ *                page (1..16 when the sequence owns a page); sequence b has
+ *                kv = (pages - 1) * 16 + length_info[b] rows, 0 without pages
+ * kv row r of sequence b is slot r % 16 of page page_values[page_indptr[b] +
+ * r / 16]; the tree mask, the q rows and the outputs are those of tree_attn
+ * with that kv length.  Slots past a sequence's kv length are never used (their
+ * contents may be anything, NaN included).  The pages assert that this kernel
+ * has no RoPE: rotary_mode must be 0 (else TA_ERR_UNSUPPORTED), and the pages'
+ * position arguments (k_rope_pos_offset, q_rope_position) are therefore not
+ * taken.  Inconsistent page tables (indptr not ending at nnz_pages, a
+ * length_info outside 1..16) are reported by tree_attn_device_status and
+ * nothing is computed.  q, pages and out must be 16-byte aligned; the
+ * workspace follows tree_attn's rules.  Asynchronous on stream. */
+ta_status tree_attn_paged(const void* q, const int32_t* q_indptr, const void* pages,
+                          const int32_t* page_indptr, const int32_t* page_values,
+                          const int32_t* length_info, const int32_t* mn_indptr,
+                          const int32_t* tree_order, void* out, float* lse, int32_t rotary_mode,
+                          float sm_scale, const ta_paged_dims* dims, void* workspace,
+                          size_t workspace_bytes, void* stream);
+
 /* Synchronises ``stream``, reads and clears the device status word that the
  * kernels of earlier calls left in ``workspace`` (TA_ERR_DEVICE_TIMEOUT if a
  * bounded wait expired, TA_ERR_CUDA on a CUDA error, else TA_OK). */

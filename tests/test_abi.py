@@ -140,3 +140,57 @@ def test_product_path_has_no_oracle_or_cpu_fallback():
             if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
                 src = open(os.path.join(root, f)).read()
                 assert "oracle" not in src.replace("oracle/", ""), f
+
+
+# --------------------------------------------------------------------------
+# paged KV cache entry point: host-side validation (no launch)
+# --------------------------------------------------------------------------
+
+def _pdims(**kw):
+    d = dict(batch_size=2, total_q=40, total_tree=40, h_q=8, h_kv=2, head_dim=128,
+             dtype=ta.TA_BF16, num_pages=12, nnz_pages=6)
+    d.update(kw)
+    return ta.PagedDims(**d)
+
+
+def _call_paged(lib, dims, **kw):
+    """tree_attn_paged with fake (never dereferenced) device pointers."""
+    fake = ctypes.c_void_p(0x10000)
+    a = dict(q=fake, q_indptr=fake, pages=fake, page_indptr=fake, page_values=fake,
+             length_info=fake, mn=fake, order=fake, out=fake, lse=fake, rotary=0, sm=0.125,
+             ws=ctypes.c_void_p(0x20000), wsb=1 << 30)
+    a.update(kw)
+    return lib.tree_attn_paged(a["q"], a["q_indptr"], a["pages"], a["page_indptr"],
+                               a["page_values"], a["length_info"], a["mn"], a["order"], a["out"],
+                               a["lse"], a["rotary"], a["sm"], ctypes.byref(dims), a["ws"],
+                               a["wsb"], None)
+
+
+def test_paged_workspace_size(lib):
+    n = ta.paged_workspace_size(_pdims())
+    assert n > 0 and n % 256 == 0
+    # the same layout as the contiguous call with nnz_pages * 16 kv rows
+    assert n == ta.workspace_size(_dims(total_q=40, total_kv=6 * 16, total_tree=40, h_q=8,
+                                        h_kv=2, head_dim=128, dtype=ta.TA_BF16))
+    assert ta.paged_workspace_size(_pdims(num_pages=0)) == 0
+    assert ta.paged_workspace_size(_pdims(head_dim=96)) == 0
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(rotary=1), ta.TA_ERR_UNSUPPORTED),            # the pages assert: no RoPE here
+    (dict(page_indptr=None), ta.TA_ERR_INVALID_ARGUMENT),
+    (dict(length_info=None), ta.TA_ERR_INVALID_ARGUMENT),
+    (dict(page_values=None), ta.TA_ERR_INVALID_ARGUMENT),
+    (dict(pages=None), ta.TA_ERR_INVALID_ARGUMENT),
+    (dict(pages=ctypes.c_void_p(0x10008)), ta.TA_ERR_INVALID_ARGUMENT),   # not 16-aligned
+    (dict(sm=float("nan")), ta.TA_ERR_INVALID_ARGUMENT),
+    (dict(wsb=16), ta.TA_ERR_INVALID_ARGUMENT),
+])
+def test_paged_host_validation_rejects_before_launch(lib, kw, expect):
+    assert _call_paged(lib, _pdims(), **kw) == expect
+
+
+def test_paged_bad_dims(lib):
+    assert _call_paged(lib, _pdims(num_pages=0)) == ta.TA_ERR_INVALID_ARGUMENT
+    assert _call_paged(lib, _pdims(head_dim=96)) == ta.TA_ERR_UNSUPPORTED
+    assert _call_paged(lib, _pdims(total_q=0)) == ta.TA_OK

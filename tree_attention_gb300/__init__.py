@@ -25,7 +25,7 @@ __all__ = [
     "TA_OK", "TA_ERR_INVALID_ARGUMENT", "TA_ERR_UNSUPPORTED", "TA_ERR_CUDA",
     "TA_ERR_DEVICE_TIMEOUT", "TreeAttnError", "Dims", "lib", "lib_path", "workspace_size",
     "tree_attn", "plan", "run", "device_status", "status_string", "mask_dense", "check_inputs",
-    "TreeAttention",
+    "TreeAttention", "PagedDims", "make_paged_dims", "paged_workspace_size", "tree_attn_paged",
 ]
 
 TA_OK = 0
@@ -52,6 +52,14 @@ class Dims(ctypes.Structure):
                 ("h_q", ctypes.c_int32), ("h_kv", ctypes.c_int32),
                 ("head_dim", ctypes.c_int32), ("dtype", ctypes.c_int),
                 ("rotary_mode", ctypes.c_int32)]
+
+
+class PagedDims(ctypes.Structure):
+    _fields_ = [("batch_size", ctypes.c_int32), ("total_q", ctypes.c_int32),
+                ("total_tree", ctypes.c_int32), ("h_q", ctypes.c_int32),
+                ("h_kv", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("dtype", ctypes.c_int), ("num_pages", ctypes.c_int32),
+                ("nnz_pages", ctypes.c_int32)]
 
 
 _lib = None
@@ -92,6 +100,12 @@ def lib() -> ctypes.CDLL:
     L.tree_attn_mask_dense.restype = ctypes.c_int
     L.tree_attn_check_inputs.argtypes = [i32p, i32p, i32p, i32p, i32p, ctypes.POINTER(Dims)]
     L.tree_attn_check_inputs.restype = ctypes.c_int
+    L.tree_attn_paged_workspace_size.argtypes = [ctypes.POINTER(PagedDims)]
+    L.tree_attn_paged_workspace_size.restype = sz
+    L.tree_attn_paged.argtypes = [vp, i32p, vp, i32p, i32p, i32p, i32p, i32p, vp, vp,
+                                  ctypes.c_int32, ctypes.c_float, ctypes.POINTER(PagedDims), vp,
+                                  sz, vp]
+    L.tree_attn_paged.restype = ctypes.c_int
     _lib = L
     return L
 
@@ -180,6 +194,44 @@ def tree_attn_noalloc(q, q_indptr, k, v, kv_indptr, q_rope_position, mn_indptr, 
                                  _stream_ptr(stream))
     if st != TA_OK:
         raise TreeAttnError(st, "tree_attn_noalloc")
+
+
+def make_paged_dims(q: torch.Tensor, pages: torch.Tensor, q_indptr: torch.Tensor,
+                    page_values: torch.Tensor, tree_order: torch.Tensor) -> PagedDims:
+    return PagedDims(batch_size=q_indptr.numel() - 1, total_q=q.shape[0],
+                     total_tree=tree_order.shape[0], h_q=q.shape[1], h_kv=pages.shape[2],
+                     head_dim=q.shape[2], dtype=_dtype_code(q.dtype), num_pages=pages.shape[0],
+                     nnz_pages=page_values.numel())
+
+
+def paged_workspace_size(dims: PagedDims) -> int:
+    return int(lib().tree_attn_paged_workspace_size(ctypes.byref(dims)))
+
+
+def tree_attn_paged(q, q_indptr, pages, page_indptr, page_values, length_info, mn_indptr,
+                    tree_order, out, lse, rotary_mode: int, sm_scale: float,
+                    workspace: torch.Tensor, stream=None) -> None:
+    """Enqueue tree attention over a paged KV cache (``pages [num_pages, 2,
+    h_kv, 16, d]``, page table ``page_indptr``/``page_values``, last-page
+    lengths ``length_info``); layouts as in ``include/tree_attn.h``."""
+    for name, t in (("q", q), ("pages", pages), ("out", out)):
+        _check_dev(name, t, q.dtype)
+    for name, t in (("q_indptr", q_indptr), ("page_indptr", page_indptr),
+                    ("page_values", page_values), ("length_info", length_info),
+                    ("mn_indptr", mn_indptr), ("tree_order", tree_order)):
+        _check_dev(name, t, torch.int32)
+    _check_dev("lse", lse, torch.float32)
+    _check_dev("workspace", workspace)
+    if pages.dim() != 5 or pages.shape[1] != 2 or pages.shape[3] != 16:
+        raise ValueError("pages must be [num_pages, 2, h_kv, 16, head_dim]")
+    dims = make_paged_dims(q, pages, q_indptr, page_values, tree_order)
+    st = lib().tree_attn_paged(_ptr(q), _ptr(q_indptr), _ptr(pages), _ptr(page_indptr),
+                               _ptr(page_values), _ptr(length_info), _ptr(mn_indptr),
+                               _ptr(tree_order), _ptr(out), _ptr(lse), int(rotary_mode),
+                               float(sm_scale), ctypes.byref(dims), _ptr(workspace),
+                               workspace.numel() * workspace.element_size(), _stream_ptr(stream))
+    if st != TA_OK:
+        raise TreeAttnError(st, "tree_attn_paged")
 
 
 def plan(q, q_indptr, k, kv_indptr, q_rope_position, mn_indptr, tree_order,

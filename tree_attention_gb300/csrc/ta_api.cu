@@ -84,6 +84,28 @@ bool make_map(CUtensorMap* m, const void* base, ta_dtype dt, int rows, int heads
   return r == CUDA_SUCCESS;
 }
 
+// 5-D tensor map over the paged cache [pages, 2, h_kv, 16, d] (d fastest)
+// with a {64, 16, 1, 1, 1} box (one page's 16 slots of one column block) and
+// 128-byte swizzle; an out-of-range page index reads zeros.
+bool make_pages_map(CUtensorMap* m, const void* base, ta_dtype dt, int num_pages, int h_kv,
+                    int d) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t gdim[5] = {(cuuint64_t)d, (cuuint64_t)ta::kPageSize, (cuuint64_t)h_kv, 2,
+                              (cuuint64_t)num_pages};
+  const cuuint64_t row = (cuuint64_t)d * 2;
+  const cuuint64_t gstride[4] = {row, row * ta::kPageSize, row * ta::kPageSize * h_kv,
+                                 row * ta::kPageSize * h_kv * 2};
+  const cuuint32_t box[5] = {64u, (cuuint32_t)ta::kPageSize, 1u, 1u, 1u};
+  const cuuint32_t estride[5] = {1u, 1u, 1u, 1u, 1u};
+  const CUtensorMapDataType t =
+      dt == TA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  const CUresult r = fn(m, t, 5, const_cast<void*>(base), gdim, gstride, box, estride,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 }  // namespace
 
 extern "C" {
@@ -243,11 +265,11 @@ ta_status launch_run_checked(const void* q, const void* k, const void* v, const 
   cudaError_t e;
   const bool bf16 = dims->dtype == TA_BF16;
   if (D == 64)
-    e = bf16 ? ta::launch_attn<64, true>(tm_q, tm_k, tm_v, ap, grid, st)
-             : ta::launch_attn<64, false>(tm_q, tm_k, tm_v, ap, grid, st);
+    e = bf16 ? ta::launch_attn<64, true, false>(tm_q, tm_k, tm_v, ap, grid, st)
+             : ta::launch_attn<64, false, false>(tm_q, tm_k, tm_v, ap, grid, st);
   else
-    e = bf16 ? ta::launch_attn<128, true>(tm_q, tm_k, tm_v, ap, grid, st)
-             : ta::launch_attn<128, false>(tm_q, tm_k, tm_v, ap, grid, st);
+    e = bf16 ? ta::launch_attn<128, true, false>(tm_q, tm_k, tm_v, ap, grid, st)
+             : ta::launch_attn<128, false, false>(tm_q, tm_k, tm_v, ap, grid, st);
   return e == cudaSuccess ? TA_OK : TA_ERR_CUDA;
 }
 
@@ -440,6 +462,145 @@ ta_status tree_attn_noalloc(const void* q, const int32_t* q_indptr, const void* 
   return tree_attn(q, q_indptr, k, v, kv_indptr, q_rope_position, mn_indptr, tree_order, out,
                    lse, rotary_mode, rope_scale, rope_theta, sm_scale, dims, ws,
                    kNoAllocScratchBytes, stream);
+}
+
+}  // extern "C"
+
+
+// ---------------------------------------------------------------------------
+// paged KV cache
+// ---------------------------------------------------------------------------
+namespace {
+
+bool paged_dims_valid(const ta_paged_dims* d) {
+  if (!d) return false;
+  if (d->batch_size < 1 || d->total_q < 0 || d->total_tree < 0) return false;
+  if (d->h_q < 1 || d->h_kv < 1 || d->h_q % d->h_kv != 0) return false;
+  if (d->dtype != TA_FP16 && d->dtype != TA_BF16) return false;
+  if (d->head_dim < 1 || d->num_pages < 1 || d->nnz_pages < 0) return false;
+  if ((int64_t)d->nnz_pages * ta::kPageSize > INT32_MAX) return false;
+  return true;
+}
+
+// The contiguous-layout dims whose workspace serves a paged call: the kv
+// rows of the batch are at most nnz_pages * 16.
+ta_dims as_dims(const ta_paged_dims* d) {
+  ta_dims x{};
+  x.batch_size = d->batch_size;
+  x.total_q = d->total_q;
+  x.total_kv = d->nnz_pages * ta::kPageSize;
+  x.total_tree = d->total_tree;
+  x.h_q = d->h_q;
+  x.h_kv = d->h_kv;
+  x.head_dim = d->head_dim;
+  x.dtype = d->dtype;
+  x.rotary_mode = 0;
+  return x;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t tree_attn_paged_workspace_size(const ta_paged_dims* dims) {
+  if (!paged_dims_valid(dims)) return 0;
+  const ta_dims d = as_dims(dims);
+  return tree_attn_workspace_size(&d);
+}
+
+ta_status tree_attn_paged(const void* q, const int32_t* q_indptr, const void* pages,
+                          const int32_t* page_indptr, const int32_t* page_values,
+                          const int32_t* length_info, const int32_t* mn_indptr,
+                          const int32_t* tree_order, void* out, float* lse, int32_t rotary_mode,
+                          float sm_scale, const ta_paged_dims* dims, void* workspace,
+                          size_t workspace_bytes, void* stream) {
+  if (!paged_dims_valid(dims)) return TA_ERR_INVALID_ARGUMENT;
+  if (rotary_mode != 0) return TA_ERR_UNSUPPORTED;   // as the pages assert for this kernel
+  const ta_dims d = as_dims(dims);
+  const ta_status sup = dims_supported(&d);
+  if (sup != TA_OK) return sup;
+  if (!q_indptr || !page_indptr || !length_info || !mn_indptr || !workspace || !pages)
+    return TA_ERR_INVALID_ARGUMENT;
+  if (dims->nnz_pages > 0 && !page_values) return TA_ERR_INVALID_ARGUMENT;
+  if (dims->total_tree > 0 && !tree_order) return TA_ERR_INVALID_ARGUMENT;
+  if (!aligned(workspace, 256) || !aligned(pages, 16)) return TA_ERR_INVALID_ARGUMENT;
+  const size_t need = tree_attn_workspace_size(&d);
+  if (need == 0) return TA_ERR_UNSUPPORTED;
+  if (workspace_bytes < need) return TA_ERR_INVALID_ARGUMENT;
+  if (dims->total_q > 0 && dims->nnz_pages == 0) return TA_ERR_INVALID_ARGUMENT;
+  ta_status s = check_run_args(q, pages, pages, out, lse, sm_scale, &d);
+  if (s != TA_OK) return s;
+  if (dims->total_q == 0) return TA_OK;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int g = d.h_q / d.h_kv;
+  const int R = ta::rows_per_item(g);
+  const WsLayout L = layout_of(&d);
+  const WsPtrs w = ws_ptrs(workspace, L);
+  const int nsm = sm_count();
+  if (nsm <= 0) return TA_ERR_CUDA;
+  // plan: kv lengths from the page table
+  ta::PlanParams pp{};
+  pp.q_indptr = q_indptr;
+  pp.kv_indptr = nullptr;
+  pp.mn_indptr = mn_indptr;
+  pp.tree_order = tree_order;
+  pp.rope_pos = nullptr;
+  pp.paged = 1;
+  pp.page_indptr = page_indptr;
+  pp.length_info = length_info;
+  pp.nnz_pages = dims->nnz_pages;
+  pp.batch = d.batch_size;
+  pp.g = g;
+  pp.R = R;
+  pp.h_kv = d.h_kv;
+  pp.head_dim = d.head_dim;
+  pp.total_q = d.total_q;
+  pp.total_kv = d.total_kv;
+  pp.total_tree = d.total_tree;
+  pp.rotary = 0;
+  pp.max_pairs = L.max_pairs;
+  pp.rope_scale = 1.f;
+  pp.rope_theta = 1.f;
+  for (int i = 0; i < 64; ++i) pp.rope_den[i] = 1.f;
+  pp.hdr = w.hdr;
+  pp.sorted = w.sorted;
+  pp.classes = w.classes;
+  pp.rope_cs = w.rope_cs;
+  if (ta::launch_plan(pp, (int)L.max_pairs, st) != cudaSuccess) return TA_ERR_CUDA;
+  // run: K and V tiles gathered page by page from the pool
+  CUtensorMap tm_q, tm_pages;
+  if (!make_map(&tm_q, q, d.dtype, d.total_q, d.h_q, d.head_dim, g, R) ||
+      !make_pages_map(&tm_pages, pages, d.dtype, dims->num_pages, d.h_kv, d.head_dim))
+    return TA_ERR_CUDA;
+  ta::AttnParams ap{};
+  ap.tree_order = tree_order;
+  ap.out = out;
+  ap.lse = lse;
+  ap.sorted = w.sorted;
+  ap.classes = w.classes;
+  ap.rope_cs = w.rope_cs;
+  ap.hdr = w.hdr;
+  ap.page_values = page_values;
+  ap.num_pages = dims->num_pages;
+  ap.h_q = d.h_q;
+  ap.h_kv = d.h_kv;
+  ap.g = g;
+  ap.R = R;
+  ap.rotary = 0;
+  ap.max_pairs = L.max_pairs;
+  ap.scale_log2 = sm_scale * 1.4426950408889634f;
+  ap.timeout_ns = kDeviceWaitLimitNs;
+  const int64_t max_items = L.max_pairs * d.h_kv;
+  const int grid = (int)(max_items < nsm ? max_items : nsm);
+  const bool bf16 = d.dtype == TA_BF16;
+  cudaError_t e;
+  if (d.head_dim == 64)
+    e = bf16 ? ta::launch_attn<64, true, true>(tm_q, tm_pages, tm_pages, ap, grid, st)
+             : ta::launch_attn<64, false, true>(tm_q, tm_pages, tm_pages, ap, grid, st);
+  else
+    e = bf16 ? ta::launch_attn<128, true, true>(tm_q, tm_pages, tm_pages, ap, grid, st)
+             : ta::launch_attn<128, false, true>(tm_q, tm_pages, tm_pages, ap, grid, st);
+  return e == cudaSuccess ? TA_OK : TA_ERR_CUDA;
 }
 
 }  // extern "C"

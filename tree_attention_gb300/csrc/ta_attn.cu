@@ -158,7 +158,7 @@ struct TileIter {
 // ---------------------------------------------------------------------------
 // producer warp (lane 0 issues; all lanes stage mask intervals)
 // ---------------------------------------------------------------------------
-template <int D>
+template <int D, bool PAGED>
 __device__ void run_producer(const Pipe& pp, const CUtensorMap* tm_q, const CUtensorMap* tm_k,
                              const CUtensorMap* tm_v, const AttnParams& p, int lane) {
   using C = Cfg<D>;
@@ -222,22 +222,45 @@ __device__ void run_producer(const Pipe& pp, const CUtensorMap* tm_q, const CUte
         const int stage = kv_it % kStages;
         const uint32_t empty_par = ((kv_it / kStages) & 1) ^ 1;
         const uint32_t bytes = (uint32_t)C::kKVBytes;
+        // paged cache: kv tile j is logical pages 4j .. 4j+3 of the sequence;
+        // lanes 0-3 look up their physical pages, a missing page (past the
+        // sequence's last) takes an out-of-range page index, read as zeros
+        int ph0 = 0, ph1 = 0, ph2 = 0, ph3 = 0;
+        if constexpr (PAGED) {
+          const int np = (r.kv + kPageSize - 1) / kPageSize;
+          const int lp = j * (kBlockN / kPageSize) + lane;
+          int phys = p.num_pages;
+          if (lane < kBlockN / kPageSize && lp < np) phys = __ldg(p.page_values + r.kv_base + lp);
+          ph0 = __shfl_sync(0xffffffffu, phys, 0);
+          ph1 = __shfl_sync(0xffffffffu, phys, 1);
+          ph2 = __shfl_sync(0xffffffffu, phys, 2);
+          ph3 = __shfl_sync(0xffffffffu, phys, 3);
+        }
+        // one K or V tile into ``dst`` (kv plane 0 = K, 1 = V of the paged cache)
+        auto load_tile = [&](uint8_t* dst, const CUtensorMap* map, uint64_t* bar, int plane) {
+#pragma unroll
+          for (int a = 0; a < C::kAtoms; ++a) {
+            if constexpr (PAGED) {
+              const int phs[4] = {ph0, ph1, ph2, ph3};
+#pragma unroll
+              for (int q = 0; q < kBlockN / kPageSize; ++q)
+                tma_load_5d(dst + a * C::kKVAtomBytes + q * kPageSize * 128, map, bar, a * 64, 0,
+                            kvh, plane, phs[q]);
+            } else {
+              tma_load_3d(dst + a * C::kKVAtomBytes, map, bar, a * 64, kvh, row0);
+            }
+          }
+        };
         if (!pp.warp_wait(B_K_EMPTY + stage, empty_par)) { aborted = true; break; }
         if (lane == 0) {
           mbar_arrive_expect_tx(&pp.bar[B_K_FULL + stage], bytes);
-#pragma unroll
-          for (int a = 0; a < C::kAtoms; ++a)
-            tma_load_3d(sK + stage * C::kKVBytes + a * C::kKVAtomBytes, tm_k,
-                        &pp.bar[B_K_FULL + stage], a * 64, kvh, row0);
+          load_tile(sK + stage * C::kKVBytes, tm_k, &pp.bar[B_K_FULL + stage], 0);
         }
         ++issued_k;
         if (!pp.warp_wait(B_V_EMPTY + stage, empty_par)) { aborted = true; break; }
         if (lane == 0) {
           mbar_arrive_expect_tx(&pp.bar[B_V_FULL + stage], bytes);
-#pragma unroll
-          for (int a = 0; a < C::kAtoms; ++a)
-            tma_load_3d(sV + stage * C::kKVBytes + a * C::kKVAtomBytes, tm_v,
-                        &pp.bar[B_V_FULL + stage], a * 64, kvh, row0);
+          load_tile(sV + stage * C::kKVBytes, tm_v, &pp.bar[B_V_FULL + stage], 1);
         }
         ++issued_v;
         // column intervals of a partial tile for the mask (FULL tiles need none)
@@ -461,7 +484,7 @@ __device__ void rope_q_rows(uint8_t* tile, const float2* __restrict__ cs, long l
   }
 }
 
-template <int D, bool BF16>
+template <int D, bool BF16, bool PAGED>
 __device__ void run_softmax(const Pipe& pp, const AttnParams& p, int sw, int lane) {
   using C = Cfg<D>;
   const int wq = sw;                          // TMEM lane quadrant (warp index mod 4)
@@ -611,6 +634,23 @@ __device__ void run_softmax(const Pipe& pp, const AttnParams& p, int sw, int lan
             tmem_st32(t_row + C::kTmemO + oc * 32, o);
           }
         }
+        if constexpr (PAGED) {
+          // the last page of a sequence may be partly filled: its remaining
+          // slots hold whatever the cache holds (not necessarily finite), so
+          // the V rows from the sequence's end to the next 16-row step of the
+          // PV are zeroed before the PV reads them (P is 0 there)
+          if (nvalid < kBlockN && (nvalid & 15)) {
+            if (!pp.warp_wait(B_V_FULL + stage, (gi / kStages) & 1)) return;
+            const int r0 = nvalid, nr = ((nvalid + 15) & ~15) - nvalid;
+            uint8_t* vt = pp.smem + C::kOffV + stage * C::kKVBytes;
+            for (int i = wq * 32 + lane; i < nr * 8 * C::kAtoms; i += 128) {
+              const int a = i / (nr * 8), rem = i % (nr * 8);
+              *reinterpret_cast<uint4*>(vt + a * C::kKVAtomBytes + (r0 + rem / 8) * 128 +
+                                        (rem % 8) * 16) = make_uint4(0u, 0u, 0u, 0u);
+            }
+            fence_proxy_async_smem();
+          }
+        }
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
@@ -686,7 +726,7 @@ __device__ void run_softmax(const Pipe& pp, const AttnParams& p, int sw, int lan
 }
 
 // ---------------------------------------------------------------------------
-template <int D, bool BF16>
+template <int D, bool BF16, bool PAGED>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const AttnParams p) {
@@ -752,12 +792,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   pdl_wait();
 
   if (pw == 0) {
-    run_producer<D>(pp, &tm_q, &tm_k, &tm_v, p, lane);
+    run_producer<D, PAGED>(pp, &tm_q, &tm_k, &tm_v, p, lane);
   } else if (pw == 1) {
     if (lane == 0) run_mma<D, BF16>(pp, p);
   } else {
     // softmax warp pw - 2 of this pipeline; its TMEM lane quadrant is warp % 4
-    run_softmax<D, BF16>(pp, p, warp & 3, lane);
+    run_softmax<D, BF16, PAGED>(pp, p, warp & 3, lane);
   }
   __syncwarp();
 
@@ -781,30 +821,31 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
-template <int D, bool BF16>
+template <int D, bool BF16, bool PAGED>
 cudaError_t launch_attn(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
                         const AttnParams& p, int grid, cudaStream_t stream) {
   using C = Cfg<D>;
   static_assert(C::kSmemAlloc <= 227 * 1024, "shared memory budget");
   static_assert(B_COUNT <= 32, "barrier area");
-  auto kern = attn_kernel<D, BF16>;
+  auto kern = attn_kernel<D, BF16, PAGED>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemAlloc);
   if (e != cudaSuccess) return e;
   return launch_pdl(kern, dim3(grid), dim3(kThreads), C::kSmemAlloc, stream, tm_q, tm_k, tm_v, p);
 }
 
-template cudaError_t launch_attn<64, false>(const CUtensorMap&, const CUtensorMap&,
-                                            const CUtensorMap&, const AttnParams&, int,
-                                            cudaStream_t);
-template cudaError_t launch_attn<64, true>(const CUtensorMap&, const CUtensorMap&,
-                                           const CUtensorMap&, const AttnParams&, int,
-                                           cudaStream_t);
-template cudaError_t launch_attn<128, false>(const CUtensorMap&, const CUtensorMap&,
-                                             const CUtensorMap&, const AttnParams&, int,
-                                             cudaStream_t);
-template cudaError_t launch_attn<128, true>(const CUtensorMap&, const CUtensorMap&,
-                                            const CUtensorMap&, const AttnParams&, int,
-                                            cudaStream_t);
+#define TA_INSTANTIATE(D, BF, PG)                                                       \
+  template cudaError_t launch_attn<D, BF, PG>(const CUtensorMap&, const CUtensorMap&, \
+                                              const CUtensorMap&, const AttnParams&, int, \
+                                              cudaStream_t);
+TA_INSTANTIATE(64, false, false)
+TA_INSTANTIATE(64, true, false)
+TA_INSTANTIATE(128, false, false)
+TA_INSTANTIATE(128, true, false)
+TA_INSTANTIATE(64, false, true)
+TA_INSTANTIATE(64, true, true)
+TA_INSTANTIATE(128, false, true)
+TA_INSTANTIATE(128, true, true)
+#undef TA_INSTANTIATE
 
 }  // namespace ta

@@ -38,6 +38,12 @@ struct PlanParams {
   const int32_t* mn_indptr;
   const int32_t* tree_order;
   const int32_t* rope_pos;  // may be null when rotary == 0
+  // paged KV cache (paged != 0): kv rows come from 16-slot pages; kv_indptr
+  // is unused, the kv length of sequence b is (pages - 1) * 16 + length_info[b]
+  int paged;
+  const int32_t* page_indptr;
+  const int32_t* length_info;
+  int nnz_pages;
   int batch, g, R, h_kv, head_dim, total_q, total_kv, total_tree, rotary;
   int64_t max_pairs;
   float rope_scale, rope_theta;
@@ -58,6 +64,8 @@ struct AttnParams {
   const uint8_t* classes;
   const float2* rope_cs;
   WsHeader* hdr;
+  const int32_t* page_values;   // paged KV cache: physical page of each (sequence, page)
+  int num_pages;                // pages in the pool (an out-of-range page reads zeros)
   int h_q, h_kv, g, R, rotary;
   int64_t max_pairs;  // capacity of the record tables in the workspace
   float scale_log2;   // sm_scale * log2(e)
@@ -79,7 +87,7 @@ cudaError_t launch_mask_dense(const int32_t* q_indptr, const int32_t* kv_indptr,
                               int total_q, int max_kv, uint8_t* vis, cudaStream_t stream);
 
 // Persistent tree-attention kernel.
-template <int D, bool BF16>
+template <int D, bool BF16, bool PAGED>
 cudaError_t launch_attn(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
                         const AttnParams& p, int grid, cudaStream_t stream);
 

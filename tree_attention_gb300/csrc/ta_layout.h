@@ -16,6 +16,7 @@ constexpr int kBlockM = 128;
 constexpr int kBlockN = 64;
 constexpr int kKvBoxRows = 64;   // kv rows per TMA box (one box per kv tile)
 constexpr int kMaxGroup = 128;   // largest supported h_q / h_kv
+constexpr int kPageSize = 16;    // kv slots per page of a paged KV cache
 
 // Tile classes computed by the plan kernel for each (q tile, kv tile).
 constexpr uint8_t kTileEmpty = 0;    // no (row, column) pair visible: skipped

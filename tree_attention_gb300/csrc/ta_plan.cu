@@ -89,6 +89,25 @@ __device__ __forceinline__ int lower_bound(const int* keys, int n, int x) {
   return lo;
 }
 
+// kv rows and kv base of sequence b: contiguous (kv_indptr) or paged (the
+// ``_get_kv_chunk_len`` of the page "_kernel_common.py" without a sliding
+// window: (pages - 1) * 16 + last_page_len, 0 without pages; the base is then
+// the sequence's first page-table entry)
+__device__ __forceinline__ int seq_kv_len(const PlanParams& p, int b) {
+  if (!p.paged) return p.kv_indptr[b + 1] - p.kv_indptr[b];
+  const int np = p.page_indptr[b + 1] - p.page_indptr[b];
+  return np > 0 ? (np - 1) * kPageSize + p.length_info[b] : 0;
+}
+__device__ __forceinline__ int seq_kv_base(const PlanParams& p, int b) {
+  return p.paged ? p.page_indptr[b] : p.kv_indptr[b];
+}
+// a paged sequence's own table entries must be consistent
+__device__ __forceinline__ bool seq_pages_bad(const PlanParams& p, int b) {
+  if (!p.paged) return false;
+  const int np = p.page_indptr[b + 1] - p.page_indptr[b];
+  return np < 0 || (np > 0 && (p.length_info[b] < 1 || p.length_info[b] > kPageSize));
+}
+
 __device__ __forceinline__ long long seg_bytes(int kv) {
   return ((kv + kBlockN - 1) / kBlockN + 15) / 16 * 16;
 }
@@ -128,9 +147,10 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanParams p) 
   }
   for (int i = tid; i < kCostBuckets; i += kPlanThreads) s_hist[i] = 0;
   if (tid == 0) {
-    s_bad = (p.q_indptr[0] != 0 || p.kv_indptr[0] != 0 || p.mn_indptr[0] != 0 ||
-             p.q_indptr[B] != p.total_q || p.kv_indptr[B] != p.total_kv ||
-             p.mn_indptr[B] != p.total_tree);
+    const bool kv_bad = p.paged ? (p.page_indptr[0] != 0 || p.page_indptr[B] != p.nnz_pages)
+                                : (p.kv_indptr[0] != 0 || p.kv_indptr[B] != p.total_kv);
+    s_bad = (p.q_indptr[0] != 0 || p.mn_indptr[0] != 0 || kv_bad ||
+             p.q_indptr[B] != p.total_q || p.mn_indptr[B] != p.total_tree);
     s_count = 0;
     s_rank = 0;
   }
@@ -145,9 +165,9 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanParams p) 
   int bad = 0;
   for (int b = b_lo; b < b_hi; ++b) {
     const int qo = p.q_indptr[b + 1] - p.q_indptr[b];
-    const int kv = p.kv_indptr[b + 1] - p.kv_indptr[b];
+    const int kv = seq_kv_len(p, b);
     const int tl = p.mn_indptr[b + 1] - p.mn_indptr[b];
-    if (qo < 0 || tl < qo || kv < tl) {
+    if (qo < 0 || tl < qo || kv < tl || seq_pages_bad(p, b)) {
       bad = 1;
       continue;
     }
@@ -194,7 +214,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanParams p) 
     long long tcum = ex_tiles, scum = ex_seg;
     for (int b = b_lo; b < b_hi; ++b) {
       const int qo = p.q_indptr[b + 1] - p.q_indptr[b];
-      const int kv = p.kv_indptr[b + 1] - p.kv_indptr[b];
+      const int kv = seq_kv_len(p, b);
       const long long tiles = (qo + R - 1) / R;
       if (pair < tcum + tiles) {
         const int t = (int)(pair - tcum);
@@ -215,7 +235,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanParams p) 
     int cnt = 0;
     for (int b = b_lo; b < min(b_hi, pb + 1); ++b) {
       const int qo = p.q_indptr[b + 1] - p.q_indptr[b];
-      const int kv = p.kv_indptr[b + 1] - p.kv_indptr[b];
+      const int kv = seq_kv_len(p, b);
       const int tiles = (qo + R - 1) / R;
       const int t_end = b < pb ? tiles : pt;
       for (int t = 0; t < t_end; ++t) cnt += pair_cost(qo, kv, R, t) == pc;
@@ -231,8 +251,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanParams p) 
     const long long pos = (long long)s_hist[s_pair_cost] + s_rank;
     const int q0 = p.q_indptr[b];
     const int qo = p.q_indptr[b + 1] - q0;
-    const int kv_base = p.kv_indptr[b];
-    const int kv = p.kv_indptr[b + 1] - kv_base;
+    const int kv_base = seq_kv_base(p, b);
+    const int kv = seq_kv_len(p, b);
     const int tree_base = p.mn_indptr[b];
     const int tl = p.mn_indptr[b + 1] - tree_base;
     const int ts = kv - tl;
