@@ -434,6 +434,139 @@ def run_gb300(args):
     return 0
 
 
+def run_gb300_paged(args):
+    """The paged-KV path (``tree_attn_paged``) on the named workload's shapes,
+    its K/V moved into 16-slot pages in a scattered order.  The pages' paged
+    kernel has no RoPE, so the workload runs with RoPE off.  ``tree_attn_paged``
+    is one call (plan + attention kernel); the roofline covers that call."""
+    import dataclasses
+    import tree_attention_gb300 as ta
+    from tree_attention_gb300 import build as ta_build
+
+    rank, local, world = dist_info()
+    init_dist(world, "nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    ta_build.build()
+    ta.lib()
+    w = dataclasses.replace(wl.config(WORKLOADS[args.workload]), rotary_mode=0)
+    flops = wl.algorithmic_flops(w)
+    nbytes = wl.algorithmic_bytes(w)
+    pk = wl.paged_from(w, seed=17, fill=0.0)
+
+    def i32(a):
+        return torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32))
+
+    host = {"q": w.q.contiguous(), "pages": pk.pages.contiguous(), "q_indptr": i32(w.q_indptr),
+            "page_indptr": i32(pk.page_indptr), "page_values": i32(pk.page_values),
+            "length_info": i32(pk.last_page_len), "mn_indptr": i32(w.mn_indptr),
+            "tree_order": i32(w.tree_order.reshape(-1, 2))}
+    sb = sum(t.numel() * t.element_size() for t in host.values()) + w.q.numel() * 2
+    n_sets = args.sets or max(1, min(16, math.ceil(2.2 * L2_BYTES / sb)))
+    l2_note = (f"rotating {n_sets} input/output sets ({n_sets * sb / 1e6:.0f} MB > 2x L2)"
+               if n_sets > 1 else f"inputs larger than L2 ({sb / 1e6:.0f} MB)")
+    sets = []
+    for _ in range(n_sets):
+        d = {k: v.to(dev) for k, v in host.items()}
+        d["out"] = torch.empty_like(d["q"])
+        d["lse"] = torch.empty(d["q"].shape[:2], dtype=torch.float32, device=dev)
+        dims = ta.make_paged_dims(d["q"], d["pages"], d["q_indptr"], d["page_values"],
+                                  d["tree_order"])
+        d["ws"] = torch.zeros(ta.paged_workspace_size(dims), dtype=torch.uint8, device=dev)
+        sets.append(d)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(d):
+        ta.tree_attn_paged(d["q"], d["q_indptr"], d["pages"], d["page_indptr"], d["page_values"],
+                           d["length_info"], d["mn_indptr"], d["tree_order"], d["out"], d["lse"],
+                           0, w.sm_scale, d["ws"], stream)
+
+    for i in range(args.warmup):
+        step(sets[i % n_sets])
+    torch.cuda.synchronize(dev)
+    K = args.steps
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    t_start.record(stream)
+    for i in range(K):
+        step(sets[i % n_sets])
+    t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    clk = clocks.stop()
+    max_ms = max_over_ranks(t_start.elapsed_time(t_end), world, dev)
+    for d in sets:
+        st = ta.device_status(d["ws"], stream)
+        if st != ta.TA_OK:
+            raise RuntimeError(f"device status after timing: {ta.status_string(st)}")
+
+    # end to end with host buffers: inputs in, out and lse back, every step
+    hp = {k: v.pin_memory() for k, v in host.items()}
+    host_out = torch.empty(w.q.shape, dtype=w.q.dtype).pin_memory()
+    host_lse = torch.empty(w.q.shape[:2], dtype=torch.float32).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in hp.values())
+    d2h = host_out.numel() * host_out.element_size() + host_lse.numel() * 4
+
+    def e2e_step(d):
+        for k in hp:
+            d[k].copy_(hp[k], non_blocking=True)
+        step(d)
+        host_out.copy_(d["out"], non_blocking=True)
+        host_lse.copy_(d["lse"], non_blocking=True)
+
+    for i in range(min(args.warmup, 3)):
+        e2e_step(sets[i % n_sets])
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(K):
+        e2e_step(sets[i % n_sets])
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
+
+    peaks, peak_src = measured_peaks()
+    call_s = max_ms / K / 1e3
+    if nbytes / (peaks["hbm_gbs"] * 1e9) >= flops / (peaks["bf16_tflops"] * 1e12):
+        roof = {"bound": "hbm", "achieved": nbytes / call_s / 1e9, "peak": peaks["hbm_gbs"],
+                "unit": "GB/s"}
+    else:
+        roof = {"bound": "tensor", "achieved": flops / call_s / 1e12,
+                "peak": peaks["bf16_tflops"], "unit": "TFLOP/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["traffic"] = None
+    roof["peak_source"] = peak_src
+    roof["kernel"] = "tree_attn_paged call (plan kernel + paged attention kernel)"
+    roof["kernel_ms"] = max_ms / K
+    cfg = _config_dict(w, l2_note)
+    cfg.update({"paged": True, "page_size": wl.PAGE_SIZE, "num_pages": int(pk.pages.shape[0]),
+                "note": "the pages' paged kernel has no RoPE: run with rotary off"})
+    line = {
+        "metric": METRIC,
+        "value": weak_scaling_value(flops * K, world, max_ms / 1e3) / 1e12,
+        "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": max_ms / K, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": w.dtype, "data": "synthetic", "config": cfg,
+        "tokens_per_s": weak_scaling_value(w.total_q * K, world, max_ms / 1e3),
+        "roofline": roof,
+        "e2e": {"value": weak_scaling_value(flops * K, world, e2e_ms / 1e3) / 1e12, "unit": UNIT,
+                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
+        "gpu_launches": 2 * K,   # per step: plan kernel, paged attention kernel
+        "clocks": clk,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -443,10 +576,14 @@ def main(argv=None):
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--sets", type=int, default=0, help="input/output buffer sets to rotate")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--paged", action="store_true",
+                    help="time the paged-KV path (tree_attn_paged) on the workload's shapes")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)   # at least three untimed warm-up steps
     if args.impl == "reference":
         return run_reference(args)
+    if args.paged:
+        return run_gb300_paged(args)
     return run_gb300(args)
 
 
