@@ -212,8 +212,10 @@ ta_status launch_plan_checked(const int32_t* q_indptr, const int32_t* kv_indptr,
   pp.sorted = w.sorted;
   pp.classes = w.classes;
   pp.rope_cs = w.rope_cs;
+  // with RoPE, enough CTAs (6 per SM) that the latency-bound cos/sin table
+  // is spread over many warps
   int plan_grid = (int)L.max_pairs;
-  if (rotary_mode == 1 && plan_grid < 2 * nsm) plan_grid = 2 * nsm;
+  if (rotary_mode == 1 && plan_grid < 6 * nsm) plan_grid = 6 * nsm;
   return ta::launch_plan(pp, plan_grid, st) == cudaSuccess ? TA_OK : TA_ERR_CUDA;
 }
 

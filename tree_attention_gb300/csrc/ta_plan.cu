@@ -147,14 +147,20 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanParams p) 
   }
   for (int i = tid; i < kCostBuckets; i += kPlanThreads) s_hist[i] = 0;
   if (tid == 0) {
-    const bool kv_bad = p.paged ? (p.page_indptr[0] != 0 || p.page_indptr[B] != p.nnz_pages)
-                                : (p.kv_indptr[0] != 0 || p.kv_indptr[B] != p.total_kv);
-    s_bad = (p.q_indptr[0] != 0 || p.mn_indptr[0] != 0 || kv_bad ||
-             p.q_indptr[B] != p.total_q || p.mn_indptr[B] != p.total_tree);
+    s_bad = 0;
     s_count = 0;
     s_rank = 0;
   }
   __syncthreads();
+  // the ends of the index arrays, read by the last thread alongside the
+  // sequences' entries below (one round trip for both)
+  if (tid == kPlanThreads - 1) {
+    const bool kv_bad = p.paged ? (p.page_indptr[0] != 0 || p.page_indptr[B] != p.nnz_pages)
+                                : (p.kv_indptr[0] != 0 || p.kv_indptr[B] != p.total_kv);
+    if (p.q_indptr[0] != 0 || p.mn_indptr[0] != 0 || kv_bad || p.q_indptr[B] != p.total_q ||
+        p.mn_indptr[B] != p.total_tree)
+      atomicOr(&s_bad, 1);
+  }
 
   // ---- 1. the (sequence, q tile) pairs: every CTA walks the whole batch
   // (the ``advance_tile_batch`` walk of the page "_kernel_common.py", done up
@@ -230,6 +236,18 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanParams p) 
   }
   __syncthreads();
   const bool has_pair = ok && pair < total_tiles;
+  // the pair's q rows' enter indices, loaded now so that the round trip
+  // overlaps the ranking below
+  int key = INT_MAX, nrows = 0;
+  if (has_pair && tid < kGroup) {
+    const int b = s_pair_b;
+    const int qo = p.q_indptr[b + 1] - p.q_indptr[b];
+    const int tree_base = p.mn_indptr[b];
+    const int tl = p.mn_indptr[b + 1] - tree_base;
+    const int r0 = s_pair_t * R;
+    nrows = min(R, qo - r0);
+    if (tid < nrows) key = p.tree_order[2 * (tree_base + r0 + tid + tl - qo)];
+  }
   if (has_pair) {
     const int pb = s_pair_b, pt = s_pair_t, pc = s_pair_cost;
     int cnt = 0;
@@ -257,25 +275,40 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanParams p) 
     const int tl = p.mn_indptr[b + 1] - tree_base;
     const int ts = kv - tl;
     const int r0 = t * R;
-    const int nrows = min(R, qo - r0);
-    s_keys[tid] = tid < nrows ? p.tree_order[2 * (tree_base + r0 + tid + tl - qo)] : INT_MAX;
-    group_sync(kBarA);
     // exact classification from the DFS intervals of ``_check_tree_order``
     // (page "tree_attn.py"): the rows' enter indices are sorted (bitonic, one
     // key per thread) and, for each kv column, two binary searches count the
     // rows inside the column's [enter, exit) interval
-    for (int k = 2; k <= kBlockM; k <<= 1) {
-      for (int j = k >> 1; j > 0; j >>= 1) {
-        const int ixj = tid ^ j;
-        if (ixj > tid) {
-          const int a = s_keys[tid], c = s_keys[ixj];
-          const bool up = (tid & k) == 0;
-          if ((a > c) == up) {
-            s_keys[tid] = c;
-            s_keys[ixj] = a;
+    if (nrows <= 32) {
+      // one warp, shuffles only
+      if (tid < 32) {
+        int x = key;
+        for (int k = 2; k <= 32; k <<= 1) {
+          for (int j = k >> 1; j > 0; j >>= 1) {
+            const int y = __shfl_xor_sync(0xffffffffu, x, j);
+            const bool keep_min = ((tid & j) == 0) == ((tid & k) == 0);
+            x = keep_min ? min(x, y) : max(x, y);
           }
         }
-        group_sync(kBarA);
+        s_keys[tid] = x;
+      }
+      group_sync(kBarA);
+    } else {
+      s_keys[tid] = key;
+      group_sync(kBarA);
+      for (int k = 2; k <= kBlockM; k <<= 1) {
+        for (int j = k >> 1; j > 0; j >>= 1) {
+          const int ixj = tid ^ j;
+          if (ixj > tid) {
+            const int a = s_keys[tid], c = s_keys[ixj];
+            const bool up = (tid & k) == 0;
+            if ((a > c) == up) {
+              s_keys[tid] = c;
+              s_keys[ixj] = a;
+            }
+          }
+          group_sync(kBarA);
+        }
       }
     }
     const int kvt = (kv + kBlockN - 1) / kBlockN;
