@@ -13,5 +13,5 @@ rotary embedding of ``_rope`` from the page "_kernel_common.py"
 """
 from .tree_attn_ref import (  # noqa: F401
     rope_inv_freq_denominators, rope_cos_sin, apply_rope, visibility, tree_attention,
-    tree_attention_workload, paged_kv_lengths, tree_attention_paged, PAGE_SIZE,
+    tree_attention_workload, paged_kv_lengths, tree_attention_paged, PAGE_SIZE, merge_states,
 )

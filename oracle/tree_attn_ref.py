@@ -25,6 +25,9 @@ Functions and the passages they restate:
                          output the softmax-weighted sum of v and the
                          log-sum-exp in base 2 (``m + log2(d)`` with scores
                          pre-multiplied by log2(e)).
+* ``merge_states``    -- combining attention states over disjoint kv sets
+                         through their base-2 log-sum-exps (the ``lse_store``
+                         epilogue of page "tree_attn.py" defines the lse).
 * ``paged_kv_lengths``,
   ``tree_attention_paged`` -- ``_get_kv_chunk_len`` (page "_kernel_common.py")
                          and ``tree_attn_with_paged_kv_cache_cpu`` (page
@@ -291,3 +294,29 @@ def tree_attention_workload(w, seqs: Optional[Iterable[int]] = None) -> Tuple[np
     return tree_attention(w.q, w.q_indptr, w.k, w.v, w.kv_indptr, w.rope_position,
                           w.mn_indptr, w.tree_order, w.rotary_mode, w.rope_scale,
                           w.rope_theta, w.sm_scale, seqs=seqs)
+
+
+# --------------------------------------------------------------------------
+# merging partial attention states (split-KV)
+# --------------------------------------------------------------------------
+
+def merge_states(outs, lses) -> Tuple[np.ndarray, np.ndarray]:
+    """Combines attention states over disjoint sets of kv columns into the
+    state over their union.  ``outs [n, ..., d]`` are the normalised partial
+    outputs, ``lses [n, ...]`` their base-2 log-sum-exps (the ``m + log2(d)``
+    of ``lse_store``, page "tree_attn.py", which is what makes partial
+    attentions mergeable): ``lse = log2(sum_i 2^lse_i)`` and ``out = sum_i
+    2^(lse_i - lse) * out_i``.  Parts with ``lse = -inf`` (nothing visible)
+    contribute nothing; if every part has ``-inf``, ``out = 0`` and
+    ``lse = -inf``.  float64."""
+    outs = np.asarray(outs, dtype=np.float64)
+    lses = np.asarray(lses, dtype=np.float64)
+    m = np.max(lses, axis=0)
+    any_fin = np.isfinite(m)
+    m0 = np.where(any_fin, m, 0.0)
+    w = np.where(np.isfinite(lses), np.exp2(lses - m0[None]), 0.0)        # [n, ...]
+    z = np.sum(w, axis=0)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        lse = np.where(any_fin, m0 + np.log2(z), -np.inf)
+        out = np.where(any_fin[..., None], np.sum(w[..., None] * outs, axis=0) / z[..., None], 0.0)
+    return out, lse

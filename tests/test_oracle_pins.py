@@ -470,3 +470,62 @@ def test_paged_rejects_rope():
     with pytest.raises(ValueError):
         oracle.tree_attention_paged(w.q, w.q_indptr, pk.pages, pk.page_indptr, pk.page_values,
                                     pk.last_page_len, w.mn_indptr, w.tree_order, 1, w.sm_scale)
+
+
+# --------------------------------------------------------------------------
+# merging partial attention states (split-KV)
+# --------------------------------------------------------------------------
+
+def _masked_oracle(w, keep):
+    """The oracle restricted to the kv columns where ``keep(b, c)`` holds:
+    the same computation with the other columns' v and scores removed, done
+    here by replacing the tree visibility (a plain boolean restriction)."""
+    real = oracle.tree_attn_ref.visibility
+
+    def restricted(q_indptr, kv_indptr, mn_indptr, order, b):
+        vis = real(q_indptr, kv_indptr, mn_indptr, order, b)
+        cols = np.arange(vis.shape[1])
+        return vis & keep(b, cols)[None, :]
+
+    oracle.tree_attn_ref.visibility = restricted
+    try:
+        return oracle.tree_attention_workload(w)
+    finally:
+        oracle.tree_attn_ref.visibility = real
+
+
+@pytest.mark.parametrize("parts", [2, 3, 5])
+def test_merge_of_disjoint_column_sets_equals_the_whole(parts):
+    rng = np.random.default_rng(parts)
+    w = wl.build_workload("m", [wl.random_tree(30, rng), wl.chain_tree(12)], h_q=4, h_kv=2,
+                          head_dim=16, dtype="fp16", tensor_seed=parts, prefix_lens=[50, 7])
+    o_all, l_all = oracle.tree_attention_workload(w)
+    # columns dealt to parts in a scrambled pattern (not contiguous ranges)
+    lab = [rng.integers(0, parts, size=int(w.kv_indptr[b + 1] - w.kv_indptr[b]))
+           for b in range(w.batch_size)]
+    outs, lses = [], []
+    for i in range(parts):
+        o, l = _masked_oracle(w, lambda b, c, i=i: lab[b][c] == i)
+        outs.append(o)
+        lses.append(l)
+    o_m, l_m = oracle.merge_states(outs, lses)
+    assert np.allclose(o_m, o_all, rtol=0, atol=1e-12)
+    fin = np.isfinite(l_all)
+    assert np.array_equal(fin, np.isfinite(l_m))
+    assert np.allclose(l_m[fin], l_all[fin], rtol=0, atol=1e-12)
+
+
+def test_merge_closed_forms():
+    o1 = np.array([[1.0, 2.0]]); o2 = np.array([[3.0, 6.0]])
+    # equal lse: the average; lse grows by one (base 2)
+    o, l = oracle.merge_states([o1, o2], [np.array([0.5]), np.array([0.5])])
+    assert np.allclose(o, [[2.0, 4.0]]) and np.allclose(l, [1.5])
+    # a part with nothing visible contributes nothing
+    o, l = oracle.merge_states([o1, o2], [np.array([3.0]), np.array([-np.inf])])
+    assert np.allclose(o, o1) and np.allclose(l, [3.0])
+    # nothing visible anywhere
+    o, l = oracle.merge_states([o1, o2], [np.array([-np.inf]), np.array([-np.inf])])
+    assert np.all(o == 0) and np.all(np.isneginf(l))
+    # weights 2^lse: lse 1 and 0 -> weights 2/3 and 1/3
+    o, l = oracle.merge_states([o1, o2], [np.array([1.0]), np.array([0.0])])
+    assert np.allclose(o, (2 * o1 + o2) / 3) and np.allclose(l, [np.log2(3.0)])
