@@ -38,6 +38,15 @@ import workloads as wl  # noqa: E402
 METRIC = "tree-attn TFLOP/s (unmasked pairs) + % of roofline, 1 GB300"
 UNIT = "TFLOP/s"
 WORKLOADS = {name: i + 1 for i, name in enumerate(wl.CONFIG_NAMES)}
+# beyond the five workloads: few sequences with a 32768-token prefix (the case
+# split-KV is for)
+EXTRA_WORKLOADS = {"long-prefix": lambda: wl.long_prefix()}
+
+
+def make_workload(name: str):
+    if name in WORKLOADS:
+        return wl.config(WORKLOADS[name])
+    return EXTRA_WORKLOADS[name]()
 L2_BYTES = 129 * 2 ** 20
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
@@ -235,7 +244,7 @@ def run_reference(args):
     rank, _, world = dist_info()
     if rank != 0:
         return 0
-    w = wl.config(WORKLOADS[args.workload])
+    w = make_workload(args.workload)
     per_step_budget = max(0.5, 150.0 / (args.steps + args.warmup))
     seqs = oracle_sample(w, per_step_budget)
     for _ in range(args.warmup):
@@ -280,7 +289,7 @@ def run_gb300(args):
     dev = torch.device("cuda", local)
     ta_build.build()
     ta.lib()
-    w = wl.config(WORKLOADS[args.workload])
+    w = make_workload(args.workload)
     flops = wl.algorithmic_flops(w)
     nbytes = wl.algorithmic_bytes(w)
     sb = set_bytes(w)
@@ -449,7 +458,7 @@ def run_gb300_paged(args):
     dev = torch.device("cuda", local)
     ta_build.build()
     ta.lib()
-    w = dataclasses.replace(wl.config(WORKLOADS[args.workload]), rotary_mode=0)
+    w = dataclasses.replace(make_workload(args.workload), rotary_mode=0)
     flops = wl.algorithmic_flops(w)
     nbytes = wl.algorithmic_bytes(w)
     pk = wl.paged_from(w, seed=17, fill=0.0)
@@ -567,23 +576,162 @@ def run_gb300_paged(args):
     return 0
 
 
+def run_gb300_split(args):
+    """The split-KV path (``tree_attn_split``: plan, key rotation, attention
+    over kv chunks, merge) on the named workload, with the unsplit
+    ``tree_attn`` timed on the same buffers in the same run for comparison.
+    The roofline covers the whole split call."""
+    import tree_attention_gb300 as ta
+    from tree_attention_gb300 import build as ta_build
+
+    rank, local, world = dist_info()
+    init_dist(world, "nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    ta_build.build()
+    ta.lib()
+    w = make_workload(args.workload)
+    flops = wl.algorithmic_flops(w)
+    nbytes = wl.algorithmic_bytes(w)
+    sb = set_bytes(w)
+    n_sets = args.sets or max(1, min(16, math.ceil(2.2 * L2_BYTES / sb)))
+    l2_note = (f"rotating {n_sets} input/output sets ({n_sets * sb / 1e6:.0f} MB > 2x L2)"
+               if n_sets > 1 else f"inputs larger than L2 ({sb / 1e6:.0f} MB)")
+    base = wl.device_inputs(w, dev)
+    mc, ct = args.max_chunks, args.chunk_tiles
+    sets = []
+    for i in range(n_sets):
+        d = {k: (v.clone() if v is not None else None) for k, v in base.items()}
+        d["out"] = torch.empty_like(d["q"])
+        d["lse"] = torch.empty(d["q"].shape[:2], dtype=torch.float32, device=dev)
+        dims = ta.make_dims(d["q"], d["k"], d["q_indptr"], d["tree_order"], w.rotary_mode)
+        d["ws"] = torch.zeros(ta.split_workspace_size(dims, mc), dtype=torch.uint8, device=dev)
+        d["ws1"] = torch.zeros(ta.workspace_size(dims), dtype=torch.uint8, device=dev)
+        sets.append(d)
+    stream = torch.cuda.current_stream(dev)
+    keys_in = ["q", "k", "v", "q_indptr", "kv_indptr", "mn_indptr", "tree_order",
+               "q_rope_position"]
+
+    def step(d):
+        ta.tree_attn_split(d["q"], d["q_indptr"], d["k"], d["v"], d["kv_indptr"],
+                           d["q_rope_position"], d["mn_indptr"], d["tree_order"], d["out"],
+                           d["lse"], w.rotary_mode, w.rope_scale, w.rope_theta, w.sm_scale, mc,
+                           ct, d["ws"], stream)
+
+    def step_unsplit(d):
+        ta.tree_attn(d["q"], d["q_indptr"], d["k"], d["v"], d["kv_indptr"], d["q_rope_position"],
+                     d["mn_indptr"], d["tree_order"], d["out"], d["lse"], w.rotary_mode,
+                     w.rope_scale, w.rope_theta, w.sm_scale, d["ws1"], stream)
+
+    K = args.steps
+
+    def timed(fn):
+        for i in range(args.warmup):
+            fn(sets[i % n_sets])
+        torch.cuda.synchronize(dev)
+        barrier(world)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for i in range(K):
+            fn(sets[i % n_sets])
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier(world)
+        return max_over_ranks(a.elapsed_time(b), world, dev)
+
+    unsplit_ms = timed(step_unsplit)
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    max_ms = timed(step)
+    clk = clocks.stop()
+    for d in sets:
+        for key in ("ws", "ws1"):
+            st = ta.device_status(d[key], stream)
+            if st != ta.TA_OK:
+                raise RuntimeError(f"device status after timing: {ta.status_string(st)}")
+
+    # end to end through the public call with host buffers
+    host = {k: (base[k].cpu().pin_memory() if base[k] is not None else None) for k in keys_in}
+    host_out = torch.empty(base["q"].shape, dtype=base["q"].dtype).pin_memory()
+    host_lse = torch.empty(base["q"].shape[:2], dtype=torch.float32).pin_memory()
+    h2d = sum(host[k].numel() * host[k].element_size() for k in keys_in if host[k] is not None)
+    d2h = host_out.numel() * host_out.element_size() + host_lse.numel() * 4
+
+    def e2e_step(d):
+        for k in keys_in:
+            if host[k] is not None:
+                d[k].copy_(host[k], non_blocking=True)
+        step(d)
+        host_out.copy_(d["out"], non_blocking=True)
+        host_lse.copy_(d["lse"], non_blocking=True)
+
+    e2e_ms = timed(e2e_step)
+
+    peaks, peak_src = measured_peaks()
+    call_s = max_ms / K / 1e3
+    if nbytes / (peaks["hbm_gbs"] * 1e9) >= flops / (peaks["bf16_tflops"] * 1e12):
+        roof = {"bound": "hbm", "achieved": nbytes / call_s / 1e9, "peak": peaks["hbm_gbs"],
+                "unit": "GB/s"}
+    else:
+        roof = {"bound": "tensor", "achieved": flops / call_s / 1e12,
+                "peak": peaks["bf16_tflops"], "unit": "TFLOP/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["traffic"] = None
+    roof["peak_source"] = peak_src
+    roof["kernel"] = ("tree_attn_split call (plan, key rotation, attention over kv chunks, "
+                      "merge)")
+    roof["kernel_ms"] = max_ms / K
+    roof["t_roof_8tbs_us"] = max(nbytes / 8e12, flops / (peaks["bf16_tflops"] * 1e12)) * 1e6
+    cfg = _config_dict(w, l2_note)
+    cfg.update({"split_kv": True, "max_chunks": mc, "chunk_tiles": ct or "auto"})
+    line = {
+        "metric": METRIC,
+        "value": weak_scaling_value(flops * K, world, max_ms / 1e3) / 1e12,
+        "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": max_ms / K, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": w.dtype, "data": "synthetic", "config": cfg,
+        "tokens_per_s": weak_scaling_value(w.total_q * K, world, max_ms / 1e3),
+        "unsplit_ms_per_step": unsplit_ms / K,
+        "roofline": roof,
+        "e2e": {"value": weak_scaling_value(flops * K, world, e2e_ms / 1e3) / 1e12, "unit": UNIT,
+                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
+        # per step: plan kernel, key-rotation kernel (RoPE only), attention kernel, merge kernel
+        "gpu_launches": (4 if w.rotary_mode == 1 else 3) * K,
+        "clocks": clk,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=10)
-    ap.add_argument("--workload", default="spec-decode", choices=list(WORKLOADS))
+    ap.add_argument("--workload", default="spec-decode",
+                    choices=list(WORKLOADS) + list(EXTRA_WORKLOADS))
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--sets", type=int, default=0, help="input/output buffer sets to rotate")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--paged", action="store_true",
                     help="time the paged-KV path (tree_attn_paged) on the workload's shapes")
+    ap.add_argument("--split", action="store_true",
+                    help="time the split-KV path (tree_attn_split), the unsplit call beside it")
+    ap.add_argument("--max-chunks", type=int, default=16, help="split-KV: chunks per pair, max")
+    ap.add_argument("--chunk-tiles", type=int, default=0,
+                    help="split-KV: kv tiles per chunk (0: chosen by the plan)")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)   # at least three untimed warm-up steps
     if args.impl == "reference":
         return run_reference(args)
     if args.paged:
         return run_gb300_paged(args)
+    if args.split:
+        return run_gb300_split(args)
     return run_gb300(args)
 
 

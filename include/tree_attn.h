@@ -224,6 +224,59 @@ ta_status tree_attn_paged(const void* q, const int32_t* q_indptr, const void* pa
                           float sm_scale, const ta_paged_dims* dims, void* workspace,
                           size_t workspace_bytes, void* stream);
 
+/* ---- Split-KV ------------------------------------------------------------
+ * The same tree attention with the kv tiles of long (sequence, q tile) pairs
+ * cut into chunks that run as separate work items, so that a batch of few
+ * but long sequences (a long shared prefix before a small draft tree) still
+ * covers every SM.  The pages have no split-KV; it rests on the base-2 LSE
+ * their ``lse_store`` epilogue emits (page "tree_attn.py"), which is what
+ * merges attention over disjoint kv sets: each chunk writes its float32
+ * partial output O_i / l_i and lse_i to the workspace, and a merge kernel
+ * forms lse = log2(sum_i 2^lse_i) and out = sum_i 2^(lse_i - lse) O_i / l_i.
+ * Results equal tree_attn's up to float32 rounding order (not bit for bit).
+ *
+ * Bytes of device workspace tree_attn_split needs for these dims and chunk
+ * cap: tree_attn_workspace_size's plus, per possible work record
+ * (((total_q + R - 1) / R + batch_size) * max_chunks of them, R the q rows per
+ * tile), an h_kv x 128 x head_dim float32 partial output and its lse.
+ * 0 on invalid dims or max_chunks outside 1..16. */
+size_t tree_attn_split_workspace_size(const ta_dims* dims, int32_t max_chunks);
+
+/* tree_attn with split-KV (one call: plan, attention, merge).  Arguments as
+ * for tree_attn, plus:
+ *   max_chunks   1..16, the most chunks one (sequence, q tile) pair is cut
+ *                into (1: no split, the result is then tree_attn's exactly)
+ *   chunk_tiles  target chunk length in kv tiles of 64 columns (>= 0); a pair
+ *                whose kv tiles up to its last row's own slot number c gets
+ *                min(max_chunks, ceil(c / chunk_tiles)) chunks.  0 lets the
+ *                plan choose it from the batch's total work: a quarter of one
+ *                pipeline's share of it (two pipelines per SM), at least 16.
+ * The chunks of a pair split the range of its kv tiles up to its last
+ * non-empty tile into equal lengths.  workspace must hold at least
+ * tree_attn_split_workspace_size(dims, max_chunks) bytes, with tree_attn's
+ * other rules.  Asynchronous on stream. */
+ta_status tree_attn_split(const void* q, const int32_t* q_indptr, const void* k, const void* v,
+                          const int32_t* kv_indptr, const int32_t* q_rope_position,
+                          const int32_t* mn_indptr, const int32_t* tree_order, void* out,
+                          float* lse, int32_t rotary_mode, float rope_scale, float rope_theta,
+                          float sm_scale, int32_t max_chunks, int32_t chunk_tiles,
+                          const ta_dims* dims, void* workspace, size_t workspace_bytes,
+                          void* stream);
+
+/* Merges n_parts attention states over disjoint kv sets of the same rows
+ * into the state over their union, with the base-2 LSE rule above (parts of
+ * lse = -inf contribute nothing; a row whose parts are all -inf gets out = 0
+ * and lse = -inf).  Layouts (device, contiguous):
+ *   parts  [n_parts, rows, head_dim] dtype, each part normalised (as
+ *          tree_attn's out); rows = total_q * h_q for tree_attn outputs
+ *   lses   [n_parts, rows] float32, base-2
+ *   out    [rows, head_dim] dtype (written);  lse [rows] float32 (written)
+ * head_dim 64 or 128 (else TA_ERR_UNSUPPORTED); parts and out 16-byte
+ * aligned.  Asynchronous on stream. */
+ta_status tree_attn_merge_states(const void* parts, const float* lses, int32_t n_parts,
+                                 int64_t rows, int32_t head_dim, ta_dtype dtype, void* out,
+                                 float* lse, void* stream);
+
 /* Synchronises ``stream``, reads and clears the device status word that the
  * kernels of earlier calls left in ``workspace`` (TA_ERR_DEVICE_TIMEOUT if a
  * bounded wait expired, TA_ERR_CUDA on a CUDA error, else TA_OK). */

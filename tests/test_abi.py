@@ -194,3 +194,85 @@ def test_paged_bad_dims(lib):
     assert _call_paged(lib, _pdims(num_pages=0)) == ta.TA_ERR_INVALID_ARGUMENT
     assert _call_paged(lib, _pdims(head_dim=96)) == ta.TA_ERR_UNSUPPORTED
     assert _call_paged(lib, _pdims(total_q=0)) == ta.TA_OK
+
+
+# --------------------------------------------------------------------------
+# split-KV and the stand-alone state merge: host-side validation (no launch)
+# --------------------------------------------------------------------------
+
+def _round256(x):
+    return (x + 255) // 256 * 256
+
+
+def test_split_workspace_size(lib):
+    d = _dims()
+    plain = ta.workspace_size(d)
+    # one chunk per pair is the unsplit layout
+    assert ta.split_workspace_size(d, 1) == plain
+    # g = 2 -> 64 q rows per tile: 1 + 2 pairs at most; per record an
+    # h_kv x 128 x d float32 partial output and its lse, plus the merge table
+    max_pairs = (19 + 63) // 64 + 2
+    for mc in (2, 7, 16):
+        recs = max_pairs * mc
+        extra = (_round256(recs * 64) - _round256(max_pairs * 64) + _round256(max_pairs * 16)
+                 + _round256(recs * 2 * 128 * 64 * 4) + _round256(recs * 2 * 128 * 4))
+        assert ta.split_workspace_size(d, mc) == plain + extra
+    assert ta.split_workspace_size(d, 0) == 0
+    assert ta.split_workspace_size(d, ta.MAX_CHUNKS + 1) == 0
+    assert ta.split_workspace_size(_dims(head_dim=96), 4) == 0
+
+
+def _call_split(lib, dims, max_chunks=4, chunk_tiles=0, **kw):
+    fake = ctypes.c_void_p(0x10000)
+    a = dict(q=fake, q_indptr=fake, k=fake, v=fake, kv_indptr=fake, pos=fake, mn=fake,
+             order=fake, out=fake, lse=fake, rotary=0, rs=1.0, rt=1e4, sm=0.125,
+             ws=ctypes.c_void_p(0x20000), wsb=1 << 30)
+    a.update(kw)
+    return lib.tree_attn_split(a["q"], a["q_indptr"], a["k"], a["v"], a["kv_indptr"], a["pos"],
+                               a["mn"], a["order"], a["out"], a["lse"], a["rotary"], a["rs"],
+                               a["rt"], a["sm"], max_chunks, chunk_tiles, ctypes.byref(dims),
+                               a["ws"], a["wsb"], None)
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(max_chunks=0), ta.TA_ERR_INVALID_ARGUMENT),
+    (dict(max_chunks=17), ta.TA_ERR_INVALID_ARGUMENT),
+    (dict(chunk_tiles=-1), ta.TA_ERR_INVALID_ARGUMENT),
+    (dict(q=None), ta.TA_ERR_INVALID_ARGUMENT),
+    (dict(ws=None), ta.TA_ERR_INVALID_ARGUMENT),
+    (dict(rotary=1, pos=None), ta.TA_ERR_INVALID_ARGUMENT),
+    (dict(sm=float("nan")), ta.TA_ERR_INVALID_ARGUMENT),
+    (dict(ws=ctypes.c_void_p(0x20010)), ta.TA_ERR_INVALID_ARGUMENT),
+])
+def test_split_host_validation_rejects_before_launch(lib, kw, expect):
+    assert _call_split(lib, _dims(), **kw) == expect
+
+
+def test_split_workspace_must_hold_the_partial_states(lib):
+    d = _dims()
+    need = ta.split_workspace_size(d, 8)
+    assert _call_split(lib, d, max_chunks=8, wsb=need - 256) == ta.TA_ERR_INVALID_ARGUMENT
+    assert _call_split(lib, _dims(total_q=0), max_chunks=8, wsb=need) == ta.TA_OK
+    assert _call_split(lib, _dims(head_dim=96)) == ta.TA_ERR_UNSUPPORTED
+
+
+def _call_merge(lib, n=2, rows=10, d=128, dtype=ta.TA_BF16, **kw):
+    fake = ctypes.c_void_p(0x10000)
+    a = dict(parts=fake, lses=fake, out=fake, lse=fake)
+    a.update(kw)
+    return lib.tree_attn_merge_states(a["parts"], a["lses"], n, rows, d, dtype, a["out"],
+                                      a["lse"], None)
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(n=0), ta.TA_ERR_INVALID_ARGUMENT),
+    (dict(rows=-1), ta.TA_ERR_INVALID_ARGUMENT),
+    (dict(dtype=5), ta.TA_ERR_INVALID_ARGUMENT),
+    (dict(d=96), ta.TA_ERR_UNSUPPORTED),
+    (dict(parts=None), ta.TA_ERR_INVALID_ARGUMENT),
+    (dict(lse=None), ta.TA_ERR_INVALID_ARGUMENT),
+    (dict(out=ctypes.c_void_p(0x10004)), ta.TA_ERR_INVALID_ARGUMENT),
+    (dict(rows=0, parts=None), ta.TA_OK),
+])
+def test_merge_states_host_validation(lib, kw, expect):
+    assert _call_merge(lib, **kw) == expect

@@ -26,6 +26,7 @@ __all__ = [
     "TA_ERR_DEVICE_TIMEOUT", "TreeAttnError", "Dims", "lib", "lib_path", "workspace_size",
     "tree_attn", "plan", "run", "device_status", "status_string", "mask_dense", "check_inputs",
     "TreeAttention", "PagedDims", "make_paged_dims", "paged_workspace_size", "tree_attn_paged",
+    "MAX_CHUNKS", "split_workspace_size", "tree_attn_split", "merge_states",
 ]
 
 TA_OK = 0
@@ -35,6 +36,7 @@ TA_ERR_CUDA = 3
 TA_ERR_DEVICE_TIMEOUT = 4
 TA_FP16 = 0
 TA_BF16 = 1
+MAX_CHUNKS = 16   # split-KV: most chunks per (sequence, q tile) pair
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 lib_path = os.path.join(_PKG, "libtreeattn.so")
@@ -106,6 +108,16 @@ def lib() -> ctypes.CDLL:
                                   ctypes.c_int32, ctypes.c_float, ctypes.POINTER(PagedDims), vp,
                                   sz, vp]
     L.tree_attn_paged.restype = ctypes.c_int
+    L.tree_attn_split_workspace_size.argtypes = [ctypes.POINTER(Dims), ctypes.c_int32]
+    L.tree_attn_split_workspace_size.restype = sz
+    L.tree_attn_split.argtypes = [vp, i32p, vp, vp, i32p, i32p, i32p, i32p, vp, vp,
+                                  ctypes.c_int32, ctypes.c_float, ctypes.c_float, ctypes.c_float,
+                                  ctypes.c_int32, ctypes.c_int32, ctypes.POINTER(Dims), vp, sz,
+                                  vp]
+    L.tree_attn_split.restype = ctypes.c_int
+    L.tree_attn_merge_states.argtypes = [vp, vp, ctypes.c_int32, ctypes.c_int64, ctypes.c_int32,
+                                         ctypes.c_int, vp, vp, vp]
+    L.tree_attn_merge_states.restype = ctypes.c_int
     _lib = L
     return L
 
@@ -232,6 +244,61 @@ def tree_attn_paged(q, q_indptr, pages, page_indptr, page_values, length_info, m
                                workspace.numel() * workspace.element_size(), _stream_ptr(stream))
     if st != TA_OK:
         raise TreeAttnError(st, "tree_attn_paged")
+
+
+def split_workspace_size(dims: Dims, max_chunks: int) -> int:
+    return int(lib().tree_attn_split_workspace_size(ctypes.byref(dims), int(max_chunks)))
+
+
+def tree_attn_split(q, q_indptr, k, v, kv_indptr, q_rope_position, mn_indptr, tree_order, out,
+                    lse, rotary_mode: int, rope_scale: float, rope_theta: float,
+                    sm_scale: float, max_chunks: int, chunk_tiles: int,
+                    workspace: torch.Tensor, stream=None) -> None:
+    """``tree_attn`` with split-KV: pairs with many kv tiles are cut into up
+    to ``max_chunks`` chunks of about ``chunk_tiles`` 64-column tiles (0: the
+    plan picks the length), whose partial states a merge kernel combines.
+    ``workspace`` holds ``split_workspace_size(dims, max_chunks)`` bytes."""
+    for name, t in (("q", q), ("k", k), ("v", v), ("out", out)):
+        _check_dev(name, t, q.dtype)
+    for name, t in (("q_indptr", q_indptr), ("kv_indptr", kv_indptr), ("mn_indptr", mn_indptr),
+                    ("tree_order", tree_order), ("q_rope_position", q_rope_position)):
+        _check_dev(name, t, torch.int32)
+    _check_dev("lse", lse, torch.float32)
+    _check_dev("workspace", workspace)
+    dims = make_dims(q, k, q_indptr, tree_order, rotary_mode)
+    st = lib().tree_attn_split(_ptr(q), _ptr(q_indptr), _ptr(k), _ptr(v), _ptr(kv_indptr),
+                               _ptr(q_rope_position), _ptr(mn_indptr), _ptr(tree_order),
+                               _ptr(out), _ptr(lse), int(rotary_mode), float(rope_scale),
+                               float(rope_theta), float(sm_scale), int(max_chunks),
+                               int(chunk_tiles), ctypes.byref(dims), _ptr(workspace),
+                               workspace.numel() * workspace.element_size(), _stream_ptr(stream))
+    if st != TA_OK:
+        raise TreeAttnError(st, "tree_attn_split")
+
+
+def merge_states(parts: torch.Tensor, lses: torch.Tensor, out: Optional[torch.Tensor] = None,
+                 lse: Optional[torch.Tensor] = None, stream=None):
+    """Merge ``n`` attention states over disjoint kv sets: ``parts [n, ...,
+    d]`` (fp16/bf16, normalised) and base-2 ``lses [n, ...]`` (float32) into
+    ``out [..., d]`` and ``lse [...]`` (returned)."""
+    _check_dev("parts", parts)
+    _check_dev("lses", lses, torch.float32)
+    if parts.dim() < 2 or tuple(lses.shape) != tuple(parts.shape[:-1]):
+        raise ValueError("parts must be [n, ..., d] and lses [n, ...]")
+    n, d = parts.shape[0], parts.shape[-1]
+    rows = lses[0].numel() if n else 0
+    if out is None:
+        out = torch.empty(parts.shape[1:], dtype=parts.dtype, device=parts.device)
+    if lse is None:
+        lse = torch.empty(lses.shape[1:], dtype=torch.float32, device=parts.device)
+    _check_dev("out", out, parts.dtype)
+    _check_dev("lse", lse, torch.float32)
+    st = lib().tree_attn_merge_states(_ptr(parts), _ptr(lses), int(n), int(rows), int(d),
+                                      _dtype_code(parts.dtype), _ptr(out), _ptr(lse),
+                                      _stream_ptr(stream))
+    if st != TA_OK:
+        raise TreeAttnError(st, "tree_attn_merge_states")
+    return out, lse
 
 
 def plan(q, q_indptr, k, kv_indptr, q_rope_position, mn_indptr, tree_order,

@@ -19,7 +19,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(PKG, "libtreeattn.so")
-SOURCES = ["ta_api.cu", "ta_plan.cu", "ta_attn.cu"]
+SOURCES = ["ta_api.cu", "ta_plan.cu", "ta_attn.cu", "ta_merge.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
               "--expt-relaxed-constexpr", "-I", INCLUDE, "-I", CSRC]

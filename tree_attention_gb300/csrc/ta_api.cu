@@ -59,9 +59,20 @@ ta_status dims_supported(const ta_dims* d) {
   return TA_OK;
 }
 
-WsLayout layout_of(const ta_dims* d) {
+WsLayout layout_of(const ta_dims* d, int max_chunks = 1) {
   return ta::make_ws_layout(d->batch_size, d->total_q, d->total_kv, d->h_q / d->h_kv, d->h_kv,
-                            d->head_dim, d->rotary_mode != 0);
+                            d->head_dim, d->rotary_mode != 0, max_chunks);
+}
+
+// Workspace bytes for dims and a split-KV chunk cap (1: unsplit); 0 when the
+// dims are invalid or unsupported or a table index would overflow int32.
+size_t ws_size(const ta_dims* d, int max_chunks) {
+  if (!dims_valid(d) || dims_supported(d) != TA_OK) return 0;
+  if (max_chunks < 1 || max_chunks > ta::kMaxChunks) return 0;
+  const WsLayout L = layout_of(d, max_chunks);
+  if (L.class_bytes >= (int64_t)INT32_MAX || L.max_records * d->h_kv >= (int64_t)INT32_MAX)
+    return 0;
+  return L.total;
 }
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
@@ -110,11 +121,10 @@ bool make_pages_map(CUtensorMap* m, const void* base, ta_dtype dt, int num_pages
 
 extern "C" {
 
-size_t tree_attn_workspace_size(const ta_dims* dims) {
-  if (!dims_valid(dims) || dims_supported(dims) != TA_OK) return 0;
-  const WsLayout L = layout_of(dims);
-  if (L.class_bytes >= (int64_t)INT32_MAX) return 0;
-  return L.total;
+size_t tree_attn_workspace_size(const ta_dims* dims) { return ws_size(dims, 1); }
+
+size_t tree_attn_split_workspace_size(const ta_dims* dims, int32_t max_chunks) {
+  return ws_size(dims, max_chunks);
 }
 
 }  // extern "C"
@@ -124,8 +134,10 @@ namespace {
 // Checks shared by the plan and run halves.
 ta_status check_common(const int32_t* q_indptr, const int32_t* kv_indptr,
                        const int32_t* mn_indptr, const int32_t* tree_order, int32_t rotary_mode,
-                       const ta_dims* dims, const void* workspace, size_t workspace_bytes) {
+                       const ta_dims* dims, const void* workspace, size_t workspace_bytes,
+                       int max_chunks = 1) {
   if (!dims_valid(dims)) return TA_ERR_INVALID_ARGUMENT;
+  if (max_chunks < 1 || max_chunks > ta::kMaxChunks) return TA_ERR_INVALID_ARGUMENT;
   const ta_status sup = dims_supported(dims);
   if (sup != TA_OK) return sup;
   if (!q_indptr || !kv_indptr || !mn_indptr || !workspace) return TA_ERR_INVALID_ARGUMENT;
@@ -133,7 +145,7 @@ ta_status check_common(const int32_t* q_indptr, const int32_t* kv_indptr,
   if (rotary_mode != 0 && rotary_mode != 1) return TA_ERR_INVALID_ARGUMENT;
   if (rotary_mode != dims->rotary_mode) return TA_ERR_INVALID_ARGUMENT;
   if (!aligned(workspace, 256)) return TA_ERR_INVALID_ARGUMENT;
-  const size_t need = tree_attn_workspace_size(dims);
+  const size_t need = ws_size(dims, max_chunks);
   if (need == 0) return TA_ERR_UNSUPPORTED;
   if (workspace_bytes < need) return TA_ERR_INVALID_ARGUMENT;
   if (dims->total_q > 0 && dims->total_kv == 0) return TA_ERR_INVALID_ARGUMENT;  // qo <= T <= kv
@@ -165,22 +177,30 @@ struct WsPtrs {
   ta::ItemRec* sorted;
   uint8_t* classes;
   float2* rope_cs;
+  int4* merge;        // split-KV only
+  float* part_o;
+  float* part_lse;
 };
 
 WsPtrs ws_ptrs(void* workspace, const WsLayout& L) {
   uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const bool split = L.max_records > L.max_pairs;
   return WsPtrs{reinterpret_cast<WsHeader*>(ws),
-                reinterpret_cast<ta::ItemRec*>(ws + L.off_sorted), ws + L.off_classes,
-                reinterpret_cast<float2*>(ws + L.off_rope)};
+                reinterpret_cast<ta::ItemRec*>(ws + L.off_sorted),
+                ws + L.off_classes,
+                reinterpret_cast<float2*>(ws + L.off_rope),
+                split ? reinterpret_cast<int4*>(ws + L.off_merge) : nullptr,
+                split ? reinterpret_cast<float*>(ws + L.off_part_o) : nullptr,
+                split ? reinterpret_cast<float*>(ws + L.off_part_lse) : nullptr};
 }
 
 ta_status launch_plan_checked(const int32_t* q_indptr, const int32_t* kv_indptr,
                               const int32_t* q_rope_position, const int32_t* mn_indptr,
                               const int32_t* tree_order, int32_t rotary_mode, float rope_scale,
                               float rope_theta, const ta_dims* dims, void* workspace,
-                              cudaStream_t st) {
+                              cudaStream_t st, int max_chunks = 1, int chunk_tiles = 0) {
   const int g = dims->h_q / dims->h_kv;
-  const WsLayout L = layout_of(dims);
+  const WsLayout L = layout_of(dims, max_chunks);
   const WsPtrs w = ws_ptrs(workspace, L);
   const int nsm = sm_count();
   if (nsm <= 0) return TA_ERR_CUDA;
@@ -200,6 +220,10 @@ ta_status launch_plan_checked(const int32_t* q_indptr, const int32_t* kv_indptr,
   pp.total_tree = dims->total_tree;
   pp.rotary = rotary_mode;
   pp.max_pairs = L.max_pairs;
+  pp.max_chunks = max_chunks;
+  pp.chunk_tiles = chunk_tiles;
+  pp.pipes = 2 * nsm;
+  pp.merge = w.merge;
   pp.rope_scale = rope_scale;
   pp.rope_theta = rope_theta;
   for (int i = 0; i < 64; ++i) pp.rope_den[i] = 1.f;
@@ -223,11 +247,11 @@ ta_status launch_run_checked(const void* q, const void* k, const void* v, const 
                              const int32_t* kv_indptr, const int32_t* mn_indptr,
                              const int32_t* tree_order, void* out, float* lse,
                              int32_t rotary_mode, float sm_scale, const ta_dims* dims,
-                             void* workspace, cudaStream_t st) {
+                             void* workspace, cudaStream_t st, int max_chunks = 1) {
   const int g = dims->h_q / dims->h_kv;
   const int R = ta::rows_per_item(g);
   const int D = dims->head_dim;
-  const WsLayout L = layout_of(dims);
+  const WsLayout L = layout_of(dims, max_chunks);
   const WsPtrs w = ws_ptrs(workspace, L);
   const int nsm = sm_count();
   if (nsm <= 0) return TA_ERR_CUDA;
@@ -259,10 +283,12 @@ ta_status launch_run_checked(const void* q, const void* k, const void* v, const 
   ap.g = g;
   ap.R = R;
   ap.rotary = rotary_mode;
-  ap.max_pairs = L.max_pairs;
+  ap.max_records = L.max_records;
   ap.scale_log2 = sm_scale * 1.4426950408889634f;
   ap.timeout_ns = kDeviceWaitLimitNs;
-  const int64_t max_items = L.max_pairs * dims->h_kv;
+  ap.part_o = w.part_o;
+  ap.part_lse = w.part_lse;
+  const int64_t max_items = L.max_records * dims->h_kv;
   const int grid = (int)(max_items < nsm ? max_items : nsm);
   cudaError_t e;
   const bool bf16 = dims->dtype == TA_BF16;
@@ -272,7 +298,26 @@ ta_status launch_run_checked(const void* q, const void* k, const void* v, const 
   else
     e = bf16 ? ta::launch_attn<128, true, false>(tm_q, tm_k, tm_v, ap, grid, st)
              : ta::launch_attn<128, false, false>(tm_q, tm_k, tm_v, ap, grid, st);
-  return e == cudaSuccess ? TA_OK : TA_ERR_CUDA;
+  if (e != cudaSuccess) return TA_ERR_CUDA;
+  if (max_chunks > 1) {
+    // split-KV: the chunks' partial states of every split pair into out / lse
+    ta::MergeParams mp{};
+    mp.merge = w.merge;
+    mp.part_o = w.part_o;
+    mp.part_lse = w.part_lse;
+    mp.out = out;
+    mp.lse = lse;
+    mp.hdr = w.hdr;
+    mp.max_pairs = L.max_pairs;
+    mp.max_records = L.max_records;
+    mp.h_q = dims->h_q;
+    mp.h_kv = dims->h_kv;
+    mp.g = g;
+    const int64_t units = L.max_pairs * dims->h_kv * (ta::kBlockM / 32);
+    const int mgrid = (int)(units < 4 * nsm ? units : 4 * nsm);
+    if (ta::launch_merge(mp, D, bf16, mgrid, st) != cudaSuccess) return TA_ERR_CUDA;
+  }
+  return TA_OK;
 }
 
 }  // namespace
@@ -330,6 +375,51 @@ ta_status tree_attn(const void* q, const int32_t* q_indptr, const void* k, const
   if (s != TA_OK) return s;
   return launch_run_checked(q, k, v, q_indptr, kv_indptr, mn_indptr, tree_order, out, lse,
                             rotary_mode, sm_scale, dims, workspace, st);
+}
+
+ta_status tree_attn_split(const void* q, const int32_t* q_indptr, const void* k, const void* v,
+                          const int32_t* kv_indptr, const int32_t* q_rope_position,
+                          const int32_t* mn_indptr, const int32_t* tree_order, void* out,
+                          float* lse, int32_t rotary_mode, float rope_scale, float rope_theta,
+                          float sm_scale, int32_t max_chunks, int32_t chunk_tiles,
+                          const ta_dims* dims, void* workspace, size_t workspace_bytes,
+                          void* stream) {
+  if (chunk_tiles < 0) return TA_ERR_INVALID_ARGUMENT;
+  ta_status s = check_common(q_indptr, kv_indptr, mn_indptr, tree_order, rotary_mode, dims,
+                             workspace, workspace_bytes, max_chunks);
+  if (s != TA_OK) return s;
+  s = check_plan_args(q_rope_position, rotary_mode, rope_scale, rope_theta, dims);
+  if (s != TA_OK) return s;
+  s = check_run_args(q, k, v, out, lse, sm_scale, dims);
+  if (s != TA_OK) return s;
+  if (dims->total_q == 0) return TA_OK;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  s = launch_plan_checked(q_indptr, kv_indptr, q_rope_position, mn_indptr, tree_order,
+                          rotary_mode, rope_scale, rope_theta, dims, workspace, st, max_chunks,
+                          chunk_tiles);
+  if (s != TA_OK) return s;
+  return launch_run_checked(q, k, v, q_indptr, kv_indptr, mn_indptr, tree_order, out, lse,
+                            rotary_mode, sm_scale, dims, workspace, st, max_chunks);
+}
+
+ta_status tree_attn_merge_states(const void* parts, const float* lses, int32_t n_parts,
+                                 int64_t rows, int32_t head_dim, ta_dtype dtype, void* out,
+                                 float* lse, void* stream) {
+  if (n_parts < 1 || rows < 0) return TA_ERR_INVALID_ARGUMENT;
+  if (dtype != TA_FP16 && dtype != TA_BF16) return TA_ERR_INVALID_ARGUMENT;
+  if (head_dim < 1) return TA_ERR_INVALID_ARGUMENT;
+  if (head_dim != 64 && head_dim != 128) return TA_ERR_UNSUPPORTED;
+  if (rows == 0) return TA_OK;
+  if (!parts || !lses || !out || !lse) return TA_ERR_INVALID_ARGUMENT;
+  if (!aligned(parts, 16) || !aligned(out, 16)) return TA_ERR_INVALID_ARGUMENT;
+  const int nsm = sm_count();
+  if (nsm <= 0) return TA_ERR_CUDA;
+  const int64_t ctas = (rows + 7) / 8;   // 8 rows (warps) per CTA
+  const int grid = (int)(ctas < 8 * nsm ? ctas : 8 * nsm);
+  const cudaError_t e =
+      ta::launch_merge_states(parts, lses, n_parts, (long long)rows, head_dim, dtype == TA_BF16,
+                              out, lse, grid, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? TA_OK : TA_ERR_CUDA;
 }
 
 ta_status tree_attn_device_status(void* workspace, void* stream) {
@@ -561,6 +651,10 @@ ta_status tree_attn_paged(const void* q, const int32_t* q_indptr, const void* pa
   pp.total_tree = d.total_tree;
   pp.rotary = 0;
   pp.max_pairs = L.max_pairs;
+  pp.max_chunks = 1;
+  pp.chunk_tiles = 0;
+  pp.pipes = 2 * nsm;
+  pp.merge = nullptr;
   pp.rope_scale = 1.f;
   pp.rope_theta = 1.f;
   for (int i = 0; i < 64; ++i) pp.rope_den[i] = 1.f;
@@ -589,10 +683,12 @@ ta_status tree_attn_paged(const void* q, const int32_t* q_indptr, const void* pa
   ap.g = g;
   ap.R = R;
   ap.rotary = 0;
-  ap.max_pairs = L.max_pairs;
+  ap.max_records = L.max_records;
   ap.scale_log2 = sm_scale * 1.4426950408889634f;
   ap.timeout_ns = kDeviceWaitLimitNs;
-  const int64_t max_items = L.max_pairs * d.h_kv;
+  ap.part_o = nullptr;
+  ap.part_lse = nullptr;
+  const int64_t max_items = L.max_records * d.h_kv;
   const int grid = (int)(max_items < nsm ? max_items : nsm);
   const bool bf16 = d.dtype == TA_BF16;
   cudaError_t e;

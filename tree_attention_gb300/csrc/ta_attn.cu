@@ -115,19 +115,28 @@ struct Pipe {
   }
 };
 
-// Iterates the non-empty kv tiles of a work item: from the record's inline
-// 2-bit classes for short sequences, else from the plan's class bytes.
+// Iterates the non-empty kv tiles of a work item from its first tile
+// (tile_lo, past 0 for a split-KV chunk): from the record's inline 2-bit
+// classes for short sequences, else from the plan's class bytes.
 struct TileIter {
   const uint8_t* cls;
   int kvt, j;
   bool inl;
   uint32_t w0, w1, w2, w3;   // inline classes, or the current 16 class bytes
   __device__ TileIter(const ItemRec& r, const uint8_t* classes)
-      : cls(classes + r.class_off), kvt(r.kvt), j(-1), inl(r.kvt <= kInlineTiles) {
+      : cls(classes + r.class_off), kvt(r.kvt), j(r.tile_lo - 1), inl(r.kvt <= kInlineTiles) {
     w0 = r.cls2[0];
     w1 = r.cls2[1];
     w2 = r.cls2[2];
     w3 = 0;
+    if (!inl && (r.tile_lo & 15)) {
+      // a range that starts inside a 16-tile group: load that group now
+      const uint4 v = __ldg(reinterpret_cast<const uint4*>(cls + (r.tile_lo & ~15)));
+      w0 = v.x;
+      w1 = v.y;
+      w2 = v.z;
+      w3 = v.w;
+    }
   }
   // advances to the next non-empty tile; returns its class (0 when done)
   __device__ int next() {
@@ -167,7 +176,7 @@ __device__ void run_producer(const Pipe& pp, const CUtensorMap* tm_q, const CUte
   uint8_t* sV = pp.smem + C::kOffV;
   int2* sEX = reinterpret_cast<int2*>(pp.smem + C::kOffEX);
   // the plan kernel wrote the item count; never trust it beyond the table size
-  const unsigned long long cap = (unsigned long long)p.max_pairs * (unsigned long long)p.h_kv;
+  const unsigned long long cap = (unsigned long long)p.max_records * (unsigned long long)p.h_kv;
   const unsigned long long n_items = *(volatile unsigned int*)&p.hdr->num_items;
   const unsigned int num_items = (unsigned int)(n_items < cap ? n_items : cap);
   const int g = p.g, R = p.R;
@@ -269,7 +278,8 @@ __device__ void run_producer(const Pipe& pp, const CUtensorMap* tm_q, const CUte
 #pragma unroll
           for (int q = 0; q < kBlockN / 32; ++q)
             ex[q * 32 + lane] =
-                column_interval(p.tree_order, r.tree_base, j * kBlockN + q * 32 + lane, r.kv, r.ts);
+                column_interval(p.tree_order, r.tree_base, j * kBlockN + q * 32 + lane, r.kv,
+                                r.kv - r.tl);
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&pp.bar[B_EX_FULL + stage]);
@@ -515,7 +525,7 @@ __device__ void run_softmax(const Pipe& pp, const AttnParams& p, int sw, int lan
       if (p.rotary) {
         // q row r of the tile takes the position of its own tree node's kv slot
         // (the first cos/sin batch is fetched while the Q tile lands)
-        const long long qtok0 = (long long)r.kv_base + r.ts + (r.tl - r.qo) + (long long)r.t * R;
+        const long long qtok0 = (long long)r.kv_base + (r.kv - r.qo) + (long long)r.t * R;
         const RopeRange rr = rope_range<D>(r.nq, g, wq);
         float4 cv[2][4];
         rope_load<D>(cv, p.rope_cs, qtok0, rr, 0, lane);
@@ -663,6 +673,40 @@ __device__ void run_softmax(const Pipe& pp, const AttnParams& p, int sw, int lan
     }
     const float inv = l > 0.f ? 1.f / l : 0.f;
     const float lse_v = l > 0.f ? m_ref + log2f(l) : -INFINITY;
+    if (r.part >= 0) {
+      // split-KV chunk: O / l and lse in float32 into the record's partial
+      // state (packed row = TMEM lane), merged with the pair's other chunks
+      // by the merge kernel
+      const size_t prow = ((size_t)r.part * p.h_kv + kvh) * kBlockM + row;
+      if (valid) p.part_lse[prow] = lse_v;
+      float4* po = reinterpret_cast<float4*>(p.part_o + prow * D);
+#pragma unroll
+      for (int oc = 0; oc < D / 32; ++oc) {
+        float o[32];
+        if (r.n_tiles > 0) {
+          tmem_ld32(t_row + C::kTmemO + oc * 32, o);
+          tmem_wait_ld();
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = 0.f;
+        }
+        if (oc == D / 32 - 1) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0 && r.n_tiles > 0) mbar_arrive(&pp.bar[B_O_FREE]);
+        }
+        if (valid) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            po[oc * 8 + i] = make_float4(o[4 * i] * inv, o[4 * i + 1] * inv, o[4 * i + 2] * inv,
+                                         o[4 * i + 3] * inv);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&pp.bar[B_ITEM_EMPTY + slot]);
+      ++it;
+      continue;
+    }
     if (valid) p.lse[orow] = lse_v;
     // O / l in the storage dtype: 64 columns per TMEM round trip, written 32
     // columns (64 bytes per row) at a time through the warp's staging buffer,

@@ -46,12 +46,18 @@ struct PlanParams {
   int nnz_pages;
   int batch, g, R, h_kv, head_dim, total_q, total_kv, total_tree, rotary;
   int64_t max_pairs;
+  // split-KV: a pair's kv tiles are cut into up to max_chunks records of
+  // about chunk_tiles tiles (0: chosen from the batch's total work so that
+  // the items cover the ``pipes`` pipelines of the attention grid a few
+  // times); max_chunks == 1 disables it
+  int max_chunks, chunk_tiles, pipes;
+  int4* merge;       // per pair (split-KV): q_row0, q rows, chunks, first record
   float rope_scale, rope_theta;
   // fl32(theta^(2i/d)) for i < d/2, the RoPE frequency denominators of
   // ``_rope`` (page "_kernel_common.py"), rounded once from float64 on the host
   float rope_den[64];
   WsHeader* hdr;
-  ItemRec* sorted;   // one record per (sequence, q tile), longest first
+  ItemRec* sorted;   // one record per (sequence, q tile) or chunk of one, longest first
   uint8_t* classes;
   float2* rope_cs;
 };
@@ -67,9 +73,24 @@ struct AttnParams {
   const int32_t* page_values;   // paged KV cache: physical page of each (sequence, page)
   int num_pages;                // pages in the pool (an out-of-range page reads zeros)
   int h_q, h_kv, g, R, rotary;
-  int64_t max_pairs;  // capacity of the record tables in the workspace
-  float scale_log2;   // sm_scale * log2(e)
+  int64_t max_records;  // capacity of the record table in the workspace
+  float scale_log2;     // sm_scale * log2(e)
   unsigned long long timeout_ns;
+  // split-KV partial states of the records with part >= 0: O / l in float32
+  // [record][h_kv][128 packed rows][d] and the base-2 lse [record][h_kv][128]
+  float* part_o;
+  float* part_lse;
+};
+
+struct MergeParams {
+  const int4* merge;           // per pair: q_row0, q rows, chunks, first record
+  const float* part_o;
+  const float* part_lse;
+  void* out;
+  float* lse;
+  const WsHeader* hdr;         // num_pairs
+  int64_t max_pairs, max_records;
+  int h_q, h_kv, g;
 };
 
 // Plan kernel: sequence/tile enumeration, tile classification, LPT ordering
@@ -85,6 +106,17 @@ cudaError_t launch_krot(const void* k, void* krot, const float2* rope_cs, int to
 cudaError_t launch_mask_dense(const int32_t* q_indptr, const int32_t* kv_indptr,
                               const int32_t* mn_indptr, const int32_t* tree_order, int batch,
                               int total_q, int max_kv, uint8_t* vis, cudaStream_t stream);
+
+// Split-KV: combines the partial states of every split pair into out / lse
+// (the base-2 log-sum-exp merge of attention states over disjoint kv sets).
+cudaError_t launch_merge(const MergeParams& p, int head_dim, bool bf16, int grid,
+                         cudaStream_t stream);
+
+// Stand-alone merge of n_parts attention states per row: parts [n][rows][d]
+// and lses [n][rows] -> out [rows][d], lse [rows].
+cudaError_t launch_merge_states(const void* parts, const float* lses, int n_parts,
+                                long long rows, int head_dim, bool bf16, void* out, float* lse,
+                                int grid, cudaStream_t stream);
 
 // Persistent tree-attention kernel.
 template <int D, bool BF16, bool PAGED>

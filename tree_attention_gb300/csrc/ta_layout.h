@@ -34,24 +34,26 @@ struct WsHeader {
   unsigned int queue_done;  // attention CTAs finished (the last one resets the queue)
   unsigned int error;       // DEVERR_* bits, cleared by tree_attn_device_status
   unsigned int num_pairs;   // (sequence, q tile) pairs found by the plan kernel
-  unsigned int num_items;   // num_pairs * h_kv, 0 if the index arrays are invalid
+  unsigned int num_items;   // work records * h_kv, 0 if the index arrays are invalid
   unsigned int reserved;    // unused (zero)
   unsigned int pad[10];
 };
 static_assert(sizeof(WsHeader) == 64, "header size");
 
-// Everything the attention kernel needs about one (sequence, q tile) pair,
-// written by the plan kernel so that a work item costs one 64-byte load.
+// Everything the attention kernel needs about one (sequence, q tile) pair --
+// or, with split-KV, about one chunk of a pair's kv tiles -- written by the
+// plan kernel so that a work item costs one 64-byte load.
 struct ItemRec {
-  int32_t b;          // sequence
+  int32_t part;       // split-KV: this chunk's partial-state slot (-1: not split)
   int32_t t;          // q tile within the sequence
   int32_t q_row0;     // global index of the tile's first q row
   int32_t nq;         // q rows of the sequence inside this tile
-  int32_t qo, kv;     // q rows / kv rows of the sequence
-  int32_t tl, ts;     // tree nodes, tree start (= prefix length)
+  int32_t qo, kv;     // q rows / kv rows of the sequence (tree start = kv - tl)
+  int32_t tl;         // tree nodes
+  int32_t tile_lo;    // first kv tile of this item's range (0 unless split)
   int32_t kv_base;    // kv_indptr[b]
   int32_t tree_base;  // mn_indptr[b]
-  int32_t n_tiles;    // non-empty kv tiles
+  int32_t n_tiles;    // non-empty kv tiles of this item, from tile_lo on
   int32_t class_off;  // byte offset of the pair's kv-tile classes (16-aligned)
   int32_t kvt;        // kv tiles of the sequence
   uint32_t cls2[3];   // if kvt <= kInlineTiles: tile j's class in bits 2(j%16).. of word j/16
@@ -72,32 +74,50 @@ inline int64_t round_up(int64_t a, int64_t b) { return ceil_div(a, b) * b; }
 // q rows per work item for group size g.
 inline int rows_per_item(int g) { return kBlockM / g; }
 
+constexpr int kMaxChunks = 16;  // split-KV: chunks per (sequence, q tile) at most
+
 struct WsLayout {
   int64_t max_pairs;    // upper bound on (sequence, q tile) pairs
+  int64_t max_records;  // upper bound on work records (pairs, or pair chunks when split)
   int64_t class_bytes;  // bound on the class table
-  size_t off_sorted, off_classes, off_rope, off_krot, total;
+  size_t off_sorted, off_classes, off_rope, off_krot;
+  size_t off_merge, off_part_o, off_part_lse;   // split-KV only (else empty)
+  size_t total;
 };
 
 // Workspace layout for the given sizes (all offsets 256-byte aligned):
-//   header | ItemRec sorted[max_pairs] (longest-first order)
+//   header | ItemRec sorted[max_records] (longest-first order)
 //   | uint8 classes[]
 //   and with RoPE: | float2 rope_cs[total_kv][head_dim / 2] (rows of q tokens)
 //                  | rotated k [total_kv][h_kv][head_dim] (storage dtype)
+//   and with split-KV: | int4 merge[max_pairs] (per pair: q_row0, nq, chunks,
+//                        first record) | float part_o[max_records][h_kv][128][d]
+//                        | float part_lse[max_records][h_kv][128]
+// ``max_chunks`` (1..kMaxChunks) caps the split-KV chunks of a pair; 1 lays
+// out the unsplit workspace.
 inline WsLayout make_ws_layout(int64_t batch, int64_t total_q, int64_t total_kv, int g,
-                               int h_kv, int head_dim, bool rotary) {
+                               int h_kv, int head_dim, bool rotary, int max_chunks = 1) {
   WsLayout L{};
   const int64_t R = rows_per_item(g);
+  const bool split = max_chunks > 1;
   L.max_pairs = ceil_div(total_q, R) + batch;
+  L.max_records = L.max_pairs * (split ? max_chunks : 1);
   L.class_bytes = L.max_pairs * round_up(ceil_div(total_kv, kBlockN), 16);
   size_t off = 256;
   L.off_sorted = off;
-  off += round_up(L.max_pairs * (int64_t)sizeof(ItemRec), 256);
+  off += round_up(L.max_records * (int64_t)sizeof(ItemRec), 256);
   L.off_classes = off;
   off += round_up(L.class_bytes, 256);
   L.off_rope = off;
   if (rotary) off += round_up(total_kv * (int64_t)(head_dim / 2) * 8, 256);
   L.off_krot = off;
   if (rotary) off += round_up(total_kv * (int64_t)h_kv * head_dim * 2, 256);
+  L.off_merge = off;
+  if (split) off += round_up(L.max_pairs * 16, 256);
+  L.off_part_o = off;
+  if (split) off += round_up(L.max_records * h_kv * kBlockM * (int64_t)head_dim * 4, 256);
+  L.off_part_lse = off;
+  if (split) off += round_up(L.max_records * h_kv * kBlockM * 4, 256);
   L.total = off;
   return L;
 }

@@ -9,7 +9,8 @@
 //      estimated cost -- no global barrier, no serial tail;
 //   2. (warps 0-3) classifies every kv tile of its pair as EMPTY / PARTIAL /
 //      FULL exactly from the DFS intervals of ``_check_tree_order`` (page
-//      "tree_attn.py") and writes the pair's item record;
+//      "tree_attn.py") and writes the pair's item record -- with split-KV, one
+//      record per chunk of the pair's kv tiles plus the pair's merge record;
 //   3. (all warps) fills its share of the RoPE cos/sin table, one entry per
 //      (kv token, frequency), in the float32 steps of ``_rope``.
 #include <cuda_runtime.h>
@@ -115,16 +116,40 @@ __device__ __forceinline__ long long seg_bytes(int kv) {
 // Estimated cost of q tile t of a sequence, in kv tiles, for the
 // longest-first order: the kv tiles up to the tile's last row's own slot
 // (exact for trees whose nodes come after their parents, as in a causal
-// prefix; only the order of the work depends on it).
-__device__ __forceinline__ int pair_cost(int qo, int kv, int R, int t) {
+// prefix; only the order and the split of the work depend on it).
+__device__ __forceinline__ int pair_tiles(int qo, int kv, int R, int t) {
   const long long end = (long long)kv - max(0LL, (long long)qo - (long long)(t + 1) * R);
-  return (int)min((long long)kCostBuckets - 1, (end + kBlockN - 1) / kBlockN);
+  return (int)((end + kBlockN - 1) / kBlockN);
+}
+
+// Split-KV: chunks of a pair of estimated cost ``tiles`` (1 when not split).
+__device__ __forceinline__ int pair_chunks(int tiles, int chunk_tiles, int max_chunks) {
+  if (max_chunks <= 1) return 1;
+  return max(1, min(max_chunks, (tiles + chunk_tiles - 1) / chunk_tiles));
+}
+
+// Cost bucket of each of a pair's records: its chunks' estimated cost.
+__device__ __forceinline__ int record_bucket(int tiles, int chunks) {
+  return min(kCostBuckets - 1, (tiles + chunks - 1) / chunks);
+}
+
+// Split-KV chunk size when the caller leaves it to the plan: about a quarter
+// of the per-pipeline share of the batch's work, at least kMinChunkTiles so
+// that a chunk's fixed costs (its Q tile, its partial state written and read
+// back) stay small against its kv tiles.
+constexpr int kMinChunkTiles = 16;
+__device__ __forceinline__ int auto_chunk_tiles(long long total_tiles, int h_kv, int pipes) {
+  const long long per = (total_tiles * h_kv + 4LL * pipes - 1) / (4LL * pipes);
+  return (int)max((long long)kMinChunkTiles, min(per, (long long)INT_MAX));
 }
 
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanParams p) {
   __shared__ long long s_scan_a[9], s_scan_b[9];
   __shared__ int s_keys[kBlockM];
-  __shared__ int s_pair_b, s_pair_t, s_pair_cost;
+  __shared__ int s_pair_b, s_pair_t, s_pair_cost, s_pair_chunks;
+  __shared__ long long s_total_cost;
+  __shared__ int s_last;
+  __shared__ int s_ccount[kMaxChunks];
   __shared__ long long s_pair_off;
   __shared__ int s_bad, s_rank;
   __shared__ int s_any[kPassTiles], s_notall[kPassTiles];
@@ -150,7 +175,10 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanParams p) 
     s_bad = 0;
     s_count = 0;
     s_rank = 0;
+    s_total_cost = 0;
+    s_last = 0;
   }
+  if (tid < kMaxChunks) s_ccount[tid] = 0;
   __syncthreads();
   // the ends of the index arrays, read by the last thread alongside the
   // sequences' entries below (one round trip for both)
@@ -167,7 +195,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanParams p) 
   // front), validating the index arrays and counting pairs per cost
   const int per = (B + kPlanThreads - 1) / kPlanThreads;
   const int b_lo = min(B, tid * per), b_hi = min(B, b_lo + per);
-  long long my_tiles = 0, my_seg = 0;
+  const bool split = p.max_chunks > 1;
+  long long my_tiles = 0, my_seg = 0, my_cost = 0;
   int bad = 0;
   for (int b = b_lo; b < b_hi; ++b) {
     const int qo = p.q_indptr[b + 1] - p.q_indptr[b];
@@ -180,20 +209,40 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanParams p) 
     const int tiles = (qo + R - 1) / R;
     my_tiles += tiles;
     my_seg += (long long)tiles * seg_bytes(kv);
-    for (int t = 0; t < tiles; ++t) atomicAdd(&s_hist[pair_cost(qo, kv, R, t)], 1);
+    for (int t = 0; t < tiles; ++t) {
+      const int c = pair_tiles(qo, kv, R, t);
+      if (split)
+        my_cost += c;
+      else
+        atomicAdd(&s_hist[min(kCostBuckets - 1, c)], 1);
+    }
   }
   if (bad) atomicOr(&s_bad, 1);
+  if (split && my_cost) atomicAdd((unsigned long long*)&s_total_cost, (unsigned long long)my_cost);
   long long ex_tiles = my_tiles, ex_seg = my_seg, total_tiles, total_seg;
   exclusive_scan2(ex_tiles, ex_seg, total_tiles, total_seg, s_scan_a, s_scan_b, 0, kPlanThreads,
                   [] { __syncthreads(); });
   const bool ok = !s_bad && total_tiles <= p.max_pairs;
   const long long n_pairs = ok ? total_tiles : 0;
-  if (blockIdx.x == 0 && tid == 0) {
-    p.hdr->num_pairs = (unsigned int)n_pairs;
-    p.hdr->num_items = (unsigned int)(n_pairs * p.h_kv);
-    p.hdr->queue_head = 0;
-    p.hdr->queue_done = 0;
-    if (!ok) atomicOr(&p.hdr->error, DEVERR_BAD_INDPTR);
+  // split-KV: every CTA derives the same chunking from the same totals, and
+  // each pair adds its chunk count to the bucket of its chunks' cost
+  const int chunk_tiles =
+      !split ? 1 : (p.chunk_tiles > 0 ? p.chunk_tiles
+                                      : auto_chunk_tiles(s_total_cost, p.h_kv, p.pipes));
+  if (split) {
+    for (int b = b_lo; b < b_hi; ++b) {
+      const int qo = p.q_indptr[b + 1] - p.q_indptr[b];
+      const int kv = seq_kv_len(p, b);
+      const int tl = p.mn_indptr[b + 1] - p.mn_indptr[b];
+      if (qo < 0 || tl < qo || kv < tl || seq_pages_bad(p, b)) continue;
+      const int tiles = (qo + R - 1) / R;
+      for (int t = 0; t < tiles; ++t) {
+        const int c = pair_tiles(qo, kv, R, t);
+        const int nch = pair_chunks(c, chunk_tiles, p.max_chunks);
+        atomicAdd(&s_hist[record_bucket(c, nch)], nch);
+      }
+    }
+    __syncthreads();
   }
 
   // ---- 2. where each cost bucket starts in the longest-first order: the
@@ -211,6 +260,14 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanParams p) 
       s_hist[c] = (int)start;
       start += v;
     }
+    // tot: the work records (one per pair, or one per chunk when split)
+    if (blockIdx.x == 0 && tid == 0) {
+      p.hdr->num_pairs = (unsigned int)n_pairs;
+      p.hdr->num_items = ok ? (unsigned int)(tot * p.h_kv) : 0u;
+      p.hdr->queue_head = 0;
+      p.hdr->queue_done = 0;
+      if (!ok) atomicOr(&p.hdr->error, DEVERR_BAD_INDPTR);
+    }
   }
 
   // ---- 3. this CTA's pair and its place: the bucket's start plus the pairs
@@ -227,7 +284,10 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanParams p) 
         s_pair_b = b;
         s_pair_t = t;
         s_pair_off = scum + (long long)t * seg_bytes(kv);
-        s_pair_cost = pair_cost(qo, kv, R, t);
+        const int c = pair_tiles(qo, kv, R, t);
+        const int nch = pair_chunks(c, chunk_tiles, p.max_chunks);
+        s_pair_chunks = nch;
+        s_pair_cost = record_bucket(c, nch);
         break;
       }
       tcum += tiles;
@@ -249,6 +309,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanParams p) 
     if (tid < nrows) key = p.tree_order[2 * (tree_base + r0 + tid + tl - qo)];
   }
   if (has_pair) {
+    // records of the same bucket that come earlier in (sequence, q tile) order
     const int pb = s_pair_b, pt = s_pair_t, pc = s_pair_cost;
     int cnt = 0;
     for (int b = b_lo; b < min(b_hi, pb + 1); ++b) {
@@ -256,7 +317,11 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanParams p) 
       const int kv = seq_kv_len(p, b);
       const int tiles = (qo + R - 1) / R;
       const int t_end = b < pb ? tiles : pt;
-      for (int t = 0; t < t_end; ++t) cnt += pair_cost(qo, kv, R, t) == pc;
+      for (int t = 0; t < t_end; ++t) {
+        const int c = pair_tiles(qo, kv, R, t);
+        const int nch = pair_chunks(c, chunk_tiles, p.max_chunks);
+        cnt += record_bucket(c, nch) == pc ? nch : 0;
+      }
     }
     if (cnt) atomicAdd(&s_rank, cnt);
   }
@@ -342,31 +407,50 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanParams p) 
         const uint8_t cls =
             !s_any[i] ? kTileEmpty : ((!s_notall[i] && !ragged) ? kTileFull : kTilePartial);
         p.classes[off + j] = cls;
-        if (cls != kTileEmpty) atomicAdd(&s_count, 1);
+        if (cls != kTileEmpty) {
+          atomicAdd(&s_count, 1);
+          if (split) atomicMax(&s_last, j + 1);
+        }
         if (kvt <= kInlineTiles) atomicOr(&s_cls2[j >> 4], (uint32_t)cls << (2 * (j & 15)));
       }
       group_sync(kBarA);
     }
-    if (tid == 0) {
+    // split-KV: the tiles up to the last non-empty one are cut into nch
+    // ranges of (nearly) equal length; each range's non-empty tiles are
+    // counted from the classes just written (this group's own stores)
+    const int nch = s_pair_chunks;
+    const int last = s_last;
+    if (nch > 1) {
+      for (int j = tid; j < last; j += kGroup) {
+        if (p.classes[off + j] == kTileEmpty) continue;
+        int c = 0;
+        while (c + 1 < nch && j >= (int)((long long)last * (c + 1) / nch)) ++c;
+        atomicAdd(&s_ccount[c], 1);
+      }
+      group_sync(kBarA);
+    }
+    if (tid < nch) {
       ItemRec r;
-      r.b = b;
+      r.part = nch > 1 ? (int32_t)(pos + tid) : -1;
       r.t = t;
       r.q_row0 = q0 + r0;
       r.nq = nrows;
       r.qo = qo;
       r.kv = kv;
       r.tl = tl;
-      r.ts = ts;
+      r.tile_lo = nch > 1 ? (int32_t)((long long)last * tid / nch) : 0;
       r.kv_base = kv_base;
       r.tree_base = tree_base;
-      r.n_tiles = s_count;
+      r.n_tiles = nch > 1 ? s_ccount[tid] : s_count;
       r.class_off = (int32_t)off;
       r.kvt = kvt;
       r.cls2[0] = s_cls2[0];
       r.cls2[1] = s_cls2[1];
       r.cls2[2] = s_cls2[2];
-      p.sorted[pos] = r;
+      p.sorted[pos + tid] = r;
     }
+    if (tid == 0 && p.merge)
+      p.merge[pair] = make_int4(q0 + r0, nrows, nch, (int)pos);
   }
 
   // ---- 5. the RoPE cos/sin table, one entry per (kv token, frequency), in

@@ -37,7 +37,7 @@ __all__ = [
     "Workload", "chain_tree", "star_tree", "binary_tree", "random_tree",
     "spec_decode_tree", "main_chain_tree", "tree_intervals", "tree_depths",
     "ancestors", "build_workload", "config", "CONFIG_NAMES", "visible_pairs",
-    "algorithmic_bytes", "algorithmic_flops",
+    "algorithmic_bytes", "algorithmic_flops", "long_prefix",
 ]
 
 # --------------------------------------------------------------------------
@@ -333,6 +333,23 @@ def config(idx: int, *, batch_scale: float = 1.0) -> Workload:
     parents = [chain_tree(n), star_tree(n), binary_tree(n), random_tree(n, trng)][:keep(4)]
     return build_workload("degenerate", parents, h_q=16, h_kv=16, head_dim=128,
                           dtype="fp16", tensor_seed=tseed, rotary_mode=0)
+
+
+def long_prefix(batch: int = 4, prefix: int = 32768, nodes: int = 64, seed: int = 6) -> Workload:
+    """Few sequences with a long shared-history prefix: ``batch`` draft trees
+    of ``nodes`` nodes shaped as in the spec-decode workload (depth <= 8,
+    branching <= 4) after a causal prefix of ``prefix`` tokens, h_q=32 h_kv=8
+    d=128 bf16 N(0,1), inline RoPE theta=1e4 at positions ``0..prefix-1`` then
+    ``prefix + depth``.  With few (sequence, q tile) pairs each reading tens of
+    thousands of kv columns, it is the case split-KV exists for.  Tree seed
+    ``1000 + seed``, tensor seed ``2000 + seed``."""
+    trng = np.random.default_rng(1000 + seed)
+    parents = [spec_decode_tree(nodes, trng) for _ in range(batch)]
+    positions = [np.concatenate([np.arange(prefix), prefix + tree_depths(p)]) for p in parents]
+    return build_workload(f"long-prefix-{prefix}", parents, h_q=32, h_kv=8, head_dim=128,
+                          dtype="bf16", tensor_seed=2000 + seed,
+                          prefix_lens=[prefix] * batch, positions=positions, rotary_mode=1,
+                          rope_scale=1.0, rope_theta=1e4)
 
 
 # --------------------------------------------------------------------------
