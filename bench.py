@@ -315,8 +315,9 @@ def run_gb300(args):
                 d["ws"], stream)
         if ev is not None:
             ev[1].record(stream)
-        ta.run(d["q"], d["k"], d["v"], d["q_indptr"], d["kv_indptr"], d["mn_indptr"],
-               d["tree_order"], d["out"], d["lse"], w.rotary_mode, w.sm_scale, d["ws"], stream)
+        ta.run(d["q"], d["k"], d["v"], d["q_indptr"], d["kv_indptr"], d["q_rope_position"],
+               d["mn_indptr"], d["tree_order"], d["out"], d["lse"], w.rotary_mode, w.rope_scale,
+               w.rope_theta, w.sm_scale, d["ws"], stream)
         if ev is not None:
             ev[2].record(stream)
 

@@ -72,7 +72,7 @@ typedef struct {
 /* Bytes of device workspace ``tree_attn`` needs for these sizes (a multiple
  * of 256; 0 on invalid dims).  The workspace holds the per-launch work plan
  * (tile classes, the cost-ordered work queue), a device status word and,
- * with RoPE, the cos/sin table of the q tokens and the rotated k
+ * with RoPE, the cos/sin table of the kv tokens and the rotated k
  * (total_kv * h_kv * head_dim elements, rotated once per call instead of
  * once per q tile that reads it).  It depends on the dims only, so one
  * allocation serves every call with the same dims. */
@@ -122,12 +122,14 @@ ta_status tree_attn(const void* q, const int32_t* q_indptr, const void* k, const
  * across calls (every layer of a model verifies the same draft tree):
  *   tree_attn_plan  enumerates the (sequence, q tile) work items, classifies
  *                   every (q tile, kv tile) pair as empty / partial / full
- *                   from the DFS intervals, orders the items longest-first
- *                   and, if rotary_mode == 1, fills the RoPE cos/sin table of
- *                   every kv token; it reads only the index arrays and
- *                   positions.
- *   tree_attn_run   the attention kernel proper, consuming the plan that the
- *                   last tree_attn_plan (or tree_attn) left in ``workspace``.
+ *                   from the DFS intervals and orders the items
+ *                   longest-first; it reads only the index arrays (the RoPE
+ *                   arguments are validated, not used).
+ *   tree_attn_run   with rotary_mode == 1 the RoPE of every kv token (its
+ *                   cos/sin from q_rope_position, rope_scale and rope_theta,
+ *                   and its rotated keys), then the attention kernel proper,
+ *                   consuming the plan that the last tree_attn_plan (or
+ *                   tree_attn) left in ``workspace``.
  * tree_attn_run must follow a plan made on the same workspace with the same
  * dims, index-array contents, positions, rotary_mode, rope_scale and
  * rope_theta; q, k, v, out, lse and sm_scale may change between runs.
@@ -139,8 +141,9 @@ ta_status tree_attn_plan(const int32_t* q_indptr, const int32_t* kv_indptr,
                          size_t workspace_bytes, void* stream);
 
 ta_status tree_attn_run(const void* q, const void* k, const void* v, const int32_t* q_indptr,
-                        const int32_t* kv_indptr, const int32_t* mn_indptr,
-                        const int32_t* tree_order, void* out, float* lse, int32_t rotary_mode,
+                        const int32_t* kv_indptr, const int32_t* q_rope_position,
+                        const int32_t* mn_indptr, const int32_t* tree_order, void* out,
+                        float* lse, int32_t rotary_mode, float rope_scale, float rope_theta,
                         float sm_scale, const ta_dims* dims, void* workspace,
                         size_t workspace_bytes, void* stream);
 

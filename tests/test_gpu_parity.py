@@ -252,25 +252,59 @@ def test_bad_index_arrays_are_reported_not_computed():
 # RoPE table: float32 cos/sin rounded correctly (as the oracle takes them)
 # --------------------------------------------------------------------------
 
-@pytest.mark.parametrize("idx", [2, 3, 4])
-def test_rope_table_matches_correctly_rounded_cos_sin(idx):
-    """The plan kernel's per-token cos/sin table (the workspace region
-    before the rotated keys) equals float32-rounded cos/sin of the pages' float32 angle;
-    only rare near-ties (true value within ~1e-4 ulp of a rounding midpoint)
-    may differ by one ulp."""
+def _rope_regions(w, attn):
+    """The kv tokens' cos/sin table and the rotated keys: the last two
+    regions of a tree_attn workspace with RoPE."""
+    def r256(x):
+        return (x + 255) // 256 * 256
+    half = w.head_dim // 2
+    tab_b = w.total_kv * half * 8
+    krot_b = w.total_kv * w.h_kv * w.head_dim * 2
+    off_krot = attn.workspace.numel() - r256(krot_b)
+    off_tab = off_krot - r256(tab_b)
+    tab = attn.workspace[off_tab:off_tab + tab_b].cpu().numpy().view(np.float32)
+    krot = attn.workspace[off_krot:off_krot + krot_b].cpu().view(w.k.dtype)
+    return tab.reshape(-1, half, 2), krot.reshape(w.total_kv, w.h_kv, w.head_dim)
+
+
+def _run_rope(idx):
     w = wl.config(idx)
     d = wl.device_inputs(w)
     attn = ta.TreeAttention(d["q"], d["k"], d["q_indptr"], d["tree_order"], w.rotary_mode,
                             w.rope_scale, w.rope_theta, w.sm_scale)
     attn(**d)
     assert ta.device_status(attn.workspace) == ta.TA_OK
-    half = w.head_dim // 2
-    nbytes = w.total_kv * half * 8
-    krot = w.total_kv * w.h_kv * w.head_dim * 2     # rotated keys follow the table
-    off = attn.workspace.numel() - ((krot + 255) // 256) * 256 - ((nbytes + 255) // 256) * 256
-    tab = attn.workspace[off:off + nbytes].cpu().numpy().view(np.float32).reshape(-1, half, 2)
+    return w, attn
+
+
+@pytest.mark.parametrize("idx", [2, 3, 4])
+def test_rope_table_matches_correctly_rounded_cos_sin(idx):
+    """The per-kv-token cos/sin table (written by the key-rotation kernel,
+    read by the attention kernel for its q rows) equals float32-rounded
+    cos/sin of the pages' float32 angle; only rare near-ties (true value
+    within ~1e-4 ulp of a rounding midpoint) may differ by one ulp."""
+    w, attn = _run_rope(idx)
+    tab, _ = _rope_regions(w, attn)
     c, s = oracle.rope_cos_sin(w.rope_position, w.head_dim, w.rope_theta, w.rope_scale)
     bad = int(np.sum(tab[..., 0] != c) + np.sum(tab[..., 1] != s))
     assert bad <= max(2, c.size * 2 // 100000), f"{bad} of {2 * c.size} entries differ"
     ulps = np.abs(tab[..., 0].view(np.int32).astype(np.int64) - c.view(np.int32))
     assert ulps.max() <= 1
+
+
+@pytest.mark.parametrize("idx", [2, 3, 4])
+def test_rotated_keys_match_oracle_rope(idx):
+    """The key-rotation kernel gives the oracle's ``apply_rope`` of k (the pages' float32 steps, one rounding
+    to the storage dtype); a near-tie cos/sin may move an element by one
+    storage ulp, rarely."""
+    w, attn = _run_rope(idx)
+    _, krot = _rope_regions(w, attn)
+    ref = oracle.apply_rope(w.k, w.rope_position, w.rope_theta, w.rope_scale)
+    diff = krot != ref
+    n_bad = int(diff.sum())
+    assert n_bad <= max(4, ref.numel() // 100000), f"{n_bad} of {ref.numel()} elements differ"
+    if n_bad:
+        a = krot[diff].float()
+        b = ref[diff].float()
+        ulp = 2.0 ** -7 if w.dtype == "bf16" else 2.0 ** -10
+        assert bool(((a - b).abs() <= ulp * b.abs().clamp_min(2.0 ** -14) * 1.01).all())

@@ -86,8 +86,9 @@ def lib() -> ctypes.CDLL:
     L.tree_attn_plan.argtypes = [i32p, i32p, i32p, i32p, i32p, ctypes.c_int32, ctypes.c_float,
                                  ctypes.c_float, ctypes.POINTER(Dims), vp, sz, vp]
     L.tree_attn_plan.restype = ctypes.c_int
-    L.tree_attn_run.argtypes = [vp, vp, vp, i32p, i32p, i32p, i32p, vp, vp, ctypes.c_int32,
-                                ctypes.c_float, ctypes.POINTER(Dims), vp, sz, vp]
+    L.tree_attn_run.argtypes = [vp, vp, vp, i32p, i32p, i32p, i32p, i32p, vp, vp,
+                                ctypes.c_int32, ctypes.c_float, ctypes.c_float, ctypes.c_float,
+                                ctypes.POINTER(Dims), vp, sz, vp]
     L.tree_attn_run.restype = ctypes.c_int
     L.tree_attn_noalloc.argtypes = [vp, i32p, vp, vp, i32p, i32p, i32p, i32p, vp, vp,
                                     ctypes.c_int32, ctypes.c_float, ctypes.c_float,
@@ -316,15 +317,17 @@ def plan(q, q_indptr, k, kv_indptr, q_rope_position, mn_indptr, tree_order,
         raise TreeAttnError(st, "tree_attn_plan")
 
 
-def run(q, k, v, q_indptr, kv_indptr, mn_indptr, tree_order, out, lse, rotary_mode: int,
-        sm_scale: float, workspace: torch.Tensor, stream=None) -> None:
-    """Enqueue the attention kernel on the plan held in ``workspace``."""
+def run(q, k, v, q_indptr, kv_indptr, q_rope_position, mn_indptr, tree_order, out, lse,
+        rotary_mode: int, rope_scale: float, rope_theta: float, sm_scale: float,
+        workspace: torch.Tensor, stream=None) -> None:
+    """Enqueue the key rotation (RoPE) and the attention kernel on the plan
+    held in ``workspace``."""
     dims = make_dims(q, k, q_indptr, tree_order, rotary_mode)
     st = lib().tree_attn_run(_ptr(q), _ptr(k), _ptr(v), _ptr(q_indptr), _ptr(kv_indptr),
-                             _ptr(mn_indptr), _ptr(tree_order), _ptr(out), _ptr(lse),
-                             int(rotary_mode), float(sm_scale), ctypes.byref(dims),
-                             _ptr(workspace), workspace.numel() * workspace.element_size(),
-                             _stream_ptr(stream))
+                             _ptr(q_rope_position), _ptr(mn_indptr), _ptr(tree_order), _ptr(out),
+                             _ptr(lse), int(rotary_mode), float(rope_scale), float(rope_theta),
+                             float(sm_scale), ctypes.byref(dims), _ptr(workspace),
+                             workspace.numel() * workspace.element_size(), _stream_ptr(stream))
     if st != TA_OK:
         raise TreeAttnError(st, "tree_attn_run")
 

@@ -194,11 +194,21 @@ WsPtrs ws_ptrs(void* workspace, const WsLayout& L) {
                 split ? reinterpret_cast<float*>(ws + L.off_part_lse) : nullptr};
 }
 
+// fl32(theta^(2i/d)) for i < d/2, the RoPE frequency denominators of
+// ``_rope`` (page "_kernel_common.py"), rounded once from float64; 1 past d/2
+void rope_denominators(float rope_theta, int head_dim, float* den) {
+  for (int i = 0; i < 64; ++i) den[i] = 1.f;
+  const double l2 = std::log2((double)rope_theta);
+  for (int i = 0; i < head_dim / 2; ++i)
+    den[i] = (float)std::exp2(l2 * ((2.0 * i) / (double)head_dim));
+}
+
+// The plan kernel (work records, tile classes, longest-first order); RoPE
+// needs nothing from it.
 ta_status launch_plan_checked(const int32_t* q_indptr, const int32_t* kv_indptr,
-                              const int32_t* q_rope_position, const int32_t* mn_indptr,
-                              const int32_t* tree_order, int32_t rotary_mode, float rope_scale,
-                              float rope_theta, const ta_dims* dims, void* workspace,
-                              cudaStream_t st, int max_chunks = 1, int chunk_tiles = 0) {
+                              const int32_t* mn_indptr, const int32_t* tree_order,
+                              const ta_dims* dims, void* workspace, cudaStream_t st,
+                              int max_chunks = 1, int chunk_tiles = 0) {
   const int g = dims->h_q / dims->h_kv;
   const WsLayout L = layout_of(dims, max_chunks);
   const WsPtrs w = ws_ptrs(workspace, L);
@@ -209,7 +219,6 @@ ta_status launch_plan_checked(const int32_t* q_indptr, const int32_t* kv_indptr,
   pp.kv_indptr = kv_indptr;
   pp.mn_indptr = mn_indptr;
   pp.tree_order = tree_order;
-  pp.rope_pos = q_rope_position;
   pp.batch = dims->batch_size;
   pp.g = g;
   pp.R = ta::rows_per_item(g);
@@ -218,35 +227,22 @@ ta_status launch_plan_checked(const int32_t* q_indptr, const int32_t* kv_indptr,
   pp.total_q = dims->total_q;
   pp.total_kv = dims->total_kv;
   pp.total_tree = dims->total_tree;
-  pp.rotary = rotary_mode;
   pp.max_pairs = L.max_pairs;
   pp.max_chunks = max_chunks;
   pp.chunk_tiles = chunk_tiles;
   pp.pipes = 2 * nsm;
   pp.merge = w.merge;
-  pp.rope_scale = rope_scale;
-  pp.rope_theta = rope_theta;
-  for (int i = 0; i < 64; ++i) pp.rope_den[i] = 1.f;
-  if (rotary_mode == 1) {
-    const double l2 = std::log2((double)rope_theta);
-    for (int i = 0; i < dims->head_dim / 2; ++i)
-      pp.rope_den[i] = (float)std::exp2(l2 * ((2.0 * i) / (double)dims->head_dim));
-  }
   pp.hdr = w.hdr;
   pp.sorted = w.sorted;
   pp.classes = w.classes;
-  pp.rope_cs = w.rope_cs;
-  // with RoPE, enough CTAs (6 per SM) that the latency-bound cos/sin table
-  // is spread over many warps
-  int plan_grid = (int)L.max_pairs;
-  if (rotary_mode == 1 && plan_grid < 6 * nsm) plan_grid = 6 * nsm;
-  return ta::launch_plan(pp, plan_grid, st) == cudaSuccess ? TA_OK : TA_ERR_CUDA;
+  return ta::launch_plan(pp, (int)L.max_pairs, st) == cudaSuccess ? TA_OK : TA_ERR_CUDA;
 }
 
 ta_status launch_run_checked(const void* q, const void* k, const void* v, const int32_t* q_indptr,
-                             const int32_t* kv_indptr, const int32_t* mn_indptr,
-                             const int32_t* tree_order, void* out, float* lse,
-                             int32_t rotary_mode, float sm_scale, const ta_dims* dims,
+                             const int32_t* kv_indptr, const int32_t* q_rope_position,
+                             const int32_t* mn_indptr, const int32_t* tree_order, void* out,
+                             float* lse, int32_t rotary_mode, float rope_scale,
+                             float rope_theta, float sm_scale, const ta_dims* dims,
                              void* workspace, cudaStream_t st, int max_chunks = 1) {
   const int g = dims->h_q / dims->h_kv;
   const int R = ta::rows_per_item(g);
@@ -260,8 +256,16 @@ ta_status launch_run_checked(const void* q, const void* k, const void* v, const 
   const void* k_attn = k;
   if (rotary_mode == 1) {
     void* krot = static_cast<uint8_t*>(workspace) + L.off_krot;
-    if (ta::launch_krot(k, krot, w.rope_cs, dims->total_kv, dims->h_kv, D,
-                        dims->dtype == TA_BF16, 4 * nsm, st) != cudaSuccess)
+    ta::KrotParams kp{};
+    rope_denominators(rope_theta, D, kp.rope_den);
+    kp.rope_scale = rope_scale;
+    kp.total_kv = dims->total_kv;
+    kp.h_kv = dims->h_kv;
+    // one resident wave at most (8 warps per CTA, one token per warp at a time)
+    const int64_t want = ((int64_t)dims->total_kv + 7) / 8;
+    const int kgrid = (int)(want < 4 * nsm ? want : 4 * nsm);
+    if (ta::launch_krot(k, krot, q_rope_position, w.rope_cs, kp, D, dims->dtype == TA_BF16,
+                        kgrid, st) != cudaSuccess)
       return TA_ERR_CUDA;
     k_attn = krot;
   }
@@ -313,8 +317,8 @@ ta_status launch_run_checked(const void* q, const void* k, const void* v, const 
     mp.h_q = dims->h_q;
     mp.h_kv = dims->h_kv;
     mp.g = g;
-    const int64_t units = L.max_pairs * dims->h_kv * (ta::kBlockM / 32);
-    const int mgrid = (int)(units < 4 * nsm ? units : 4 * nsm);
+    const int64_t units = L.max_pairs * dims->h_kv * (ta::kBlockM / 8);   // 8 rows each
+    const int mgrid = (int)(units < 16 * nsm ? units : 16 * nsm);
     if (ta::launch_merge(mp, D, bf16, mgrid, st) != cudaSuccess) return TA_ERR_CUDA;
   }
   return TA_OK;
@@ -335,25 +339,27 @@ ta_status tree_attn_plan(const int32_t* q_indptr, const int32_t* kv_indptr,
   s = check_plan_args(q_rope_position, rotary_mode, rope_scale, rope_theta, dims);
   if (s != TA_OK) return s;
   if (dims->total_q == 0) return TA_OK;
-  return launch_plan_checked(q_indptr, kv_indptr, q_rope_position, mn_indptr, tree_order,
-                             rotary_mode, rope_scale, rope_theta, dims, workspace,
+  return launch_plan_checked(q_indptr, kv_indptr, mn_indptr, tree_order, dims, workspace,
                              static_cast<cudaStream_t>(stream));
 }
 
 ta_status tree_attn_run(const void* q, const void* k, const void* v, const int32_t* q_indptr,
-                        const int32_t* kv_indptr, const int32_t* mn_indptr,
-                        const int32_t* tree_order, void* out, float* lse, int32_t rotary_mode,
+                        const int32_t* kv_indptr, const int32_t* q_rope_position,
+                        const int32_t* mn_indptr, const int32_t* tree_order, void* out,
+                        float* lse, int32_t rotary_mode, float rope_scale, float rope_theta,
                         float sm_scale, const ta_dims* dims, void* workspace,
                         size_t workspace_bytes, void* stream) {
   ta_status s = check_common(q_indptr, kv_indptr, mn_indptr, tree_order, rotary_mode, dims,
                              workspace, workspace_bytes);
   if (s != TA_OK) return s;
+  s = check_plan_args(q_rope_position, rotary_mode, rope_scale, rope_theta, dims);
+  if (s != TA_OK) return s;
   s = check_run_args(q, k, v, out, lse, sm_scale, dims);
   if (s != TA_OK) return s;
   if (dims->total_q == 0) return TA_OK;
-  return launch_run_checked(q, k, v, q_indptr, kv_indptr, mn_indptr, tree_order, out, lse,
-                            rotary_mode, sm_scale, dims, workspace,
-                            static_cast<cudaStream_t>(stream));
+  return launch_run_checked(q, k, v, q_indptr, kv_indptr, q_rope_position, mn_indptr, tree_order,
+                            out, lse, rotary_mode, rope_scale, rope_theta, sm_scale, dims,
+                            workspace, static_cast<cudaStream_t>(stream));
 }
 
 ta_status tree_attn(const void* q, const int32_t* q_indptr, const void* k, const void* v,
@@ -370,11 +376,11 @@ ta_status tree_attn(const void* q, const int32_t* q_indptr, const void* k, const
   if (s != TA_OK) return s;
   if (dims->total_q == 0) return TA_OK;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  s = launch_plan_checked(q_indptr, kv_indptr, q_rope_position, mn_indptr, tree_order,
-                          rotary_mode, rope_scale, rope_theta, dims, workspace, st);
+  s = launch_plan_checked(q_indptr, kv_indptr, mn_indptr, tree_order, dims, workspace, st);
   if (s != TA_OK) return s;
-  return launch_run_checked(q, k, v, q_indptr, kv_indptr, mn_indptr, tree_order, out, lse,
-                            rotary_mode, sm_scale, dims, workspace, st);
+  return launch_run_checked(q, k, v, q_indptr, kv_indptr, q_rope_position, mn_indptr,
+                            tree_order, out, lse, rotary_mode, rope_scale, rope_theta,
+                            sm_scale, dims, workspace, st);
 }
 
 ta_status tree_attn_split(const void* q, const int32_t* q_indptr, const void* k, const void* v,
@@ -394,12 +400,12 @@ ta_status tree_attn_split(const void* q, const int32_t* q_indptr, const void* k,
   if (s != TA_OK) return s;
   if (dims->total_q == 0) return TA_OK;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  s = launch_plan_checked(q_indptr, kv_indptr, q_rope_position, mn_indptr, tree_order,
-                          rotary_mode, rope_scale, rope_theta, dims, workspace, st, max_chunks,
-                          chunk_tiles);
+  s = launch_plan_checked(q_indptr, kv_indptr, mn_indptr, tree_order, dims, workspace, st,
+                          max_chunks, chunk_tiles);
   if (s != TA_OK) return s;
-  return launch_run_checked(q, k, v, q_indptr, kv_indptr, mn_indptr, tree_order, out, lse,
-                            rotary_mode, sm_scale, dims, workspace, st, max_chunks);
+  return launch_run_checked(q, k, v, q_indptr, kv_indptr, q_rope_position, mn_indptr,
+                            tree_order, out, lse, rotary_mode, rope_scale, rope_theta,
+                            sm_scale, dims, workspace, st, max_chunks);
 }
 
 ta_status tree_attn_merge_states(const void* parts, const float* lses, int32_t n_parts,
@@ -636,7 +642,6 @@ ta_status tree_attn_paged(const void* q, const int32_t* q_indptr, const void* pa
   pp.kv_indptr = nullptr;
   pp.mn_indptr = mn_indptr;
   pp.tree_order = tree_order;
-  pp.rope_pos = nullptr;
   pp.paged = 1;
   pp.page_indptr = page_indptr;
   pp.length_info = length_info;
@@ -649,19 +654,14 @@ ta_status tree_attn_paged(const void* q, const int32_t* q_indptr, const void* pa
   pp.total_q = d.total_q;
   pp.total_kv = d.total_kv;
   pp.total_tree = d.total_tree;
-  pp.rotary = 0;
   pp.max_pairs = L.max_pairs;
   pp.max_chunks = 1;
   pp.chunk_tiles = 0;
   pp.pipes = 2 * nsm;
   pp.merge = nullptr;
-  pp.rope_scale = 1.f;
-  pp.rope_theta = 1.f;
-  for (int i = 0; i < 64; ++i) pp.rope_den[i] = 1.f;
   pp.hdr = w.hdr;
   pp.sorted = w.sorted;
   pp.classes = w.classes;
-  pp.rope_cs = w.rope_cs;
   if (ta::launch_plan(pp, (int)L.max_pairs, st) != cudaSuccess) return TA_ERR_CUDA;
   // run: K and V tiles gathered page by page from the pool
   CUtensorMap tm_q, tm_pages;

@@ -523,8 +523,8 @@ __device__ void run_softmax(const Pipe& pp, const AttnParams& p, int sw, int lan
     float m_ref = -INFINITY, l = 0.f;
     if (r.n_tiles > 0) {
       if (p.rotary) {
-        // q row r of the tile takes the position of its own tree node's kv slot
-        // (the first cos/sin batch is fetched while the Q tile lands)
+        // q row r of the tile takes the position of its own tree node's kv
+        // slot (the first cos/sin batch is fetched while the Q tile lands)
         const long long qtok0 = (long long)r.kv_base + (r.kv - r.qo) + (long long)r.t * R;
         const RopeRange rr = rope_range<D>(r.nq, g, wq);
         float4 cv[2][4];

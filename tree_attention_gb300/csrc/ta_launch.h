@@ -37,14 +37,13 @@ struct PlanParams {
   const int32_t* kv_indptr;
   const int32_t* mn_indptr;
   const int32_t* tree_order;
-  const int32_t* rope_pos;  // may be null when rotary == 0
   // paged KV cache (paged != 0): kv rows come from 16-slot pages; kv_indptr
   // is unused, the kv length of sequence b is (pages - 1) * 16 + length_info[b]
   int paged;
   const int32_t* page_indptr;
   const int32_t* length_info;
   int nnz_pages;
-  int batch, g, R, h_kv, head_dim, total_q, total_kv, total_tree, rotary;
+  int batch, g, R, h_kv, head_dim, total_q, total_kv, total_tree;
   int64_t max_pairs;
   // split-KV: a pair's kv tiles are cut into up to max_chunks records of
   // about chunk_tiles tiles (0: chosen from the batch's total work so that
@@ -52,14 +51,9 @@ struct PlanParams {
   // times); max_chunks == 1 disables it
   int max_chunks, chunk_tiles, pipes;
   int4* merge;       // per pair (split-KV): q_row0, q rows, chunks, first record
-  float rope_scale, rope_theta;
-  // fl32(theta^(2i/d)) for i < d/2, the RoPE frequency denominators of
-  // ``_rope`` (page "_kernel_common.py"), rounded once from float64 on the host
-  float rope_den[64];
   WsHeader* hdr;
   ItemRec* sorted;   // one record per (sequence, q tile) or chunk of one, longest first
   uint8_t* classes;
-  float2* rope_cs;
 };
 
 struct AttnParams {
@@ -68,7 +62,7 @@ struct AttnParams {
   float* lse;
   const ItemRec* sorted;
   const uint8_t* classes;
-  const float2* rope_cs;
+  const float2* rope_cs;   // [total_kv][head_dim / 2] cos/sin per kv token (RoPE)
   WsHeader* hdr;
   const int32_t* page_values;   // paged KV cache: physical page of each (sequence, page)
   int num_pages;                // pages in the pool (an out-of-range page reads zeros)
@@ -93,14 +87,25 @@ struct MergeParams {
   int h_q, h_kv, g;
 };
 
-// Plan kernel: sequence/tile enumeration, tile classification, LPT ordering
-// and the RoPE cos/sin table.  ``grid`` >= max_pairs.
+// Plan kernel: sequence/tile enumeration, tile classification and LPT
+// ordering.  ``grid`` >= max_pairs.
 cudaError_t launch_plan(const PlanParams& p, int grid, cudaStream_t stream);
 
-// Rotates every key once: krot[t, h, :] = rope(k[t, h, :]) with the plan's
-// cos/sin table (rows of all kv tokens).
-cudaError_t launch_krot(const void* k, void* krot, const float2* rope_cs, int total_kv, int h_kv,
-                        int head_dim, bool bf16, int grid, cudaStream_t stream);
+// Key rotation: the RoPE frequency denominators fl32(theta^(2i/d)) for
+// i < d/2 (``_rope``, page "_kernel_common.py"; rounded once from float64 on
+// the host), the position scale and the sizes.
+struct KrotParams {
+  float rope_den[64];
+  float rope_scale;
+  int total_kv, h_kv;
+};
+
+// RoPE of every kv token: the cos/sin table row of token t at position
+// rope_pos[t] (rope_cs[t][i] = (cos, sin) of frequency i) and the rotated
+// keys krot[t, h, :] = rope(k[t, h, :]).
+cudaError_t launch_krot(const void* k, void* krot, const int32_t* rope_pos, float2* rope_cs,
+                        const KrotParams& kp, int head_dim, bool bf16, int grid,
+                        cudaStream_t stream);
 
 // Dense mask export (test helper).
 cudaError_t launch_mask_dense(const int32_t* q_indptr, const int32_t* kv_indptr,

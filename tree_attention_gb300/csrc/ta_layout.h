@@ -88,7 +88,8 @@ struct WsLayout {
 // Workspace layout for the given sizes (all offsets 256-byte aligned):
 //   header | ItemRec sorted[max_records] (longest-first order)
 //   | uint8 classes[]
-//   and with RoPE: | float2 rope_cs[total_kv][head_dim / 2] (rows of q tokens)
+//   and with RoPE: | float2 rope_cs[total_kv][head_dim / 2] (cos / sin of
+//                    every kv token's position; q rows read their own node's)
 //                  | rotated k [total_kv][h_kv][head_dim] (storage dtype)
 //   and with split-KV: | int4 merge[max_pairs] (per pair: q_row0, nq, chunks,
 //                        first record) | float part_o[max_records][h_kv][128][d]

@@ -117,11 +117,48 @@ __device__ __forceinline__ void merge_row(int n, LseOf lse_of, OOf o_of, uint16_
   if (lane == 0) *lse_out = z > 0.f ? m + log2f(z) : -INFINITY;
 }
 
-// Split-KV merge: a unit is a quarter (32 packed rows) of one (pair, kv
-// head); warp w of the CTA takes the unit's rows w, w + 8, ...  (packed row =
-// q row * g + head in the group, the row order of the attention kernel's
-// tiles).
-constexpr int kMergeQuarters = kBlockM / 32;
+// merge_row for n <= kMax parts with every load of the row in flight at once:
+// the lanes fetch the lses while all parts' rows are loaded into registers.
+template <int D, bool BF16, int kMax, typename LseOf, typename OOf>
+__device__ __forceinline__ void merge_row_few(int n, LseOf lse_of, OOf o_of, uint16_t* out_row,
+                                              float* lse_out, int lane) {
+  constexpr int V = D / 32;
+  const float lc = lane < n ? lse_of(lane) : -INFINITY;
+  RowVec<D> o[kMax];
+#pragma unroll
+  for (int c = 0; c < kMax; ++c)
+    if (c < n) o[c] = o_of(c);
+  float m = lc;
+#pragma unroll
+  for (int s = 16; s > 0; s >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, s));
+  const float wl = (m == -INFINITY || lc == -INFINITY) ? 0.f : exp2f(lc - m);
+  float z = wl;
+#pragma unroll
+  for (int s = 16; s > 0; s >>= 1) z += __shfl_xor_sync(0xffffffffu, z, s);
+  float acc[V];
+#pragma unroll
+  for (int i = 0; i < V; ++i) acc[i] = 0.f;
+#pragma unroll
+  for (int c = 0; c < kMax; ++c) {
+    if (c < n) {
+      const float w = __shfl_sync(0xffffffffu, wl, c);
+#pragma unroll
+      for (int i = 0; i < V; ++i) acc[i] += w != 0.f ? w * o[c].v[i] : 0.f;
+    }
+  }
+  const float inv = z > 0.f ? 1.f / z : 0.f;
+#pragma unroll
+  for (int i = 0; i < V; ++i) acc[i] *= inv;
+  store_half<D, BF16>(out_row, acc, lane);
+  if (lane == 0) *lse_out = z > 0.f ? m + log2f(z) : -INFINITY;
+}
+
+// Split-KV merge: a unit is 8 packed rows of one (pair, kv head), one row per
+// warp (packed row = q row * g + head in the group, the row order of the
+// attention kernel's tiles).
+constexpr int kMergeRowsPerUnit = kMergeThreads / 32;
+constexpr int kMergeUnitsPerItem = kBlockM / kMergeRowsPerUnit;
+static_assert(kMaxChunks <= 32, "one lane per chunk's lse");
 
 template <int D, bool BF16>
 __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeParams p) {
@@ -130,27 +167,25 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeParams 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const unsigned int np = *(volatile const unsigned int*)&p.hdr->num_pairs;
   const long long n_pairs = (long long)np < p.max_pairs ? (long long)np : p.max_pairs;
-  const long long units = n_pairs * p.h_kv * kMergeQuarters;
+  const long long units = n_pairs * p.h_kv * kMergeUnitsPerItem;
   const int g = p.g;
   uint16_t* outp = static_cast<uint16_t*>(p.out);
   for (long long u = blockIdx.x; u < units; u += gridDim.x) {
-    const int quarter = (int)(u % kMergeQuarters);
-    const long long ph = u / kMergeQuarters;
+    const int part8 = (int)(u % kMergeUnitsPerItem);
+    const long long ph = u / kMergeUnitsPerItem;
     const int pair = (int)(ph / p.h_kv), kvh = (int)(ph % p.h_kv);
     const int4 mr = p.merge[pair];   // q_row0, q rows, chunks, first record
-    if (mr.z <= 1 || mr.w < 0 || (long long)mr.w + mr.z > p.max_records) continue;
-    const int rows = min(mr.y * g, (quarter + 1) * 32);
-    for (int pr = quarter * 32 + warp; pr < rows; pr += kMergeThreads / 32) {
-      const int qr = pr / g, hh = pr - qr * g;
-      const size_t orow = (size_t)(mr.x + qr) * p.h_q + (size_t)kvh * g + hh;
-      auto slot = [&](int c) {
-        return (((size_t)(mr.w + c)) * p.h_kv + kvh) * kBlockM + pr;
-      };
-      merge_row<D, BF16>(
-          mr.z, [&](int c) { return __ldg(p.part_lse + slot(c)); },
-          [&](int c) { return load_f32<D>(p.part_o + slot(c) * D, lane); }, outp + orow * D,
-          p.lse + orow, lane);
-    }
+    if (mr.z <= 1 || mr.z > kMaxChunks || mr.w < 0 || (long long)mr.w + mr.z > p.max_records)
+      continue;
+    const int pr = part8 * kMergeRowsPerUnit + warp;
+    if (pr >= mr.y * g) continue;
+    const int qr = pr / g, hh = pr - qr * g;
+    const size_t orow = (size_t)(mr.x + qr) * p.h_q + (size_t)kvh * g + hh;
+    auto slot = [&](int c) { return (((size_t)(mr.w + c)) * p.h_kv + kvh) * kBlockM + pr; };
+    merge_row_few<D, BF16, kMaxChunks>(
+        mr.z, [&](int c) { return __ldg(p.part_lse + slot(c)); },
+        [&](int c) { return load_f32<D>(p.part_o + slot(c) * D, lane); }, outp + orow * D,
+        p.lse + orow, lane);
   }
 }
 
@@ -164,10 +199,12 @@ __global__ void __launch_bounds__(kMergeThreads)
   const long long warps = (long long)gridDim.x * (kMergeThreads / 32);
   for (long long row = (long long)blockIdx.x * (kMergeThreads / 32) + (threadIdx.x >> 5);
        row < rows; row += warps) {
-    merge_row<D, BF16>(
-        n, [&](int c) { return __ldg(lses + (size_t)c * rows + row); },
-        [&](int c) { return load_half<D, BF16>(parts + ((size_t)c * rows + row) * D, lane); },
-        out + row * D, lse + row, lane);
+    auto lse_of = [&](int c) { return __ldg(lses + (size_t)c * rows + row); };
+    auto o_of = [&](int c) { return load_half<D, BF16>(parts + ((size_t)c * rows + row) * D, lane); };
+    if (n <= 8)
+      merge_row_few<D, BF16, 8>(n, lse_of, o_of, out + row * D, lse + row, lane);
+    else
+      merge_row<D, BF16>(n, lse_of, o_of, out + row * D, lse + row, lane);
   }
 }
 

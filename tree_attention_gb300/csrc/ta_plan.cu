@@ -11,8 +11,6 @@
 //      FULL exactly from the DFS intervals of ``_check_tree_order`` (page
 //      "tree_attn.py") and writes the pair's item record -- with split-KV, one
 //      record per chunk of the pair's kv tiles plus the pair's merge record;
-//   3. (all warps) fills its share of the RoPE cos/sin table, one entry per
-//      (kv token, frequency), in the float32 steps of ``_rope``.
 #include <cuda_runtime.h>
 
 #include <climits>
@@ -155,8 +153,6 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanParams p) 
   __shared__ int s_any[kPassTiles], s_notall[kPassTiles];
   __shared__ uint32_t s_cls2[3];
   __shared__ int s_count;
-  __shared__ float s_den[64];
-  __shared__ float4 s_sct[27];
   __shared__ int s_hist[kCostBuckets];
 
   pdl_wait();
@@ -164,12 +160,6 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanParams p) 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int B = p.batch, R = p.R;
   // ---- 0. constants and counters of this CTA
-  if (p.rotary) {
-    if (tid < 64) s_den[tid] = p.rope_den[tid];
-    if (tid < 27)
-      s_sct[tid] = make_float4(kSinCosTable[tid][0], kSinCosTable[tid][1], kSinCosTable[tid][2],
-                               kSinCosTable[tid][3]);
-  }
   for (int i = tid; i < kCostBuckets; i += kPlanThreads) s_hist[i] = 0;
   if (tid == 0) {
     s_bad = 0;
@@ -377,6 +367,10 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanParams p) 
       }
     }
     const int kvt = (kv + kBlockN - 1) / kBlockN;
+    // tiles wholly inside the causal prefix are FULL for every row (a pair
+    // has at least one row, and such a tile ends at or before the tree
+    // start, so it is not ragged): their columns need no look-up
+    const int prefix_tiles = ts / kBlockN;
     if (tid < 3) s_cls2[tid] = 0;
     // up to kPassTiles kv tiles per pass; every thread takes every 128th
     // column of the pass and folds its verdict into per-tile flags
@@ -388,7 +382,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanParams p) 
       }
       group_sync(kBarA);
       const int c_end = min(kv, (j0 + nt) * kBlockN);
-      for (int c = j0 * kBlockN + tid; c < c_end; c += kGroup) {
+      for (int c = max(j0, prefix_tiles) * kBlockN + tid; c < c_end; c += kGroup) {
         int cnt;
         if (c < ts) {
           cnt = nrows;
@@ -405,7 +399,9 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanParams p) 
         const int j = j0 + i;
         const bool ragged = (j + 1) * kBlockN > kv;
         const uint8_t cls =
-            !s_any[i] ? kTileEmpty : ((!s_notall[i] && !ragged) ? kTileFull : kTilePartial);
+            j < prefix_tiles
+                ? kTileFull
+                : (!s_any[i] ? kTileEmpty : ((!s_notall[i] && !ragged) ? kTileFull : kTilePartial));
         p.classes[off + j] = cls;
         if (cls != kTileEmpty) {
           atomicAdd(&s_count, 1);
@@ -453,81 +449,42 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanParams p) 
       p.merge[pair] = make_int4(q0 + r0, nrows, nch, (int)pos);
   }
 
-  // ---- 5. the RoPE cos/sin table, one entry per (kv token, frequency), in
-  // the float32 steps of ``_rope`` (page "_kernel_common.py"): angle =
-  // fl32(fl32(pos * scale) / fl32(theta^(2i/d))), cos and sin of it rounded
-  // correctly to float32 (cr_sincosf).  8-token chunks are dealt out over
-  // every warp of the grid, first to the warps with nothing else to do.
-  if (p.rotary) {
-    const int D = p.head_dim, half = D / 2;
-    // warp ranks: the CTAs without a pair first (all 8 warps), then warps
-    // 4-7 of the CTAs with one, then their warps 0-3 (busy classifying)
-    const long long grid = gridDim.x;
-    const long long n_busy = ok ? min(total_tiles, grid) : 0;   // CTAs with a pair: 0..n_busy-1
-    const long long idle_warps = (grid - n_busy) * 8;
-    long long rank;
-    if (!has_pair)
-      rank = ((long long)blockIdx.x - n_busy) * 8 + warp;
-    else if (warp >= 4)
-      rank = idle_warps + (long long)blockIdx.x * 4 + (warp - 4);
-    else
-      rank = idle_warps + n_busy * 4 + (long long)blockIdx.x * 4 + warp;
-    // tokens per chunk: enough to cover the table in about one chunk per
-    // warp, even (two tokens per step), at most 32 (one per lane)
-    const long long per_warp = ((long long)p.total_kv + grid * 8 - 1) / (grid * 8);
-    const int kChunk = (int)min(32LL, max(2LL, (per_warp + 1) & ~1LL));
-    const long long n_chunks = ((long long)p.total_kv + kChunk - 1) / kChunk;
-    // lane l computes frequencies (2l, 2l+1) (d = 128) or, for d = 64, lanes
-    // 0..15 compute them and lanes 16..31 repeat the work of lanes 0..15
-    const int pl = (D == 128) ? lane : (lane & 15);
-    const float den0 = s_den[2 * pl], den1 = s_den[2 * pl + 1];
-    for (long long ch = rank; ch < n_chunks; ch += grid * 8) {
-      const long long base = ch * kChunk;
-      const int ntok = (int)min((long long)kChunk, (long long)p.total_kv - base);
-      const int my_pos = lane < ntok ? p.rope_pos[base + lane] : 0;
-      // two tokens per step: four independent sin/cos evaluations in flight
-      for (int u = 0; u < ntok; u += 2) {
-        const bool two = u + 1 < ntok;
-        const int pos_a = __shfl_sync(0xffffffffu, my_pos, u);
-        const int pos_b = __shfl_sync(0xffffffffu, my_pos, two ? u + 1 : u);
-        const float sa = __fmul_rn((float)pos_a, p.rope_scale);
-        const float sb = __fmul_rn((float)pos_b, p.rope_scale);
-        float s0a, c0a, s1a, c1a, s0b, c0b, s1b, c1b;
-        cr_sincosf(__fdiv_rn(sa, den0), &s0a, &c0a, s_sct);
-        cr_sincosf(__fdiv_rn(sa, den1), &s1a, &c1a, s_sct);
-        cr_sincosf(__fdiv_rn(sb, den0), &s0b, &c0b, s_sct);
-        cr_sincosf(__fdiv_rn(sb, den1), &s1b, &c1b, s_sct);
-        if (D == 128 || lane < 16) {
-          float4* row = reinterpret_cast<float4*>(p.rope_cs + (base + u) * half);
-          row[pl] = make_float4(c0a, s0a, c1a, s1a);
-          if (two) row[half / 2 + pl] = make_float4(c0b, s0b, c1b, s1b);
-        }
-      }
-    }
-  }
 }
 
-// One warp per kv token at a time: lane l holds the cos/sin of frequencies
-// (2l', 2l'+1) (one float4 of the table row) and rotates those element pairs
-// of every kv head -- words l' of the first half and d/4 + l' of the second
-// half of the head's row -- with the float32 steps of ``_rope``.  For d = 64
-// lanes 16..31 take the odd heads.
+// RoPE (``_rope`` on the page "_kernel_common.py") of every kv token, once
+// per call: one warp per token at a time, lane l evaluates the cos/sin of
+// frequencies (2l', 2l'+1) in the pages' float32 steps -- angle =
+// fl32(fl32(pos * scale) / fl32(theta^(2i/d))), cos and sin of it rounded
+// correctly to float32 (cr_sincosf) -- writes them to the token's row of the
+// cos/sin table (read by the attention kernel for its q rows) and rotates
+// those element pairs of every kv head: words l' of the first half and
+// d/4 + l' of the second half of the head's row.  For d = 64 lanes 16..31
+// take the odd heads.  The token's keys are loaded before the sin/cos
+// evaluation, so the loads are in flight while it runs.
 template <bool BF16, int D>
 __global__ void __launch_bounds__(256) krot_kernel(const uint32_t* __restrict__ k,
                                                    uint32_t* __restrict__ krot,
-                                                   const float4* __restrict__ cs, int total_kv,
-                                                   int h_kv) {
+                                                   const int32_t* __restrict__ pos,
+                                                   float4* __restrict__ cs,
+                                                   const KrotParams kp) {
   constexpr int kWords = D / 2;  // 32-bit words per head row
+  __shared__ float4 s_sct[27];
   const int lane = threadIdx.x & 31;
   const int pl = (D == 128) ? lane : (lane & 15);
   const int h0 = (D == 128) ? 0 : (lane >> 4);
   constexpr int hstep = (D == 128) ? 1 : 2;
+  if (threadIdx.x < 27)
+    s_sct[threadIdx.x] = make_float4(kSinCosTable[threadIdx.x][0], kSinCosTable[threadIdx.x][1],
+                                     kSinCosTable[threadIdx.x][2], kSinCosTable[threadIdx.x][3]);
+  const float den0 = kp.rope_den[2 * pl], den1 = kp.rope_den[2 * pl + 1];
+  __syncthreads();
   pdl_wait();
   pdl_trigger();
+  const int h_kv = kp.h_kv;
   const long long warps = (long long)gridDim.x * (blockDim.x / 32);
   for (long long tok = (long long)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
-       tok < total_kv; tok += warps) {
-    const float4 c = __ldg(cs + tok * (D / 4) + pl);  // (cos, sin) of 2 frequencies
+       tok < kp.total_kv; tok += warps) {
+    const int ps = __ldg(pos + tok);
     for (int hb = h0; hb < h_kv; hb += 8 * hstep) {
       uint32_t w0[8], w1[8];
 #pragma unroll
@@ -539,6 +496,13 @@ __global__ void __launch_bounds__(256) krot_kernel(const uint32_t* __restrict__ 
           w1[u] = __ldg(k + e + kWords / 2 + pl);
         }
       }
+      float c0, s0, c1, s1;
+      {
+        const float sc = __fmul_rn((float)ps, kp.rope_scale);
+        cr_sincosf(__fdiv_rn(sc, den0), &s0, &c0, s_sct);
+        cr_sincosf(__fdiv_rn(sc, den1), &s1, &c1, s_sct);
+      }
+      if (hb == h0 && (D == 128 || lane < 16)) cs[tok * (D / 4) + pl] = make_float4(c0, s0, c1, s1);
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
         const int h = hb + u * hstep;
@@ -546,10 +510,10 @@ __global__ void __launch_bounds__(256) krot_kernel(const uint32_t* __restrict__ 
           const float2 x0 = unpack2<BF16>(w0[u]);
           const float2 x1 = unpack2<BF16>(w1[u]);
           // first half: cos*x[j] + sin*(-x[j+d/2]); second half: cos*x[j] + sin*x[j-d/2]
-          const float y0a = __fadd_rn(__fmul_rn(c.x, x0.x), __fmul_rn(c.y, -x1.x));
-          const float y0b = __fadd_rn(__fmul_rn(c.z, x0.y), __fmul_rn(c.w, -x1.y));
-          const float y1a = __fadd_rn(__fmul_rn(c.x, x1.x), __fmul_rn(c.y, x0.x));
-          const float y1b = __fadd_rn(__fmul_rn(c.z, x1.y), __fmul_rn(c.w, x0.y));
+          const float y0a = __fadd_rn(__fmul_rn(c0, x0.x), __fmul_rn(s0, -x1.x));
+          const float y0b = __fadd_rn(__fmul_rn(c1, x0.y), __fmul_rn(s1, -x1.y));
+          const float y1a = __fadd_rn(__fmul_rn(c0, x1.x), __fmul_rn(s0, x0.x));
+          const float y1b = __fadd_rn(__fmul_rn(c1, x1.y), __fmul_rn(s1, x0.y));
           const long long e = (tok * h_kv + h) * kWords;
           krot[e + pl] = pack2<BF16>(y0a, y0b);
           krot[e + kWords / 2 + pl] = pack2<BF16>(y1a, y1b);
@@ -593,29 +557,22 @@ cudaError_t launch_plan(const PlanParams& p, int grid, cudaStream_t stream) {
   return launch_pdl(plan_kernel, dim3(grid), dim3(kPlanThreads), 0, stream, p);
 }
 
-cudaError_t launch_krot(const void* k, void* krot, const float2* rope_cs, int total_kv, int h_kv,
-                        int head_dim, bool bf16, int grid, cudaStream_t stream) {
-  if (total_kv <= 0) return cudaSuccess;
+cudaError_t launch_krot(const void* k, void* krot, const int32_t* rope_pos, float2* rope_cs,
+                        const KrotParams& kp, int head_dim, bool bf16, int grid,
+                        cudaStream_t stream) {
+  if (kp.total_kv <= 0) return cudaSuccess;
   const uint32_t* kin = static_cast<const uint32_t*>(k);
   uint32_t* kout = static_cast<uint32_t*>(krot);
-  const float4* cs = reinterpret_cast<const float4*>(rope_cs);
-  cudaError_t e;
-  if (head_dim == 128) {
-    if (bf16)
-      e = launch_pdl(krot_kernel<true, 128>, dim3(grid), dim3(256), 0, stream, kin, kout,
-                     cs, total_kv, h_kv);
-    else
-      e = launch_pdl(krot_kernel<false, 128>, dim3(grid), dim3(256), 0, stream, kin, kout,
-                     cs, total_kv, h_kv);
-  } else {
-    if (bf16)
-      e = launch_pdl(krot_kernel<true, 64>, dim3(grid), dim3(256), 0, stream, kin, kout,
-                     cs, total_kv, h_kv);
-    else
-      e = launch_pdl(krot_kernel<false, 64>, dim3(grid), dim3(256), 0, stream, kin, kout,
-                     cs, total_kv, h_kv);
-  }
-  return e;
+  float4* cs = reinterpret_cast<float4*>(rope_cs);
+  if (head_dim == 128)
+    return bf16 ? launch_pdl(krot_kernel<true, 128>, dim3(grid), dim3(256), 0, stream, kin, kout,
+                             rope_pos, cs, kp)
+                : launch_pdl(krot_kernel<false, 128>, dim3(grid), dim3(256), 0, stream, kin,
+                             kout, rope_pos, cs, kp);
+  return bf16 ? launch_pdl(krot_kernel<true, 64>, dim3(grid), dim3(256), 0, stream, kin, kout,
+                           rope_pos, cs, kp)
+              : launch_pdl(krot_kernel<false, 64>, dim3(grid), dim3(256), 0, stream, kin, kout,
+                           rope_pos, cs, kp);
 }
 
 cudaError_t launch_mask_dense(const int32_t* q_indptr, const int32_t* kv_indptr,
