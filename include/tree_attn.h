@@ -285,6 +285,12 @@ ta_status tree_attn_merge_states(const void* parts, const float* lses, int32_t n
  * bounded wait expired, TA_ERR_CUDA on a CUDA error, else TA_OK). */
 ta_status tree_attn_device_status(void* workspace, void* stream);
 
+/* The CUDA runtime's description of the error behind the calling thread's
+ * most recent TA_ERR_CUDA ("no error" if there was none; static storage).
+ * A failure that has no CUDA error of its own (no device, a tensor map the
+ * driver rejects) reads as an invalid-value error. */
+const char* tree_attn_last_cuda_error(void);
+
 /* Human-readable name of a status code (static storage). */
 const char* tree_attn_status_string(ta_status s);
 

@@ -276,3 +276,19 @@ def _call_merge(lib, n=2, rows=10, d=128, dtype=ta.TA_BF16, **kw):
 ])
 def test_merge_states_host_validation(lib, kw, expect):
     assert _call_merge(lib, **kw) == expect
+
+
+def test_last_cuda_error_names_the_failure(lib):
+    """A launching call that fails in CUDA returns TA_ERR_CUDA and leaves the
+    CUDA error's text for tree_attn_last_cuda_error (here: no device).  The
+    binding's exception carries it."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("needs a machine without a GPU (the call would launch)")
+    fake = ctypes.c_void_p(0x10000)
+    st = lib.tree_attn_merge_states(fake, fake, 2, 10, 128, ta.TA_BF16, fake, fake, None)
+    assert st == ta.TA_ERR_CUDA
+    msg = ta.last_cuda_error()
+    assert msg and msg != "no error"
+    err = ta.TreeAttnError(st, "tree_attn_merge_states")
+    assert msg in str(err)

@@ -26,7 +26,7 @@ __all__ = [
     "TA_ERR_DEVICE_TIMEOUT", "TreeAttnError", "Dims", "lib", "lib_path", "workspace_size",
     "tree_attn", "plan", "run", "device_status", "status_string", "mask_dense", "check_inputs",
     "TreeAttention", "PagedDims", "make_paged_dims", "paged_workspace_size", "tree_attn_paged",
-    "MAX_CHUNKS", "split_workspace_size", "tree_attn_split", "merge_states",
+    "MAX_CHUNKS", "split_workspace_size", "tree_attn_split", "merge_states", "last_cuda_error",
 ]
 
 TA_OK = 0
@@ -44,7 +44,10 @@ lib_path = os.path.join(_PKG, "libtreeattn.so")
 
 class TreeAttnError(RuntimeError):
     def __init__(self, status: int, what: str):
-        super().__init__(f"{what}: {status_string(status)} ({status})")
+        msg = f"{what}: {status_string(status)} ({status})"
+        if status == TA_ERR_CUDA:
+            msg += f": {last_cuda_error()}"
+        super().__init__(msg)
         self.status = status
 
 
@@ -96,6 +99,8 @@ def lib() -> ctypes.CDLL:
     L.tree_attn_noalloc.restype = ctypes.c_int
     L.tree_attn_device_status.argtypes = [vp, vp]
     L.tree_attn_device_status.restype = ctypes.c_int
+    L.tree_attn_last_cuda_error.argtypes = []
+    L.tree_attn_last_cuda_error.restype = ctypes.c_char_p
     L.tree_attn_status_string.argtypes = [ctypes.c_int]
     L.tree_attn_status_string.restype = ctypes.c_char_p
     L.tree_attn_mask_dense.argtypes = [i32p, i32p, i32p, i32p, ctypes.c_int32, ctypes.c_int32,
@@ -128,6 +133,14 @@ def status_string(status: int) -> str:
         return lib().tree_attn_status_string(int(status)).decode()
     except RuntimeError:
         return f"status {status}"
+
+
+def last_cuda_error() -> str:
+    """The CUDA error behind this thread's most recent TA_ERR_CUDA."""
+    try:
+        return lib().tree_attn_last_cuda_error().decode()
+    except RuntimeError:
+        return "unknown"
 
 
 def _dtype_code(t: torch.dtype) -> int:

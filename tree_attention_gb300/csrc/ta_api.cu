@@ -22,6 +22,20 @@ namespace {
 
 constexpr unsigned long long kDeviceWaitLimitNs = 2000000000ull;  // 2 s per bounded wait
 
+// The CUDA error behind this thread's last TA_ERR_CUDA (cudaSuccess if none).
+thread_local cudaError_t g_last_cuda_error = cudaSuccess;
+
+// TA_ERR_CUDA for a failed CUDA call, remembering its error; TA_OK otherwise.
+ta_status cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return TA_OK;
+  g_last_cuda_error = e;
+  return TA_ERR_CUDA;
+}
+
+// TA_ERR_CUDA for a failed step with no CUDA error of its own (a tensor map
+// the driver rejects, no device), recorded as an invalid value.
+ta_status cuda_failure() { return cuda_status(cudaErrorInvalidValue); }
+
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   static std::once_flag once;
@@ -213,7 +227,7 @@ ta_status launch_plan_checked(const int32_t* q_indptr, const int32_t* kv_indptr,
   const WsLayout L = layout_of(dims, max_chunks);
   const WsPtrs w = ws_ptrs(workspace, L);
   const int nsm = sm_count();
-  if (nsm <= 0) return TA_ERR_CUDA;
+  if (nsm <= 0) return cuda_failure();
   ta::PlanParams pp{};
   pp.q_indptr = q_indptr;
   pp.kv_indptr = kv_indptr;
@@ -235,7 +249,7 @@ ta_status launch_plan_checked(const int32_t* q_indptr, const int32_t* kv_indptr,
   pp.hdr = w.hdr;
   pp.sorted = w.sorted;
   pp.classes = w.classes;
-  return ta::launch_plan(pp, (int)L.max_pairs, st) == cudaSuccess ? TA_OK : TA_ERR_CUDA;
+  return cuda_status(ta::launch_plan(pp, (int)L.max_pairs, st));
 }
 
 ta_status launch_run_checked(const void* q, const void* k, const void* v, const int32_t* q_indptr,
@@ -250,7 +264,7 @@ ta_status launch_run_checked(const void* q, const void* k, const void* v, const 
   const WsLayout L = layout_of(dims, max_chunks);
   const WsPtrs w = ws_ptrs(workspace, L);
   const int nsm = sm_count();
-  if (nsm <= 0) return TA_ERR_CUDA;
+  if (nsm <= 0) return cuda_failure();
   // with RoPE the keys are rotated once per call (every q tile of a sequence
   // reads them) and the attention kernel loads the rotated copy
   const void* k_attn = k;
@@ -264,16 +278,16 @@ ta_status launch_run_checked(const void* q, const void* k, const void* v, const 
     // one resident wave at most (8 warps per CTA, one token per warp at a time)
     const int64_t want = ((int64_t)dims->total_kv + 7) / 8;
     const int kgrid = (int)(want < 4 * nsm ? want : 4 * nsm);
-    if (ta::launch_krot(k, krot, q_rope_position, w.rope_cs, kp, D, dims->dtype == TA_BF16,
-                        kgrid, st) != cudaSuccess)
-      return TA_ERR_CUDA;
+    const cudaError_t ke = ta::launch_krot(k, krot, q_rope_position, w.rope_cs, kp, D,
+                                           dims->dtype == TA_BF16, kgrid, st);
+    if (ke != cudaSuccess) return cuda_status(ke);
     k_attn = krot;
   }
   CUtensorMap tm_q, tm_k, tm_v;
   if (!make_map(&tm_q, q, dims->dtype, dims->total_q, dims->h_q, D, g, R) ||
       !make_map(&tm_k, k_attn, dims->dtype, dims->total_kv, dims->h_kv, D, 1, ta::kKvBoxRows) ||
       !make_map(&tm_v, v, dims->dtype, dims->total_kv, dims->h_kv, D, 1, ta::kKvBoxRows))
-    return TA_ERR_CUDA;
+    return cuda_failure();
   ta::AttnParams ap{};
   ap.tree_order = tree_order;
   ap.out = out;
@@ -302,7 +316,7 @@ ta_status launch_run_checked(const void* q, const void* k, const void* v, const 
   else
     e = bf16 ? ta::launch_attn<128, true, false>(tm_q, tm_k, tm_v, ap, grid, st)
              : ta::launch_attn<128, false, false>(tm_q, tm_k, tm_v, ap, grid, st);
-  if (e != cudaSuccess) return TA_ERR_CUDA;
+  if (e != cudaSuccess) return cuda_status(e);
   if (max_chunks > 1) {
     // split-KV: the chunks' partial states of every split pair into out / lse
     ta::MergeParams mp{};
@@ -319,7 +333,8 @@ ta_status launch_run_checked(const void* q, const void* k, const void* v, const 
     mp.g = g;
     const int64_t units = L.max_pairs * dims->h_kv * (ta::kBlockM / 8);   // 8 rows each
     const int mgrid = (int)(units < 16 * nsm ? units : 16 * nsm);
-    if (ta::launch_merge(mp, D, bf16, mgrid, st) != cudaSuccess) return TA_ERR_CUDA;
+    const cudaError_t me = ta::launch_merge(mp, D, bf16, mgrid, st);
+    if (me != cudaSuccess) return cuda_status(me);
   }
   return TA_OK;
 }
@@ -419,28 +434,34 @@ ta_status tree_attn_merge_states(const void* parts, const float* lses, int32_t n
   if (!parts || !lses || !out || !lse) return TA_ERR_INVALID_ARGUMENT;
   if (!aligned(parts, 16) || !aligned(out, 16)) return TA_ERR_INVALID_ARGUMENT;
   const int nsm = sm_count();
-  if (nsm <= 0) return TA_ERR_CUDA;
+  if (nsm <= 0) return cuda_failure();
   const int64_t ctas = (rows + 7) / 8;   // 8 rows (warps) per CTA
   const int grid = (int)(ctas < 8 * nsm ? ctas : 8 * nsm);
   const cudaError_t e =
       ta::launch_merge_states(parts, lses, n_parts, (long long)rows, head_dim, dtype == TA_BF16,
                               out, lse, grid, static_cast<cudaStream_t>(stream));
-  return e == cudaSuccess ? TA_OK : TA_ERR_CUDA;
+  return cuda_status(e);
 }
 
 ta_status tree_attn_device_status(void* workspace, void* stream) {
   if (!workspace) return TA_ERR_INVALID_ARGUMENT;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (cudaStreamSynchronize(st) != cudaSuccess) return TA_ERR_CUDA;
+  cudaError_t e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_status(e);
   WsHeader* hdr = static_cast<WsHeader*>(workspace);
   unsigned int err = 0;
-  if (cudaMemcpy(&err, &hdr->error, sizeof(err), cudaMemcpyDeviceToHost) != cudaSuccess)
-    return TA_ERR_CUDA;
-  if (err != 0 && cudaMemset(&hdr->error, 0, sizeof(err)) != cudaSuccess) return TA_ERR_CUDA;
+  e = cudaMemcpy(&err, &hdr->error, sizeof(err), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_status(e);
+  if (err != 0) {
+    e = cudaMemset(&hdr->error, 0, sizeof(err));
+    if (e != cudaSuccess) return cuda_status(e);
+  }
   if (err & ta::DEVERR_TIMEOUT) return TA_ERR_DEVICE_TIMEOUT;
   if (err & ta::DEVERR_BAD_INDPTR) return TA_ERR_INVALID_ARGUMENT;
   return TA_OK;
 }
+
+const char* tree_attn_last_cuda_error(void) { return cudaGetErrorString(g_last_cuda_error); }
 
 const char* tree_attn_status_string(ta_status s) {
   switch (s) {
@@ -463,7 +484,7 @@ ta_status tree_attn_mask_dense(const int32_t* q_indptr, const int32_t* kv_indptr
   const cudaError_t e = ta::launch_mask_dense(q_indptr, kv_indptr, mn_indptr, tree_order,
                                               batch_size, total_q, max_kv, vis,
                                               static_cast<cudaStream_t>(stream));
-  return e == cudaSuccess ? TA_OK : TA_ERR_CUDA;
+  return cuda_status(e);
 }
 
 ta_status tree_attn_check_inputs(const int32_t* q_indptr, const int32_t* kv_indptr,
@@ -549,14 +570,14 @@ ta_status tree_attn_noalloc(const void* q, const int32_t* q_indptr, const void* 
   if (need == 0) return dims_supported(dims) != TA_OK ? TA_ERR_UNSUPPORTED : TA_ERR_INVALID_ARGUMENT;
   if (need > kNoAllocScratchBytes) return TA_ERR_UNSUPPORTED;  // problem too large for the scratch
   void* ws = noalloc_scratch_address();
-  if (ws == nullptr) return TA_ERR_CUDA;
+  if (ws == nullptr) return cuda_failure();
   // the work-queue and plan counters must start at zero (the status word at
   // offset 8 is left as it is)
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   uint8_t* hdr = static_cast<uint8_t*>(ws);
-  if (cudaMemsetAsync(hdr, 0, 8, st) != cudaSuccess ||
-      cudaMemsetAsync(hdr + 12, 0, sizeof(WsHeader) - 12, st) != cudaSuccess)
-    return TA_ERR_CUDA;
+  cudaError_t e = cudaMemsetAsync(hdr, 0, 8, st);
+  if (e == cudaSuccess) e = cudaMemsetAsync(hdr + 12, 0, sizeof(WsHeader) - 12, st);
+  if (e != cudaSuccess) return cuda_status(e);
   return tree_attn(q, q_indptr, k, v, kv_indptr, q_rope_position, mn_indptr, tree_order, out,
                    lse, rotary_mode, rope_scale, rope_theta, sm_scale, dims, ws,
                    kNoAllocScratchBytes, stream);
@@ -635,7 +656,7 @@ ta_status tree_attn_paged(const void* q, const int32_t* q_indptr, const void* pa
   const WsLayout L = layout_of(&d);
   const WsPtrs w = ws_ptrs(workspace, L);
   const int nsm = sm_count();
-  if (nsm <= 0) return TA_ERR_CUDA;
+  if (nsm <= 0) return cuda_failure();
   // plan: kv lengths from the page table
   ta::PlanParams pp{};
   pp.q_indptr = q_indptr;
@@ -662,12 +683,13 @@ ta_status tree_attn_paged(const void* q, const int32_t* q_indptr, const void* pa
   pp.hdr = w.hdr;
   pp.sorted = w.sorted;
   pp.classes = w.classes;
-  if (ta::launch_plan(pp, (int)L.max_pairs, st) != cudaSuccess) return TA_ERR_CUDA;
+  const cudaError_t pe = ta::launch_plan(pp, (int)L.max_pairs, st);
+  if (pe != cudaSuccess) return cuda_status(pe);
   // run: K and V tiles gathered page by page from the pool
   CUtensorMap tm_q, tm_pages;
   if (!make_map(&tm_q, q, d.dtype, d.total_q, d.h_q, d.head_dim, g, R) ||
       !make_pages_map(&tm_pages, pages, d.dtype, dims->num_pages, d.h_kv, d.head_dim))
-    return TA_ERR_CUDA;
+    return cuda_failure();
   ta::AttnParams ap{};
   ap.tree_order = tree_order;
   ap.out = out;
@@ -698,7 +720,7 @@ ta_status tree_attn_paged(const void* q, const int32_t* q_indptr, const void* pa
   else
     e = bf16 ? ta::launch_attn<128, true, true>(tm_q, tm_pages, tm_pages, ap, grid, st)
              : ta::launch_attn<128, false, true>(tm_q, tm_pages, tm_pages, ap, grid, st);
-  return e == cudaSuccess ? TA_OK : TA_ERR_CUDA;
+  return cuda_status(e);
 }
 
 }  // extern "C"
