@@ -44,11 +44,13 @@ enum Bar : int {
   B_K_FULL,                              // [kStages]
   B_V_FULL = B_K_FULL + kStages,         // [kStages]
   B_EX_FULL = B_V_FULL + kStages,        // [kStages]
-  B_K_EMPTY = B_EX_FULL + kStages,       // [kStages] QK read the K stage
-  B_V_EMPTY = B_K_EMPTY + kStages,       // [kStages] PV read the V stage (softmax done with EX)
-  B_S_FULL = B_V_EMPTY + kStages,        // [2] score buffer written
+  // a K (V) stage is free again when the QK (PV) of the tile in it has
+  // completed: with two stages and two score buffers, tile c uses stage and
+  // buffer c & 1, so the producer waits on S_FULL (PV_DONE) of that index
+  // and the MMA thread commits nothing extra per tile
+  B_S_FULL = B_EX_FULL + kStages,        // [2] score buffer written (K stage read)
   B_P_FULL = B_S_FULL + 2,               // [2] P written over the score buffer
-  B_PV_DONE = B_P_FULL + 2,              // [2] PV reading that P is complete
+  B_PV_DONE = B_P_FULL + 2,              // [2] PV reading that P is complete (V stage read)
   B_O_FREE = B_PV_DONE + 2,
   B_DRAIN,
   B_COUNT
@@ -260,13 +262,13 @@ __device__ void run_producer(const Pipe& pp, const CUtensorMap* tm_q, const CUte
             }
           }
         };
-        if (!pp.warp_wait(B_K_EMPTY + stage, empty_par)) { aborted = true; break; }
+        if (!pp.warp_wait(B_S_FULL + stage, empty_par)) { aborted = true; break; }
         if (lane == 0) {
           mbar_arrive_expect_tx(&pp.bar[B_K_FULL + stage], bytes);
           load_tile(sK + stage * C::kKVBytes, tm_k, &pp.bar[B_K_FULL + stage], 0);
         }
         ++issued_k;
-        if (!pp.warp_wait(B_V_EMPTY + stage, empty_par)) { aborted = true; break; }
+        if (!pp.warp_wait(B_PV_DONE + stage, empty_par)) { aborted = true; break; }
         if (lane == 0) {
           mbar_arrive_expect_tx(&pp.bar[B_V_FULL + stage], bytes);
           load_tile(sV + stage * C::kKVBytes, tm_v, &pp.bar[B_V_FULL + stage], 1);
@@ -354,7 +356,6 @@ __device__ void run_mma(const Pipe& pp, const AttnParams& p) {
           umma_f16(d_s, dq0 + qo, dk + ko, idesc, k > 0 ? 1u : 0u);
         }
         umma_commit(&pp.bar[B_S_FULL + sb]);
-        umma_commit(&pp.bar[B_K_EMPTY + stage]);
         issued_any = true;
         if (m == r.n_tiles - 1) umma_commit(&pp.bar[B_Q_EMPTY]);
         return true;
@@ -389,7 +390,6 @@ __device__ void run_mma(const Pipe& pp, const AttnParams& p) {
                             idesc_pv, (n > 0 || k > 0) ? 1u : 0u);
         }
         umma_commit(&pp.bar[B_PV_DONE + pb]);
-        umma_commit(&pp.bar[B_V_EMPTY + stage]);
         nv_cur = nv_next;
       }
       if (!ok) break;
@@ -803,8 +803,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bar[B_K_FULL + i], 1);
       mbar_init(&bar[B_V_FULL + i], 1);
       mbar_init(&bar[B_EX_FULL + i], 1);
-      mbar_init(&bar[B_K_EMPTY + i], 1);
-      mbar_init(&bar[B_V_EMPTY + i], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bar[B_S_FULL + i], 1);
