@@ -27,6 +27,7 @@ __all__ = [
     "tree_attn", "plan", "run", "device_status", "status_string", "mask_dense", "check_inputs",
     "TreeAttention", "PagedDims", "make_paged_dims", "paged_workspace_size", "tree_attn_paged",
     "MAX_CHUNKS", "split_workspace_size", "tree_attn_split", "merge_states", "last_cuda_error",
+    "folds_rotation",
 ]
 
 TA_OK = 0
@@ -141,6 +142,14 @@ def last_cuda_error() -> str:
         return lib().tree_attn_last_cuda_error().decode()
     except RuntimeError:
         return "unknown"
+
+
+def folds_rotation(total_kv: int, device=None) -> bool:
+    """Whether the one-call entry points fold the key rotation into the plan
+    kernel (problems of at most 64 kv tokens per SM), i.e. launch two kernels
+    instead of three under RoPE."""
+    idx = torch.cuda.current_device() if device is None else device
+    return total_kv <= 64 * torch.cuda.get_device_properties(idx).multi_processor_count
 
 
 def _dtype_code(t: torch.dtype) -> int:

@@ -217,12 +217,38 @@ void rope_denominators(float rope_theta, int head_dim, float* den) {
     den[i] = (float)std::exp2(l2 * ((2.0 * i) / (double)head_dim));
 }
 
-// The plan kernel (work records, tile classes, longest-first order); RoPE
-// needs nothing from it.
+// The key rotation of a call with RoPE: K, positions and RoPE constants.
+struct RopeArgs {
+  const void* k;
+  const int32_t* pos;
+  float scale, theta;
+};
+
+ta::KrotParams krot_params(const ta_dims* dims, const RopeArgs& ra) {
+  ta::KrotParams kp{};
+  rope_denominators(ra.theta, dims->head_dim, kp.rope_den);
+  kp.rope_scale = ra.scale;
+  kp.total_kv = dims->total_kv;
+  kp.h_kv = dims->h_kv;
+  return kp;
+}
+
+// Whether a one-call entry point folds the key rotation into the plan
+// kernel: when the rotation is a short latency tail (at most 64 kv tokens
+// per SM, about two per rotating warp) that the plan's idle warps absorb;
+// a larger rotation runs as its own kernel, which measured faster.
+bool fold_rotation(const ta_dims* dims, int nsm) {
+  return dims->rotary_mode == 1 && (int64_t)dims->total_kv <= 64LL * nsm;
+}
+
+// The plan kernel (work records, tile classes, longest-first order).  With
+// ``rope`` it also does the run's key rotation on its idle warps, over a
+// grid of at least 4 CTAs per SM.
 ta_status launch_plan_checked(const int32_t* q_indptr, const int32_t* kv_indptr,
                               const int32_t* mn_indptr, const int32_t* tree_order,
                               const ta_dims* dims, void* workspace, cudaStream_t st,
-                              int max_chunks = 1, int chunk_tiles = 0) {
+                              int max_chunks = 1, int chunk_tiles = 0,
+                              const RopeArgs* rope = nullptr) {
   const int g = dims->h_q / dims->h_kv;
   const WsLayout L = layout_of(dims, max_chunks);
   const WsPtrs w = ws_ptrs(workspace, L);
@@ -249,7 +275,17 @@ ta_status launch_plan_checked(const int32_t* q_indptr, const int32_t* kv_indptr,
   pp.hdr = w.hdr;
   pp.sorted = w.sorted;
   pp.classes = w.classes;
-  return cuda_status(ta::launch_plan(pp, (int)L.max_pairs, st));
+  int grid = (int)L.max_pairs;
+  if (rope != nullptr && dims->total_kv > 0) {
+    pp.rot = 1 + 2 * (dims->head_dim == 128) + (dims->dtype == TA_BF16);
+    pp.rot_k = static_cast<const uint32_t*>(rope->k);
+    pp.rot_out = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(workspace) + L.off_krot);
+    pp.rot_pos = rope->pos;
+    pp.rot_cs = reinterpret_cast<float4*>(w.rope_cs);
+    pp.kp = krot_params(dims, *rope);
+    if (grid < 4 * nsm) grid = 4 * nsm;
+  }
+  return cuda_status(ta::launch_plan(pp, grid, st));
 }
 
 ta_status launch_run_checked(const void* q, const void* k, const void* v, const int32_t* q_indptr,
@@ -257,7 +293,8 @@ ta_status launch_run_checked(const void* q, const void* k, const void* v, const 
                              const int32_t* mn_indptr, const int32_t* tree_order, void* out,
                              float* lse, int32_t rotary_mode, float rope_scale,
                              float rope_theta, float sm_scale, const ta_dims* dims,
-                             void* workspace, cudaStream_t st, int max_chunks = 1) {
+                             void* workspace, cudaStream_t st, int max_chunks = 1,
+                             bool keys_rotated = false) {
   const int g = dims->h_q / dims->h_kv;
   const int R = ta::rows_per_item(g);
   const int D = dims->head_dim;
@@ -266,21 +303,21 @@ ta_status launch_run_checked(const void* q, const void* k, const void* v, const 
   const int nsm = sm_count();
   if (nsm <= 0) return cuda_failure();
   // with RoPE the keys are rotated once per call (every q tile of a sequence
-  // reads them) and the attention kernel loads the rotated copy
+  // reads them) -- by the plan kernel of a one-call entry point, else here --
+  // and the attention kernel loads the rotated copy
   const void* k_attn = k;
   if (rotary_mode == 1) {
     void* krot = static_cast<uint8_t*>(workspace) + L.off_krot;
-    ta::KrotParams kp{};
-    rope_denominators(rope_theta, D, kp.rope_den);
-    kp.rope_scale = rope_scale;
-    kp.total_kv = dims->total_kv;
-    kp.h_kv = dims->h_kv;
-    // one resident wave at most (8 warps per CTA, one token per warp at a time)
-    const int64_t want = ((int64_t)dims->total_kv + 7) / 8;
-    const int kgrid = (int)(want < 4 * nsm ? want : 4 * nsm);
-    const cudaError_t ke = ta::launch_krot(k, krot, q_rope_position, w.rope_cs, kp, D,
-                                           dims->dtype == TA_BF16, kgrid, st);
-    if (ke != cudaSuccess) return cuda_status(ke);
+    if (!keys_rotated) {
+      const ta::KrotParams kp =
+          krot_params(dims, RopeArgs{k, q_rope_position, rope_scale, rope_theta});
+      // one resident wave at most (8 warps per CTA, one token per warp at a time)
+      const int64_t want = ((int64_t)dims->total_kv + 7) / 8;
+      const int kgrid = (int)(want < 4 * nsm ? want : 4 * nsm);
+      const cudaError_t ke = ta::launch_krot(k, krot, q_rope_position, w.rope_cs, kp, D,
+                                             dims->dtype == TA_BF16, kgrid, st);
+      if (ke != cudaSuccess) return cuda_status(ke);
+    }
     k_attn = krot;
   }
   CUtensorMap tm_q, tm_k, tm_v;
@@ -391,11 +428,14 @@ ta_status tree_attn(const void* q, const int32_t* q_indptr, const void* k, const
   if (s != TA_OK) return s;
   if (dims->total_q == 0) return TA_OK;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  s = launch_plan_checked(q_indptr, kv_indptr, mn_indptr, tree_order, dims, workspace, st);
+  const RopeArgs ra{k, q_rope_position, rope_scale, rope_theta};
+  const bool rot = fold_rotation(dims, sm_count());
+  s = launch_plan_checked(q_indptr, kv_indptr, mn_indptr, tree_order, dims, workspace, st, 1, 0,
+                          rot ? &ra : nullptr);
   if (s != TA_OK) return s;
   return launch_run_checked(q, k, v, q_indptr, kv_indptr, q_rope_position, mn_indptr,
                             tree_order, out, lse, rotary_mode, rope_scale, rope_theta,
-                            sm_scale, dims, workspace, st);
+                            sm_scale, dims, workspace, st, 1, rot);
 }
 
 ta_status tree_attn_split(const void* q, const int32_t* q_indptr, const void* k, const void* v,
@@ -415,12 +455,14 @@ ta_status tree_attn_split(const void* q, const int32_t* q_indptr, const void* k,
   if (s != TA_OK) return s;
   if (dims->total_q == 0) return TA_OK;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const RopeArgs ra{k, q_rope_position, rope_scale, rope_theta};
+  const bool rot = fold_rotation(dims, sm_count());
   s = launch_plan_checked(q_indptr, kv_indptr, mn_indptr, tree_order, dims, workspace, st,
-                          max_chunks, chunk_tiles);
+                          max_chunks, chunk_tiles, rot ? &ra : nullptr);
   if (s != TA_OK) return s;
   return launch_run_checked(q, k, v, q_indptr, kv_indptr, q_rope_position, mn_indptr,
                             tree_order, out, lse, rotary_mode, rope_scale, rope_theta,
-                            sm_scale, dims, workspace, st, max_chunks);
+                            sm_scale, dims, workspace, st, max_chunks, rot);
 }
 
 ta_status tree_attn_merge_states(const void* parts, const float* lses, int32_t n_parts,

@@ -32,6 +32,15 @@ inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, siz
   return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
 }
 
+// Key rotation: the RoPE frequency denominators fl32(theta^(2i/d)) for
+// i < d/2 (``_rope``, page "_kernel_common.py"; rounded once from float64 on
+// the host), the position scale and the sizes.
+struct KrotParams {
+  float rope_den[64];
+  float rope_scale;
+  int total_kv, h_kv;
+};
+
 struct PlanParams {
   const int32_t* q_indptr;
   const int32_t* kv_indptr;
@@ -51,6 +60,15 @@ struct PlanParams {
   // times); max_chunks == 1 disables it
   int max_chunks, chunk_tiles, pipes;
   int4* merge;       // per pair (split-KV): q_row0, q rows, chunks, first record
+  // one-call entry points: the plan kernel also does the key rotation of the
+  // run (krot_kernel's work) on the warps the plan leaves idle.  rot: 0 none,
+  // else 1 + 2 * (head_dim == 128) + (dtype == bf16)
+  int rot;
+  const uint32_t* rot_k;
+  uint32_t* rot_out;
+  const int32_t* rot_pos;
+  float4* rot_cs;
+  KrotParams kp;
   WsHeader* hdr;
   ItemRec* sorted;   // one record per (sequence, q tile) or chunk of one, longest first
   uint8_t* classes;
@@ -91,14 +109,6 @@ struct MergeParams {
 // ordering.  ``grid`` >= max_pairs.
 cudaError_t launch_plan(const PlanParams& p, int grid, cudaStream_t stream);
 
-// Key rotation: the RoPE frequency denominators fl32(theta^(2i/d)) for
-// i < d/2 (``_rope``, page "_kernel_common.py"; rounded once from float64 on
-// the host), the position scale and the sizes.
-struct KrotParams {
-  float rope_den[64];
-  float rope_scale;
-  int total_kv, h_kv;
-};
 
 // RoPE of every kv token: the cos/sin table row of token t at position
 // rope_pos[t] (rope_cs[t][i] = (cos, sin) of frequency i) and the rotated

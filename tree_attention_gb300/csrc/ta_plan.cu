@@ -11,6 +11,9 @@
 //      FULL exactly from the DFS intervals of ``_check_tree_order`` (page
 //      "tree_attn.py") and writes the pair's item record -- with split-KV, one
 //      record per chunk of the pair's kv tiles plus the pair's merge record;
+//   3. for the one-call entry points, (the warps with no classification to
+//      do) the run's key rotation: every kv token's RoPE cos/sin and rotated
+//      keys.
 #include <cuda_runtime.h>
 
 #include <climits>
@@ -141,6 +144,77 @@ __device__ __forceinline__ int auto_chunk_tiles(long long total_tiles, int h_kv,
   return (int)max((long long)kMinChunkTiles, min(per, (long long)INT_MAX));
 }
 
+// RoPE (``_rope`` on the page "_kernel_common.py") of one kv token, by one
+// warp: lane l evaluates the cos/sin of frequencies (2l', 2l'+1) in the
+// pages' float32 steps -- angle = fl32(fl32(pos * scale) / fl32(theta^(2i/d))),
+// cos and sin of it rounded correctly to float32 (cr_sincosf) -- writes them
+// to the token's row of the cos/sin table (read by the attention kernel for
+// its q rows) and rotates those element pairs of every kv head: words l' of
+// the first half and d/4 + l' of the second half of the head's row.  For
+// d = 64 lanes 16..31 take the odd heads.  The first heads' keys are loaded
+// before the sin/cos evaluation, so the loads are in flight while it runs.
+template <bool BF16, int D>
+__device__ __forceinline__ void rope_token(const uint32_t* __restrict__ k,
+                                           uint32_t* __restrict__ krot, float4* __restrict__ cs,
+                                           long long tok, int ps, const KrotParams& kp,
+                                           const float4* sct, int lane) {
+  constexpr int kWords = D / 2;  // 32-bit words per head row
+  const int pl = (D == 128) ? lane : (lane & 15);
+  const int h0 = (D == 128) ? 0 : (lane >> 4);
+  constexpr int hstep = (D == 128) ? 1 : 2;
+  const int h_kv = kp.h_kv;
+  uint32_t w0[8], w1[8];
+  auto load = [&](int hb) {
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int h = hb + u * hstep;
+      if (h < h_kv) {
+        const long long e = (tok * h_kv + h) * kWords;
+        w0[u] = __ldg(k + e + pl);
+        w1[u] = __ldg(k + e + kWords / 2 + pl);
+      }
+    }
+  };
+  load(h0);
+  float c0, s0, c1, s1;
+  {
+    const float sc = __fmul_rn((float)ps, kp.rope_scale);
+    cr_sincosf(__fdiv_rn(sc, kp.rope_den[2 * pl]), &s0, &c0, sct);
+    cr_sincosf(__fdiv_rn(sc, kp.rope_den[2 * pl + 1]), &s1, &c1, sct);
+  }
+  if (D == 128 || lane < 16) cs[tok * (D / 4) + pl] = make_float4(c0, s0, c1, s1);
+  for (int hb = h0; hb < h_kv; hb += 8 * hstep) {
+    if (hb != h0) load(hb);
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int h = hb + u * hstep;
+      if (h < h_kv) {
+        const float2 x0 = unpack2<BF16>(w0[u]);
+        const float2 x1 = unpack2<BF16>(w1[u]);
+        // first half: cos*x[j] + sin*(-x[j+d/2]); second half: cos*x[j] + sin*x[j-d/2]
+        const float y0a = __fadd_rn(__fmul_rn(c0, x0.x), __fmul_rn(s0, -x1.x));
+        const float y0b = __fadd_rn(__fmul_rn(c1, x0.y), __fmul_rn(s1, -x1.y));
+        const float y1a = __fadd_rn(__fmul_rn(c0, x1.x), __fmul_rn(s0, x0.x));
+        const float y1b = __fadd_rn(__fmul_rn(c1, x1.y), __fmul_rn(s1, x0.y));
+        const long long e = (tok * h_kv + h) * kWords;
+        krot[e + pl] = pack2<BF16>(y0a, y0b);
+        krot[e + kWords / 2 + pl] = pack2<BF16>(y1a, y1b);
+      }
+    }
+  }
+}
+
+// Warp ``rank`` of ``nwarps`` takes kv tokens rank, rank + nwarps, ...  (not
+// inlined: the plan kernel calls one of four instances, which would
+// otherwise bloat its code)
+template <bool BF16, int D>
+__device__ __noinline__ void rope_tokens(const uint32_t* k, uint32_t* krot, const int32_t* pos, float4* cs,
+                            const KrotParams& kp, const float4* sct, long long rank,
+                            long long nwarps, int lane) {
+  for (long long tok = rank; tok < kp.total_kv; tok += nwarps)
+    rope_token<BF16, D>(k, krot, cs, tok, __ldg(pos + tok), kp, sct, lane);
+}
+
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanParams p) {
   __shared__ long long s_scan_a[9], s_scan_b[9];
   __shared__ int s_keys[kBlockM];
@@ -154,6 +228,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanParams p) 
   __shared__ uint32_t s_cls2[3];
   __shared__ int s_count;
   __shared__ int s_hist[kCostBuckets];
+  __shared__ float4 s_sct[27];
 
   pdl_wait();
   pdl_trigger();
@@ -161,6 +236,9 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanParams p) 
   const int B = p.batch, R = p.R;
   // ---- 0. constants and counters of this CTA
   for (int i = tid; i < kCostBuckets; i += kPlanThreads) s_hist[i] = 0;
+  if (p.rot && tid < 27)
+    s_sct[tid] = make_float4(kSinCosTable[tid][0], kSinCosTable[tid][1], kSinCosTable[tid][2],
+                             kSinCosTable[tid][3]);
   if (tid == 0) {
     s_bad = 0;
     s_count = 0;
@@ -449,78 +527,55 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanParams p) 
       p.merge[pair] = make_int4(q0 + r0, nrows, nch, (int)pos);
   }
 
+  // ---- 5. (one-call entry points) the run's key rotation: every kv token's
+  // cos/sin and rotated keys (rope_token), dealt out over the warps with no
+  // classification to do -- all warps of the CTAs without a pair and warps
+  // 4-7 of the CTAs with one -- so that it adds nothing to the classifying
+  // warps' critical path
+  if (p.rot && !(has_pair && warp < 4)) {
+    const long long grid = gridDim.x;
+    const long long n_busy = ok ? min(total_tiles, grid) : 0;   // CTAs with a pair: 0..n_busy-1
+    const long long idle_warps = (grid - n_busy) * 8;
+    const long long rank = !has_pair ? ((long long)blockIdx.x - n_busy) * 8 + warp
+                                     : idle_warps + (long long)blockIdx.x * 4 + (warp - 4);
+    const long long nw = idle_warps + n_busy * 4;
+    switch (p.rot) {
+      case 1:
+        rope_tokens<false, 64>(p.rot_k, p.rot_out, p.rot_pos, p.rot_cs, p.kp, s_sct, rank, nw, lane);
+        break;
+      case 2:
+        rope_tokens<true, 64>(p.rot_k, p.rot_out, p.rot_pos, p.rot_cs, p.kp, s_sct, rank, nw, lane);
+        break;
+      case 3:
+        rope_tokens<false, 128>(p.rot_k, p.rot_out, p.rot_pos, p.rot_cs, p.kp, s_sct, rank, nw,
+                                lane);
+        break;
+      default:
+        rope_tokens<true, 128>(p.rot_k, p.rot_out, p.rot_pos, p.rot_cs, p.kp, s_sct, rank, nw,
+                               lane);
+        break;
+    }
+  }
 }
 
-// RoPE (``_rope`` on the page "_kernel_common.py") of every kv token, once
-// per call: one warp per token at a time, lane l evaluates the cos/sin of
-// frequencies (2l', 2l'+1) in the pages' float32 steps -- angle =
-// fl32(fl32(pos * scale) / fl32(theta^(2i/d))), cos and sin of it rounded
-// correctly to float32 (cr_sincosf) -- writes them to the token's row of the
-// cos/sin table (read by the attention kernel for its q rows) and rotates
-// those element pairs of every kv head: words l' of the first half and
-// d/4 + l' of the second half of the head's row.  For d = 64 lanes 16..31
-// take the odd heads.  The token's keys are loaded before the sin/cos
-// evaluation, so the loads are in flight while it runs.
+// The key-rotation kernel of the two-launch run (tree_attn_run): one warp per
+// kv token at a time.
 template <bool BF16, int D>
 __global__ void __launch_bounds__(256) krot_kernel(const uint32_t* __restrict__ k,
                                                    uint32_t* __restrict__ krot,
                                                    const int32_t* __restrict__ pos,
                                                    float4* __restrict__ cs,
                                                    const KrotParams kp) {
-  constexpr int kWords = D / 2;  // 32-bit words per head row
   __shared__ float4 s_sct[27];
-  const int lane = threadIdx.x & 31;
-  const int pl = (D == 128) ? lane : (lane & 15);
-  const int h0 = (D == 128) ? 0 : (lane >> 4);
-  constexpr int hstep = (D == 128) ? 1 : 2;
   if (threadIdx.x < 27)
     s_sct[threadIdx.x] = make_float4(kSinCosTable[threadIdx.x][0], kSinCosTable[threadIdx.x][1],
                                      kSinCosTable[threadIdx.x][2], kSinCosTable[threadIdx.x][3]);
-  const float den0 = kp.rope_den[2 * pl], den1 = kp.rope_den[2 * pl + 1];
   __syncthreads();
   pdl_wait();
   pdl_trigger();
-  const int h_kv = kp.h_kv;
-  const long long warps = (long long)gridDim.x * (blockDim.x / 32);
-  for (long long tok = (long long)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
-       tok < kp.total_kv; tok += warps) {
-    const int ps = __ldg(pos + tok);
-    for (int hb = h0; hb < h_kv; hb += 8 * hstep) {
-      uint32_t w0[8], w1[8];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int h = hb + u * hstep;
-        if (h < h_kv) {
-          const long long e = (tok * h_kv + h) * kWords;
-          w0[u] = __ldg(k + e + pl);
-          w1[u] = __ldg(k + e + kWords / 2 + pl);
-        }
-      }
-      float c0, s0, c1, s1;
-      {
-        const float sc = __fmul_rn((float)ps, kp.rope_scale);
-        cr_sincosf(__fdiv_rn(sc, den0), &s0, &c0, s_sct);
-        cr_sincosf(__fdiv_rn(sc, den1), &s1, &c1, s_sct);
-      }
-      if (hb == h0 && (D == 128 || lane < 16)) cs[tok * (D / 4) + pl] = make_float4(c0, s0, c1, s1);
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int h = hb + u * hstep;
-        if (h < h_kv) {
-          const float2 x0 = unpack2<BF16>(w0[u]);
-          const float2 x1 = unpack2<BF16>(w1[u]);
-          // first half: cos*x[j] + sin*(-x[j+d/2]); second half: cos*x[j] + sin*x[j-d/2]
-          const float y0a = __fadd_rn(__fmul_rn(c0, x0.x), __fmul_rn(s0, -x1.x));
-          const float y0b = __fadd_rn(__fmul_rn(c1, x0.y), __fmul_rn(s1, -x1.y));
-          const float y1a = __fadd_rn(__fmul_rn(c0, x1.x), __fmul_rn(s0, x0.x));
-          const float y1b = __fadd_rn(__fmul_rn(c1, x1.y), __fmul_rn(s1, x0.y));
-          const long long e = (tok * h_kv + h) * kWords;
-          krot[e + pl] = pack2<BF16>(y0a, y0b);
-          krot[e + kWords / 2 + pl] = pack2<BF16>(y1a, y1b);
-        }
-      }
-    }
-  }
+  const long long nwarps = (long long)gridDim.x * (blockDim.x / 32);
+  const long long rank = (long long)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
+  rope_tokens<BF16, D>(k, krot, pos, cs, kp, s_sct, rank, nwarps, threadIdx.x & 31);
 }
 
 __global__ void mask_dense_kernel(const int32_t* __restrict__ q_indptr,
