@@ -460,17 +460,30 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanParams p) 
       }
       group_sync(kBarA);
       const int c_end = min(kv, (j0 + nt) * kBlockN);
-      for (int c = max(j0, prefix_tiles) * kBlockN + tid; c < c_end; c += kGroup) {
-        int cnt;
-        if (c < ts) {
-          cnt = nrows;
-        } else {
-          const int2 iv = reinterpret_cast<const int2*>(p.tree_order)[tree_base + c - ts];
-          cnt = max(0, lower_bound(s_keys, nrows, iv.y) - lower_bound(s_keys, nrows, iv.x));
+      // kColBatch columns per thread per step, their intervals loaded before
+      // any is used, so that the loads' round trips overlap
+      constexpr int kColBatch = 8;
+      const int2* order2 = reinterpret_cast<const int2*>(p.tree_order) + tree_base;
+      for (int c0 = max(j0, prefix_tiles) * kBlockN + tid; c0 < c_end;
+           c0 += kGroup * kColBatch) {
+        int2 iv[kColBatch];
+#pragma unroll
+        for (int u = 0; u < kColBatch; ++u) {
+          const int c = c0 + u * kGroup;
+          iv[u] = (c < c_end && c >= ts) ? order2[c - ts] : make_int2(0, 0);
         }
-        const int jt = c / kBlockN - j0;
-        if (cnt > 0 && !s_any[jt]) s_any[jt] = 1;
-        if (cnt != nrows && !s_notall[jt]) s_notall[jt] = 1;
+#pragma unroll
+        for (int u = 0; u < kColBatch; ++u) {
+          const int c = c0 + u * kGroup;
+          if (c >= c_end) break;
+          // prefix columns (of the tile that holds the tree start) are seen by every row
+          const int cnt =
+              c < ts ? nrows
+                     : max(0, lower_bound(s_keys, nrows, iv[u].y) - lower_bound(s_keys, nrows, iv[u].x));
+          const int jt = c / kBlockN - j0;
+          if (cnt > 0 && !s_any[jt]) s_any[jt] = 1;
+          if (cnt != nrows && !s_notall[jt]) s_notall[jt] = 1;
+        }
       }
       group_sync(kBarA);
       for (int i = tid; i < nt; i += kGroup) {
