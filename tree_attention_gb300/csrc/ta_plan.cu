@@ -7,13 +7,12 @@
 //      up front), validating the index arrays, and places its own pair in the
 //      longest-first (LPT) order of the attention kernel's work queue by an
 //      estimated cost -- no global barrier, no serial tail;
-//   2. (warps 0-3) classifies every kv tile of its pair as EMPTY / PARTIAL /
+//   2. (all warps) classifies every kv tile of its pair as EMPTY / PARTIAL /
 //      FULL exactly from the DFS intervals of ``_check_tree_order`` (page
 //      "tree_attn.py") and writes the pair's item record -- with split-KV, one
 //      record per chunk of the pair's kv tiles plus the pair's merge record;
-//   3. for the one-call entry points, (the warps with no classification to
-//      do) the run's key rotation: every kv token's RoPE cos/sin and rotated
-//      keys.
+//   3. for the one-call entry points, (the CTAs without a pair first) the
+//      run's key rotation: every kv token's RoPE cos/sin and rotated keys.
 #include <cuda_runtime.h>
 
 #include <climits>
@@ -367,7 +366,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanParams p) 
   // the pair's q rows' enter indices, loaded now so that the round trip
   // overlaps the ranking below
   int key = INT_MAX, nrows = 0;
-  if (has_pair && tid < kGroup) {
+  if (has_pair) {
     const int b = s_pair_b;
     const int qo = p.q_indptr[b + 1] - p.q_indptr[b];
     const int tree_base = p.mn_indptr[b];
@@ -395,8 +394,9 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanParams p) 
   }
   __syncthreads();
 
-  // ---- 4. warps 0-3 classify the pair's kv tiles and write its record
-  if (tid < kGroup && has_pair) {
+  // ---- 4. classify the pair's kv tiles (warps 0-3 sort the rows' keys,
+  // then all warps take the columns) and write its record
+  if (has_pair) {
     const int b = s_pair_b, t = s_pair_t;
     const long long off = s_pair_off;
     const long long pos = (long long)s_hist[s_pair_cost] + s_rank;
@@ -410,9 +410,12 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanParams p) 
     const int r0 = t * R;
     // exact classification from the DFS intervals of ``_check_tree_order``
     // (page "tree_attn.py"): the rows' enter indices are sorted (bitonic, one
-    // key per thread) and, for each kv column, two binary searches count the
-    // rows inside the column's [enter, exit) interval
-    if (nrows <= 32) {
+    // key per thread); a kv column is seen by some row iff the first key not
+    // below its enter index is below its exit index, and by every row iff
+    // its interval holds the smallest and the largest key
+    if (tid >= kGroup) {
+      // warps 4-7 wait for the sorted keys below
+    } else if (nrows <= 32) {
       // one warp, shuffles only
       if (tid < 32) {
         int x = key;
@@ -444,49 +447,54 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanParams p) 
         }
       }
     }
+    if (tid < 3) s_cls2[tid] = 0;
+    __syncthreads();
+    const int kmin = s_keys[0], kmax = s_keys[nrows - 1];
     const int kvt = (kv + kBlockN - 1) / kBlockN;
     // tiles wholly inside the causal prefix are FULL for every row (a pair
     // has at least one row, and such a tile ends at or before the tree
     // start, so it is not ragged): their columns need no look-up
     const int prefix_tiles = ts / kBlockN;
-    if (tid < 3) s_cls2[tid] = 0;
-    // up to kPassTiles kv tiles per pass; every thread takes every 128th
+    // up to kPassTiles kv tiles per pass; every thread takes every 256th
     // column of the pass and folds its verdict into per-tile flags
     for (int j0 = 0; j0 < kvt; j0 += kPassTiles) {
       const int nt = min(kPassTiles, kvt - j0);
-      for (int i = tid; i < nt; i += kGroup) {
+      for (int i = tid; i < nt; i += kPlanThreads) {
         s_any[i] = 0;
         s_notall[i] = 0;
       }
-      group_sync(kBarA);
+      __syncthreads();
       const int c_end = min(kv, (j0 + nt) * kBlockN);
       // kColBatch columns per thread per step, their intervals loaded before
       // any is used, so that the loads' round trips overlap
       constexpr int kColBatch = 8;
       const int2* order2 = reinterpret_cast<const int2*>(p.tree_order) + tree_base;
       for (int c0 = max(j0, prefix_tiles) * kBlockN + tid; c0 < c_end;
-           c0 += kGroup * kColBatch) {
+           c0 += kPlanThreads * kColBatch) {
         int2 iv[kColBatch];
 #pragma unroll
         for (int u = 0; u < kColBatch; ++u) {
-          const int c = c0 + u * kGroup;
+          const int c = c0 + u * kPlanThreads;
           iv[u] = (c < c_end && c >= ts) ? order2[c - ts] : make_int2(0, 0);
         }
 #pragma unroll
         for (int u = 0; u < kColBatch; ++u) {
-          const int c = c0 + u * kGroup;
+          const int c = c0 + u * kPlanThreads;
           if (c >= c_end) break;
           // prefix columns (of the tile that holds the tree start) are seen by every row
-          const int cnt =
-              c < ts ? nrows
-                     : max(0, lower_bound(s_keys, nrows, iv[u].y) - lower_bound(s_keys, nrows, iv[u].x));
+          bool any = true, all = true;
+          if (c >= ts) {
+            const int lo = lower_bound(s_keys, nrows, iv[u].x);
+            any = lo < nrows && s_keys[lo] < iv[u].y;
+            all = iv[u].x <= kmin && kmax < iv[u].y;
+          }
           const int jt = c / kBlockN - j0;
-          if (cnt > 0 && !s_any[jt]) s_any[jt] = 1;
-          if (cnt != nrows && !s_notall[jt]) s_notall[jt] = 1;
+          if (any && !s_any[jt]) s_any[jt] = 1;
+          if (!all && !s_notall[jt]) s_notall[jt] = 1;
         }
       }
-      group_sync(kBarA);
-      for (int i = tid; i < nt; i += kGroup) {
+      __syncthreads();
+      for (int i = tid; i < nt; i += kPlanThreads) {
         const int j = j0 + i;
         const bool ragged = (j + 1) * kBlockN > kv;
         const uint8_t cls =
@@ -500,21 +508,21 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanParams p) 
         }
         if (kvt <= kInlineTiles) atomicOr(&s_cls2[j >> 4], (uint32_t)cls << (2 * (j & 15)));
       }
-      group_sync(kBarA);
+      __syncthreads();
     }
     // split-KV: the tiles up to the last non-empty one are cut into nch
     // ranges of (nearly) equal length; each range's non-empty tiles are
-    // counted from the classes just written (this group's own stores)
+    // counted from the classes just written (this CTA's own stores)
     const int nch = s_pair_chunks;
     const int last = s_last;
     if (nch > 1) {
-      for (int j = tid; j < last; j += kGroup) {
+      for (int j = tid; j < last; j += kPlanThreads) {
         if (p.classes[off + j] == kTileEmpty) continue;
         int c = 0;
         while (c + 1 < nch && j >= (int)((long long)last * (c + 1) / nch)) ++c;
         atomicAdd(&s_ccount[c], 1);
       }
-      group_sync(kBarA);
+      __syncthreads();
     }
     if (tid < nch) {
       ItemRec r;
@@ -541,17 +549,17 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanParams p) 
   }
 
   // ---- 5. (one-call entry points) the run's key rotation: every kv token's
-  // cos/sin and rotated keys (rope_token), dealt out over the warps with no
-  // classification to do -- all warps of the CTAs without a pair and warps
-  // 4-7 of the CTAs with one -- so that it adds nothing to the classifying
-  // warps' critical path
-  if (p.rot && !(has_pair && warp < 4)) {
+  // cos/sin and rotated keys (rope_token), dealt out over the warps of the
+  // grid, those of the CTAs without a pair first: the folded rotation is
+  // small (fewer tokens than those warps, typically), so the classifying
+  // CTAs take part only when it is not
+  if (p.rot) {
     const long long grid = gridDim.x;
     const long long n_busy = ok ? min(total_tiles, grid) : 0;   // CTAs with a pair: 0..n_busy-1
     const long long idle_warps = (grid - n_busy) * 8;
     const long long rank = !has_pair ? ((long long)blockIdx.x - n_busy) * 8 + warp
-                                     : idle_warps + (long long)blockIdx.x * 4 + (warp - 4);
-    const long long nw = idle_warps + n_busy * 4;
+                                     : idle_warps + (long long)blockIdx.x * 8 + warp;
+    const long long nw = grid * 8;
     switch (p.rot) {
       case 1:
         rope_tokens<false, 64>(p.rot_k, p.rot_out, p.rot_pos, p.rot_cs, p.kp, s_sct, rank, nw, lane);
