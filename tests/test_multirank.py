@@ -97,3 +97,30 @@ def test_reference_arm_other_ranks_exit_without_work(monkeypatch):
         rc = bench.main(["--impl", "reference", "--gpus", "2", "--steps", "1", "--warmup", "3"])
     assert rc in (0, None)
     assert buf.getvalue() == ""
+
+
+def test_reference_arm_prints_the_contract_line(monkeypatch):
+    """``bench.py --impl reference`` (rank 0, one process) times the oracle on
+    the host cores and prints one JSON line with the contract's keys: the
+    arm's name, the metric and unit, a cpu_baseline describing the run, and
+    an e2e object with no host/device bytes."""
+    import json
+    import bench
+    for k in ("RANK", "LOCAL_RANK", "WORLD_SIZE"):
+        monkeypatch.delenv(k, raising=False)
+    buf = io.StringIO()
+    with contextlib.redirect_stdout(buf):
+        rc = bench.main(["--impl", "reference", "--workload", "tiny", "--steps", "1",
+                         "--warmup", "3"])
+    assert rc in (0, None)
+    lines = [ln for ln in buf.getvalue().splitlines() if ln.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference"
+    assert d["metric"] == bench.METRIC and d["unit"] == bench.UNIT
+    assert d["value"] > 0 and d["n_gpus"] == 1 and d["steps"] == 1 and d["warmup"] == 3
+    assert d["higher_is_better"] is True and d["config"]["workload"] == "tiny"
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"]
+    assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}
