@@ -171,7 +171,7 @@ struct TileIter {
 // ---------------------------------------------------------------------------
 template <int D, bool PAGED>
 __device__ void run_producer(const Pipe& pp, const CUtensorMap* tm_q, const CUtensorMap* tm_k,
-                             const CUtensorMap* tm_v, const AttnParams& p, int lane) {
+                             const CUtensorMap* tm_v, const AttnParams& p, int pipe, int lane) {
   using C = Cfg<D>;
   uint8_t* sQ = pp.smem + C::kOffQ;
   uint8_t* sK = pp.smem + C::kOffK;
@@ -185,9 +185,11 @@ __device__ void run_producer(const Pipe& pp, const CUtensorMap* tm_q, const CUte
   uint32_t it = 0, kv_it = 0, q_it = 0;
   uint32_t issued_k = 0, issued_v = 0;   // loads issued (stage = count % kStages)
   bool aborted = false;
-  unsigned int idx = 0;
-  if (lane == 0) idx = atomicAdd(&p.hdr->queue_head, 1u);
-  idx = __shfl_sync(0xffffffffu, idx, 0);
+  // the first item of every pipeline is fixed (pipeline p of CTA b takes
+  // item 2b + p, the items being in longest-first order already), the rest
+  // come from the queue, which starts after those 2 x grid items
+  const unsigned int n_static = (unsigned int)(kPipes * gridDim.x);
+  unsigned int idx = (unsigned int)(kPipes * blockIdx.x + pipe);
   // lanes 0-3 hold the next record (16 bytes each), fetched one item ahead
   int4 rec_next = make_int4(0, 0, 0, 0);
   if (idx < num_items && lane < 4)
@@ -208,7 +210,7 @@ __device__ void run_producer(const Pipe& pp, const CUtensorMap* tm_q, const CUte
     // pop the next index now; its round trip overlaps this item's issue
     unsigned int nidx = 0;
     if (lane == 0) {
-      nidx = atomicAdd(&p.hdr->queue_head, 1u);
+      nidx = n_static + atomicAdd(&p.hdr->queue_head, 1u);
       s.valid = 1;
       s.kvh = kvh;
     }
@@ -834,7 +836,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   pdl_wait();
 
   if (pw == 0) {
-    run_producer<D, PAGED>(pp, &tm_q, &tm_k, &tm_v, p, lane);
+    run_producer<D, PAGED>(pp, &tm_q, &tm_k, &tm_v, p, pipe, lane);
   } else if (pw == 1) {
     if (lane == 0) run_mma<D, BF16>(pp, p);
   } else {
