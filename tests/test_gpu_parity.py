@@ -308,3 +308,40 @@ def test_rotated_keys_match_oracle_rope(idx):
         b = ref[diff].float()
         ulp = 2.0 ** -7 if w.dtype == "bf16" else 2.0 ** -10
         assert bool(((a - b).abs() <= ulp * b.abs().clamp_min(2.0 ** -14) * 1.01).all())
+
+
+@pytest.mark.parametrize("idx", [2, 3])
+def test_plan_once_run_per_layer(idx):
+    """tree_attn_plan once, tree_attn_run for two layers with different q/k/v
+    on the same plan (the key rotation runs in the run half): each layer
+    matches the oracle, and the first equals the one-call tree_attn bit for
+    bit (same kernels and arithmetic; the one-call path folds the rotation of
+    small problems into its plan kernel)."""
+    import dataclasses
+    w1 = wl.config(idx, batch_scale=0.25)
+    gen = torch.Generator().manual_seed(4321 + idx)
+    tdt = w1.q.dtype
+    w2 = dataclasses.replace(
+        w1, q=torch.randn(w1.q.shape, generator=gen, dtype=torch.float32).to(tdt),
+        k=torch.randn(w1.k.shape, generator=gen, dtype=torch.float32).to(tdt),
+        v=torch.randn(w1.v.shape, generator=gen, dtype=torch.float32).to(tdt))
+    d1, d2 = wl.device_inputs(w1), wl.device_inputs(w2)
+    dims = ta.make_dims(d1["q"], d1["k"], d1["q_indptr"], d1["tree_order"], w1.rotary_mode)
+    ws = torch.zeros(ta.workspace_size(dims), dtype=torch.uint8, device="cuda")
+    ta.plan(d1["q"], d1["q_indptr"], d1["k"], d1["kv_indptr"], d1["q_rope_position"],
+            d1["mn_indptr"], d1["tree_order"], w1.rotary_mode, w1.rope_scale, w1.rope_theta, ws)
+    outs = []
+    for w, d in ((w1, d1), (w2, d2)):
+        out = torch.empty_like(d["q"])
+        lse = torch.empty(d["q"].shape[:2], dtype=torch.float32, device="cuda")
+        ta.run(d["q"], d["k"], d["v"], d["q_indptr"], d["kv_indptr"], d["q_rope_position"],
+               d["mn_indptr"], d["tree_order"], out, lse, w.rotary_mode, w.rope_scale,
+               w.rope_theta, w.sm_scale, ws)
+        assert ta.device_status(ws) == ta.TA_OK
+        assert_parity(w, out.float().cpu().numpy(), lse.cpu().numpy())
+        outs.append((out, lse))
+    attn = ta.TreeAttention(d1["q"], d1["k"], d1["q_indptr"], d1["tree_order"], w1.rotary_mode,
+                            w1.rope_scale, w1.rope_theta, w1.sm_scale)
+    out1, lse1 = attn(**d1)
+    assert ta.device_status(attn.workspace) == ta.TA_OK
+    assert torch.equal(out1, outs[0][0]) and torch.equal(lse1, outs[0][1])
