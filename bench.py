@@ -4,11 +4,13 @@
 One step = one ``tree_attn`` call = the plan kernel (work enumeration, tile
 classification), with RoPE the key rotation with its cos/sin table (folded
 into the plan kernel for small problems), and the persistent attention
-kernel, over one batch of the named synthetic workload.  Prints one JSON line
-(rank 0).
+kernel, over one batch of the named synthetic workload (default: the
+ragged-large workload, the largest of the benchmark set).  Prints one JSON
+line (rank 0) whose ``per_config`` object holds the same measurement for the
+spec-decode, prefix+tree, ragged-large and degenerate workloads.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
-                  [--impl gb300|reference]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--repeats R]
+                  [--workload NAME] [--impl gb300|reference]
 
 Under torchrun each rank runs its own copy of the workload on its own GPU
 (weak scaling, no data-path collective); the step time is the max over ranks.
@@ -281,17 +283,32 @@ def _config_dict(w, l2_note):
     return d
 
 
-def run_gb300(args):
-    import tree_attention_gb300 as ta
-    from tree_attention_gb300 import build as ta_build
+PER_CONFIG = ("spec-decode", "prefix+tree", "ragged-large", "degenerate")
 
-    rank, local, world = dist_info()
-    init_dist(world, "nccl")
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    ta_build.build()
-    ta.lib()
-    w = make_workload(args.workload)
+
+def _roofline(nbytes, flops, seconds, peaks):
+    """The bound that applies to ``nbytes`` / ``flops`` (the slower of HBM
+    copy bandwidth and the bf16 tensor peak) and the fraction reached in
+    ``seconds``."""
+    if nbytes / (peaks["hbm_gbs"] * 1e9) >= flops / (peaks["bf16_tflops"] * 1e12):
+        r = {"bound": "hbm", "achieved": nbytes / seconds / 1e9, "peak": peaks["hbm_gbs"],
+             "unit": "GB/s"}
+    else:
+        r = {"bound": "tensor", "achieved": flops / seconds / 1e12,
+             "peak": peaks["bf16_tflops"], "unit": "TFLOP/s"}
+    r["frac"] = r["achieved"] / r["peak"]
+    return r
+
+
+def measure_workload(ta, w, args, dev, stream, world, local, headline=False):
+    """Times the one-call ``tree_attn`` step on workload ``w``: ``repeats``
+    runs of exactly ``steps`` back-to-back steps (each run bracketed by a
+    barrier and a device synchronisation, CUDA events on the launching
+    stream), the median run giving ms per step; then a second pass through
+    the plan / run entry points with events between the launches for the
+    per-kernel split.  With ``headline`` it also samples clocks during the
+    timed runs (stretching the repeats so that the sampler sees them) and
+    measures the end-to-end call with host buffers."""
     flops = wl.algorithmic_flops(w)
     nbytes = wl.algorithmic_bytes(w)
     sb = set_bytes(w)
@@ -307,7 +324,6 @@ def run_gb300(args):
         dims = ta.make_dims(d["q"], d["k"], d["q_indptr"], d["tree_order"], w.rotary_mode)
         d["ws"] = torch.zeros(ta.workspace_size(dims), dtype=torch.uint8, device=dev)
         sets.append(d)
-    stream = torch.cuda.current_stream(dev)
 
     def step(d):
         # one call: plan kernel, key rotation under RoPE, attention kernel
@@ -328,47 +344,77 @@ def run_gb300(args):
                w.rope_theta, w.sm_scale, d["ws"], stream)
         ev[2].record(stream)
 
+    def check_status(when):
+        for d in sets:
+            st = ta.device_status(d["ws"], stream)
+            if st != ta.TA_OK:
+                raise RuntimeError(f"{w.name}: device status {when}: {ta.status_string(st)}")
+
+    K = args.steps
     for i in range(args.warmup):
         step(sets[i % n_sets])
     torch.cuda.synchronize(dev)
-    for d in sets:
-        st = ta.device_status(d["ws"], stream)
-        if st != ta.TA_OK:
-            raise RuntimeError(f"device status after warm-up: {ta.status_string(st)}")
+    check_status("after warm-up")
 
-    # timed region: K steps back to back, events only around the whole run
-    # (an event between two launches is a stream operation of its own and
-    # would break the overlap of programmatic dependent launch)
-    K = args.steps
-    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    clocks = ClockSampler(local)
-    clocks.start()
-    time.sleep(0.3)
-    barrier(world)
-    torch.cuda.synchronize(dev)
-    t_start.record(stream)
-    for i in range(K):
-        step(sets[i % n_sets])
-    t_end.record(stream)
-    torch.cuda.synchronize(dev)
-    barrier(world)
-    clk = clocks.stop()
-    total_ms = t_start.elapsed_time(t_end)
-    max_ms = max_over_ranks(total_ms, world, dev)
-    # per-kernel split for the roofline: a second pass through the plan / run
-    # entry points with events between the plan and the run launches
+    def timed_run():
+        # events only around the whole run: an event between two launches is
+        # a stream operation of its own and would break the overlap of
+        # programmatic dependent launch
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier(world)
+        torch.cuda.synchronize(dev)
+        a.record(stream)
+        for i in range(K):
+            step(sets[i % n_sets])
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier(world)
+        return max_over_ranks(a.elapsed_time(b), world, dev)
+
+    repeats = max(1, args.repeats)
+    clk = None
+    if headline:
+        # enough repeats that the timed runs span about a second of clock samples
+        probe = timed_run()
+        repeats = max(repeats, min(400, math.ceil(1000.0 / max(probe, 1e-3))))
+        clocks = ClockSampler(local)
+        clocks.start()
+        time.sleep(0.3)
+    runs = [timed_run() for _ in range(repeats)]
+    if headline:
+        clk = clocks.stop()
+    run_ms = statistics.median(runs)
+    ms_step = run_ms / K
+    # per-kernel split for the roofline
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
     for i in range(K):
         step_two_launch(sets[i % n_sets], evs[i])
     torch.cuda.synchronize(dev)
-    attn_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
-    plan_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
-    for d in sets:
-        st = ta.device_status(d["ws"], stream)
-        if st != ta.TA_OK:
-            raise RuntimeError(f"device status after timing: {ta.status_string(st)}")
+    attn_ms = statistics.median(e[1].elapsed_time(e[2]) for e in evs)
+    plan_ms = statistics.median(e[0].elapsed_time(e[1]) for e in evs)
+    check_status("after timing")
 
-    # end to end through the public call with host buffers
+    peaks, peak_src = measured_peaks()
+    roof = _roofline(nbytes, flops, attn_ms / 1e3, peaks)
+    roof["traffic"] = recorded_traffic(w.name)
+    roof["peak_source"] = peak_src
+    step_roof = _roofline(nbytes, flops, ms_step / 1e3, peaks)
+    res = {
+        "workload": w.name, "ms_per_step": ms_step, "runs": repeats, "steps_per_run": K,
+        "run_ms_min": min(runs) / K, "run_ms_max": max(runs) / K,
+        "tflops": flops / (ms_step / 1e3) / 1e12,
+        "tokens_per_s": w.total_q / (ms_step / 1e3),
+        "bound": roof["bound"], "frac": roof["frac"], "step_frac": step_roof["frac"],
+        "attn_kernel_ms": attn_ms, "plan_kernel_ms": plan_ms, "traffic": roof["traffic"],
+        "algorithmic_bytes": nbytes, "algorithmic_flops": flops,
+        "gpu_launches_per_step": 2 + (w.rotary_mode == 1 and not ta.folds_rotation(w.total_kv)),
+        "l2": l2_note,
+    }
+    if not headline:
+        return res, None
+
+    # end to end through the public call with host buffers: this step's inputs
+    # in from pinned host memory, out and lse back, every step
     keys_in = ["q", "k", "v", "q_indptr", "kv_indptr", "mn_indptr", "tree_order",
                "q_rope_position"]
     host = {k: (base[k].cpu().pin_memory() if base[k] is not None else None) for k in keys_in}
@@ -376,77 +422,95 @@ def run_gb300(args):
     host_lse = torch.empty(base["q"].shape[:2], dtype=torch.float32).pin_memory()
     h2d = sum(host[k].numel() * host[k].element_size() for k in keys_in if host[k] is not None)
     d2h = host_out.numel() * host_out.element_size() + host_lse.numel() * 4
-    for i in range(min(args.warmup, 3)):
-        d = sets[i % n_sets]
+
+    def e2e_step(d):
         for k in keys_in:
             if host[k] is not None:
                 d[k].copy_(host[k], non_blocking=True)
-        ta.tree_attn(d["q"], d["q_indptr"], d["k"], d["v"], d["kv_indptr"],
-                     d["q_rope_position"], d["mn_indptr"], d["tree_order"], d["out"], d["lse"],
-                     w.rotary_mode, w.rope_scale, w.rope_theta, w.sm_scale, d["ws"], stream)
+        step(d)
         host_out.copy_(d["out"], non_blocking=True)
         host_lse.copy_(d["lse"], non_blocking=True)
+
+    for i in range(min(args.warmup, 3)):
+        e2e_step(sets[i % n_sets])
     torch.cuda.synchronize(dev)
     barrier(world)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for i in range(K):
-        d = sets[i % n_sets]
-        for k in keys_in:
-            if host[k] is not None:
-                d[k].copy_(host[k], non_blocking=True)
-        ta.tree_attn(d["q"], d["q_indptr"], d["k"], d["v"], d["kv_indptr"],
-                     d["q_rope_position"], d["mn_indptr"], d["tree_order"], d["out"], d["lse"],
-                     w.rotary_mode, w.rope_scale, w.rope_theta, w.sm_scale, d["ws"], stream)
-        host_out.copy_(d["out"], non_blocking=True)
-        host_lse.copy_(d["lse"], non_blocking=True)
+        e2e_step(sets[i % n_sets])
     e1.record(stream)
     torch.cuda.synchronize(dev)
     barrier(world)
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
-    for d in sets:
-        if ta.device_status(d["ws"], stream) != ta.TA_OK:
-            raise RuntimeError("device status after the end-to-end pass")
+    check_status("after the end-to-end pass")
+    extra = {"roofline": roof, "clocks": clk, "e2e_ms": e2e_ms, "h2d": h2d, "d2h": d2h,
+             "l2_note": l2_note, "flops": flops}
+    return res, extra
 
-    peaks, peak_src = measured_peaks()
-    t_hbm = nbytes / (peaks["hbm_gbs"] * 1e9)
-    t_tc = flops / (peaks["bf16_tflops"] * 1e12)
-    attn_s = attn_ms / 1e3
-    if t_hbm >= t_tc:
-        roof = {"bound": "hbm", "achieved": nbytes / attn_s / 1e9, "peak": peaks["hbm_gbs"],
-                "unit": "GB/s"}
-    else:
-        roof = {"bound": "tensor", "achieved": flops / attn_s / 1e12,
-                "peak": peaks["bf16_tflops"], "unit": "TFLOP/s"}
-    roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = recorded_traffic(w.name)
-    roof["peak_source"] = peak_src
+
+def run_gb300(args):
+    import tree_attention_gb300 as ta
+    from tree_attention_gb300 import build as ta_build
+
+    rank, local, world = dist_info()
+    init_dist(world, "nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    ta_build.build()
+    ta.lib()
+    stream = torch.cuda.current_stream(dev)
+    w = make_workload(args.workload)
+    head, extra = measure_workload(ta, w, args, dev, stream, world, local, headline=True)
+    per_config = {}
+    if not args.no_per_config:
+        for name in PER_CONFIG:
+            if name == w.name:
+                per_config[name] = head
+                continue
+            res, _ = measure_workload(ta, make_workload(name), args, dev, stream, world, local)
+            per_config[name] = res
+            torch.cuda.empty_cache()
+
+    K = args.steps
+    ms = head["ms_per_step"]
+    flops = extra["flops"]
+    roof = dict(extra["roofline"])
     roof["kernel"] = ("run: attn_kernel (persistent tcgen05 tree attention), after the key "
                       "rotation under RoPE (timed through the plan / run entry points)")
-    roof["kernel_ms"] = attn_ms
-    roof["plan_kernel_ms"] = plan_ms
-    roof["note"] = ("kernel_ms: the run half (key rotation under RoPE + attention kernel) timed "
-                    "with events between the launches, so without launch overlap; the timed "
-                    "one-call step overlaps its launches (and folds a small rotation into the "
-                    "plan kernel), so ms_per_step can be below kernel_ms")
-    roof["t_roof_8tbs_us"] = max(nbytes / 8e12, flops / (peaks["bf16_tflops"] * 1e12)) * 1e6
-    roof["step_frac_of_t_roof"] = roof["t_roof_8tbs_us"] / (max_ms / K * 1e3)
-
+    roof["kernel_ms"] = head["attn_kernel_ms"]
+    roof["plan_kernel_ms"] = head["plan_kernel_ms"]
+    roof["note"] = ("kernel_ms: median over the steps of the run half (key rotation under RoPE "
+                    "+ attention kernel) timed with events between the launches, so without "
+                    "launch overlap; the timed one-call step overlaps its launches, so "
+                    "ms_per_step can be below plan + kernel")
+    peaks, _ = measured_peaks()
+    roof["t_roof_8tbs_us"] = max(head["algorithmic_bytes"] / 8e12,
+                                 flops / (peaks["bf16_tflops"] * 1e12)) * 1e6
+    roof["step_frac_of_t_roof"] = roof["t_roof_8tbs_us"] / (ms * 1e3)
+    clk = extra["clocks"]
+    if clk:
+        clk["ms_per_step_x_sm_mhz"] = ms * clk["sm_mhz"]
     line = {
         "metric": METRIC,
-        "value": weak_scaling_value(flops * K, world, max_ms / 1e3) / 1e12,
+        "value": weak_scaling_value(flops, world, ms / 1e3) / 1e12,
         "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
-        "ms_per_step": max_ms / K, "higher_is_better": True, "scaling": "weak",
+        "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
-        "config": _config_dict(w, l2_note),
-        "tokens_per_s": weak_scaling_value(w.total_q * K, world, max_ms / 1e3),
+        "config": _config_dict(w, extra["l2_note"]),
+        "timing": (f"median of {head['runs']} runs of {K} steps (min {head['run_ms_min']:.4f}, "
+                   f"max {head['run_ms_max']:.4f} ms per step), CUDA events on the launching "
+                   f"stream, max over ranks"),
+        "tokens_per_s": weak_scaling_value(w.total_q, world, ms / 1e3),
         "roofline": roof,
-        "e2e": {"value": weak_scaling_value(flops * K, world, e2e_ms / 1e3) / 1e12, "unit": UNIT,
-                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
-        # per step: plan kernel, key-rotation kernel (RoPE, unless the plan
-        # kernel folds it in: small problems), attention kernel
-        "gpu_launches": (2 + (w.rotary_mode == 1 and not ta.folds_rotation(w.total_kv))) * K,
+        "e2e": {"value": weak_scaling_value(flops * K, world, extra["e2e_ms"] / 1e3) / 1e12,
+                "unit": UNIT, "h2d_bytes_per_step": int(extra["h2d"]),
+                "d2h_bytes_per_step": int(extra["d2h"])},
+        # per timed run: plan kernel, key-rotation kernel (RoPE, unless the
+        # plan kernel folds it in: small problems), attention kernel
+        "gpu_launches": head["gpu_launches_per_step"] * K,
         "clocks": clk,
+        "per_config": per_config,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w)
@@ -727,10 +791,14 @@ def main(argv=None):
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=10)
-    ap.add_argument("--workload", default="spec-decode",
+    ap.add_argument("--workload", default="ragged-large",
                     choices=list(WORKLOADS) + list(EXTRA_WORKLOADS))
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--sets", type=int, default=0, help="input/output buffer sets to rotate")
+    ap.add_argument("--repeats", type=int, default=5,
+                    help="timed runs of --steps steps each; the median run is reported")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="time only --workload, not the four benchmark workloads beside it")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--paged", action="store_true",
                     help="time the paged-KV path (tree_attn_paged) on the workload's shapes")

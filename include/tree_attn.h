@@ -171,6 +171,14 @@ ta_status tree_attn_noalloc(const void* q, const int32_t* q_indptr, const void* 
                             float* lse, int32_t rotary_mode, float rope_scale, float rope_theta,
                             float sm_scale, const ta_dims* dims, void* stream);
 
+/* Synchronises ``stream`` and reads and clears the device status word that
+ * earlier tree_attn_noalloc calls on the current device left in the static
+ * scratch array (the caller never sees that array's address): TA_OK,
+ * TA_ERR_DEVICE_TIMEOUT if a bounded wait expired, TA_ERR_INVALID_ARGUMENT if
+ * the index arrays broke the layout rules (nothing was computed), TA_ERR_CUDA
+ * on a CUDA error.  Like tree_attn_device_status, but for the array. */
+ta_status tree_attn_noalloc_device_status(void* stream);
+
 /* ---- Paged KV cache ------------------------------------------------------
  * The same tree attention with K and V held in a paged cache, as the page
  * "tree_attn.py" generates it in ``tree_attn_with_paged_kv_cache`` (GPU) and
@@ -284,6 +292,25 @@ ta_status tree_attn_merge_states(const void* parts, const float* lses, int32_t n
  * kernels of earlier calls left in ``workspace`` (TA_ERR_DEVICE_TIMEOUT if a
  * bounded wait expired, TA_ERR_CUDA on a CUDA error, else TA_OK). */
 ta_status tree_attn_device_status(void* workspace, void* stream);
+
+/* Test hooks for the failure detection of this library (the pages have no
+ * counterpart; their only checks are compile-time asserts such as
+ * ``check_thread_limits`` on the page "_kernel_common.py").  Every hand-off
+ * between the warps of the attention kernel is an mbarrier wait bounded by a
+ * wall-clock limit (2 s); when one runs out the kernel records
+ * TA_ERR_DEVICE_TIMEOUT in the workspace status word, lets its in-flight
+ * copies and tensor-core operations land, frees its tensor memory and
+ * returns, and tree_attn_device_status reports it.  These hooks let a test
+ * take that path on purpose, for the attention kernels launched by later
+ * calls made on the calling host thread:
+ *   wait_limit_ns  the limit of every bounded wait (0: the default 2 s)
+ *   stall          1: the MMA thread of every pipeline first waits on a
+ *                  barrier that nothing arrives on, so that this wait runs
+ *                  out after wait_limit_ns and every other warp then gives up
+ *                  its own waits; 0: normal operation
+ * Returns TA_ERR_INVALID_ARGUMENT for stall outside {0, 1}.  Not for
+ * production use: a stalled call computes nothing. */
+ta_status tree_attn_set_wait_hooks(uint64_t wait_limit_ns, int32_t stall);
 
 /* The CUDA runtime's description of the error behind the calling thread's
  * most recent TA_ERR_CUDA ("no error" if there was none; static storage).

@@ -292,3 +292,10 @@ def test_last_cuda_error_names_the_failure(lib):
     assert msg and msg != "no error"
     err = ta.TreeAttnError(st, "tree_attn_merge_states")
     assert msg in str(err)
+
+
+def test_wait_hooks_validate_and_reset(lib):
+    """The test hooks of the failure detection are host-only settings."""
+    assert lib.tree_attn_set_wait_hooks(0, 2) == ta.TA_ERR_INVALID_ARGUMENT
+    assert lib.tree_attn_set_wait_hooks(1000, 1) == ta.TA_OK
+    assert lib.tree_attn_set_wait_hooks(0, 0) == ta.TA_OK

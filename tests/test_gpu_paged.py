@@ -129,3 +129,29 @@ def test_paged_bad_page_table_is_reported():
     st = ta.device_status(ws)
     assert st == ta.TA_ERR_INVALID_ARGUMENT or st != ta.TA_OK
     assert torch.all(out == 7.0)             # nothing computed
+
+
+@pytest.mark.parametrize("name,seqs", [("degenerate", [1, 3]), ("ragged-large", [0, 1, 2, 63])])
+def test_paged_full_size_benchmark_shape(name, seqs):
+    """The paged path at a benchmarked full-size shape (the workload ``bench.py
+    --paged`` times: every sequence's K/V scattered over 16-slot pages, RoPE
+    off as the pages' paged kernel has none), checked against the paged oracle
+    on a subset of its sequences (the oracle is too slow for all of them)."""
+    import dataclasses
+    idx = {"degenerate": 5, "ragged-large": 4}[name]
+    w = dataclasses.replace(wl.config(idx), rotary_mode=0)
+    pk = wl.paged_from(w, seed=17)
+    out, lse = _paged_gpu(w, pk)
+    out = out.float().cpu().numpy()
+    lse = lse.cpu().numpy()
+    assert np.isfinite(out).all(), "a slot no sequence owns reached the output"
+    ro, rl = oracle.tree_attention_paged(w.q, w.q_indptr, pk.pages, pk.page_indptr,
+                                         pk.page_values, pk.last_page_len, w.mn_indptr,
+                                         w.tree_order, 0, w.sm_scale, seqs=seqs)
+    rows = np.concatenate([np.arange(w.q_indptr[b], w.q_indptr[b + 1]) for b in seqs])
+    err_o = float(np.max(np.abs(out[rows] - ro[rows])))
+    assert err_o <= TOL_OUT[w.dtype], f"out max|err| {err_o}"
+    fin = np.isfinite(rl[rows])
+    assert np.array_equal(fin, np.isfinite(lse[rows]))
+    err_l = float(np.max(np.abs(lse[rows][fin] - rl[rows][fin])))
+    assert err_l <= TOL_LSE, f"lse max|err| {err_l}"

@@ -61,3 +61,32 @@ def test_noalloc_matches_tree_attn_on_two_calls_in_a_row(idx):
         assert np.isfinite(o).all() and np.isfinite(l).all()
         assert np.max(np.abs(o - ref_out)) <= TOL_OUT[w.dtype]
         assert np.max(np.abs(l - ref_lse)) <= TOL_LSE
+        assert ta.noalloc_device_status() == ta.TA_OK
+
+
+@pytest.mark.gpu
+def test_noalloc_reports_bad_index_arrays_then_recovers():
+    """The status word lives in the static array, which the caller cannot
+    address: tree_attn_noalloc_device_status reads and clears it.  Index
+    arrays that break the layout rules are reported and nothing is computed;
+    the next valid call reports TA_OK."""
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    w = wl.config(1)
+    d = wl.device_inputs(w)
+    assert ta.noalloc_device_status() == ta.TA_OK
+    bad = dict(d)
+    bad["q_indptr"] = d["q_indptr"].clone()
+    bad["q_indptr"][-1] += 1                       # no longer ends at total_q
+    out = torch.full_like(d["q"], 7.0)
+    lse = torch.full(d["q"].shape[:2], 7.0, dtype=torch.float32, device="cuda")
+    ta.tree_attn_noalloc(bad["q"], bad["q_indptr"], bad["k"], bad["v"], bad["kv_indptr"],
+                         bad["q_rope_position"], bad["mn_indptr"], bad["tree_order"], out, lse,
+                         w.rotary_mode, w.rope_scale, w.rope_theta, w.sm_scale)
+    assert ta.noalloc_device_status() == ta.TA_ERR_INVALID_ARGUMENT
+    assert torch.all(out == 7.0) and torch.all(lse == 7.0)
+    ta.tree_attn_noalloc(d["q"], d["q_indptr"], d["k"], d["v"], d["kv_indptr"],
+                         d["q_rope_position"], d["mn_indptr"], d["tree_order"], out, lse,
+                         w.rotary_mode, w.rope_scale, w.rope_theta, w.sm_scale)
+    assert ta.noalloc_device_status() == ta.TA_OK
+    assert np.isfinite(out.float().cpu().numpy()).all()

@@ -27,7 +27,7 @@ __all__ = [
     "tree_attn", "plan", "run", "device_status", "status_string", "mask_dense", "check_inputs",
     "TreeAttention", "PagedDims", "make_paged_dims", "paged_workspace_size", "tree_attn_paged",
     "MAX_CHUNKS", "split_workspace_size", "tree_attn_split", "merge_states", "last_cuda_error",
-    "folds_rotation",
+    "folds_rotation", "noalloc_device_status", "set_wait_hooks",
 ]
 
 TA_OK = 0
@@ -100,6 +100,10 @@ def lib() -> ctypes.CDLL:
     L.tree_attn_noalloc.restype = ctypes.c_int
     L.tree_attn_device_status.argtypes = [vp, vp]
     L.tree_attn_device_status.restype = ctypes.c_int
+    L.tree_attn_noalloc_device_status.argtypes = [vp]
+    L.tree_attn_noalloc_device_status.restype = ctypes.c_int
+    L.tree_attn_set_wait_hooks.argtypes = [ctypes.c_uint64, ctypes.c_int32]
+    L.tree_attn_set_wait_hooks.restype = ctypes.c_int
     L.tree_attn_last_cuda_error.argtypes = []
     L.tree_attn_last_cuda_error.restype = ctypes.c_char_p
     L.tree_attn_status_string.argtypes = [ctypes.c_int]
@@ -357,6 +361,21 @@ def run(q, k, v, q_indptr, kv_indptr, q_rope_position, mn_indptr, tree_order, ou
 def device_status(workspace: torch.Tensor, stream=None) -> int:
     """Synchronise the stream and return (and clear) the device status."""
     return int(lib().tree_attn_device_status(_ptr(workspace), _stream_ptr(stream)))
+
+
+def noalloc_device_status(stream=None) -> int:
+    """Synchronise the stream and return (and clear) the device status that
+    ``tree_attn_noalloc`` calls left in the library's static scratch array."""
+    return int(lib().tree_attn_noalloc_device_status(_stream_ptr(stream)))
+
+
+def set_wait_hooks(wait_limit_ns: int = 0, stall: bool = False) -> None:
+    """Test hook: the bounded-wait limit of later calls on this thread (0:
+    the default) and whether their MMA threads first wait on a barrier that
+    nothing arrives on (so that the wait runs out)."""
+    st = lib().tree_attn_set_wait_hooks(int(wait_limit_ns), 1 if stall else 0)
+    if st != TA_OK:
+        raise TreeAttnError(st, "tree_attn_set_wait_hooks")
 
 
 def mask_dense(q_indptr, kv_indptr, mn_indptr, tree_order, total_q: int, max_kv: int,

@@ -25,6 +25,14 @@ constexpr unsigned long long kDeviceWaitLimitNs = 2000000000ull;  // 2 s per bou
 // The CUDA error behind this thread's last TA_ERR_CUDA (cudaSuccess if none).
 thread_local cudaError_t g_last_cuda_error = cudaSuccess;
 
+// Test hooks of the calling thread (tree_attn_set_wait_hooks): the bounded
+// wait limit of the attention kernels it launches (0: kDeviceWaitLimitNs) and
+// whether their MMA threads first wait on a barrier that nothing arrives on.
+thread_local unsigned long long g_wait_limit_ns = 0;
+thread_local int g_stall = 0;
+
+unsigned long long wait_limit_ns() { return g_wait_limit_ns ? g_wait_limit_ns : kDeviceWaitLimitNs; }
+
 // TA_ERR_CUDA for a failed CUDA call, remembering its error; TA_OK otherwise.
 ta_status cuda_status(cudaError_t e) {
   if (e == cudaSuccess) return TA_OK;
@@ -344,7 +352,8 @@ ta_status launch_run_checked(const void* q, const void* k, const void* v, const 
   ap.rotary = rotary_mode;
   ap.max_records = L.max_records;
   ap.scale_log2 = sm_scale * 1.4426950408889634f;
-  ap.timeout_ns = kDeviceWaitLimitNs;
+  ap.timeout_ns = wait_limit_ns();
+  ap.debug_stall = g_stall;
   ap.part_o = w.part_o;
   ap.part_lse = w.part_lse;
   const int64_t max_items = L.max_records * dims->h_kv;
@@ -509,6 +518,13 @@ ta_status tree_attn_device_status(void* workspace, void* stream) {
 
 const char* tree_attn_last_cuda_error(void) { return cudaGetErrorString(g_last_cuda_error); }
 
+ta_status tree_attn_set_wait_hooks(uint64_t wait_limit_ns, int32_t stall) {
+  if (stall != 0 && stall != 1) return TA_ERR_INVALID_ARGUMENT;
+  g_wait_limit_ns = wait_limit_ns;
+  g_stall = stall;
+  return TA_OK;
+}
+
 const char* tree_attn_status_string(ta_status s) {
   switch (s) {
     case TA_OK: return "TA_OK";
@@ -587,7 +603,9 @@ __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 constexpr int kMaxDevices = 256;
 
 // Device address of the scratch array on the current device, looked up once
-// per device (the first call on a device does this set-up).
+// per device (the first call on a device does this set-up).  The cached
+// address belongs to the device's primary context: it does not survive a
+// cudaDeviceReset of that device.
 void* noalloc_scratch_address() {
   static std::mutex mu;
   static void* addr[kMaxDevices] = {};
@@ -627,6 +645,12 @@ ta_status tree_attn_noalloc(const void* q, const int32_t* q_indptr, const void* 
   return tree_attn(q, q_indptr, k, v, kv_indptr, q_rope_position, mn_indptr, tree_order, out,
                    lse, rotary_mode, rope_scale, rope_theta, sm_scale, dims, ws,
                    kNoAllocScratchBytes, stream);
+}
+
+ta_status tree_attn_noalloc_device_status(void* stream) {
+  void* ws = noalloc_scratch_address();
+  if (ws == nullptr) return cuda_failure();
+  return tree_attn_device_status(ws, stream);
 }
 
 }  // extern "C"
@@ -753,7 +777,8 @@ ta_status tree_attn_paged(const void* q, const int32_t* q_indptr, const void* pa
   ap.rotary = 0;
   ap.max_records = L.max_records;
   ap.scale_log2 = sm_scale * 1.4426950408889634f;
-  ap.timeout_ns = kDeviceWaitLimitNs;
+  ap.timeout_ns = wait_limit_ns();
+  ap.debug_stall = g_stall;
   ap.part_o = nullptr;
   ap.part_lse = nullptr;
   const int64_t max_items = L.max_records * d.h_kv;

@@ -53,6 +53,7 @@ enum Bar : int {
   B_PV_DONE = B_P_FULL + 2,              // [2] PV reading that P is complete (V stage read)
   B_O_FREE = B_PV_DONE + 2,
   B_DRAIN,
+  B_STALL,                               // test hook: nothing ever arrives on it
   B_COUNT
 };
 
@@ -326,7 +327,10 @@ __device__ void run_mma(const Pipe& pp, const AttnParams& p) {
   const int q_bar = p.rotary ? B_Q_READY : B_Q_FULL;
   uint32_t it = 0, kv_it = 0, q_it = 0, o_it = 0;
   bool issued_any = false;
-  for (;;) {
+  // test hook: a wait that runs out before any MMA is issued (the other warps
+  // then find the abort flag in their own waits)
+  if (p.debug_stall) pp.wait(B_STALL, 0);
+  for (; !p.debug_stall;) {
     const int slot = it % kSlots;
     if (!pp.wait(B_ITEM_FULL + slot, (it / kSlots) & 1)) break;
     const Item& s = pp.items[slot];
@@ -497,7 +501,20 @@ __device__ void rope_q_rows(uint8_t* tile, const float2* __restrict__ cs, long l
 }
 
 template <int D, bool BF16, bool PAGED>
+__device__ void softmax_loop(const Pipe& pp, const AttnParams& p, int sw, int lane);
+
+// The softmax warps' loop; on every way out (the work is done, or a bounded
+// wait gave up) the warp waits for its own TMEM loads and stores to finish
+// before the CTA frees the TMEM.
+template <int D, bool BF16, bool PAGED>
 __device__ void run_softmax(const Pipe& pp, const AttnParams& p, int sw, int lane) {
+  softmax_loop<D, BF16, PAGED>(pp, p, sw, lane);
+  tmem_wait_ld();
+  tmem_wait_st();
+}
+
+template <int D, bool BF16, bool PAGED>
+__device__ void softmax_loop(const Pipe& pp, const AttnParams& p, int sw, int lane) {
   using C = Cfg<D>;
   const int wq = sw;                          // TMEM lane quadrant (warp index mod 4)
   const int row = wq * 32 + lane;             // packed row = TMEM lane
@@ -813,6 +830,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(&bar[B_O_FREE], 4);
     mbar_init(&bar[B_DRAIN], 1);
+    mbar_init(&bar[B_STALL], 1);
     if (pipe == 0) cta->abort = 0;
     mbar_fence_init();
     tma_prefetch_desc(&tm_q);

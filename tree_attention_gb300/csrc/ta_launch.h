@@ -88,6 +88,9 @@ struct AttnParams {
   int64_t max_records;  // capacity of the record table in the workspace
   float scale_log2;     // sm_scale * log2(e)
   unsigned long long timeout_ns;
+  // test hook: the MMA threads first wait on a barrier that nothing arrives
+  // on, so that the bounded wait runs out and the abort path runs
+  int debug_stall;
   // split-KV partial states of the records with part >= 0: O / l in float32
   // [record][h_kv][128 packed rows][d] and the base-2 lse [record][h_kv][128]
   float* part_o;
