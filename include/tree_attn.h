@@ -257,11 +257,11 @@ size_t tree_attn_split_workspace_size(const ta_dims* dims, int32_t max_chunks);
  * for tree_attn, plus:
  *   max_chunks   1..16, the most chunks one (sequence, q tile) pair is cut
  *                into (1: no split, the result is then tree_attn's exactly)
- *   chunk_tiles  target chunk length in kv tiles of 64 columns (>= 0); a pair
- *                whose kv tiles up to its last row's own slot number c gets
- *                min(max_chunks, ceil(c / chunk_tiles)) chunks.  0 lets the
- *                plan choose it from the batch's total work: a quarter of one
- *                pipeline's share of it (two pipelines per SM), at least 16.
+ *   chunk_tiles  target chunk length in kv tiles of 128 columns (>= 0); a
+ *                pair whose kv tiles up to its last row's own slot number c
+ *                gets min(max_chunks, ceil(c / chunk_tiles)) chunks.  0 lets
+ *                the plan choose it from the batch's total work: a quarter of
+ *                one SM's share of it, at least 8.
  * The chunks of a pair split the range of its kv tiles up to its last
  * non-empty tile into equal lengths.  workspace must hold at least
  * tree_attn_split_workspace_size(dims, max_chunks) bytes, with tree_attn's

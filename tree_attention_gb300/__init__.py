@@ -282,7 +282,7 @@ def tree_attn_split(q, q_indptr, k, v, kv_indptr, q_rope_position, mn_indptr, tr
                     sm_scale: float, max_chunks: int, chunk_tiles: int,
                     workspace: torch.Tensor, stream=None) -> None:
     """``tree_attn`` with split-KV: pairs with many kv tiles are cut into up
-    to ``max_chunks`` chunks of about ``chunk_tiles`` 64-column tiles (0: the
+    to ``max_chunks`` chunks of about ``chunk_tiles`` 128-column tiles (0: the
     plan picks the length), whose partial states a merge kernel combines.
     ``workspace`` holds ``split_workspace_size(dims, max_chunks)`` bytes."""
     for name, t in (("q", q), ("k", k), ("v", v), ("out", out)):

@@ -278,7 +278,7 @@ ta_status launch_plan_checked(const int32_t* q_indptr, const int32_t* kv_indptr,
   pp.max_pairs = L.max_pairs;
   pp.max_chunks = max_chunks;
   pp.chunk_tiles = chunk_tiles;
-  pp.pipes = 2 * nsm;
+  pp.pipes = nsm;   // one attention pipeline per SM
   pp.merge = w.merge;
   pp.hdr = w.hdr;
   pp.sorted = w.sorted;
@@ -748,7 +748,7 @@ ta_status tree_attn_paged(const void* q, const int32_t* q_indptr, const void* pa
   pp.max_pairs = L.max_pairs;
   pp.max_chunks = 1;
   pp.chunk_tiles = 0;
-  pp.pipes = 2 * nsm;
+  pp.pipes = nsm;   // one attention pipeline per SM
   pp.merge = nullptr;
   pp.hdr = w.hdr;
   pp.sorted = w.sorted;

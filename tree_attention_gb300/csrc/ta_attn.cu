@@ -4,18 +4,27 @@
 // (per q row and head: masked online softmax of sm_scale * q.k in log2
 // units, output O / d and lse = m + log2(d)), re-designed for one GB300 SM.
 //
-// Each CTA runs two independent pipelines side by side (so that one hides
-// the other's latencies); both pop (sequence, q tile, kv head) work items
-// from one longest-first queue.  A pipeline is six warps:
-//   producer   stages the item's work, TMA-loads the packed Q tile and the
-//              item's non-empty K/V tiles (64 kv rows each) into a 2-stage
-//              ring, with each partial tile's column intervals beside it
-//   MMA        one thread issues tcgen05.mma: S = Q K^T into one of two TMEM
-//              score buffers, then O += P V with P read from TMEM
-//   softmax    four warps, one TMEM lane (= packed row) per thread: inline
-//              RoPE of the Q tile, tree mask, online softmax with a lazily
-//              moved reference max, P (fp16/bf16) written over its own score
-//              buffer in TMEM, O rescale, final O / l and lse stores
+// One CTA per SM pops (sequence, q tile, kv head) work items from a
+// longest-first queue and streams their non-empty kv tiles of 128 columns
+// through one tensor-core pipeline.  Tensor memory holds two score buffers
+// (S0, S1: 128 columns each) and two output accumulators (O0, O1: one per
+// item in flight), so that the QK^T of tile c + 1 overlaps the softmax of
+// tile c and one item's epilogue overlaps the next item's first tiles.
+// Warp roles:
+//   warp 0      producer: stages each item's record, TMA-loads its packed Q
+//               tile (two buffers) and its K/V tiles (two stages), with each
+//               partial tile's column intervals beside them
+//   warp 1      MMA issuer (one thread): S = Q K^T and O += P V
+//               (tcgen05.mma, M = 128, N = 128), P read from tensor memory;
+//               it runs over one stream of tiles across item boundaries,
+//               issuing the QK^T of tile c + 2 right after the PV of tile c
+//   warps 4-7   softmax: one TMEM lane (= packed row) per thread: tree mask,
+//               online softmax with a lazily moved reference max, P
+//               (fp16/bf16) written over the first half of its score buffer,
+//               the rare rescale of O
+//   warps 8-11  correction: RoPE of each item's Q tile (before the item's
+//               first QK^T) and the epilogue of the item before it (O / l
+//               and lse from tensor memory to global memory)
 // Keys arrive rotated (the run rotates them once per call).  Every cross-warp
 // hand-off is an mbarrier with a bounded wait.
 #include <cuda_runtime.h>
@@ -29,33 +38,52 @@
 namespace ta {
 namespace {
 
-constexpr int kPipes = 2;
-constexpr int kWarpsPerPipe = 6;
-constexpr int kThreads = kPipes * kWarpsPerPipe * 32;
-constexpr int kStages = 2;   // K/V ring depth per pipeline
-constexpr int kSlots = 2;    // work-item slots per pipeline
+constexpr int kThreads = 384;
+constexpr int kStages = 2;   // K/V ring depth = score buffers (tile c uses stage c & 1)
+constexpr int kSlots = 4;    // work-item slots (producer, MMA, softmax, correction)
+constexpr int kWarpProducer = 0;
+constexpr int kWarpMma = 1;
+constexpr int kWarpSoftmax = 4;      // warps 4..7
+constexpr int kWarpCorrection = 8;   // warps 8..11
+
+// Register split (setmaxnreg) of the 384 threads' launch allocation of 168
+// each (64,512 in all): the producer / MMA warpgroup and the correction
+// warpgroup give registers up, the softmax warpgroup -- one TMEM lane of 128
+// scores per thread -- takes them, so that its exponentials overlap.
+constexpr uint32_t kRegsLaunch = 168;
+constexpr uint32_t kRegsIssue = 80;        // warps 0-3
+constexpr uint32_t kRegsSoftmax = 248;     // warps 4-7
+constexpr uint32_t kRegsCorrection = 152;  // warps 8-11
+static_assert(128 * (kRegsIssue + kRegsSoftmax + kRegsCorrection) <= kThreads * kRegsLaunch,
+              "register split exceeds the launch allocation");
+
+// The QK^T of tile c + 2 overwrites the score buffer whose P the PV of tile c
+// reads; tcgen05.mma operations issued by one thread execute in issue order,
+// so it is issued right after that PV without waiting for its completion.
+constexpr bool kQkAfterPvInIssueOrder = true;
 
 enum Bar : int {
-  B_ITEM_FULL = 0,                       // [kSlots]
-  B_ITEM_EMPTY = B_ITEM_FULL + kSlots,   // [kSlots]
-  B_Q_FULL = B_ITEM_EMPTY + kSlots,
-  B_Q_READY,
-  B_Q_EMPTY,
-  B_K_FULL,                              // [kStages]
-  B_V_FULL = B_K_FULL + kStages,         // [kStages]
-  B_EX_FULL = B_V_FULL + kStages,        // [kStages]
-  // a K (V) stage is free again when the QK (PV) of the tile in it has
-  // completed: with two stages and two score buffers, tile c uses stage and
-  // buffer c & 1, so the producer waits on S_FULL (PV_DONE) of that index
-  // and the MMA thread commits nothing extra per tile
-  B_S_FULL = B_EX_FULL + kStages,        // [2] score buffer written (K stage read)
-  B_P_FULL = B_S_FULL + 2,               // [2] P written over the score buffer
-  B_PV_DONE = B_P_FULL + 2,              // [2] PV reading that P is complete (V stage read)
-  B_O_FREE = B_PV_DONE + 2,
-  B_DRAIN,
-  B_STALL,                               // test hook: nothing ever arrives on it
+  B_ITEM_FULL = 0,                     // [kSlots] record staged
+  B_ITEM_EMPTY = B_ITEM_FULL + kSlots, // [kSlots] MMA + 4 softmax + 4 correction warps done with it
+  B_Q_FULL = B_ITEM_EMPTY + kSlots,    // [2] Q buffer landed
+  B_Q_READY = B_Q_FULL + 2,            // [2] Q buffer rotated (RoPE)
+  B_Q_EMPTY = B_Q_READY + 2,           // [2] the last QK^T reading the Q buffer done
+  B_K_FULL = B_Q_EMPTY + 2,            // [kStages]
+  B_V_FULL = B_K_FULL + kStages,       // [kStages]
+  B_EX_FULL = B_V_FULL + kStages,      // [kStages] column intervals of a partial tile
+  // tile c uses K/V stage and score buffer c & 1: the producer frees a K (V)
+  // stage on S_FULL (PV_DONE) of that index, so no separate release commits
+  B_S_FULL = B_EX_FULL + kStages,      // [2] score buffer written (K stage read)
+  B_P_FULL = B_S_FULL + 2,             // [2] P written over the score buffer
+  B_PV_DONE = B_P_FULL + 2,            // [2] PV reading that P done (V stage read)
+  B_O_FULL = B_PV_DONE + 2,            // [2] the item's last PV into O buffer done
+  B_O_FREE = B_O_FULL + 2,             // [2] correction read O buffer and its (m, l)
+  B_ML_FULL = B_O_FREE + 2,            // [2] softmax wrote the rows' (m, l) of the item
+  B_DRAIN = B_ML_FULL + 2,
+  B_STALL,                             // test hook: nothing ever arrives on it
   B_COUNT
 };
+constexpr int kBarSlots = 48;
 
 struct Item {
   ItemRec r;
@@ -67,27 +95,24 @@ template <int D>
 struct Cfg {
   static constexpr int kAtoms = D / 64;               // 128-byte column blocks per row
   static constexpr int kQAtomBytes = kBlockM * 128;    // 128 rows x 128 bytes
-  static constexpr int kKVAtomBytes = kBlockN * 128;   // 64 rows x 128 bytes
+  static constexpr int kKVAtomBytes = kBlockN * 128;   // 128 rows x 128 bytes
   static constexpr int kQBytes = kAtoms * kQAtomBytes;
   static constexpr int kKVBytes = kAtoms * kKVAtomBytes;
-  static constexpr int kOstBytes = 32 * 64;            // per softmax warp: 32 rows x 64 bytes
-  // one pipeline's shared memory
-  static constexpr int kOffQ = 0;
-  static constexpr int kOffK = kOffQ + kQBytes;
-  static constexpr int kOffV = kOffK + kStages * kKVBytes;
-  static constexpr int kOffEX = kOffV + kStages * kKVBytes;    // [kStages][kBlockN] int2
-  static constexpr int kOffOst = kOffEX + kStages * kBlockN * 8;
+  static constexpr int kOstBytes = 32 * 64;            // per correction warp: 32 rows x 64 bytes
+  static constexpr int kOffQ = 0;                                   // [2] Q buffers
+  static constexpr int kOffK = kOffQ + 2 * kQBytes;                 // [kStages]
+  static constexpr int kOffV = kOffK + kStages * kKVBytes;          // [kStages]
+  static constexpr int kOffEX = kOffV + kStages * kKVBytes;         // int2 [kStages][kBlockN]
+  static constexpr int kOffML = kOffEX + kStages * kBlockN * 8;     // float2 [2][kBlockM]
+  static constexpr int kOffOst = kOffML + 2 * kBlockM * 8;          // [4 warps]
   static constexpr int kOffItems = kOffOst + 4 * kOstBytes;
   static constexpr int kOffBar = kOffItems + kSlots * (int)sizeof(Item);
-  static constexpr int kPipeUsed = kOffBar + 32 * 8;
-  static constexpr int kPipeBytes = (kPipeUsed + 1023) / 1024 * 1024;
-  // CTA-wide: TMEM address and abort flag after both pipelines
-  static constexpr int kOffCta = kPipes * kPipeBytes;
-  static constexpr int kSmemAlloc = kOffCta + 128 + 1024;   // room to align the base to 1024
+  static constexpr int kOffCta = kOffBar + kBarSlots * 8;
+  static constexpr int kUsed = kOffCta + 64;
+  static constexpr int kSmemAlloc = kUsed + 1024;   // room to align the base to 1024
   static constexpr uint32_t kTmemCols = 512;
-  static constexpr uint32_t kTmemPipe = 256;   // columns per pipeline
-  static constexpr uint32_t kTmemO = 0;        // accumulator
-  static constexpr uint32_t kTmemS = 128;      // score buffer sb at 128 + 64 * sb (P over it)
+  static constexpr uint32_t kTmemS = 0;      // score buffer sb at 128 * sb (P over its first half)
+  static constexpr uint32_t kTmemO = 256;    // O buffer ob at 256 + 128 * ob
 };
 
 struct CtaShared {
@@ -95,14 +120,14 @@ struct CtaShared {
   int abort;
 };
 
-struct Pipe {
-  uint8_t* smem;     // this pipeline's shared memory
+struct Ctx {
+  uint8_t* smem;
   uint64_t* bar;
   Item* items;
   volatile int* abort;
   unsigned int* dev_error;
   unsigned long long limit_ns;
-  uint32_t tmem;     // this pipeline's first TMEM column (lane 0)
+  uint32_t tmem;     // first TMEM column (lane 0)
   __device__ bool wait(int b, uint32_t parity) const {
     return mbar_wait(&bar[b], parity, abort, dev_error, limit_ns);
   }
@@ -126,6 +151,7 @@ struct TileIter {
   int kvt, j;
   bool inl;
   uint32_t w0, w1, w2, w3;   // inline classes, or the current 16 class bytes
+  __device__ TileIter() : cls(nullptr), kvt(0), j(0), inl(true), w0(0), w1(0), w2(0), w3(0) {}
   __device__ TileIter(const ItemRec& r, const uint8_t* classes)
       : cls(classes + r.class_off), kvt(r.kvt), j(r.tile_lo - 1), inl(r.kvt <= kInlineTiles) {
     w0 = r.cls2[0];
@@ -171,13 +197,13 @@ struct TileIter {
 // producer warp (lane 0 issues; all lanes stage mask intervals)
 // ---------------------------------------------------------------------------
 template <int D, bool PAGED>
-__device__ void run_producer(const Pipe& pp, const CUtensorMap* tm_q, const CUtensorMap* tm_k,
-                             const CUtensorMap* tm_v, const AttnParams& p, int pipe, int lane) {
+__device__ void run_producer(const Ctx& cx, const CUtensorMap* tm_q, const CUtensorMap* tm_k,
+                             const CUtensorMap* tm_v, const AttnParams& p, int lane) {
   using C = Cfg<D>;
-  uint8_t* sQ = pp.smem + C::kOffQ;
-  uint8_t* sK = pp.smem + C::kOffK;
-  uint8_t* sV = pp.smem + C::kOffV;
-  int2* sEX = reinterpret_cast<int2*>(pp.smem + C::kOffEX);
+  uint8_t* sQ = cx.smem + C::kOffQ;
+  uint8_t* sK = cx.smem + C::kOffK;
+  uint8_t* sV = cx.smem + C::kOffV;
+  int2* sEX = reinterpret_cast<int2*>(cx.smem + C::kOffEX);
   // the plan kernel wrote the item count; never trust it beyond the table size
   const unsigned long long cap = (unsigned long long)p.max_records * (unsigned long long)p.h_kv;
   const unsigned long long n_items = *(volatile unsigned int*)&p.hdr->num_items;
@@ -186,23 +212,23 @@ __device__ void run_producer(const Pipe& pp, const CUtensorMap* tm_q, const CUte
   uint32_t it = 0, kv_it = 0, q_it = 0;
   uint32_t issued_k = 0, issued_v = 0;   // loads issued (stage = count % kStages)
   bool aborted = false;
-  // the first item of every pipeline is fixed (pipeline p of CTA b takes
-  // item 2b + p, the items being in longest-first order already), the rest
-  // come from the queue, which starts after those 2 x grid items
-  const unsigned int n_static = (unsigned int)(kPipes * gridDim.x);
-  unsigned int idx = (unsigned int)(kPipes * blockIdx.x + pipe);
+  // the first item of every CTA is fixed (CTA b takes item b, the items being
+  // in longest-first order already), the rest come from the queue, which
+  // starts after those grid items
+  const unsigned int n_static = gridDim.x;
+  unsigned int idx = blockIdx.x;
   // lanes 0-3 hold the next record (16 bytes each), fetched one item ahead
   int4 rec_next = make_int4(0, 0, 0, 0);
   if (idx < num_items && lane < 4)
     rec_next = __ldg(reinterpret_cast<const int4*>(p.sorted + idx / p.h_kv) + lane);
   for (;;) {
     const int slot = it % kSlots;
-    if (!pp.warp_wait(B_ITEM_EMPTY + slot, ((it / kSlots) & 1) ^ 1)) { aborted = true; break; }
-    Item& s = pp.items[slot];
+    if (!cx.warp_wait(B_ITEM_EMPTY + slot, ((it / kSlots) & 1) ^ 1)) { aborted = true; break; }
+    Item& s = cx.items[slot];
     if (idx >= num_items) {
       if (lane == 0) {
         s.valid = 0;
-        mbar_arrive(&pp.bar[B_ITEM_FULL + slot]);
+        mbar_arrive(&cx.bar[B_ITEM_FULL + slot]);
       }
       break;
     }
@@ -217,15 +243,16 @@ __device__ void run_producer(const Pipe& pp, const CUtensorMap* tm_q, const CUte
     }
     __syncwarp();
     const ItemRec r = s.r;
-    if (lane == 0) mbar_arrive(&pp.bar[B_ITEM_FULL + slot]);
+    if (lane == 0) mbar_arrive(&cx.bar[B_ITEM_FULL + slot]);
     if (r.n_tiles > 0) {
-      if (!pp.warp_wait(B_Q_EMPTY, (q_it & 1) ^ 1)) { aborted = true; break; }
+      const int qb = q_it & 1;
+      if (!cx.warp_wait(B_Q_EMPTY + qb, ((q_it >> 1) & 1) ^ 1)) { aborted = true; break; }
       if (lane == 0) {
-        mbar_arrive_expect_tx(&pp.bar[B_Q_FULL], (uint32_t)(C::kAtoms * 128 * g * R));
+        mbar_arrive_expect_tx(&cx.bar[B_Q_FULL + qb], (uint32_t)(C::kAtoms * 128 * g * R));
 #pragma unroll
         for (int a = 0; a < C::kAtoms; ++a)
-          tma_load_3d(sQ + a * C::kQAtomBytes, tm_q, &pp.bar[B_Q_FULL], a * 64, kvh * g,
-                      r.q_row0);
+          tma_load_3d(sQ + qb * C::kQBytes + a * C::kQAtomBytes, tm_q, &cx.bar[B_Q_FULL + qb],
+                      a * 64, kvh * g, r.q_row0);
       }
       ++q_it;
       TileIter ti(r, p.classes);
@@ -236,58 +263,65 @@ __device__ void run_producer(const Pipe& pp, const CUtensorMap* tm_q, const CUte
         const int stage = kv_it % kStages;
         const uint32_t empty_par = ((kv_it / kStages) & 1) ^ 1;
         const uint32_t bytes = (uint32_t)C::kKVBytes;
-        // paged cache: kv tile j is logical pages 4j .. 4j+3 of the sequence;
-        // lanes 0-3 look up their physical pages, a missing page (past the
-        // sequence's last) takes an out-of-range page index, read as zeros
-        int ph0 = 0, ph1 = 0, ph2 = 0, ph3 = 0;
+        // paged cache: kv tile j is logical pages 8j .. 8j+7 of the sequence;
+        // lanes 0-7 look up their physical pages (shared with the warp), a
+        // missing page (past the sequence's last) takes an out-of-range page
+        // index, read as zeros
+        constexpr int kPagesPerTile = kBlockN / kPageSize;
+        int ph[kPagesPerTile];
         if constexpr (PAGED) {
           const int np = (r.kv + kPageSize - 1) / kPageSize;
-          const int lp = j * (kBlockN / kPageSize) + lane;
+          const int lp = j * kPagesPerTile + lane;
           int phys = p.num_pages;
-          if (lane < kBlockN / kPageSize && lp < np) phys = __ldg(p.page_values + r.kv_base + lp);
-          ph0 = __shfl_sync(0xffffffffu, phys, 0);
-          ph1 = __shfl_sync(0xffffffffu, phys, 1);
-          ph2 = __shfl_sync(0xffffffffu, phys, 2);
-          ph3 = __shfl_sync(0xffffffffu, phys, 3);
+          if (lane < kPagesPerTile && lp < np) phys = __ldg(p.page_values + r.kv_base + lp);
+#pragma unroll
+          for (int q = 0; q < kPagesPerTile; ++q) ph[q] = __shfl_sync(0xffffffffu, phys, q);
         }
         // one K or V tile into ``dst`` (kv plane 0 = K, 1 = V of the paged cache)
         auto load_tile = [&](uint8_t* dst, const CUtensorMap* map, uint64_t* bar, int plane) {
 #pragma unroll
           for (int a = 0; a < C::kAtoms; ++a) {
             if constexpr (PAGED) {
-              const int phs[4] = {ph0, ph1, ph2, ph3};
 #pragma unroll
-              for (int q = 0; q < kBlockN / kPageSize; ++q)
+              for (int q = 0; q < kPagesPerTile; ++q)
                 tma_load_5d(dst + a * C::kKVAtomBytes + q * kPageSize * 128, map, bar, a * 64, 0,
-                            kvh, plane, phs[q]);
+                            kvh, plane, ph[q]);
             } else {
               tma_load_3d(dst + a * C::kKVAtomBytes, map, bar, a * 64, kvh, row0);
             }
           }
         };
-        if (!pp.warp_wait(B_S_FULL + stage, empty_par)) { aborted = true; break; }
+        if (!cx.warp_wait(B_S_FULL + stage, empty_par)) { aborted = true; break; }
         if (lane == 0) {
-          mbar_arrive_expect_tx(&pp.bar[B_K_FULL + stage], bytes);
-          load_tile(sK + stage * C::kKVBytes, tm_k, &pp.bar[B_K_FULL + stage], 0);
+          mbar_arrive_expect_tx(&cx.bar[B_K_FULL + stage], bytes);
+          load_tile(sK + stage * C::kKVBytes, tm_k, &cx.bar[B_K_FULL + stage], 0);
         }
         ++issued_k;
-        if (!pp.warp_wait(B_PV_DONE + stage, empty_par)) { aborted = true; break; }
+        if (!cx.warp_wait(B_PV_DONE + stage, empty_par)) { aborted = true; break; }
         if (lane == 0) {
-          mbar_arrive_expect_tx(&pp.bar[B_V_FULL + stage], bytes);
-          load_tile(sV + stage * C::kKVBytes, tm_v, &pp.bar[B_V_FULL + stage], 1);
+          mbar_arrive_expect_tx(&cx.bar[B_V_FULL + stage], bytes);
+          load_tile(sV + stage * C::kKVBytes, tm_v, &cx.bar[B_V_FULL + stage], 1);
         }
         ++issued_v;
-        // column intervals of a partial tile for the mask (FULL tiles need none)
+        // column intervals of a partial tile for the mask (FULL tiles need
+        // none); written after the PV of the tile two back, the last reader
+        // of this stage's intervals, has completed
+        // (as start and length: a row sees the column iff its enter index
+        // minus start is below length, compared unsigned)
         if (cls == kTilePartial) {
           int2* ex = sEX + stage * kBlockN;
 #pragma unroll
-          for (int q = 0; q < kBlockN / 32; ++q)
+          for (int q = 0; q < kBlockN / 32; ++q) {
+            const int2 iv = column_interval(p.tree_order, r.tree_base, j * kBlockN + q * 32 + lane,
+                                            r.kv, r.kv - r.tl);
+            // an empty interval (a column past the sequence's end) gets
+            // length 0, which no row passes
             ex[q * 32 + lane] =
-                column_interval(p.tree_order, r.tree_base, j * kBlockN + q * 32 + lane, r.kv,
-                                r.kv - r.tl);
+                make_int2(iv.x, iv.y > iv.x ? (int)((uint32_t)iv.y - (uint32_t)iv.x) : 0);
+          }
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(&pp.bar[B_EX_FULL + stage]);
+        if (lane == 0) mbar_arrive(&cx.bar[B_EX_FULL + stage]);
         ++kv_it;
       }
       if (aborted) break;
@@ -298,120 +332,171 @@ __device__ void run_producer(const Pipe& pp, const CUtensorMap* tm_q, const CUte
     ++it;
   }
   if (aborted && lane == 0) {
-    // let every copy already in flight land before the CTA's memory goes away
-    if (q_it > 0) pp.drain_wait(B_Q_FULL, (q_it - 1) & 1);
-    // the last load issued into each stage: load i went to stage i % kStages
-    // and completes that stage's phase i / kStages
+    // let every copy already in flight land before the CTA's memory goes away:
+    // the last load issued into each Q buffer and each K / V stage (load i
+    // went to buffer i % 2 and completes that buffer's phase i / 2)
+    for (uint32_t i = q_it > 2 ? q_it - 2 : 0; i < q_it; ++i)
+      cx.drain_wait(B_Q_FULL + (i & 1), (i >> 1) & 1);
     for (uint32_t i = issued_k > kStages ? issued_k - kStages : 0; i < issued_k; ++i)
-      pp.drain_wait(B_K_FULL + i % kStages, (i / kStages) & 1);
+      cx.drain_wait(B_K_FULL + i % kStages, (i / kStages) & 1);
     for (uint32_t i = issued_v > kStages ? issued_v - kStages : 0; i < issued_v; ++i)
-      pp.drain_wait(B_V_FULL + i % kStages, (i / kStages) & 1);
+      cx.drain_wait(B_V_FULL + i % kStages, (i / kStages) & 1);
   }
 }
 
 // ---------------------------------------------------------------------------
 // MMA warp (one thread)
 // ---------------------------------------------------------------------------
+// One stream of tiles across item boundaries, two cursors over it: the QK^T
+// cursor runs up to two tiles ahead of the PV cursor (tile c uses score
+// buffer and K/V stage c & 1), so the tensor core computes S for the next
+// tile while the softmax works on the current one.  The QK^T cursor enters
+// the next item only when it is due (lazily): entering waits for the item's
+// Q tile, whose RoPE the correction warps do after the epilogue of the item
+// two back, which needs the PVs the cursor would otherwise hold up.
 template <int D, bool BF16>
-__device__ void run_mma(const Pipe& pp, const AttnParams& p) {
+__device__ void run_mma(const Ctx& cx, const AttnParams& p) {
   using C = Cfg<D>;
-  // descriptors of k-step 0; a k-step or stage offset is added to the
+  // descriptors of k-step 0; a k-step or buffer offset is added to the
   // descriptor's 14-bit start-address field (addresses stay below 256 KB)
   static_assert(kStages == 2, "descriptor selection below assumes two stages");
-  const uint64_t dq0 = sw128_desc(smem_u32(pp.smem + C::kOffQ), 0);
-  const uint64_t dk_s0 = sw128_desc(smem_u32(pp.smem + C::kOffK), 0);
-  const uint64_t dk_s1 = dk_s0 + (uint64_t)(C::kKVBytes >> 4);
-  const uint64_t dv_s0 = sw128_desc(smem_u32(pp.smem + C::kOffV), C::kKVAtomBytes);
-  const uint64_t dv_s1 = dv_s0 + (uint64_t)(C::kKVBytes >> 4);
+  const uint64_t dq0 = sw128_desc(smem_u32(cx.smem + C::kOffQ), 0);
+  const uint64_t dq1 = dq0 + (uint64_t)(C::kQBytes >> 4);
+  const uint64_t dk0 = sw128_desc(smem_u32(cx.smem + C::kOffK), 0);
+  const uint64_t dk1 = dk0 + (uint64_t)(C::kKVBytes >> 4);
+  const uint64_t dv0 = sw128_desc(smem_u32(cx.smem + C::kOffV), C::kKVAtomBytes);
+  const uint64_t dv1 = dv0 + (uint64_t)(C::kKVBytes >> 4);
   constexpr uint32_t idesc_pv = umma_idesc_f16(BF16, 128, D, /*b_mn_major=*/true);
   const int q_bar = p.rotary ? B_Q_READY : B_Q_FULL;
-  uint32_t it = 0, kv_it = 0, q_it = 0, o_it = 0;
-  bool issued_any = false;
+  uint32_t it = 0;                  // item slots consumed
+  uint32_t qi = 0;                  // non-empty items entered (Q and O buffer = index & 1)
+  uint32_t c_qk = 0, c_pv = 0;      // tiles issued by each cursor
+  uint32_t o_cnt = 0;               // items whose PVs have started
+  // per tile, from the QK^T cursor to the PV cursor: valid kv columns (bits
+  // 0-7), first / last tile of its item (bits 8, 9), O buffer (bit 10)
+  uint64_t ring = 0;
+  bool cur = false, end = false, ok = true, issued_any = false;
+  int cur_n = 0, cur_t = 0, cur_kv = 0;
+  uint32_t cur_b = 0;
+  TileIter ti;
   // test hook: a wait that runs out before any MMA is issued (the other warps
   // then find the abort flag in their own waits)
-  if (p.debug_stall) pp.wait(B_STALL, 0);
-  for (; !p.debug_stall;) {
-    const int slot = it % kSlots;
-    if (!pp.wait(B_ITEM_FULL + slot, (it / kSlots) & 1)) break;
-    const Item& s = pp.items[slot];
-    if (!s.valid) break;
-    const ItemRec r = s.r;
-    if (r.n_tiles > 0) {
-      if (!pp.wait(q_bar, q_it & 1)) break;
-      ++q_it;
-      tc_fence_after();
-      TileIter ti(r, p.classes);
-      bool ok = true;
-      // S(c) = Q K(c)^T into score buffer c & 1, once the PV that read the P
-      // of tile c - 2 out of that buffer has completed
-      auto issue_qk = [&](int m, int nvalid) -> bool {
-        const uint32_t c = kv_it + m;
-        const int stage = c % kStages;
-        if (c >= 2 && !pp.wait(B_PV_DONE + (c & 1), ((c - 2) >> 1) & 1)) return false;
-        if (!pp.wait(B_K_FULL + stage, (c / kStages) & 1)) return false;
-        tc_fence_after();
-        const int sb = c & 1;
-        const int n_eff = (nvalid + 15) & ~15;
-        const uint32_t idesc = umma_idesc_f16(BF16, 128, n_eff, false);
-        const uint64_t dk = stage ? dk_s1 : dk_s0;
-        const uint32_t d_s = pp.tmem + C::kTmemS + 64 * sb;
-#pragma unroll
-        for (int k = 0; k < D / 16; ++k) {
-          const uint32_t qo = (uint32_t)(((k >> 2) * C::kQAtomBytes + (k & 3) * 32) >> 4);
-          const uint32_t ko = (uint32_t)(((k >> 2) * C::kKVAtomBytes + (k & 3) * 32) >> 4);
-          umma_f16(d_s, dq0 + qo, dk + ko, idesc, k > 0 ? 1u : 0u);
-        }
-        umma_commit(&pp.bar[B_S_FULL + sb]);
-        issued_any = true;
-        if (m == r.n_tiles - 1) umma_commit(&pp.bar[B_Q_EMPTY]);
-        return true;
-      };
-      ti.next();
-      int nv_cur = min(kBlockN, r.kv - ti.j * kBlockN);
-      int nv_next = 0;
-      if (!issue_qk(0, nv_cur)) break;
-      for (int n = 0; n < r.n_tiles; ++n) {
-        if (n + 1 < r.n_tiles) {
-          ti.next();
-          nv_next = min(kBlockN, r.kv - ti.j * kBlockN);
-          if (!issue_qk(n + 1, nv_next)) { ok = false; break; }
-        }
-        const uint32_t c = kv_it + n;
-        const int stage = c % kStages;
-        const int pb = c & 1;
-        if (!pp.wait(B_P_FULL + pb, (c >> 1) & 1)) { ok = false; break; }
-        if (!pp.wait(B_V_FULL + stage, (c / kStages) & 1)) { ok = false; break; }
-        if (n == 0) {
-          if (!pp.wait(B_O_FREE, (o_it & 1) ^ 1)) { ok = false; break; }
-          ++o_it;
-        }
-        tc_fence_after();
-        const int nk = (nv_cur + 15) >> 4;   // 16-row k-steps holding valid kv rows
-        const uint64_t dv = stage ? dv_s1 : dv_s0;
-        const uint32_t pcol = pp.tmem + C::kTmemS + 64 * pb;   // P: two elements per column
-#pragma unroll
-        for (int k = 0; k < kBlockN / 16; ++k) {
-          if (k < nk)
-            umma_f16_tmem_a(pp.tmem + C::kTmemO, pcol + k * 8, dv + (uint64_t)(k * 16 * 128 >> 4),
-                            idesc_pv, (n > 0 || k > 0) ? 1u : 0u);
-        }
-        umma_commit(&pp.bar[B_PV_DONE + pb]);
-        nv_cur = nv_next;
-      }
-      if (!ok) break;
-      kv_it += r.n_tiles;
-    }
-    mbar_arrive(&pp.bar[B_ITEM_EMPTY + slot]);
-    ++it;
+  if (p.debug_stall) {
+    cx.wait(B_STALL, 0);
+    ok = false;
   }
-  if (*pp.abort && issued_any) {
-    umma_commit(&pp.bar[B_DRAIN]);
-    pp.drain_wait(B_DRAIN, 0);
+
+  // moves the QK^T cursor to the next item with tiles (or to the end)
+  auto enter_item = [&]() -> bool {
+    for (;;) {
+      const int slot = it % kSlots;
+      if (!cx.wait(B_ITEM_FULL + slot, (it / kSlots) & 1)) return false;
+      const Item& s = cx.items[slot];
+      const int valid = s.valid;
+      const ItemRec r = s.r;
+      // the record is in registers: the slot is no longer needed here
+      mbar_arrive(&cx.bar[B_ITEM_EMPTY + slot]);
+      ++it;
+      if (!valid) {
+        end = true;
+        return true;
+      }
+      if (r.n_tiles > 0) {
+        if (!cx.wait(q_bar + (qi & 1), (qi >> 1) & 1)) return false;
+        cur_b = qi & 1;
+        ++qi;
+        cur = true;
+        cur_n = r.n_tiles;
+        cur_t = 0;
+        cur_kv = r.kv;
+        ti = TileIter(r, p.classes);
+        return true;
+      }
+    }
+  };
+
+  // S(c) = Q K(c)^T into score buffer c & 1
+  auto issue_qk = [&]() -> bool {
+    const uint32_t c = c_qk;
+    const int stage = c & 1;
+    ti.next();
+    const int nvalid = min(kBlockN, cur_kv - ti.j * kBlockN);
+    if (!cx.wait(B_K_FULL + stage, (c >> 1) & 1)) return false;
+    if constexpr (!kQkAfterPvInIssueOrder) {
+      if (c >= 2 && !cx.wait(B_PV_DONE + stage, ((c - 2) >> 1) & 1)) return false;
+    }
+    tc_fence_after();
+    const int n_eff = (nvalid + 15) & ~15;
+    const uint32_t idesc = umma_idesc_f16(BF16, 128, n_eff, false);
+    const uint64_t dq = cur_b ? dq1 : dq0;
+    const uint64_t dk = stage ? dk1 : dk0;
+    const uint32_t d_s = cx.tmem + C::kTmemS + 128 * stage;
+#pragma unroll
+    for (int k = 0; k < D / 16; ++k) {
+      const uint32_t qo = (uint32_t)(((k >> 2) * C::kQAtomBytes + (k & 3) * 32) >> 4);
+      const uint32_t ko = (uint32_t)(((k >> 2) * C::kKVAtomBytes + (k & 3) * 32) >> 4);
+      umma_f16(d_s, dq + qo, dk + ko, idesc, k > 0 ? 1u : 0u);
+    }
+    umma_commit(&cx.bar[B_S_FULL + stage]);
+    issued_any = true;
+    const uint32_t first = cur_t == 0, last = cur_t == cur_n - 1;
+    if (last) umma_commit(&cx.bar[B_Q_EMPTY + cur_b]);
+    const uint32_t sh = 16 * (c & 3);
+    ring = (ring & ~(0xFFFFull << sh)) |
+           ((uint64_t)((uint32_t)nvalid | (first << 8) | (last << 9) | (cur_b << 10)) << sh);
+    ++c_qk;
+    ++cur_t;
+    if (last) cur = false;
+    return true;
+  };
+
+  while (ok) {
+    // keep the QK^T cursor up to two tiles ahead of the PV cursor
+    while (!end && c_qk < c_pv + 2) {
+      if (!cur) {
+        if (!enter_item()) { ok = false; break; }
+        if (end) break;
+      }
+      if (!issue_qk()) { ok = false; break; }
+    }
+    if (!ok || c_pv == c_qk) break;
+    // O(item) += P(c) V(c)
+    const uint32_t c = c_pv;
+    const uint32_t e = (uint32_t)(ring >> (16 * (c & 3))) & 0xFFFFu;
+    const int nvalid = (int)(e & 0xFFu);
+    const bool first = (e >> 8) & 1u, last = (e >> 9) & 1u;
+    const uint32_t ob = (e >> 10) & 1u;
+    const int stage = c & 1;
+    if (!cx.wait(B_P_FULL + stage, (c >> 1) & 1)) break;
+    if (!cx.wait(B_V_FULL + stage, (c >> 1) & 1)) break;
+    // the O buffer is free once the epilogue of the item two back read it
+    if (first && !cx.wait(B_O_FREE + ob, ((o_cnt >> 1) & 1) ^ 1)) break;
+    tc_fence_after();
+    const int nk = (nvalid + 15) >> 4;   // 16-row k-steps holding valid kv rows
+    const uint64_t dv = stage ? dv1 : dv0;
+    const uint32_t pcol = cx.tmem + C::kTmemS + 128 * stage;   // P: two elements per column
+    const uint32_t d_o = cx.tmem + C::kTmemO + 128 * ob;
+#pragma unroll
+    for (int k = 0; k < kBlockN / 16; ++k) {
+      if (k < nk)
+        umma_f16_tmem_a(d_o, pcol + k * 8, dv + (uint64_t)(k * 16 * 128 >> 4), idesc_pv,
+                        (!first || k > 0) ? 1u : 0u);
+    }
+    umma_commit(&cx.bar[B_PV_DONE + stage]);
+    if (last) {
+      umma_commit(&cx.bar[B_O_FULL + ob]);
+      ++o_cnt;
+    }
+    ++c_pv;
+  }
+  if (*cx.abort && issued_any) {
+    umma_commit(&cx.bar[B_DRAIN]);
+    cx.drain_wait(B_DRAIN, 0);
   }
 }
 
 // ---------------------------------------------------------------------------
-// softmax warps: RoPE on Q, softmax, O correction, epilogue
+// RoPE of the Q tile (correction warps)
 // ---------------------------------------------------------------------------
 // Inline RoPE of this warp's 32 packed rows of the Q tile.  Task = (q row,
 // 16-byte block c of the first half of the head dimension): one load of the
@@ -500,292 +585,384 @@ __device__ void rope_q_rows(uint8_t* tile, const float2* __restrict__ cs, long l
   }
 }
 
+
+// ---------------------------------------------------------------------------
+// softmax warps
+// ---------------------------------------------------------------------------
 template <int D, bool BF16, bool PAGED>
-__device__ void softmax_loop(const Pipe& pp, const AttnParams& p, int sw, int lane);
+__device__ void softmax_loop(const Ctx& cx, const AttnParams& p, int wq, int lane) {
+  using C = Cfg<D>;
+  const int row = wq * 32 + lane;             // packed row = TMEM lane
+  const uint32_t t_row = cx.tmem + ((uint32_t)(wq * 32) << 16);
+  const int2* sEX = reinterpret_cast<const int2*>(cx.smem + C::kOffEX);
+  float2* sML = reinterpret_cast<float2*>(cx.smem + C::kOffML);
+  const float c2 = p.scale_log2;
+  const int g = p.g, R = p.R;
+  const bool in_pack = row < g * R;
+  const int qr = in_pack ? row / g : 0;
+  uint32_t it = 0, c = 0, so = 0;   // slots, tiles, items with tiles
+  for (;;) {
+    const int slot = it % kSlots;
+    if (!cx.warp_wait(B_ITEM_FULL + slot, (it / kSlots) & 1)) return;
+    const Item& s = cx.items[slot];
+    if (!s.valid) return;
+    const ItemRec r = s.r;
+    if (r.n_tiles == 0) {   // nothing to attend: the correction warps write it
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&cx.bar[B_ITEM_EMPTY + slot]);
+      ++it;
+      continue;
+    }
+    const bool valid = in_pack && qr < r.nq;
+    int e_row = INT_MIN;
+    if (valid) e_row = __ldg(&p.tree_order[2 * (r.tree_base + r.t * R + qr + r.tl - r.qo)]);
+    const uint32_t ob = so & 1;
+    float m_ref = -INFINITY, l = 0.f;
+    TileIter ti(r, p.classes);
+    for (int n = 0; n < r.n_tiles; ++n, ++c) {
+      const int cls = ti.next();
+      const int nvalid = min(kBlockN, r.kv - ti.j * kBlockN);
+      const int sb = c & 1;
+      const bool partial = cls == kTilePartial;
+      if (partial && !cx.warp_wait(B_EX_FULL + sb, (c >> 1) & 1)) return;
+      if (!cx.warp_wait(B_S_FULL + sb, (c >> 1) & 1)) return;
+      tc_fence_after();
+      const uint32_t t_s = t_row + C::kTmemS + 128 * sb;
+      // One pass over the tile's 32-column chunks (a rolled loop: the code
+      // stays small enough for the instruction cache).  Scores are taken
+      // relative to the row's running reference, t = s * c2 - m; the
+      // reference moves -- this tile's P chunks already written, l and
+      // (before this tile's PV) O rescaled -- only when a chunk's largest t
+      // exceeds 8, so that P = 2^t <= 256.
+      const int nch = (nvalid + 31) >> 5;
+      float alpha_t = 1.f;   // product of this tile's reference moves
+      float lsum = 0.f;
+#pragma unroll 1
+      for (int q = 0; q < nch; ++q) {
+        float x[32];
+        tmem_ld32(t_s + 32 * q, x);
+        const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
+        tmem_wait_ld(x);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float2 t = ffma2(make_float2(x[2 * i], x[2 * i + 1]), make_float2(c2, c2),
+                                 make_float2(-m_use, -m_use));
+          x[2 * i] = t.x;
+          x[2 * i + 1] = t.y;
+        }
+        if (partial) {
+          // column c is visible iff e_row lies in its interval, stored by
+          // the producer as (start, length): (e_row - start) < length unsigned
+          const int2* iv = sEX + sb * kBlockN + 32 * q;
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const int4 e = reinterpret_cast<const int4*>(iv)[i];
+            if (!((uint32_t)(e_row - e.x) < (uint32_t)e.y)) x[2 * i] = -INFINITY;
+            if (!((uint32_t)(e_row - e.z) < (uint32_t)e.w)) x[2 * i + 1] = -INFINITY;
+          }
+        }
+        float m4[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) m4[k] = x[k];
+#pragma unroll
+        for (int i = 4; i < 32; ++i) m4[i & 3] = fmaxf(m4[i & 3], x[i]);
+        const float tmax = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+        // a row's first visible chunk always sets its reference (nothing
+        // before it carries weight: l, O and this tile's P are 0, so the
+        // factor is 0 rather than 2^-tmax, which may not be finite)
+        const bool first_vis = m_ref == -INFINITY && tmax > -INFINITY;
+        if (__any_sync(0xffffffffu, tmax > 8.f || first_vis)) {
+          // move the reference of the rows whose max outgrew it
+          const bool mv = tmax > 8.f || first_vis;
+          const float a = mv ? (first_vis ? 0.f : ex2_approx(-tmax)) : 1.f;
+          if (mv) {
+            m_ref = m_use + tmax;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) x[i] -= tmax;
+          }
+          alpha_t *= a;
+          lsum *= a;
+          if (q > 0) {
+            // this tile's P chunks already written: rescale them in TMEM
+            tmem_wait_st();
+            for (int j = 0; j < q; ++j) {
+              uint32_t w[16];
+              tmem_ld16(t_s + 16 * j, w);
+              tmem_wait_ld(w);
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                const float2 f = unpack2<BF16>(w[i]);
+                w[i] = pack2<BF16>(f.x * a, f.y * a);
+              }
+              tmem_st16(t_s + 16 * j, w);
+            }
+          }
+        }
+        // P = 2^t (0 where masked), two per 32-bit word, over columns
+        // 16q .. 16q + 15 of the score buffer (read by the PV's k-steps 2q
+        // and 2q + 1)
+        uint32_t pk[16];
+        float2 l2 = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float p0 = ex2_approx(x[2 * i]), p1 = ex2_approx(x[2 * i + 1]);
+          l2 = fadd2(l2, make_float2(p0, p1));
+          pk[i] = pack2<BF16>(p0, p1);
+        }
+        lsum += l2.x + l2.y;
+        tmem_st16(t_s + 16 * q, pk);
+      }
+      l = l * alpha_t + lsum;
+      // rescale the running O when the reference moved (after the PV of
+      // tile c - 1, the last one that wrote it; the PV of tile c waits for
+      // P_FULL below)
+      if (n > 0 && __any_sync(0xffffffffu, alpha_t != 1.f)) {
+        const uint32_t pv = c - 1;
+        if (!cx.warp_wait(B_PV_DONE + (pv & 1), (pv >> 1) & 1)) return;
+        tc_fence_after();
+#pragma unroll 1
+        for (int oc = 0; oc < D / 32; ++oc) {
+          float o[32];
+          tmem_ld32(t_row + C::kTmemO + 128 * ob + oc * 32, o);
+          tmem_wait_ld(o);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] *= alpha_t;
+          tmem_st32(t_row + C::kTmemO + 128 * ob + oc * 32, o);
+        }
+      }
+      if constexpr (PAGED) {
+        // the last page of a sequence may be partly filled: its remaining
+        // slots hold whatever the cache holds (not necessarily finite), so
+        // the V rows from the sequence's end to the next 16-row step of the
+        // PV are zeroed before the PV reads them (P is 0 there)
+        if (nvalid < kBlockN && (nvalid & 15)) {
+          if (!cx.warp_wait(B_V_FULL + sb, (c >> 1) & 1)) return;
+          const int r0 = nvalid, nr = ((nvalid + 15) & ~15) - nvalid;
+          uint8_t* vt = cx.smem + C::kOffV + sb * C::kKVBytes;
+          for (int i = wq * 32 + lane; i < nr * 8 * C::kAtoms; i += 128) {
+            const int a = i / (nr * 8), rem = i % (nr * 8);
+            *reinterpret_cast<uint4*>(vt + a * C::kKVAtomBytes + (r0 + rem / 8) * 128 +
+                                      (rem % 8) * 16) = make_uint4(0u, 0u, 0u, 0u);
+          }
+          fence_proxy_async_smem();
+        }
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&cx.bar[B_P_FULL + sb]);
+    }
+    // the rows' (m, l) for the epilogue; the buffer is free once the
+    // epilogue of the item two back has read it
+    if (!cx.warp_wait(B_O_FREE + ob, ((so >> 1) & 1) ^ 1)) return;
+    sML[ob * kBlockM + row] = make_float2(m_ref, l);
+    __syncwarp();
+    if (lane == 0) {
+      mbar_arrive(&cx.bar[B_ML_FULL + ob]);
+      mbar_arrive(&cx.bar[B_ITEM_EMPTY + slot]);
+    }
+    ++so;
+    ++it;
+  }
+}
 
 // The softmax warps' loop; on every way out (the work is done, or a bounded
 // wait gave up) the warp waits for its own TMEM loads and stores to finish
 // before the CTA frees the TMEM.
 template <int D, bool BF16, bool PAGED>
-__device__ void run_softmax(const Pipe& pp, const AttnParams& p, int sw, int lane) {
-  softmax_loop<D, BF16, PAGED>(pp, p, sw, lane);
+__device__ void run_softmax(const Ctx& cx, const AttnParams& p, int wq, int lane) {
+  softmax_loop<D, BF16, PAGED>(cx, p, wq, lane);
   tmem_wait_ld();
   tmem_wait_st();
 }
 
-template <int D, bool BF16, bool PAGED>
-__device__ void softmax_loop(const Pipe& pp, const AttnParams& p, int sw, int lane) {
+// ---------------------------------------------------------------------------
+// correction warps: RoPE of Q, epilogues
+// ---------------------------------------------------------------------------
+// Writes one item's rows: O / l in the storage dtype and lse = m + log2(l)
+// (or, for a split-KV chunk, float32 O / l and lse into its partial state).
+// With ``has_o`` the item's O is read from TMEM buffer ``ob`` (and the buffer
+// released); without, the item attended nothing: out = 0, lse = -inf.
+template <int D, bool BF16>
+__device__ void store_item(const Ctx& cx, const AttnParams& p, const ItemRec& r, int kvh,
+                           int wq, int lane, bool has_o, uint32_t ob, float m_ref, float l) {
   using C = Cfg<D>;
-  const int wq = sw;                          // TMEM lane quadrant (warp index mod 4)
-  const int row = wq * 32 + lane;             // packed row = TMEM lane
-  const uint32_t t_row = pp.tmem + ((uint32_t)(wq * 32) << 16);
-  const int2* sEX = reinterpret_cast<const int2*>(pp.smem + C::kOffEX);
-  uint8_t* ost = pp.smem + C::kOffOst + wq * C::kOstBytes;
-  const float c2 = p.scale_log2;
-  const int g = p.g, R = p.R;
-  const bool in_pack = row < g * R;
+  const int row = wq * 32 + lane;
+  const uint32_t t_o = cx.tmem + ((uint32_t)(wq * 32) << 16) + C::kTmemO + 128 * ob;
+  uint8_t* ost = cx.smem + C::kOffOst + wq * C::kOstBytes;
+  const int g = p.g;
+  const bool in_pack = row < g * p.R;
   const int qr = in_pack ? row / g : 0;
   const int hh = in_pack ? row - qr * g : 0;
-  uint32_t it = 0, gi = 0, q_it = 0;  // gi: kv tiles processed by this pipeline
+  const bool valid = in_pack && qr < r.nq;
+  const int head = kvh * g + hh;
+  const size_t orow = (size_t)(r.q_row0 + qr) * p.h_q + head;
+  const float inv = l > 0.f ? 1.f / l : 0.f;
+  const float lse_v = l > 0.f ? m_ref + log2f(l) : -INFINITY;
+  if (r.part >= 0) {
+    // split-KV chunk: O / l and lse in float32 into the record's partial
+    // state (packed row = TMEM lane), merged with the pair's other chunks
+    // by the merge kernel
+    const size_t prow = ((size_t)r.part * p.h_kv + kvh) * kBlockM + row;
+    if (valid) p.part_lse[prow] = lse_v;
+    float4* po = reinterpret_cast<float4*>(p.part_o + prow * D);
+#pragma unroll
+    for (int oc = 0; oc < D / 32; ++oc) {
+      float o[32];
+      if (has_o) {
+        tmem_ld32(t_o + oc * 32, o);
+        tmem_wait_ld();
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) o[i] = 0.f;
+      }
+      if (oc == D / 32 - 1) {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0 && has_o) mbar_arrive(&cx.bar[B_O_FREE + ob]);
+      }
+      if (valid) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          po[oc * 8 + i] = make_float4(o[4 * i] * inv, o[4 * i + 1] * inv, o[4 * i + 2] * inv,
+                                       o[4 * i + 3] * inv);
+      }
+    }
+    return;
+  }
+  if (valid) p.lse[orow] = lse_v;
+  // O / l in the storage dtype: 64 columns per TMEM round trip, written 32
+  // columns (64 bytes per row) at a time through the warp's staging buffer,
+  // then as whole-warp 16-byte stores of 8 rows x 64 bytes
+  uint16_t* outp = reinterpret_cast<uint16_t*>(p.out);
+  long long ro[4];
+  int ok[4];
+#pragma unroll
+  for (int st = 0; st < 4; ++st) {
+    const int src = st * 8 + (lane >> 2);   // row within the quadrant
+    ro[st] = __shfl_sync(0xffffffffu, (long long)orow, src);
+    ok[st] = __shfl_sync(0xffffffffu, valid ? 1 : 0, src);
+  }
+#pragma unroll
+  for (int oc2 = 0; oc2 < D / 64; ++oc2) {
+    float oa[32], ob2[32];
+    if (has_o) {
+      tmem_ld32(t_o + oc2 * 64, oa);
+      tmem_ld32(t_o + oc2 * 64 + 32, ob2);
+      tmem_wait_ld();
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) oa[i] = ob2[i] = 0.f;
+    }
+    if (oc2 == D / 64 - 1) {
+      // O is out of TMEM: the item two later may accumulate into the buffer
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0 && has_o) mbar_arrive(&cx.bar[B_O_FREE + ob]);
+    }
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf) {
+      const int oc = oc2 * 2 + hf;
+      uint32_t pk[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const float x0 = hf ? ob2[2 * i] : oa[2 * i];
+        const float x1 = hf ? ob2[2 * i + 1] : oa[2 * i + 1];
+        pk[i] = pack2<BF16>(x0 * inv, x1 * inv);
+      }
+      __syncwarp();   // the previous chunk's readers are done with the buffer
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc)
+        *reinterpret_cast<uint4*>(ost + lane * 64 + ((cc ^ ((lane >> 1) & 3)) * 16)) =
+            make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
+      __syncwarp();
+#pragma unroll
+      for (int st = 0; st < 4; ++st) {
+        const int src = st * 8 + (lane >> 2);
+        const int cc = lane & 3;
+        const uint4 val =
+            *reinterpret_cast<const uint4*>(ost + src * 64 + ((cc ^ ((src >> 1) & 3)) * 16));
+        if (ok[st]) *reinterpret_cast<uint4*>(outp + ro[st] * D + oc * 32 + cc * 8) = val;
+      }
+    }
+  }
+}
+
+// The correction warps walk the items one behind the softmax: for each item
+// with tiles, the RoPE of its Q tile (rotary calls), then the epilogue of the
+// item before it -- so the next item's first QK^T never waits for an
+// epilogue, and the epilogue never waits for the next item's RoPE.
+template <int D, bool BF16>
+__device__ void correction_loop(const Ctx& cx, const AttnParams& p, int wq, int lane) {
+  using C = Cfg<D>;
+  const int row = wq * 32 + lane;
+  const float2* sML = reinterpret_cast<const float2*>(cx.smem + C::kOffML);
+  const int g = p.g, R = p.R;
+  uint32_t it = 0, qi = 0, oi = 0;   // slots, items with tiles (Q buffers, O buffers)
+  bool pend = false;                 // an item waits for its epilogue
+  int pend_slot = 0, pend_kvh = 0;
+  uint32_t pend_ob = 0, pend_par = 0;
+  ItemRec pend_r;
+  auto finish_pending = [&]() -> bool {
+    if (!cx.warp_wait(B_ML_FULL + pend_ob, pend_par)) return false;
+    const float2 ml = sML[pend_ob * kBlockM + row];
+    if (!cx.warp_wait(B_O_FULL + pend_ob, pend_par)) return false;
+    tc_fence_after();
+    store_item<D, BF16>(cx, p, pend_r, pend_kvh, wq, lane, true, pend_ob, ml.x, ml.y);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&cx.bar[B_ITEM_EMPTY + pend_slot]);
+    pend = false;
+    return true;
+  };
   for (;;) {
     const int slot = it % kSlots;
-    if (!pp.warp_wait(B_ITEM_FULL + slot, (it / kSlots) & 1)) return;
-    const Item& s = pp.items[slot];
-    if (!s.valid) return;
+    if (!cx.warp_wait(B_ITEM_FULL + slot, (it / kSlots) & 1)) return;
+    const Item& s = cx.items[slot];
+    if (!s.valid) break;
     const ItemRec r = s.r;
     const int kvh = s.kvh;
-    const bool valid = in_pack && qr < r.nq;
-    const int head = kvh * g + hh;
-    const size_t orow = (size_t)(r.q_row0 + qr) * p.h_q + head;
-    int e_row = INT_MIN;
-    if (valid) e_row = __ldg(&p.tree_order[2 * (r.tree_base + r.t * R + qr + r.tl - r.qo)]);
-    float m_ref = -INFINITY, l = 0.f;
     if (r.n_tiles > 0) {
       if (p.rotary) {
         // q row r of the tile takes the position of its own tree node's kv
         // slot (the first cos/sin batch is fetched while the Q tile lands)
+        const int qb = qi & 1;
         const long long qtok0 = (long long)r.kv_base + (r.kv - r.qo) + (long long)r.t * R;
         const RopeRange rr = rope_range<D>(r.nq, g, wq);
         float4 cv[2][4];
         rope_load<D>(cv, p.rope_cs, qtok0, rr, 0, lane);
-        if (!pp.warp_wait(B_Q_FULL, q_it & 1)) return;
-        rope_q_rows<D, BF16>(pp.smem + C::kOffQ, p.rope_cs, qtok0, rr, g, lane, cv);
+        if (!cx.warp_wait(B_Q_FULL + qb, (qi >> 1) & 1)) return;
+        rope_q_rows<D, BF16>(cx.smem + C::kOffQ + qb * C::kQBytes, p.rope_cs, qtok0, rr, g, lane,
+                             cv);
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&pp.bar[B_Q_READY]);
+        if (lane == 0) mbar_arrive(&cx.bar[B_Q_READY + qb]);
       }
-      ++q_it;
-      TileIter ti(r, p.classes);
-      for (int n = 0; n < r.n_tiles; ++n, ++gi) {
-        const int cls = ti.next();
-        const int nvalid = min(kBlockN, r.kv - ti.j * kBlockN);
-        const int stage = gi % kStages;
-        const int sb = gi & 1;
-        // visibility bits of this row for the tile's 64 columns
-        uint32_t mw0, mw1;
-        if (cls == kTilePartial) {
-          if (!pp.warp_wait(B_EX_FULL + stage, (gi / kStages) & 1)) return;
-          const int4* e4 = reinterpret_cast<const int4*>(sEX + stage * kBlockN);
-          mw0 = 0;
-          mw1 = 0;
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const int4 a = e4[i], b = e4[16 + i];
-            mw0 |= (uint32_t)(a.x <= e_row && e_row < a.y) << (2 * i);
-            mw0 |= (uint32_t)(a.z <= e_row && e_row < a.w) << (2 * i + 1);
-            mw1 |= (uint32_t)(b.x <= e_row && e_row < b.y) << (2 * i);
-            mw1 |= (uint32_t)(b.z <= e_row && e_row < b.w) << (2 * i + 1);
-          }
-        } else {
-          mw0 = mw1 = 0xffffffffu;  // FULL tiles are never ragged
-        }
-        if (!pp.warp_wait(B_S_FULL + sb, (gi >> 1) & 1)) return;
-        tc_fence_after();
-        const uint32_t t_s = t_row + C::kTmemS + 64 * sb;
-        // the whole 64-column score row in registers: one TMEM round trip
-        float v[64];
-        {
-          float a[32], b[32];
-          tmem_ld32(t_s, a);
-          if (nvalid > 32) tmem_ld32(t_s + 32, b);
-          tmem_wait_ld();
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            v[i] = a[i];
-            v[32 + i] = nvalid > 32 ? b[i] : 0.f;
-          }
-        }
-        // masked row max in log2 units (eight independent chains)
-        float mx8[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) mx8[k] = -INFINITY;
-        if (cls == kTileFull) {
-#pragma unroll
-          for (int i = 0; i < 64; ++i) mx8[i & 7] = fmaxf(mx8[i & 7], v[i] * c2);
-        } else {
-#pragma unroll
-          for (int i = 0; i < 64; ++i) {
-            const uint32_t bit = i < 32 ? (mw0 >> i) & 1u : (mw1 >> (i - 32)) & 1u;
-            if (bit) mx8[i & 7] = fmaxf(mx8[i & 7], v[i] * c2);
-          }
-        }
-        const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                               fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
-        // move the reference max only when it grew by more than 2^8; the
-        // final O / l and lse = m + log2(l) do not depend on the reference
-        const float m_new = fmaxf(m_ref, mx);
-        float ref = m_ref;
-        if (m_new > m_ref + 8.f) ref = m_new;
-        const float alpha = (ref == m_ref) ? 1.f : ex2_approx(m_ref - ref);
-        m_ref = ref;
-        const float m_use = (ref == -INFINITY) ? 0.f : ref;
-        // P = exp2(s * c2 - m) on visible columns, packed two per 32-bit word
-        float l8[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) l8[k] = 0.f;
-        float pk[32];
-        if (cls == kTileFull) {
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const float p0 = ex2_approx(fmaf(v[2 * i], c2, -m_use));
-            const float p1 = ex2_approx(fmaf(v[2 * i + 1], c2, -m_use));
-            l8[i & 7] += p0 + p1;
-            pk[i] = __uint_as_float(pack2<BF16>(p0, p1));
-          }
-        } else {
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const int i0 = 2 * i, i1 = 2 * i + 1;
-            const uint32_t b0 = i0 < 32 ? (mw0 >> i0) & 1u : (mw1 >> (i0 - 32)) & 1u;
-            const uint32_t b1 = i1 < 32 ? (mw0 >> i1) & 1u : (mw1 >> (i1 - 32)) & 1u;
-            const float p0 = b0 ? ex2_approx(fmaf(v[i0], c2, -m_use)) : 0.f;
-            const float p1 = b1 ? ex2_approx(fmaf(v[i1], c2, -m_use)) : 0.f;
-            l8[i & 7] += p0 + p1;
-            pk[i] = __uint_as_float(pack2<BF16>(p0, p1));
-          }
-        }
-        l = l * alpha + (((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7])));
-        // P over the first 32 columns of its own score buffer
-        tmem_st32(t_s, pk);
-        // rescale the running O when the reference moved (after the PV of
-        // tile gi - 1, the last one that wrote O)
-        if (n > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-          const uint32_t pv = gi - 1;
-          if (!pp.warp_wait(B_PV_DONE + (pv & 1), (pv >> 1) & 1)) return;
-          tc_fence_after();
-#pragma unroll
-          for (int oc = 0; oc < D / 32; ++oc) {
-            float o[32];
-            tmem_ld32(t_row + C::kTmemO + oc * 32, o);
-            tmem_wait_ld();
-#pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] *= alpha;
-            tmem_st32(t_row + C::kTmemO + oc * 32, o);
-          }
-        }
-        if constexpr (PAGED) {
-          // the last page of a sequence may be partly filled: its remaining
-          // slots hold whatever the cache holds (not necessarily finite), so
-          // the V rows from the sequence's end to the next 16-row step of the
-          // PV are zeroed before the PV reads them (P is 0 there)
-          if (nvalid < kBlockN && (nvalid & 15)) {
-            if (!pp.warp_wait(B_V_FULL + stage, (gi / kStages) & 1)) return;
-            const int r0 = nvalid, nr = ((nvalid + 15) & ~15) - nvalid;
-            uint8_t* vt = pp.smem + C::kOffV + stage * C::kKVBytes;
-            for (int i = wq * 32 + lane; i < nr * 8 * C::kAtoms; i += 128) {
-              const int a = i / (nr * 8), rem = i % (nr * 8);
-              *reinterpret_cast<uint4*>(vt + a * C::kKVAtomBytes + (r0 + rem / 8) * 128 +
-                                        (rem % 8) * 16) = make_uint4(0u, 0u, 0u, 0u);
-            }
-            fence_proxy_async_smem();
-          }
-        }
-        tmem_wait_st();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&pp.bar[B_P_FULL + sb]);
-      }
-      // epilogue: wait for the last PV (tile gi - 1), then O / l and lse
-      const uint32_t pv = gi - 1;
-      if (!pp.warp_wait(B_PV_DONE + (pv & 1), (pv >> 1) & 1)) return;
-      tc_fence_after();
+      ++qi;
     }
-    const float inv = l > 0.f ? 1.f / l : 0.f;
-    const float lse_v = l > 0.f ? m_ref + log2f(l) : -INFINITY;
-    if (r.part >= 0) {
-      // split-KV chunk: O / l and lse in float32 into the record's partial
-      // state (packed row = TMEM lane), merged with the pair's other chunks
-      // by the merge kernel
-      const size_t prow = ((size_t)r.part * p.h_kv + kvh) * kBlockM + row;
-      if (valid) p.part_lse[prow] = lse_v;
-      float4* po = reinterpret_cast<float4*>(p.part_o + prow * D);
-#pragma unroll
-      for (int oc = 0; oc < D / 32; ++oc) {
-        float o[32];
-        if (r.n_tiles > 0) {
-          tmem_ld32(t_row + C::kTmemO + oc * 32, o);
-          tmem_wait_ld();
-        } else {
-#pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] = 0.f;
-        }
-        if (oc == D / 32 - 1) {
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0 && r.n_tiles > 0) mbar_arrive(&pp.bar[B_O_FREE]);
-        }
-        if (valid) {
-#pragma unroll
-          for (int i = 0; i < 8; ++i)
-            po[oc * 8 + i] = make_float4(o[4 * i] * inv, o[4 * i + 1] * inv, o[4 * i + 2] * inv,
-                                         o[4 * i + 3] * inv);
-        }
-      }
+    if (pend && !finish_pending()) return;
+    if (r.n_tiles == 0) {
+      store_item<D, BF16>(cx, p, r, kvh, wq, lane, false, 0, -INFINITY, 0.f);
       __syncwarp();
-      if (lane == 0) mbar_arrive(&pp.bar[B_ITEM_EMPTY + slot]);
-      ++it;
-      continue;
+      if (lane == 0) mbar_arrive(&cx.bar[B_ITEM_EMPTY + slot]);
+    } else {
+      pend = true;
+      pend_slot = slot;
+      pend_r = r;
+      pend_kvh = kvh;
+      pend_ob = oi & 1;
+      pend_par = (oi >> 1) & 1;
+      ++oi;
     }
-    if (valid) p.lse[orow] = lse_v;
-    // O / l in the storage dtype: 64 columns per TMEM round trip, written 32
-    // columns (64 bytes per row) at a time through the warp's staging buffer,
-    // then as whole-warp 16-byte stores of 8 rows x 64 bytes
-    uint16_t* outp = reinterpret_cast<uint16_t*>(p.out);
-    long long ro[4];
-    int ok[4];
-#pragma unroll
-    for (int st = 0; st < 4; ++st) {
-      const int src = st * 8 + (lane >> 2);   // row within the quadrant
-      ro[st] = __shfl_sync(0xffffffffu, (long long)orow, src);
-      ok[st] = __shfl_sync(0xffffffffu, valid ? 1 : 0, src);
-    }
-#pragma unroll
-    for (int oc2 = 0; oc2 < D / 64; ++oc2) {
-      float oa[32], ob[32];
-      if (r.n_tiles > 0) {
-        tmem_ld32(t_row + C::kTmemO + oc2 * 64, oa);
-        tmem_ld32(t_row + C::kTmemO + oc2 * 64 + 32, ob);
-        tmem_wait_ld();
-      } else {
-#pragma unroll
-        for (int i = 0; i < 32; ++i) oa[i] = ob[i] = 0.f;
-      }
-      if (oc2 == D / 64 - 1) {
-        // O is out of TMEM: the next item's first PV may overwrite it
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0 && r.n_tiles > 0) mbar_arrive(&pp.bar[B_O_FREE]);
-      }
-#pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
-        const int oc = oc2 * 2 + hf;
-        uint32_t pk[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const float x0 = hf ? ob[2 * i] : oa[2 * i];
-          const float x1 = hf ? ob[2 * i + 1] : oa[2 * i + 1];
-          pk[i] = pack2<BF16>(x0 * inv, x1 * inv);
-        }
-        __syncwarp();   // the previous chunk's readers are done with the buffer
-#pragma unroll
-        for (int cc = 0; cc < 4; ++cc)
-          *reinterpret_cast<uint4*>(ost + lane * 64 + ((cc ^ ((lane >> 1) & 3)) * 16)) =
-              make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
-        __syncwarp();
-#pragma unroll
-        for (int st = 0; st < 4; ++st) {
-          const int src = st * 8 + (lane >> 2);
-          const int cc = lane & 3;
-          const uint4 val =
-              *reinterpret_cast<const uint4*>(ost + src * 64 + ((cc ^ ((src >> 1) & 3)) * 16));
-          if (ok[st]) *reinterpret_cast<uint4*>(outp + ro[st] * D + oc * 32 + cc * 8) = val;
-        }
-      }
-    }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&pp.bar[B_ITEM_EMPTY + slot]);
     ++it;
   }
+  if (pend) finish_pending();
+}
+
+template <int D, bool BF16>
+__device__ void run_correction(const Ctx& cx, const AttnParams& p, int wq, int lane) {
+  correction_loop<D, BF16>(cx, p, wq, lane);
+  tmem_wait_ld();
+  tmem_wait_st();
 }
 
 // ---------------------------------------------------------------------------
@@ -799,73 +976,76 @@ __global__ void __launch_bounds__(kThreads, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   CtaShared* cta = reinterpret_cast<CtaShared*>(smem + C::kOffCta);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int pipe = warp / kWarpsPerPipe, pw = warp % kWarpsPerPipe;
-  Pipe pp;
-  pp.smem = smem + pipe * C::kPipeBytes;
-  pp.bar = reinterpret_cast<uint64_t*>(pp.smem + C::kOffBar);
-  pp.items = reinterpret_cast<Item*>(pp.smem + C::kOffItems);
-  pp.abort = &cta->abort;
-  pp.dev_error = &p.hdr->error;
-  pp.limit_ns = p.timeout_ns;
+  Ctx cx;
+  cx.smem = smem;
+  cx.bar = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
+  cx.items = reinterpret_cast<Item*>(smem + C::kOffItems);
+  cx.abort = &cta->abort;
+  cx.dev_error = &p.hdr->error;
+  cx.limit_ns = p.timeout_ns;
 
-  if (pw == 0 && lane == 0) {
-    uint64_t* bar = pp.bar;
-    const uint32_t consumers = 1u + 4u;   // MMA thread + softmax warps
+  if (warp == 0 && lane == 0) {
+    uint64_t* bar = cx.bar;
     for (int i = 0; i < kSlots; ++i) {
       mbar_init(&bar[B_ITEM_FULL + i], 1);
-      mbar_init(&bar[B_ITEM_EMPTY + i], consumers);
+      mbar_init(&bar[B_ITEM_EMPTY + i], 1 + 4 + 4);   // MMA thread, softmax and correction warps
     }
-    mbar_init(&bar[B_Q_FULL], 1);
-    mbar_init(&bar[B_Q_READY], 4);
-    mbar_init(&bar[B_Q_EMPTY], 1);
-    for (int i = 0; i < kStages; ++i) {
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bar[B_Q_FULL + i], 1);
+      mbar_init(&bar[B_Q_READY + i], 4);
+      mbar_init(&bar[B_Q_EMPTY + i], 1);
       mbar_init(&bar[B_K_FULL + i], 1);
       mbar_init(&bar[B_V_FULL + i], 1);
       mbar_init(&bar[B_EX_FULL + i], 1);
-    }
-    for (int i = 0; i < 2; ++i) {
       mbar_init(&bar[B_S_FULL + i], 1);
       mbar_init(&bar[B_P_FULL + i], 4);
       mbar_init(&bar[B_PV_DONE + i], 1);
+      mbar_init(&bar[B_O_FULL + i], 1);
+      mbar_init(&bar[B_O_FREE + i], 4);
+      mbar_init(&bar[B_ML_FULL + i], 4);
     }
-    mbar_init(&bar[B_O_FREE], 4);
     mbar_init(&bar[B_DRAIN], 1);
     mbar_init(&bar[B_STALL], 1);
-    if (pipe == 0) cta->abort = 0;
+    cta->abort = 0;
     mbar_fence_init();
     tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
   }
-  // rows of the Q tile that no TMA box covers (g * R < 128) must read as zero
+  // rows of the Q buffers that no TMA box covers (g * R < 128) must read as zero
   if (p.g * p.R < kBlockM) {
-    uint4* q4 = reinterpret_cast<uint4*>(pp.smem + C::kOffQ);
-    for (int i = pw * 32 + lane; i < C::kQBytes / 16; i += kWarpsPerPipe * 32)
-      q4[i] = make_uint4(0, 0, 0, 0);
+    uint4* q4 = reinterpret_cast<uint4*>(smem + C::kOffQ);
+    for (int i = threadIdx.x; i < 2 * C::kQBytes / 16; i += kThreads) q4[i] = make_uint4(0, 0, 0, 0);
     fence_proxy_async_smem();
   }
-  if (warp == 1) tmem_alloc(&cta->tmem_base, C::kTmemCols);
+  if (warp == kWarpMma) tmem_alloc(&cta->tmem_base, C::kTmemCols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  pp.tmem = cta->tmem_base + pipe * C::kTmemPipe;
+  cx.tmem = cta->tmem_base;
   // everything above is private to the CTA; the plan, the rotated keys and
   // the work queue belong to the kernels before this one on the stream
   pdl_wait();
 
-  if (pw == 0) {
-    run_producer<D, PAGED>(pp, &tm_q, &tm_k, &tm_v, p, pipe, lane);
-  } else if (pw == 1) {
-    if (lane == 0) run_mma<D, BF16>(pp, p);
+  if (warp < kWarpSoftmax) {
+    regs_dec<kRegsIssue>();
+    if (warp == kWarpProducer) {
+      run_producer<D, PAGED>(cx, &tm_q, &tm_k, &tm_v, p, lane);
+    } else if (warp == kWarpMma) {
+      if (lane == 0) run_mma<D, BF16>(cx, p);
+    }
+  } else if (warp < kWarpCorrection) {
+    regs_inc<kRegsSoftmax>();
+    run_softmax<D, BF16, PAGED>(cx, p, warp & 3, lane);
   } else {
-    // softmax warp pw - 2 of this pipeline; its TMEM lane quadrant is warp % 4
-    run_softmax<D, BF16, PAGED>(pp, p, warp & 3, lane);
+    regs_dec<kRegsCorrection>();
+    run_correction<D, BF16>(cx, p, warp & 3, lane);
   }
   __syncwarp();
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) {
+  if (warp == kWarpMma) {
     tc_fence_after();
     tmem_dealloc(cta->tmem_base, C::kTmemCols);
   }
@@ -888,7 +1068,7 @@ cudaError_t launch_attn(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const 
                         const AttnParams& p, int grid, cudaStream_t stream) {
   using C = Cfg<D>;
   static_assert(C::kSmemAlloc <= 227 * 1024, "shared memory budget");
-  static_assert(B_COUNT <= 32, "barrier area");
+  static_assert(B_COUNT <= kBarSlots, "barrier area");
   auto kern = attn_kernel<D, BF16, PAGED>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemAlloc);

@@ -56,8 +56,8 @@ struct PlanParams {
   int64_t max_pairs;
   // split-KV: a pair's kv tiles are cut into up to max_chunks records of
   // about chunk_tiles tiles (0: chosen from the batch's total work so that
-  // the items cover the ``pipes`` pipelines of the attention grid a few
-  // times); max_chunks == 1 disables it
+  // the items cover the ``pipes`` pipelines of the attention grid -- one
+  // per SM -- a few times); max_chunks == 1 disables it
   int max_chunks, chunk_tiles, pipes;
   int4* merge;       // per pair (split-KV): q_row0, q rows, chunks, first record
   // one-call entry points: the plan kernel also does the key rotation of the

@@ -13,8 +13,8 @@ namespace ta {
 // the packing of the "Q_load" block of the page "tree_attn.py"), attended
 // against kv tiles of kBlockN columns.
 constexpr int kBlockM = 128;
-constexpr int kBlockN = 64;
-constexpr int kKvBoxRows = 64;   // kv rows per TMA box (one box per kv tile)
+constexpr int kBlockN = 128;
+constexpr int kKvBoxRows = 128;  // kv rows per TMA box (one box per kv tile)
 constexpr int kMaxGroup = 128;   // largest supported h_q / h_kv
 constexpr int kPageSize = 16;    // kv slots per page of a paged KV cache
 
