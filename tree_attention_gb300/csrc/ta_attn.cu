@@ -12,7 +12,8 @@
 // tile c and one item's epilogue overlaps the next item's first tiles.
 // Warp roles:
 //   warp 0      producer: stages each item's record, TMA-loads its packed Q
-//               tile (two buffers) and its K/V tiles (two stages), with each
+//               tile (two buffers) and its K tiles (two stages)
+//   warp 2      V producer: TMA-loads the V tiles (two stages) and stages each
 //               partial tile's column intervals beside them
 //   warp 1      MMA issuer (one thread): S = Q K^T and O += P V
 //               (tcgen05.mma, M = 128, N = 128), P read from tensor memory;
@@ -43,6 +44,7 @@ constexpr int kStages = 2;   // K/V ring depth = score buffers (tile c uses stag
 constexpr int kSlots = 4;    // work-item slots (producer, MMA, softmax, correction)
 constexpr int kWarpProducer = 0;
 constexpr int kWarpMma = 1;
+constexpr int kWarpProducerV = 2;
 constexpr int kWarpSoftmax = 4;      // warps 4..7
 constexpr int kWarpCorrection = 8;   // warps 8..11
 
@@ -64,7 +66,7 @@ constexpr bool kQkAfterPvInIssueOrder = true;
 
 enum Bar : int {
   B_ITEM_FULL = 0,                     // [kSlots] record staged
-  B_ITEM_EMPTY = B_ITEM_FULL + kSlots, // [kSlots] MMA + 4 softmax + 4 correction warps done with it
+  B_ITEM_EMPTY = B_ITEM_FULL + kSlots, // [kSlots] MMA, V producer, softmax and correction warps done
   B_Q_FULL = B_ITEM_EMPTY + kSlots,    // [2] Q buffer landed
   B_Q_READY = B_Q_FULL + 2,            // [2] Q buffer rotated (RoPE)
   B_Q_EMPTY = B_Q_READY + 2,           // [2] the last QK^T reading the Q buffer done
@@ -194,23 +196,56 @@ struct TileIter {
 };
 
 // ---------------------------------------------------------------------------
-// producer warp (lane 0 issues; all lanes stage mask intervals)
+// producer warps (lane 0 issues): warp 0 stages the items and loads Q and K,
+// warp 2 loads V and stages the mask intervals, so that neither kind of load
+// waits behind the other's stage release
 // ---------------------------------------------------------------------------
+// The physical pages of kv tile j of a paged sequence (logical pages 8j ..
+// 8j + 7), looked up by lanes 0-7 and shared with the warp; a page past the
+// sequence's last takes an out-of-range index, read as zeros.
+constexpr int kPagesPerTile = kBlockN / kPageSize;
+__device__ __forceinline__ void tile_pages(const AttnParams& p, const ItemRec& r, int j, int lane,
+                                           int (&ph)[kPagesPerTile]) {
+  const int np = (r.kv + kPageSize - 1) / kPageSize;
+  const int lp = j * kPagesPerTile + lane;
+  int phys = p.num_pages;
+  if (lane < kPagesPerTile && lp < np) phys = __ldg(p.page_values + r.kv_base + lp);
+#pragma unroll
+  for (int q = 0; q < kPagesPerTile; ++q) ph[q] = __shfl_sync(0xffffffffu, phys, q);
+}
+
+// One K or V tile (kv plane 0 = K, 1 = V of the paged cache) into ``dst``.
+template <int D, bool PAGED>
+__device__ __forceinline__ void load_kv_tile(uint8_t* dst, const CUtensorMap* map, uint64_t* bar,
+                                             int plane, int kvh, int row0,
+                                             const int (&ph)[kPagesPerTile]) {
+  using C = Cfg<D>;
+#pragma unroll
+  for (int a = 0; a < C::kAtoms; ++a) {
+    if constexpr (PAGED) {
+#pragma unroll
+      for (int q = 0; q < kPagesPerTile; ++q)
+        tma_load_5d(dst + a * C::kKVAtomBytes + q * kPageSize * 128, map, bar, a * 64, 0, kvh,
+                    plane, ph[q]);
+    } else {
+      tma_load_3d(dst + a * C::kKVAtomBytes, map, bar, a * 64, kvh, row0);
+    }
+  }
+}
+
 template <int D, bool PAGED>
 __device__ void run_producer(const Ctx& cx, const CUtensorMap* tm_q, const CUtensorMap* tm_k,
-                             const CUtensorMap* tm_v, const AttnParams& p, int lane) {
+                             const AttnParams& p, int lane) {
   using C = Cfg<D>;
   uint8_t* sQ = cx.smem + C::kOffQ;
   uint8_t* sK = cx.smem + C::kOffK;
-  uint8_t* sV = cx.smem + C::kOffV;
-  int2* sEX = reinterpret_cast<int2*>(cx.smem + C::kOffEX);
   // the plan kernel wrote the item count; never trust it beyond the table size
   const unsigned long long cap = (unsigned long long)p.max_records * (unsigned long long)p.h_kv;
   const unsigned long long n_items = *(volatile unsigned int*)&p.hdr->num_items;
   const unsigned int num_items = (unsigned int)(n_items < cap ? n_items : cap);
   const int g = p.g, R = p.R;
   uint32_t it = 0, kv_it = 0, q_it = 0;
-  uint32_t issued_k = 0, issued_v = 0;   // loads issued (stage = count % kStages)
+  uint32_t issued_k = 0;   // loads issued (stage = count % kStages)
   bool aborted = false;
   // the first item of every CTA is fixed (CTA b takes item b, the items being
   // in longest-first order already), the rest come from the queue, which
@@ -257,71 +292,21 @@ __device__ void run_producer(const Ctx& cx, const CUtensorMap* tm_q, const CUten
       ++q_it;
       TileIter ti(r, p.classes);
       for (int n = 0; n < r.n_tiles; ++n) {
-        const int cls = ti.next();
+        ti.next();
         const int j = ti.j;
         const int row0 = r.kv_base + j * kBlockN;
         const int stage = kv_it % kStages;
         const uint32_t empty_par = ((kv_it / kStages) & 1) ^ 1;
         const uint32_t bytes = (uint32_t)C::kKVBytes;
-        // paged cache: kv tile j is logical pages 8j .. 8j+7 of the sequence;
-        // lanes 0-7 look up their physical pages (shared with the warp), a
-        // missing page (past the sequence's last) takes an out-of-range page
-        // index, read as zeros
-        constexpr int kPagesPerTile = kBlockN / kPageSize;
         int ph[kPagesPerTile];
-        if constexpr (PAGED) {
-          const int np = (r.kv + kPageSize - 1) / kPageSize;
-          const int lp = j * kPagesPerTile + lane;
-          int phys = p.num_pages;
-          if (lane < kPagesPerTile && lp < np) phys = __ldg(p.page_values + r.kv_base + lp);
-#pragma unroll
-          for (int q = 0; q < kPagesPerTile; ++q) ph[q] = __shfl_sync(0xffffffffu, phys, q);
-        }
-        // one K or V tile into ``dst`` (kv plane 0 = K, 1 = V of the paged cache)
-        auto load_tile = [&](uint8_t* dst, const CUtensorMap* map, uint64_t* bar, int plane) {
-#pragma unroll
-          for (int a = 0; a < C::kAtoms; ++a) {
-            if constexpr (PAGED) {
-#pragma unroll
-              for (int q = 0; q < kPagesPerTile; ++q)
-                tma_load_5d(dst + a * C::kKVAtomBytes + q * kPageSize * 128, map, bar, a * 64, 0,
-                            kvh, plane, ph[q]);
-            } else {
-              tma_load_3d(dst + a * C::kKVAtomBytes, map, bar, a * 64, kvh, row0);
-            }
-          }
-        };
+        if constexpr (PAGED) tile_pages(p, r, j, lane, ph);
         if (!cx.warp_wait(B_S_FULL + stage, empty_par)) { aborted = true; break; }
         if (lane == 0) {
           mbar_arrive_expect_tx(&cx.bar[B_K_FULL + stage], bytes);
-          load_tile(sK + stage * C::kKVBytes, tm_k, &cx.bar[B_K_FULL + stage], 0);
+          load_kv_tile<D, PAGED>(sK + stage * C::kKVBytes, tm_k, &cx.bar[B_K_FULL + stage], 0, kvh,
+                                 row0, ph);
         }
         ++issued_k;
-        if (!cx.warp_wait(B_PV_DONE + stage, empty_par)) { aborted = true; break; }
-        if (lane == 0) {
-          mbar_arrive_expect_tx(&cx.bar[B_V_FULL + stage], bytes);
-          load_tile(sV + stage * C::kKVBytes, tm_v, &cx.bar[B_V_FULL + stage], 1);
-        }
-        ++issued_v;
-        // column intervals of a partial tile for the mask (FULL tiles need
-        // none); written after the PV of the tile two back, the last reader
-        // of this stage's intervals, has completed
-        // (as start and length: a row sees the column iff its enter index
-        // minus start is below length, compared unsigned)
-        if (cls == kTilePartial) {
-          int2* ex = sEX + stage * kBlockN;
-#pragma unroll
-          for (int q = 0; q < kBlockN / 32; ++q) {
-            const int2 iv = column_interval(p.tree_order, r.tree_base, j * kBlockN + q * 32 + lane,
-                                            r.kv, r.kv - r.tl);
-            // an empty interval (a column past the sequence's end) gets
-            // length 0, which no row passes
-            ex[q * 32 + lane] =
-                make_int2(iv.x, iv.y > iv.x ? (int)((uint32_t)iv.y - (uint32_t)iv.x) : 0);
-          }
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&cx.bar[B_EX_FULL + stage]);
         ++kv_it;
       }
       if (aborted) break;
@@ -333,12 +318,76 @@ __device__ void run_producer(const Ctx& cx, const CUtensorMap* tm_q, const CUten
   }
   if (aborted && lane == 0) {
     // let every copy already in flight land before the CTA's memory goes away:
-    // the last load issued into each Q buffer and each K / V stage (load i
-    // went to buffer i % 2 and completes that buffer's phase i / 2)
+    // the last load issued into each Q buffer and each K stage (load i went
+    // to buffer i % 2 and completes that buffer's phase i / 2)
     for (uint32_t i = q_it > 2 ? q_it - 2 : 0; i < q_it; ++i)
       cx.drain_wait(B_Q_FULL + (i & 1), (i >> 1) & 1);
     for (uint32_t i = issued_k > kStages ? issued_k - kStages : 0; i < issued_k; ++i)
       cx.drain_wait(B_K_FULL + i % kStages, (i / kStages) & 1);
+  }
+}
+
+template <int D, bool PAGED>
+__device__ void run_producer_v(const Ctx& cx, const CUtensorMap* tm_v, const AttnParams& p,
+                               int lane) {
+  using C = Cfg<D>;
+  uint8_t* sV = cx.smem + C::kOffV;
+  int2* sEX = reinterpret_cast<int2*>(cx.smem + C::kOffEX);
+  uint32_t it = 0, kv_it = 0, issued_v = 0;
+  bool aborted = false;
+  for (;;) {
+    const int slot = it % kSlots;
+    if (!cx.warp_wait(B_ITEM_FULL + slot, (it / kSlots) & 1)) { aborted = true; break; }
+    const Item& s = cx.items[slot];
+    const int valid = s.valid;
+    const ItemRec r = s.r;
+    const int kvh = s.kvh;
+    __syncwarp();
+    // the record is in registers: the slot is no longer needed here
+    if (lane == 0) mbar_arrive(&cx.bar[B_ITEM_EMPTY + slot]);
+    ++it;
+    if (!valid) break;
+    TileIter ti(r, p.classes);
+    for (int n = 0; n < r.n_tiles; ++n) {
+      const int cls = ti.next();
+      const int j = ti.j;
+      const int row0 = r.kv_base + j * kBlockN;
+      const int stage = kv_it % kStages;
+      int ph[kPagesPerTile];
+      if constexpr (PAGED) tile_pages(p, r, j, lane, ph);
+      // the V stage is free once the PV of the tile two back has completed
+      if (!cx.warp_wait(B_PV_DONE + stage, ((kv_it / kStages) & 1) ^ 1)) { aborted = true; break; }
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&cx.bar[B_V_FULL + stage], (uint32_t)C::kKVBytes);
+        load_kv_tile<D, PAGED>(sV + stage * C::kKVBytes, tm_v, &cx.bar[B_V_FULL + stage], 1, kvh,
+                               row0, ph);
+      }
+      ++issued_v;
+      // column intervals of a partial tile for the mask (FULL tiles need
+      // none), as start and length: a row sees the column iff its enter
+      // index minus start is below length, compared unsigned.  Written after
+      // the PV of the tile two back, the last reader of this stage's
+      // intervals, has completed.
+      if (cls == kTilePartial) {
+        int2* ex = sEX + stage * kBlockN;
+#pragma unroll
+        for (int q = 0; q < kBlockN / 32; ++q) {
+          const int2 iv = column_interval(p.tree_order, r.tree_base, j * kBlockN + q * 32 + lane,
+                                          r.kv, r.kv - r.tl);
+          // an empty interval (a column past the sequence's end) gets
+          // length 0, which no row passes
+          ex[q * 32 + lane] =
+              make_int2(iv.x, iv.y > iv.x ? (int)((uint32_t)iv.y - (uint32_t)iv.x) : 0);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&cx.bar[B_EX_FULL + stage]);
+      ++kv_it;
+    }
+    if (aborted) break;
+  }
+  if (aborted && lane == 0) {
+    // the last V load issued into each stage must land before the CTA exits
     for (uint32_t i = issued_v > kStages ? issued_v - kStages : 0; i < issued_v; ++i)
       cx.drain_wait(B_V_FULL + i % kStages, (i / kStages) & 1);
   }
@@ -425,7 +474,10 @@ __device__ void run_mma(const Ctx& cx, const AttnParams& p) {
     if constexpr (!kQkAfterPvInIssueOrder) {
       if (c >= 2 && !cx.wait(B_PV_DONE + stage, ((c - 2) >> 1) & 1)) return false;
     }
-    tc_fence_after();
+    // no tcgen05 fence here: K (TMA) and Q (TMA, or the correction warps'
+    // stores behind a proxy fence) reach the tensor core through the async
+    // proxy, ordered by the mbarrier waits alone; only hand-offs from threads
+    // that used tcgen05 operations themselves (P, O) need one
     const int n_eff = (nvalid + 15) & ~15;
     const uint32_t idesc = umma_idesc_f16(BF16, 128, n_eff, false);
     const uint64_t dq = cur_b ? dq1 : dq0;
@@ -630,11 +682,14 @@ __device__ void softmax_loop(const Ctx& cx, const AttnParams& p, int wq, int lan
       const uint32_t t_s = t_row + C::kTmemS + 128 * sb;
       // One pass over the tile's 32-column chunks (a rolled loop: the code
       // stays small enough for the instruction cache).  Scores are taken
-      // relative to the row's running reference, t = s * c2 - m; the
-      // reference moves -- this tile's P chunks already written, l and
-      // (before this tile's PV) O rescaled -- only when a chunk's largest t
-      // exceeds 8, so that P = 2^t <= 256.
+      // relative to the row's running reference, t = s * c2 - m, and P = 2^t
+      // is formed at once; only when a chunk's P sum exceeds 256 (so that
+      // some t may exceed 8), or the row has no reference yet, is the chunk's
+      // max taken and the reference moved -- this tile's P columns already
+      // written, l and (before this tile's PV) O rescaled -- and P formed
+      // again.  P = 2^t <= 256 throughout.
       const int nch = (nvalid + 31) >> 5;
+      const int2* ivs = sEX + sb * kBlockN;
       float alpha_t = 1.f;   // product of this tile's reference moves
       float lsum = 0.f;
 #pragma unroll 1
@@ -652,64 +707,75 @@ __device__ void softmax_loop(const Ctx& cx, const AttnParams& p, int wq, int lan
         }
         if (partial) {
           // column c is visible iff e_row lies in its interval, stored by
-          // the producer as (start, length): (e_row - start) < length unsigned
-          const int2* iv = sEX + sb * kBlockN + 32 * q;
+          // the V producer as (start, length): (e_row - start) < length unsigned
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
-            const int4 e = reinterpret_cast<const int4*>(iv)[i];
+            const int4 e = reinterpret_cast<const int4*>(ivs + 32 * q)[i];
             if (!((uint32_t)(e_row - e.x) < (uint32_t)e.y)) x[2 * i] = -INFINITY;
             if (!((uint32_t)(e_row - e.z) < (uint32_t)e.w)) x[2 * i + 1] = -INFINITY;
           }
         }
-        float m4[4];
+        float p[32];
+        float2 la = make_float2(0.f, 0.f), lb = make_float2(0.f, 0.f);
 #pragma unroll
-        for (int k = 0; k < 4; ++k) m4[k] = x[k];
+        for (int i = 0; i < 16; ++i) {
+          p[2 * i] = ex2_approx(x[2 * i]);
+          p[2 * i + 1] = ex2_approx(x[2 * i + 1]);
+          if (i & 1)
+            lb = fadd2(lb, make_float2(p[2 * i], p[2 * i + 1]));
+          else
+            la = fadd2(la, make_float2(p[2 * i], p[2 * i + 1]));
+        }
+        float csum = (la.x + la.y) + (lb.x + lb.y);
+        if (__any_sync(0xffffffffu, m_ref == -INFINITY || !(csum <= 256.f))) {
+          // the chunk's max: a row's first visible chunk always sets its
+          // reference (nothing before it carries weight: l, O and this
+          // tile's P are 0, so the factor is 0 rather than 2^-tmax, which
+          // may not be finite); otherwise the reference moves when the max
+          // exceeds it by more than 2^8
+          float m4[4];
 #pragma unroll
-        for (int i = 4; i < 32; ++i) m4[i & 3] = fmaxf(m4[i & 3], x[i]);
-        const float tmax = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
-        // a row's first visible chunk always sets its reference (nothing
-        // before it carries weight: l, O and this tile's P are 0, so the
-        // factor is 0 rather than 2^-tmax, which may not be finite)
-        const bool first_vis = m_ref == -INFINITY && tmax > -INFINITY;
-        if (__any_sync(0xffffffffu, tmax > 8.f || first_vis)) {
-          // move the reference of the rows whose max outgrew it
+          for (int k = 0; k < 4; ++k) m4[k] = x[k];
+#pragma unroll
+          for (int i = 4; i < 32; ++i) m4[i & 3] = fmaxf(m4[i & 3], x[i]);
+          const float tmax = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+          const bool first_vis = m_ref == -INFINITY && tmax > -INFINITY;
           const bool mv = tmax > 8.f || first_vis;
-          const float a = mv ? (first_vis ? 0.f : ex2_approx(-tmax)) : 1.f;
-          if (mv) {
-            m_ref = m_use + tmax;
+          if (__any_sync(0xffffffffu, mv)) {
+            const float a = mv ? (first_vis ? 0.f : ex2_approx(-tmax)) : 1.f;
+            const float sh = mv ? tmax : 0.f;
+            if (mv) m_ref = m_use + tmax;
+            alpha_t *= a;
+            lsum *= a;
+            csum = 0.f;
 #pragma unroll
-            for (int i = 0; i < 32; ++i) x[i] -= tmax;
-          }
-          alpha_t *= a;
-          lsum *= a;
-          if (q > 0) {
-            // this tile's P chunks already written: rescale them in TMEM
-            tmem_wait_st();
-            for (int j = 0; j < q; ++j) {
-              uint32_t w[16];
-              tmem_ld16(t_s + 16 * j, w);
-              tmem_wait_ld(w);
+            for (int i = 0; i < 32; ++i) {
+              p[i] = ex2_approx(x[i] - sh);
+              csum += p[i];
+            }
+            if (q > 0) {
+              // this tile's P chunks already written: rescale them in TMEM
+              tmem_wait_st();
+              for (int j = 0; j < q; ++j) {
+                uint32_t w[16];
+                tmem_ld16(t_s + 16 * j, w);
+                tmem_wait_ld(w);
 #pragma unroll
-              for (int i = 0; i < 16; ++i) {
-                const float2 f = unpack2<BF16>(w[i]);
-                w[i] = pack2<BF16>(f.x * a, f.y * a);
+                for (int i = 0; i < 16; ++i) {
+                  const float2 f = unpack2<BF16>(w[i]);
+                  w[i] = pack2<BF16>(f.x * a, f.y * a);
+                }
+                tmem_st16(t_s + 16 * j, w);
               }
-              tmem_st16(t_s + 16 * j, w);
             }
           }
         }
-        // P = 2^t (0 where masked), two per 32-bit word, over columns
-        // 16q .. 16q + 15 of the score buffer (read by the PV's k-steps 2q
-        // and 2q + 1)
+        lsum += csum;
+        // P, two per 32-bit word, over columns 16q .. 16q + 15 of the score
+        // buffer (read by the PV's k-steps 2q and 2q + 1)
         uint32_t pk[16];
-        float2 l2 = make_float2(0.f, 0.f);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const float p0 = ex2_approx(x[2 * i]), p1 = ex2_approx(x[2 * i + 1]);
-          l2 = fadd2(l2, make_float2(p0, p1));
-          pk[i] = pack2<BF16>(p0, p1);
-        }
-        lsum += l2.x + l2.y;
+        for (int i = 0; i < 16; ++i) pk[i] = pack2<BF16>(p[2 * i], p[2 * i + 1]);
         tmem_st16(t_s + 16 * q, pk);
       }
       l = l * alpha_t + lsum;
@@ -988,7 +1054,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* bar = cx.bar;
     for (int i = 0; i < kSlots; ++i) {
       mbar_init(&bar[B_ITEM_FULL + i], 1);
-      mbar_init(&bar[B_ITEM_EMPTY + i], 1 + 4 + 4);   // MMA thread, softmax and correction warps
+      // MMA thread, V producer, softmax and correction warps
+      mbar_init(&bar[B_ITEM_EMPTY + i], 1 + 1 + 4 + 4);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bar[B_Q_FULL + i], 1);
@@ -1030,9 +1097,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp < kWarpSoftmax) {
     regs_dec<kRegsIssue>();
     if (warp == kWarpProducer) {
-      run_producer<D, PAGED>(cx, &tm_q, &tm_k, &tm_v, p, lane);
+      run_producer<D, PAGED>(cx, &tm_q, &tm_k, p, lane);
     } else if (warp == kWarpMma) {
       if (lane == 0) run_mma<D, BF16>(cx, p);
+    } else if (warp == kWarpProducerV) {
+      run_producer_v<D, PAGED>(cx, &tm_v, p, lane);
     }
   } else if (warp < kWarpCorrection) {
     regs_inc<kRegsSoftmax>();
