@@ -209,13 +209,14 @@ def test_split_workspace_size(lib):
     plain = ta.workspace_size(d)
     # one chunk per pair is the unsplit layout
     assert ta.split_workspace_size(d, 1) == plain
-    # g = 2 -> 64 q rows per tile: 1 + 2 pairs at most; per record an
-    # h_kv x 128 x d float32 partial output and its lse, plus the merge table
-    max_pairs = (19 + 63) // 64 + 2
+    # g = 2 -> 64 q rows per Q tile, 128 per work unit of two tiles: 1 + 2
+    # pairs at most; per record an h_kv x (2 x 128) x d float32 partial output
+    # and its lse, plus the merge table
+    max_pairs = (19 + 127) // 128 + 2
     for mc in (2, 7, 16):
         recs = max_pairs * mc
         extra = (_round256(recs * 64) - _round256(max_pairs * 64) + _round256(max_pairs * 16)
-                 + _round256(recs * 2 * 128 * 64 * 4) + _round256(recs * 2 * 128 * 4))
+                 + _round256(recs * 2 * 256 * 64 * 4) + _round256(recs * 2 * 256 * 4))
         assert ta.split_workspace_size(d, mc) == plain + extra
     assert ta.split_workspace_size(d, 0) == 0
     assert ta.split_workspace_size(d, ta.MAX_CHUNKS + 1) == 0

@@ -381,7 +381,8 @@ ta_status launch_run_checked(const void* q, const void* k, const void* v, const 
     mp.h_q = dims->h_q;
     mp.h_kv = dims->h_kv;
     mp.g = g;
-    const int64_t units = L.max_pairs * dims->h_kv * (ta::kBlockM / 8);   // 8 rows each
+    const int64_t units =
+        L.max_pairs * dims->h_kv * (ta::kTilesPerUnit * ta::kBlockM / 8);   // 8 rows each
     const int mgrid = (int)(units < 16 * nsm ? units : 16 * nsm);
     const cudaError_t me = ta::launch_merge(mp, D, bf16, mgrid, st);
     if (me != cudaSuccess) return cuda_status(me);

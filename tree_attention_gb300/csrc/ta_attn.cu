@@ -4,34 +4,37 @@
 // (per q row and head: masked online softmax of sm_scale * q.k in log2
 // units, output O / d and lse = m + log2(d)), re-designed for one GB300 SM.
 //
-// One CTA per SM pops (sequence, q tile, kv head) work items from a
-// longest-first queue and streams their non-empty kv tiles of 128 columns
-// through one tensor-core pipeline.  Tensor memory holds two score buffers
-// (S0, S1: 128 columns each) and two output accumulators (O0, O1: one per
-// item in flight), so that the QK^T of tile c + 1 overlaps the softmax of
-// tile c and one item's epilogue overlaps the next item's first tiles.
-// Warp roles:
-//   warp 0      producer: stages each item's record, TMA-loads its packed Q
-//               tile (two buffers) and its K tiles (two stages)
+// One CTA per SM pops work units from a longest-first queue.  A unit is two
+// consecutive Q tiles (A and B, 128 packed rows each) of one (sequence, kv
+// head); both stream the same kv tiles of 128 columns, so every K/V tile
+// loaded into shared memory serves two Q tiles.  Tensor memory holds one
+// score buffer and one output accumulator per Q tile (S_A, S_B, O_A, O_B:
+// 128 columns each).  Warp roles:
+//   warp 0      producer: stages each unit's record, TMA-loads its Q tiles
+//               (one buffer each) and its K tiles (two stages)
+//   warp 1      MMA issuer (one thread): for kv tile t, PV_A(t-1) then
+//               QK_A(t), PV_B(t-1) then QK_B(t) (tcgen05.mma, M = 128,
+//               N = 128; P read from tensor memory), so that each tile's
+//               softmax overlaps the other tile's tensor-core work
 //   warp 2      V producer: TMA-loads the V tiles (two stages) and stages each
 //               partial tile's column intervals beside them
-//   warp 1      MMA issuer (one thread): S = Q K^T and O += P V
-//               (tcgen05.mma, M = 128, N = 128), P read from tensor memory;
-//               it runs over one stream of tiles across item boundaries,
-//               issuing the QK^T of tile c + 2 right after the PV of tile c
-//   warps 4-7   softmax: one TMEM lane (= packed row) per thread: tree mask,
-//               online softmax with a lazily moved reference max, P
-//               (fp16/bf16) written over the first half of its score buffer,
-//               the rare rescale of O
-//   warps 8-11  correction: RoPE of each item's Q tile (before the item's
-//               first QK^T) and the epilogue of the item before it (O / l
-//               and lse from tensor memory to global memory)
-// Keys arrive rotated (the run rotates them once per call).  Every cross-warp
-// hand-off is an mbarrier with a bounded wait.
+//   warps 4-7   softmax of tile A, warps 8-11 softmax of tile B (one TMEM
+//               lane = packed row per thread): tree mask, online softmax
+//               against a lazily moved reference, P (fp16/bf16) written over
+//               the first half of the tile's score buffer, the rare rescale
+//               of O
+//   warps 12-15 correction: RoPE of each unit's Q tiles (before their first
+//               QK^T) and the epilogue of the unit before it (O / l and lse
+//               from tensor memory to global memory)
+// A kv tile that is empty for one Q tile (the plan classifies each tile for
+// A and B) is skipped by that tile's QK^T, softmax and PV.  Keys arrive
+// rotated (the run rotates them once per call).  Every cross-warp hand-off
+// is an mbarrier with a bounded wait.
 #include <cuda_runtime.h>
 
 #include <climits>
 #include <cstdint>
+#include <type_traits>
 
 #include "ta_device.cuh"
 #include "ta_launch.h"
@@ -39,48 +42,44 @@
 namespace ta {
 namespace {
 
-constexpr int kThreads = 384;
-constexpr int kStages = 2;   // K/V ring depth = score buffers (tile c uses stage c & 1)
-constexpr int kSlots = 4;    // work-item slots (producer, MMA, softmax, correction)
+constexpr int kThreads = 512;
+constexpr int kStages = 2;   // K/V ring depth
+constexpr int kSlots = 4;    // work-unit slots (producer, MMA, softmax, correction)
 constexpr int kWarpProducer = 0;
 constexpr int kWarpMma = 1;
 constexpr int kWarpProducerV = 2;
-constexpr int kWarpSoftmax = 4;      // warps 4..7
-constexpr int kWarpCorrection = 8;   // warps 8..11
+constexpr int kWarpSoftmax = 4;      // warps 4..7 tile A, 8..11 tile B
+constexpr int kWarpCorrection = 12;  // warps 12..15
 
-// Register split (setmaxnreg) of the 384 threads' launch allocation of 168
-// each (64,512 in all): the producer / MMA warpgroup and the correction
-// warpgroup give registers up, the softmax warpgroup -- one TMEM lane of 128
-// scores per thread -- takes them, so that its exponentials overlap.
-constexpr uint32_t kRegsLaunch = 168;
-constexpr uint32_t kRegsIssue = 80;        // warps 0-3
-constexpr uint32_t kRegsSoftmax = 248;     // warps 4-7
-constexpr uint32_t kRegsCorrection = 152;  // warps 8-11
-static_assert(128 * (kRegsIssue + kRegsSoftmax + kRegsCorrection) <= kThreads * kRegsLaunch,
+// Register split (setmaxnreg) of the 512 threads' launch allocation of 128
+// each (65,536 in all): the producer / MMA warpgroup gives registers up, the
+// softmax and correction warpgroups take them.
+constexpr uint32_t kRegsLaunch = 128;
+constexpr uint32_t kRegsIssue = 104;       // warps 0-3
+constexpr uint32_t kRegsSoftmax = 136;     // warps 4-11
+constexpr uint32_t kRegsCorrection = 136;  // warps 12-15
+static_assert(128 * (kRegsIssue + 2 * kRegsSoftmax + kRegsCorrection) <= kThreads * kRegsLaunch,
               "register split exceeds the launch allocation");
-
-// The QK^T of tile c + 2 overwrites the score buffer whose P the PV of tile c
-// reads; tcgen05.mma operations issued by one thread execute in issue order,
-// so it is issued right after that PV without waiting for its completion.
-constexpr bool kQkAfterPvInIssueOrder = true;
+static_assert(kRegsIssue <= kRegsLaunch && kRegsSoftmax >= kRegsLaunch &&
+                  kRegsCorrection >= kRegsLaunch,
+              "the first warpgroup gives registers up, the others take them");
 
 enum Bar : int {
   B_ITEM_FULL = 0,                     // [kSlots] record staged
   B_ITEM_EMPTY = B_ITEM_FULL + kSlots, // [kSlots] MMA, V producer, softmax and correction warps done
-  B_Q_FULL = B_ITEM_EMPTY + kSlots,    // [2] Q buffer landed
-  B_Q_READY = B_Q_FULL + 2,            // [2] Q buffer rotated (RoPE)
-  B_Q_EMPTY = B_Q_READY + 2,           // [2] the last QK^T reading the Q buffer done
+  B_Q_FULL = B_ITEM_EMPTY + kSlots,    // [2] Q buffer of tile A / B landed
+  B_Q_READY = B_Q_FULL + 2,            // [2] ... rotated (RoPE)
+  B_Q_EMPTY = B_Q_READY + 2,           // [2] ... read by the unit's last QK^T
   B_K_FULL = B_Q_EMPTY + 2,            // [kStages]
   B_V_FULL = B_K_FULL + kStages,       // [kStages]
   B_EX_FULL = B_V_FULL + kStages,      // [kStages] column intervals of a partial tile
-  // tile c uses K/V stage and score buffer c & 1: the producer frees a K (V)
-  // stage on S_FULL (PV_DONE) of that index, so no separate release commits
-  B_S_FULL = B_EX_FULL + kStages,      // [2] score buffer written (K stage read)
-  B_P_FULL = B_S_FULL + 2,             // [2] P written over the score buffer
-  B_PV_DONE = B_P_FULL + 2,            // [2] PV reading that P done (V stage read)
-  B_O_FULL = B_PV_DONE + 2,            // [2] the item's last PV into O buffer done
-  B_O_FREE = B_O_FULL + 2,             // [2] correction read O buffer and its (m, l)
-  B_ML_FULL = B_O_FREE + 2,            // [2] softmax wrote the rows' (m, l) of the item
+  B_K_EMPTY = B_EX_FULL + kStages,     // [kStages] both QK^T of the tile in the stage done
+  B_V_EMPTY = B_K_EMPTY + kStages,     // [kStages] both PV of the tile in the stage done
+  B_S_FULL = B_V_EMPTY + kStages,      // [2] score buffer of tile A / B written
+  B_P_FULL = B_S_FULL + 2,             // [2] P written over it
+  B_O_FULL = B_P_FULL + 2,             // [2] the unit's last PV into O_A / O_B done
+  B_O_FREE = B_O_FULL + 2,             // [2] correction read O_A / O_B and its (m, l)
+  B_ML_FULL = B_O_FREE + 2,            // [2] softmax wrote the rows' (m, l)
   B_DRAIN = B_ML_FULL + 2,
   B_STALL,                             // test hook: nothing ever arrives on it
   B_COUNT
@@ -101,7 +100,7 @@ struct Cfg {
   static constexpr int kQBytes = kAtoms * kQAtomBytes;
   static constexpr int kKVBytes = kAtoms * kKVAtomBytes;
   static constexpr int kOstBytes = 32 * 64;            // per correction warp: 32 rows x 64 bytes
-  static constexpr int kOffQ = 0;                                   // [2] Q buffers
+  static constexpr int kOffQ = 0;                                   // [2] tile A, tile B
   static constexpr int kOffK = kOffQ + 2 * kQBytes;                 // [kStages]
   static constexpr int kOffV = kOffK + kStages * kKVBytes;          // [kStages]
   static constexpr int kOffEX = kOffV + kStages * kKVBytes;         // int2 [kStages][kBlockN]
@@ -113,8 +112,8 @@ struct Cfg {
   static constexpr int kUsed = kOffCta + 64;
   static constexpr int kSmemAlloc = kUsed + 1024;   // room to align the base to 1024
   static constexpr uint32_t kTmemCols = 512;
-  static constexpr uint32_t kTmemS = 0;      // score buffer sb at 128 * sb (P over its first half)
-  static constexpr uint32_t kTmemO = 256;    // O buffer ob at 256 + 128 * ob
+  static constexpr uint32_t kTmemS = 0;      // S of tile x at 128 * x (P over its first half)
+  static constexpr uint32_t kTmemO = 256;    // O of tile x at 256 + 128 * x
 };
 
 struct CtaShared {
@@ -145,9 +144,11 @@ struct Ctx {
   }
 };
 
-// Iterates the non-empty kv tiles of a work item from its first tile
-// (tile_lo, past 0 for a split-KV chunk): from the record's inline 2-bit
-// classes for short sequences, else from the plan's class bytes.
+// Iterates the kv tiles of a work unit that are non-empty for tile A or B
+// from its first tile (tile_lo, past 0 for a split-KV chunk): from the
+// record's inline 4-bit classes for short sequences, else from the plan's
+// class bytes.  next() returns the tile's class byte (A's class in bits 0-1,
+// B's in 2-3; 0 when done).
 struct TileIter {
   const uint8_t* cls;
   int kvt, j;
@@ -156,10 +157,8 @@ struct TileIter {
   __device__ TileIter() : cls(nullptr), kvt(0), j(0), inl(true), w0(0), w1(0), w2(0), w3(0) {}
   __device__ TileIter(const ItemRec& r, const uint8_t* classes)
       : cls(classes + r.class_off), kvt(r.kvt), j(r.tile_lo - 1), inl(r.kvt <= kInlineTiles) {
-    w0 = r.cls2[0];
-    w1 = r.cls2[1];
-    w2 = r.cls2[2];
-    w3 = 0;
+    w0 = r.cls;
+    w1 = w2 = w3 = 0;
     if (!inl && (r.tile_lo & 15)) {
       // a range that starts inside a 16-tile group: load that group now
       const uint4 v = __ldg(reinterpret_cast<const uint4*>(cls + (r.tile_lo & ~15)));
@@ -169,15 +168,13 @@ struct TileIter {
       w3 = v.w;
     }
   }
-  // advances to the next non-empty tile; returns its class (0 when done)
   __device__ int next() {
     while (true) {
       ++j;
       if (j >= kvt) return 0;
       int c;
       if (inl) {
-        const uint32_t w = j < 16 ? w0 : (j < 32 ? w1 : w2);
-        c = (w >> (2 * (j & 15))) & 3;
+        c = (w0 >> (4 * j)) & 15;
       } else {
         if ((j & 15) == 0) {
           const uint4 v = __ldg(reinterpret_cast<const uint4*>(cls + j));
@@ -195,10 +192,16 @@ struct TileIter {
   }
 };
 
+// q rows of tile x (0: A, 1: B) of a unit record
+__device__ __forceinline__ int tile_rows(const ItemRec& r, int x, int R) {
+  return max(0, min(R, r.nq - x * R));
+}
+__device__ __forceinline__ int tile_count(const ItemRec& r, int x) { return x ? r.n_b : r.n_a; }
+
 // ---------------------------------------------------------------------------
-// producer warps (lane 0 issues): warp 0 stages the items and loads Q and K,
-// warp 2 loads V and stages the mask intervals, so that neither kind of load
-// waits behind the other's stage release
+// producer warps (lane 0 issues): warp 0 stages the units and loads their Q
+// tiles and K, warp 2 loads V and stages the mask intervals, so that neither
+// kind of load waits behind the other's stage release
 // ---------------------------------------------------------------------------
 // The physical pages of kv tile j of a paged sequence (logical pages 8j ..
 // 8j + 7), looked up by lanes 0-7 and shared with the warp; a page past the
@@ -244,10 +247,10 @@ __device__ void run_producer(const Ctx& cx, const CUtensorMap* tm_q, const CUten
   const unsigned long long n_items = *(volatile unsigned int*)&p.hdr->num_items;
   const unsigned int num_items = (unsigned int)(n_items < cap ? n_items : cap);
   const int g = p.g, R = p.R;
-  uint32_t it = 0, kv_it = 0, q_it = 0;
+  uint32_t it = 0, kv_it = 0, q_it[2] = {0, 0};
   uint32_t issued_k = 0;   // loads issued (stage = count % kStages)
   bool aborted = false;
-  // the first item of every CTA is fixed (CTA b takes item b, the items being
+  // the first unit of every CTA is fixed (CTA b takes item b, the items being
   // in longest-first order already), the rest come from the queue, which
   // starts after those grid items
   const unsigned int n_static = gridDim.x;
@@ -269,7 +272,7 @@ __device__ void run_producer(const Ctx& cx, const CUtensorMap* tm_q, const CUten
     }
     if (lane < 4) reinterpret_cast<int4*>(&s.r)[lane] = rec_next;
     const int kvh = idx % p.h_kv;
-    // pop the next index now; its round trip overlaps this item's issue
+    // pop the next index now; its round trip overlaps this unit's issue
     unsigned int nidx = 0;
     if (lane == 0) {
       nidx = n_static + atomicAdd(&p.hdr->queue_head, 1u);
@@ -280,29 +283,33 @@ __device__ void run_producer(const Ctx& cx, const CUtensorMap* tm_q, const CUten
     const ItemRec r = s.r;
     if (lane == 0) mbar_arrive(&cx.bar[B_ITEM_FULL + slot]);
     if (r.n_tiles > 0) {
-      const int qb = q_it & 1;
-      if (!cx.warp_wait(B_Q_EMPTY + qb, ((q_it >> 1) & 1) ^ 1)) { aborted = true; break; }
-      if (lane == 0) {
-        mbar_arrive_expect_tx(&cx.bar[B_Q_FULL + qb], (uint32_t)(C::kAtoms * 128 * g * R));
+      // the Q tiles that attend anything (each into its own buffer)
 #pragma unroll
-        for (int a = 0; a < C::kAtoms; ++a)
-          tma_load_3d(sQ + qb * C::kQBytes + a * C::kQAtomBytes, tm_q, &cx.bar[B_Q_FULL + qb],
-                      a * 64, kvh * g, r.q_row0);
+      for (int x = 0; x < 2; ++x) {
+        if (tile_count(r, x) == 0) continue;
+        if (!cx.warp_wait(B_Q_EMPTY + x, (q_it[x] & 1) ^ 1)) { aborted = true; break; }
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&cx.bar[B_Q_FULL + x], (uint32_t)(C::kAtoms * 128 * g * R));
+#pragma unroll
+          for (int a = 0; a < C::kAtoms; ++a)
+            tma_load_3d(sQ + x * C::kQBytes + a * C::kQAtomBytes, tm_q, &cx.bar[B_Q_FULL + x],
+                        a * 64, kvh * g, r.q_row0 + x * R);
+        }
+        ++q_it[x];
       }
-      ++q_it;
+      if (aborted) break;
       TileIter ti(r, p.classes);
       for (int n = 0; n < r.n_tiles; ++n) {
         ti.next();
         const int j = ti.j;
         const int row0 = r.kv_base + j * kBlockN;
         const int stage = kv_it % kStages;
-        const uint32_t empty_par = ((kv_it / kStages) & 1) ^ 1;
-        const uint32_t bytes = (uint32_t)C::kKVBytes;
         int ph[kPagesPerTile];
         if constexpr (PAGED) tile_pages(p, r, j, lane, ph);
-        if (!cx.warp_wait(B_S_FULL + stage, empty_par)) { aborted = true; break; }
+        // the K stage is free once both QK^T of the tile two back are done
+        if (!cx.warp_wait(B_K_EMPTY + stage, ((kv_it / kStages) & 1) ^ 1)) { aborted = true; break; }
         if (lane == 0) {
-          mbar_arrive_expect_tx(&cx.bar[B_K_FULL + stage], bytes);
+          mbar_arrive_expect_tx(&cx.bar[B_K_FULL + stage], (uint32_t)C::kKVBytes);
           load_kv_tile<D, PAGED>(sK + stage * C::kKVBytes, tm_k, &cx.bar[B_K_FULL + stage], 0, kvh,
                                  row0, ph);
         }
@@ -318,10 +325,11 @@ __device__ void run_producer(const Ctx& cx, const CUtensorMap* tm_q, const CUten
   }
   if (aborted && lane == 0) {
     // let every copy already in flight land before the CTA's memory goes away:
-    // the last load issued into each Q buffer and each K stage (load i went
-    // to buffer i % 2 and completes that buffer's phase i / 2)
-    for (uint32_t i = q_it > 2 ? q_it - 2 : 0; i < q_it; ++i)
-      cx.drain_wait(B_Q_FULL + (i & 1), (i >> 1) & 1);
+    // the last load issued into each Q buffer and each K stage (load i of a
+    // stage went to stage i % 2 and completes that stage's phase i / 2)
+#pragma unroll
+    for (int x = 0; x < 2; ++x)
+      if (q_it[x] > 0) cx.drain_wait(B_Q_FULL + x, (q_it[x] - 1) & 1);
     for (uint32_t i = issued_k > kStages ? issued_k - kStages : 0; i < issued_k; ++i)
       cx.drain_wait(B_K_FULL + i % kStages, (i / kStages) & 1);
   }
@@ -355,20 +363,20 @@ __device__ void run_producer_v(const Ctx& cx, const CUtensorMap* tm_v, const Att
       const int stage = kv_it % kStages;
       int ph[kPagesPerTile];
       if constexpr (PAGED) tile_pages(p, r, j, lane, ph);
-      // the V stage is free once the PV of the tile two back has completed
-      if (!cx.warp_wait(B_PV_DONE + stage, ((kv_it / kStages) & 1) ^ 1)) { aborted = true; break; }
+      // the V stage is free once both PV of the tile two back are done
+      if (!cx.warp_wait(B_V_EMPTY + stage, ((kv_it / kStages) & 1) ^ 1)) { aborted = true; break; }
       if (lane == 0) {
         mbar_arrive_expect_tx(&cx.bar[B_V_FULL + stage], (uint32_t)C::kKVBytes);
         load_kv_tile<D, PAGED>(sV + stage * C::kKVBytes, tm_v, &cx.bar[B_V_FULL + stage], 1, kvh,
                                row0, ph);
       }
       ++issued_v;
-      // column intervals of a partial tile for the mask (FULL tiles need
+      // column intervals of a tile partial for tile A or B (FULL tiles need
       // none), as start and length: a row sees the column iff its enter
       // index minus start is below length, compared unsigned.  Written after
-      // the PV of the tile two back, the last reader of this stage's
-      // intervals, has completed.
-      if (cls == kTilePartial) {
+      // the PVs of the tile two back -- behind both softmaxes' reads of this
+      // stage's intervals -- have completed.
+      if ((cls & 3) == kTilePartial || (cls >> 2) == kTilePartial) {
         int2* ex = sEX + stage * kBlockN;
 #pragma unroll
         for (int q = 0; q < kBlockN / 32; ++q) {
@@ -396,13 +404,11 @@ __device__ void run_producer_v(const Ctx& cx, const CUtensorMap* tm_v, const Att
 // ---------------------------------------------------------------------------
 // MMA warp (one thread)
 // ---------------------------------------------------------------------------
-// One stream of tiles across item boundaries, two cursors over it: the QK^T
-// cursor runs up to two tiles ahead of the PV cursor (tile c uses score
-// buffer and K/V stage c & 1), so the tensor core computes S for the next
-// tile while the softmax works on the current one.  The QK^T cursor enters
-// the next item only when it is due (lazily): entering waits for the item's
-// Q tile, whose RoPE the correction warps do after the epilogue of the item
-// two back, which needs the PVs the cursor would otherwise hold up.
+// For kv tile t of a unit: PV_A(t-1), QK_A(t), PV_B(t-1), QK_B(t) -- a Q tile
+// for which kv tile t is empty skips that QK^T and, one tile later, that PV.
+// A QK^T overwrites the score buffer whose P the same Q tile's previous PV
+// reads; tcgen05.mma operations issued by one thread execute in issue order,
+// so it follows that PV without waiting for it.
 template <int D, bool BF16>
 __device__ void run_mma(const Ctx& cx, const AttnParams& p) {
   using C = Cfg<D>;
@@ -417,129 +423,124 @@ __device__ void run_mma(const Ctx& cx, const AttnParams& p) {
   const uint64_t dv1 = dv0 + (uint64_t)(C::kKVBytes >> 4);
   constexpr uint32_t idesc_pv = umma_idesc_f16(BF16, 128, D, /*b_mn_major=*/true);
   const int q_bar = p.rotary ? B_Q_READY : B_Q_FULL;
-  uint32_t it = 0;                  // item slots consumed
-  uint32_t qi = 0;                  // non-empty items entered (Q and O buffer = index & 1)
-  uint32_t c_qk = 0, c_pv = 0;      // tiles issued by each cursor
-  uint32_t o_cnt = 0;               // items whose PVs have started
-  // per tile, from the QK^T cursor to the PV cursor: valid kv columns (bits
-  // 0-7), first / last tile of its item (bits 8, 9), O buffer (bit 10)
-  uint64_t ring = 0;
-  bool cur = false, end = false, ok = true, issued_any = false;
-  int cur_n = 0, cur_t = 0, cur_kv = 0;
-  uint32_t cur_b = 0;
-  TileIter ti;
+  uint32_t it = 0, kc = 0;   // unit slots consumed, kv tiles (K / V stage phases)
+  // per Q tile x (bit x): parity of its PVs issued (P_FULL phase), of its
+  // units entered (Q phase), of its units whose PVs started (O_FREE phase)
+  uint32_t kp = 0, qx = 0, ox = 0;
+  bool ok = true, issued_any = false;
   // test hook: a wait that runs out before any MMA is issued (the other warps
   // then find the abort flag in their own waits)
   if (p.debug_stall) {
     cx.wait(B_STALL, 0);
     ok = false;
   }
-
-  // moves the QK^T cursor to the next item with tiles (or to the end)
-  auto enter_item = [&]() -> bool {
-    for (;;) {
-      const int slot = it % kSlots;
-      if (!cx.wait(B_ITEM_FULL + slot, (it / kSlots) & 1)) return false;
-      const Item& s = cx.items[slot];
-      const int valid = s.valid;
-      const ItemRec r = s.r;
-      // the record is in registers: the slot is no longer needed here
-      mbar_arrive(&cx.bar[B_ITEM_EMPTY + slot]);
-      ++it;
-      if (!valid) {
-        end = true;
-        return true;
-      }
-      if (r.n_tiles > 0) {
-        if (!cx.wait(q_bar + (qi & 1), (qi >> 1) & 1)) return false;
-        cur_b = qi & 1;
-        ++qi;
-        cur = true;
-        cur_n = r.n_tiles;
-        cur_t = 0;
-        cur_kv = r.kv;
-        ti = TileIter(r, p.classes);
-        return true;
-      }
-    }
-  };
-
-  // S(c) = Q K(c)^T into score buffer c & 1
-  auto issue_qk = [&]() -> bool {
-    const uint32_t c = c_qk;
-    const int stage = c & 1;
-    ti.next();
-    const int nvalid = min(kBlockN, cur_kv - ti.j * kBlockN);
-    if (!cx.wait(B_K_FULL + stage, (c >> 1) & 1)) return false;
-    if constexpr (!kQkAfterPvInIssueOrder) {
-      if (c >= 2 && !cx.wait(B_PV_DONE + stage, ((c - 2) >> 1) & 1)) return false;
-    }
-    // no tcgen05 fence here: K (TMA) and Q (TMA, or the correction warps'
-    // stores behind a proxy fence) reach the tensor core through the async
-    // proxy, ordered by the mbarrier waits alone; only hand-offs from threads
-    // that used tcgen05 operations themselves (P, O) need one
-    const int n_eff = (nvalid + 15) & ~15;
-    const uint32_t idesc = umma_idesc_f16(BF16, 128, n_eff, false);
-    const uint64_t dq = cur_b ? dq1 : dq0;
-    const uint64_t dk = stage ? dk1 : dk0;
-    const uint32_t d_s = cx.tmem + C::kTmemS + 128 * stage;
-#pragma unroll
-    for (int k = 0; k < D / 16; ++k) {
-      const uint32_t qo = (uint32_t)(((k >> 2) * C::kQAtomBytes + (k & 3) * 32) >> 4);
-      const uint32_t ko = (uint32_t)(((k >> 2) * C::kKVAtomBytes + (k & 3) * 32) >> 4);
-      umma_f16(d_s, dq + qo, dk + ko, idesc, k > 0 ? 1u : 0u);
-    }
-    umma_commit(&cx.bar[B_S_FULL + stage]);
-    issued_any = true;
-    const uint32_t first = cur_t == 0, last = cur_t == cur_n - 1;
-    if (last) umma_commit(&cx.bar[B_Q_EMPTY + cur_b]);
-    const uint32_t sh = 16 * (c & 3);
-    ring = (ring & ~(0xFFFFull << sh)) |
-           ((uint64_t)((uint32_t)nvalid | (first << 8) | (last << 9) | (cur_b << 10)) << sh);
-    ++c_qk;
-    ++cur_t;
-    if (last) cur = false;
-    return true;
-  };
-
+  using X0 = std::integral_constant<int, 0>;
+  using X1 = std::integral_constant<int, 1>;
   while (ok) {
-    // keep the QK^T cursor up to two tiles ahead of the PV cursor
-    while (!end && c_qk < c_pv + 2) {
-      if (!cur) {
-        if (!enter_item()) { ok = false; break; }
-        if (end) break;
-      }
-      if (!issue_qk()) { ok = false; break; }
+    const int slot = it % kSlots;
+    if (!cx.wait(B_ITEM_FULL + slot, (it / kSlots) & 1)) break;
+    const Item& s = cx.items[slot];
+    const int valid = s.valid;
+    const ItemRec r = s.r;
+    // the record is in registers: the slot is no longer needed here
+    mbar_arrive(&cx.bar[B_ITEM_EMPTY + slot]);
+    ++it;
+    if (!valid) break;
+    if (r.n_tiles == 0) continue;
+    const bool has0 = r.n_a > 0, has1 = r.n_b > 0;
+    if (has0) {
+      if (!cx.wait(q_bar + 0, qx & 1)) break;
+      qx ^= 1;
     }
-    if (!ok || c_pv == c_qk) break;
-    // O(item) += P(c) V(c)
-    const uint32_t c = c_pv;
-    const uint32_t e = (uint32_t)(ring >> (16 * (c & 3))) & 0xFFFFu;
-    const int nvalid = (int)(e & 0xFFu);
-    const bool first = (e >> 8) & 1u, last = (e >> 9) & 1u;
-    const uint32_t ob = (e >> 10) & 1u;
-    const int stage = c & 1;
-    if (!cx.wait(B_P_FULL + stage, (c >> 1) & 1)) break;
-    if (!cx.wait(B_V_FULL + stage, (c >> 1) & 1)) break;
-    // the O buffer is free once the epilogue of the item two back read it
-    if (first && !cx.wait(B_O_FREE + ob, ((o_cnt >> 1) & 1) ^ 1)) break;
-    tc_fence_after();
-    const int nk = (nvalid + 15) >> 4;   // 16-row k-steps holding valid kv rows
-    const uint64_t dv = stage ? dv1 : dv0;
-    const uint32_t pcol = cx.tmem + C::kTmemS + 128 * stage;   // P: two elements per column
-    const uint32_t d_o = cx.tmem + C::kTmemO + 128 * ob;
+    if (has1) {
+      if (!cx.wait(q_bar + 1, (qx >> 1) & 1)) break;
+      qx ^= 2;
+    }
+    // the PV each Q tile owes for its previous kv tile: valid kv columns
+    // (bits 0-7; 0: none), K/V stage (bit 8), that stage's phase (bit 9)
+    uint32_t pend0 = 0, pend1 = 0;
+    bool started0 = false, started1 = false;
+    auto issue_pv = [&](auto xc) -> bool {
+      constexpr int x = decltype(xc)::value;
+      uint32_t& pend = x ? pend1 : pend0;
+      bool& started = x ? started1 : started0;
+      const int nv = (int)(pend & 0xFFu), stage = (int)((pend >> 8) & 1u);
+      if (!cx.wait(B_P_FULL + x, (kp >> x) & 1)) return false;
+      if (!cx.wait(B_V_FULL + stage, (pend >> 9) & 1)) return false;
+      // O is free once the epilogue of the Q tile's previous unit read it
+      if (!started && !cx.wait(B_O_FREE + x, ((ox >> x) & 1) ^ 1)) return false;
+      tc_fence_after();
+      const int nk = (nv + 15) >> 4;   // 16-row k-steps holding valid kv rows
+      const uint64_t dv = stage ? dv1 : dv0;
+      const uint32_t pcol = cx.tmem + C::kTmemS + 128 * x;   // P: two elements per column
+      const uint32_t d_o = cx.tmem + C::kTmemO + 128 * x;
 #pragma unroll
-    for (int k = 0; k < kBlockN / 16; ++k) {
-      if (k < nk)
-        umma_f16_tmem_a(d_o, pcol + k * 8, dv + (uint64_t)(k * 16 * 128 >> 4), idesc_pv,
-                        (!first || k > 0) ? 1u : 0u);
+      for (int k = 0; k < kBlockN / 16; ++k) {
+        if (k < nk)
+          umma_f16_tmem_a(d_o, pcol + k * 8, dv + (uint64_t)(k * 16 * 128 >> 4), idesc_pv,
+                          (started || k > 0) ? 1u : 0u);
+      }
+      if (!started) {
+        started = true;
+        ox ^= 1u << x;
+      }
+      kp ^= 1u << x;
+      pend = 0;
+      return true;
+    };
+    // one Q tile's part of kv tile n: its owed PV, then its QK^T if the tile
+    // is non-empty for it
+    auto bracket = [&](auto xc, int cls, int nvalid, int stage, bool& k_ready) -> bool {
+      constexpr int x = decltype(xc)::value;
+      uint32_t& pend = x ? pend1 : pend0;
+      if (pend && !issue_pv(xc)) return false;
+      if ((cls >> (2 * x)) & 3) {
+        if (!k_ready) {
+          if (!cx.wait(B_K_FULL + stage, (kc >> 1) & 1)) return false;
+          k_ready = true;
+        }
+        // S = Q K^T of this Q tile (K from TMA, Q from TMA or the correction
+        // warps' proxy-fenced stores: no tcgen05 fence needed)
+        const uint32_t idesc = umma_idesc_f16(BF16, 128, (nvalid + 15) & ~15, false);
+        const uint64_t dq = x ? dq1 : dq0;
+        const uint64_t dk = stage ? dk1 : dk0;
+        const uint32_t d_s = cx.tmem + C::kTmemS + 128 * x;
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+          const uint32_t qo = (uint32_t)(((k >> 2) * C::kQAtomBytes + (k & 3) * 32) >> 4);
+          const uint32_t ko = (uint32_t)(((k >> 2) * C::kKVAtomBytes + (k & 3) * 32) >> 4);
+          umma_f16(d_s, dq + qo, dk + ko, idesc, k > 0 ? 1u : 0u);
+        }
+        umma_commit(&cx.bar[B_S_FULL + x]);
+        issued_any = true;
+        pend = (uint32_t)nvalid | ((uint32_t)stage << 8) | (((kc >> 1) & 1u) << 9);
+      }
+      return true;
+    };
+    TileIter ti(r, p.classes);
+    for (int n = 0; n < r.n_tiles; ++n) {
+      const int cls = ti.next();
+      const int nvalid = min(kBlockN, r.kv - ti.j * kBlockN);
+      const int stage = kc & 1;
+      bool k_ready = false;
+      if (!bracket(X0{}, cls, nvalid, stage, k_ready) || !bracket(X1{}, cls, nvalid, stage, k_ready)) {
+        ok = false;
+        break;
+      }
+      umma_commit(&cx.bar[B_K_EMPTY + stage]);                // the tile's QK^Ts are issued
+      if (n > 0) umma_commit(&cx.bar[B_V_EMPTY + (stage ^ 1)]); // and the previous tile's PVs
+      if (n == r.n_tiles - 1) {                                 // the unit's last QK^Ts
+        if (has0) umma_commit(&cx.bar[B_Q_EMPTY + 0]);
+        if (has1) umma_commit(&cx.bar[B_Q_EMPTY + 1]);
+      }
+      ++kc;
     }
-    umma_commit(&cx.bar[B_PV_DONE + stage]);
-    if (last) {
-      umma_commit(&cx.bar[B_O_FULL + ob]);
-      ++o_cnt;
-    }
-    ++c_pv;
+    if (!ok) break;
+    // the unit's last PVs; then its outputs are complete
+    if ((pend0 && !issue_pv(X0{})) || (pend1 && !issue_pv(X1{}))) break;
+    umma_commit(&cx.bar[B_V_EMPTY + ((kc - 1) & 1)]);
+    if (started0) umma_commit(&cx.bar[B_O_FULL + 0]);
+    if (started1) umma_commit(&cx.bar[B_O_FULL + 1]);
   }
   if (*cx.abort && issued_any) {
     umma_commit(&cx.bar[B_DRAIN]);
@@ -548,7 +549,7 @@ __device__ void run_mma(const Ctx& cx, const AttnParams& p) {
 }
 
 // ---------------------------------------------------------------------------
-// RoPE of the Q tile (correction warps)
+// RoPE of the Q tiles (correction warps)
 // ---------------------------------------------------------------------------
 // Inline RoPE of this warp's 32 packed rows of the Q tile.  Task = (q row,
 // 16-byte block c of the first half of the head dimension): one load of the
@@ -641,8 +642,12 @@ __device__ void rope_q_rows(uint8_t* tile, const float2* __restrict__ cs, long l
 // ---------------------------------------------------------------------------
 // softmax warps
 // ---------------------------------------------------------------------------
+
+// ---------------------------------------------------------------------------
+// softmax warps (warpgroup x: rows of Q tile x)
+// ---------------------------------------------------------------------------
 template <int D, bool BF16, bool PAGED>
-__device__ void softmax_loop(const Ctx& cx, const AttnParams& p, int wq, int lane) {
+__device__ void softmax_loop(const Ctx& cx, const AttnParams& p, int x, int wq, int lane) {
   using C = Cfg<D>;
   const int row = wq * 32 + lane;             // packed row = TMEM lane
   const uint32_t t_row = cx.tmem + ((uint32_t)(wq * 32) << 16);
@@ -652,34 +657,31 @@ __device__ void softmax_loop(const Ctx& cx, const AttnParams& p, int wq, int lan
   const int g = p.g, R = p.R;
   const bool in_pack = row < g * R;
   const int qr = in_pack ? row / g : 0;
-  uint32_t it = 0, c = 0, so = 0;   // slots, tiles, items with tiles
+  // slots, kv tiles of the units, tiles of this Q tile, units in which it attends
+  uint32_t it = 0, c = 0, kx = 0, sx = 0;
   for (;;) {
     const int slot = it % kSlots;
     if (!cx.warp_wait(B_ITEM_FULL + slot, (it / kSlots) & 1)) return;
     const Item& s = cx.items[slot];
     if (!s.valid) return;
     const ItemRec r = s.r;
-    if (r.n_tiles == 0) {   // nothing to attend: the correction warps write it
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&cx.bar[B_ITEM_EMPTY + slot]);
-      ++it;
-      continue;
-    }
-    const bool valid = in_pack && qr < r.nq;
+    const bool valid = in_pack && qr < tile_rows(r, x, R);
     int e_row = INT_MIN;
-    if (valid) e_row = __ldg(&p.tree_order[2 * (r.tree_base + r.t * R + qr + r.tl - r.qo)]);
-    const uint32_t ob = so & 1;
+    if (valid && tile_count(r, x) > 0)
+      e_row = __ldg(&p.tree_order[2 * (r.tree_base + r.r0 + x * R + qr + r.tl - r.qo)]);
     float m_ref = -INFINITY, l = 0.f;
+    bool first = true;
     TileIter ti(r, p.classes);
     for (int n = 0; n < r.n_tiles; ++n, ++c) {
-      const int cls = ti.next();
+      const int cls = (ti.next() >> (2 * x)) & 3;
+      if (cls == kTileEmpty) continue;
       const int nvalid = min(kBlockN, r.kv - ti.j * kBlockN);
-      const int sb = c & 1;
+      const int sb = c & 1;   // the kv tile's K / V stage (its column intervals)
       const bool partial = cls == kTilePartial;
       if (partial && !cx.warp_wait(B_EX_FULL + sb, (c >> 1) & 1)) return;
-      if (!cx.warp_wait(B_S_FULL + sb, (c >> 1) & 1)) return;
+      if (!cx.warp_wait(B_S_FULL + x, kx & 1)) return;
       tc_fence_after();
-      const uint32_t t_s = t_row + C::kTmemS + 128 * sb;
+      const uint32_t t_s = t_row + C::kTmemS + 128 * x;
       // One pass over the tile's 32-column chunks (a rolled loop: the code
       // stays small enough for the instruction cache).  Scores are taken
       // relative to the row's running reference, t = s * c2 - m, and P = 2^t
@@ -779,28 +781,26 @@ __device__ void softmax_loop(const Ctx& cx, const AttnParams& p, int wq, int lan
         tmem_st16(t_s + 16 * q, pk);
       }
       l = l * alpha_t + lsum;
-      // rescale the running O when the reference moved (after the PV of
-      // tile c - 1, the last one that wrote it; the PV of tile c waits for
-      // P_FULL below)
-      if (n > 0 && __any_sync(0xffffffffu, alpha_t != 1.f)) {
-        const uint32_t pv = c - 1;
-        if (!cx.warp_wait(B_PV_DONE + (pv & 1), (pv >> 1) & 1)) return;
-        tc_fence_after();
+      // rescale the running O when the reference moved: the PV of this Q
+      // tile's previous kv tile, the last one that wrote O, was issued
+      // before the QK^T whose completion S_FULL reported, so it is done
+      if (!first && __any_sync(0xffffffffu, alpha_t != 1.f)) {
 #pragma unroll 1
         for (int oc = 0; oc < D / 32; ++oc) {
           float o[32];
-          tmem_ld32(t_row + C::kTmemO + 128 * ob + oc * 32, o);
+          tmem_ld32(t_row + C::kTmemO + 128 * x + oc * 32, o);
           tmem_wait_ld(o);
 #pragma unroll
           for (int i = 0; i < 32; ++i) o[i] *= alpha_t;
-          tmem_st32(t_row + C::kTmemO + 128 * ob + oc * 32, o);
+          tmem_st32(t_row + C::kTmemO + 128 * x + oc * 32, o);
         }
       }
       if constexpr (PAGED) {
         // the last page of a sequence may be partly filled: its remaining
         // slots hold whatever the cache holds (not necessarily finite), so
         // the V rows from the sequence's end to the next 16-row step of the
-        // PV are zeroed before the PV reads them (P is 0 there)
+        // PV are zeroed before the PV reads them (P is 0 there); both Q
+        // tiles' softmax warps may write the same zeros
         if (nvalid < kBlockN && (nvalid & 15)) {
           if (!cx.warp_wait(B_V_FULL + sb, (c >> 1) & 1)) return;
           const int r0 = nvalid, nr = ((nvalid + 15) & ~15) - nvalid;
@@ -816,18 +816,21 @@ __device__ void softmax_loop(const Ctx& cx, const AttnParams& p, int wq, int lan
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&cx.bar[B_P_FULL + sb]);
+      if (lane == 0) mbar_arrive(&cx.bar[B_P_FULL + x]);
+      ++kx;
+      first = false;
     }
-    // the rows' (m, l) for the epilogue; the buffer is free once the
-    // epilogue of the item two back has read it
-    if (!cx.warp_wait(B_O_FREE + ob, ((so >> 1) & 1) ^ 1)) return;
-    sML[ob * kBlockM + row] = make_float2(m_ref, l);
+    if (tile_count(r, x) > 0) {
+      // the rows' (m, l) for the epilogue; the buffer is free once the
+      // epilogue of this Q tile's previous unit has read it
+      if (!cx.warp_wait(B_O_FREE + x, (sx & 1) ^ 1)) return;
+      sML[x * kBlockM + row] = make_float2(m_ref, l);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&cx.bar[B_ML_FULL + x]);
+      ++sx;
+    }
     __syncwarp();
-    if (lane == 0) {
-      mbar_arrive(&cx.bar[B_ML_FULL + ob]);
-      mbar_arrive(&cx.bar[B_ITEM_EMPTY + slot]);
-    }
-    ++so;
+    if (lane == 0) mbar_arrive(&cx.bar[B_ITEM_EMPTY + slot]);
     ++it;
   }
 }
@@ -836,8 +839,8 @@ __device__ void softmax_loop(const Ctx& cx, const AttnParams& p, int wq, int lan
 // wait gave up) the warp waits for its own TMEM loads and stores to finish
 // before the CTA frees the TMEM.
 template <int D, bool BF16, bool PAGED>
-__device__ void run_softmax(const Ctx& cx, const AttnParams& p, int wq, int lane) {
-  softmax_loop<D, BF16, PAGED>(cx, p, wq, lane);
+__device__ void run_softmax(const Ctx& cx, const AttnParams& p, int x, int wq, int lane) {
+  softmax_loop<D, BF16, PAGED>(cx, p, x, wq, lane);
   tmem_wait_ld();
   tmem_wait_st();
 }
@@ -845,31 +848,31 @@ __device__ void run_softmax(const Ctx& cx, const AttnParams& p, int wq, int lane
 // ---------------------------------------------------------------------------
 // correction warps: RoPE of Q, epilogues
 // ---------------------------------------------------------------------------
-// Writes one item's rows: O / l in the storage dtype and lse = m + log2(l)
-// (or, for a split-KV chunk, float32 O / l and lse into its partial state).
-// With ``has_o`` the item's O is read from TMEM buffer ``ob`` (and the buffer
-// released); without, the item attended nothing: out = 0, lse = -inf.
+// Writes Q tile x's rows of a unit: O / l in the storage dtype and
+// lse = m + log2(l) (or, for a split-KV chunk, float32 O / l and lse into its
+// partial state).  With ``has_o`` the tile's O is read from TMEM (and the
+// buffer released); without, the tile attended nothing: out = 0, lse = -inf.
 template <int D, bool BF16>
-__device__ void store_item(const Ctx& cx, const AttnParams& p, const ItemRec& r, int kvh,
-                           int wq, int lane, bool has_o, uint32_t ob, float m_ref, float l) {
+__device__ void store_tile(const Ctx& cx, const AttnParams& p, const ItemRec& r, int x, int kvh,
+                           int wq, int lane, bool has_o, float m_ref, float l) {
   using C = Cfg<D>;
   const int row = wq * 32 + lane;
-  const uint32_t t_o = cx.tmem + ((uint32_t)(wq * 32) << 16) + C::kTmemO + 128 * ob;
+  const uint32_t t_o = cx.tmem + ((uint32_t)(wq * 32) << 16) + C::kTmemO + 128 * x;
   uint8_t* ost = cx.smem + C::kOffOst + wq * C::kOstBytes;
-  const int g = p.g;
-  const bool in_pack = row < g * p.R;
+  const int g = p.g, R = p.R;
+  const bool in_pack = row < g * R;
   const int qr = in_pack ? row / g : 0;
   const int hh = in_pack ? row - qr * g : 0;
-  const bool valid = in_pack && qr < r.nq;
+  const bool valid = in_pack && qr < tile_rows(r, x, R);
   const int head = kvh * g + hh;
-  const size_t orow = (size_t)(r.q_row0 + qr) * p.h_q + head;
+  const size_t orow = (size_t)(r.q_row0 + x * R + qr) * p.h_q + head;
   const float inv = l > 0.f ? 1.f / l : 0.f;
   const float lse_v = l > 0.f ? m_ref + log2f(l) : -INFINITY;
   if (r.part >= 0) {
     // split-KV chunk: O / l and lse in float32 into the record's partial
-    // state (packed row = TMEM lane), merged with the pair's other chunks
-    // by the merge kernel
-    const size_t prow = ((size_t)r.part * p.h_kv + kvh) * kBlockM + row;
+    // state (tile x's 128 packed rows, packed row = TMEM lane), merged with
+    // the pair's other chunks by the merge kernel
+    const size_t prow = (((size_t)r.part * p.h_kv + kvh) * kTilesPerUnit + x) * kBlockM + row;
     if (valid) p.part_lse[prow] = lse_v;
     float4* po = reinterpret_cast<float4*>(p.part_o + prow * D);
 #pragma unroll
@@ -877,7 +880,7 @@ __device__ void store_item(const Ctx& cx, const AttnParams& p, const ItemRec& r,
       float o[32];
       if (has_o) {
         tmem_ld32(t_o + oc * 32, o);
-        tmem_wait_ld();
+        tmem_wait_ld(o);
       } else {
 #pragma unroll
         for (int i = 0; i < 32; ++i) o[i] = 0.f;
@@ -885,7 +888,7 @@ __device__ void store_item(const Ctx& cx, const AttnParams& p, const ItemRec& r,
       if (oc == D / 32 - 1) {
         tc_fence_before();
         __syncwarp();
-        if (lane == 0 && has_o) mbar_arrive(&cx.bar[B_O_FREE + ob]);
+        if (lane == 0 && has_o) mbar_arrive(&cx.bar[B_O_FREE + x]);
       }
       if (valid) {
 #pragma unroll
@@ -915,16 +918,17 @@ __device__ void store_item(const Ctx& cx, const AttnParams& p, const ItemRec& r,
     if (has_o) {
       tmem_ld32(t_o + oc2 * 64, oa);
       tmem_ld32(t_o + oc2 * 64 + 32, ob2);
-      tmem_wait_ld();
+      tmem_wait_ld(oa);
+      tmem_wait_ld(ob2);
     } else {
 #pragma unroll
       for (int i = 0; i < 32; ++i) oa[i] = ob2[i] = 0.f;
     }
     if (oc2 == D / 64 - 1) {
-      // O is out of TMEM: the item two later may accumulate into the buffer
+      // O is out of TMEM: the Q tile's next unit may accumulate into it
       tc_fence_before();
       __syncwarp();
-      if (lane == 0 && has_o) mbar_arrive(&cx.bar[B_O_FREE + ob]);
+      if (lane == 0 && has_o) mbar_arrive(&cx.bar[B_O_FREE + x]);
     }
 #pragma unroll
     for (int hf = 0; hf < 2; ++hf) {
@@ -954,27 +958,37 @@ __device__ void store_item(const Ctx& cx, const AttnParams& p, const ItemRec& r,
   }
 }
 
-// The correction warps walk the items one behind the softmax: for each item
-// with tiles, the RoPE of its Q tile (rotary calls), then the epilogue of the
-// item before it -- so the next item's first QK^T never waits for an
-// epilogue, and the epilogue never waits for the next item's RoPE.
+// The correction warps walk the units one behind the softmax: for each unit
+// with tiles, the RoPE of its Q tiles (rotary calls), then the epilogue of
+// the unit before it -- so a unit's first QK^T never waits for an epilogue,
+// and an epilogue never waits for the next unit's RoPE.
 template <int D, bool BF16>
 __device__ void correction_loop(const Ctx& cx, const AttnParams& p, int wq, int lane) {
   using C = Cfg<D>;
   const int row = wq * 32 + lane;
   const float2* sML = reinterpret_cast<const float2*>(cx.smem + C::kOffML);
   const int g = p.g, R = p.R;
-  uint32_t it = 0, qi = 0, oi = 0;   // slots, items with tiles (Q buffers, O buffers)
-  bool pend = false;                 // an item waits for its epilogue
+  // slots; per Q tile x (bit x): parity of its units with tiles (Q phases,
+  // O / ML phases)
+  uint32_t it = 0, qi = 0, oi = 0;
+  bool pend = false;   // a unit waits for its epilogue
   int pend_slot = 0, pend_kvh = 0;
-  uint32_t pend_ob = 0, pend_par = 0;
+  uint32_t pend_has = 0, pend_par = 0;   // bit x: tile x attends; its O / ML phase
   ItemRec pend_r;
   auto finish_pending = [&]() -> bool {
-    if (!cx.warp_wait(B_ML_FULL + pend_ob, pend_par)) return false;
-    const float2 ml = sML[pend_ob * kBlockM + row];
-    if (!cx.warp_wait(B_O_FULL + pend_ob, pend_par)) return false;
-    tc_fence_after();
-    store_item<D, BF16>(cx, p, pend_r, pend_kvh, wq, lane, true, pend_ob, ml.x, ml.y);
+#pragma unroll 1
+    for (int x = 0; x < 2; ++x) {
+      if ((pend_has >> x) & 1) {
+        const uint32_t par = (pend_par >> x) & 1;
+        if (!cx.warp_wait(B_ML_FULL + x, par)) return false;
+        const float2 ml = sML[x * kBlockM + row];
+        if (!cx.warp_wait(B_O_FULL + x, par)) return false;
+        tc_fence_after();
+        store_tile<D, BF16>(cx, p, pend_r, x, pend_kvh, wq, lane, true, ml.x, ml.y);
+      } else {
+        store_tile<D, BF16>(cx, p, pend_r, x, pend_kvh, wq, lane, false, -INFINITY, 0.f);
+      }
+    }
     __syncwarp();
     if (lane == 0) mbar_arrive(&cx.bar[B_ITEM_EMPTY + pend_slot]);
     pend = false;
@@ -988,26 +1002,32 @@ __device__ void correction_loop(const Ctx& cx, const AttnParams& p, int wq, int 
     const ItemRec r = s.r;
     const int kvh = s.kvh;
     if (r.n_tiles > 0) {
-      if (p.rotary) {
-        // q row r of the tile takes the position of its own tree node's kv
-        // slot (the first cos/sin batch is fetched while the Q tile lands)
-        const int qb = qi & 1;
-        const long long qtok0 = (long long)r.kv_base + (r.kv - r.qo) + (long long)r.t * R;
-        const RopeRange rr = rope_range<D>(r.nq, g, wq);
-        float4 cv[2][4];
-        rope_load<D>(cv, p.rope_cs, qtok0, rr, 0, lane);
-        if (!cx.warp_wait(B_Q_FULL + qb, (qi >> 1) & 1)) return;
-        rope_q_rows<D, BF16>(cx.smem + C::kOffQ + qb * C::kQBytes, p.rope_cs, qtok0, rr, g, lane,
-                             cv);
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&cx.bar[B_Q_READY + qb]);
+#pragma unroll 1
+      for (int x = 0; x < 2; ++x) {
+        if (tile_count(r, x) == 0) continue;
+        if (p.rotary) {
+          // q row r of the tile takes the position of its own tree node's kv
+          // slot (the first cos/sin batch is fetched while the Q tile lands)
+          const long long qtok0 =
+              (long long)r.kv_base + (r.kv - r.qo) + (long long)r.r0 + (long long)x * R;
+          const RopeRange rr = rope_range<D>(tile_rows(r, x, R), g, wq);
+          float4 cv[2][4];
+          rope_load<D>(cv, p.rope_cs, qtok0, rr, 0, lane);
+          if (!cx.warp_wait(B_Q_FULL + x, (qi >> x) & 1)) return;
+          rope_q_rows<D, BF16>(cx.smem + C::kOffQ + x * C::kQBytes, p.rope_cs, qtok0, rr, g,
+                               lane, cv);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&cx.bar[B_Q_READY + x]);
+        }
+        qi ^= 1u << x;
       }
-      ++qi;
     }
     if (pend && !finish_pending()) return;
     if (r.n_tiles == 0) {
-      store_item<D, BF16>(cx, p, r, kvh, wq, lane, false, 0, -INFINITY, 0.f);
+#pragma unroll 1
+      for (int x = 0; x < 2; ++x)
+        store_tile<D, BF16>(cx, p, r, x, kvh, wq, lane, false, -INFINITY, 0.f);
       __syncwarp();
       if (lane == 0) mbar_arrive(&cx.bar[B_ITEM_EMPTY + slot]);
     } else {
@@ -1015,9 +1035,9 @@ __device__ void correction_loop(const Ctx& cx, const AttnParams& p, int wq, int 
       pend_slot = slot;
       pend_r = r;
       pend_kvh = kvh;
-      pend_ob = oi & 1;
-      pend_par = (oi >> 1) & 1;
-      ++oi;
+      pend_has = (r.n_a > 0 ? 1u : 0u) | (r.n_b > 0 ? 2u : 0u);
+      pend_par = oi;
+      oi ^= pend_has;
     }
     ++it;
   }
@@ -1054,22 +1074,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* bar = cx.bar;
     for (int i = 0; i < kSlots; ++i) {
       mbar_init(&bar[B_ITEM_FULL + i], 1);
-      // MMA thread, V producer, softmax and correction warps
-      mbar_init(&bar[B_ITEM_EMPTY + i], 1 + 1 + 4 + 4);
+      // MMA thread, V producer, two softmax warpgroups and the correction warps
+      mbar_init(&bar[B_ITEM_EMPTY + i], 1 + 1 + 8 + 4);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bar[B_Q_FULL + i], 1);
       mbar_init(&bar[B_Q_READY + i], 4);
       mbar_init(&bar[B_Q_EMPTY + i], 1);
-      mbar_init(&bar[B_K_FULL + i], 1);
-      mbar_init(&bar[B_V_FULL + i], 1);
-      mbar_init(&bar[B_EX_FULL + i], 1);
       mbar_init(&bar[B_S_FULL + i], 1);
       mbar_init(&bar[B_P_FULL + i], 4);
-      mbar_init(&bar[B_PV_DONE + i], 1);
       mbar_init(&bar[B_O_FULL + i], 1);
       mbar_init(&bar[B_O_FREE + i], 4);
       mbar_init(&bar[B_ML_FULL + i], 4);
+    }
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(&bar[B_K_FULL + i], 1);
+      mbar_init(&bar[B_V_FULL + i], 1);
+      mbar_init(&bar[B_EX_FULL + i], 1);
+      mbar_init(&bar[B_K_EMPTY + i], 1);
+      mbar_init(&bar[B_V_EMPTY + i], 1);
     }
     mbar_init(&bar[B_DRAIN], 1);
     mbar_init(&bar[B_STALL], 1);
@@ -1105,9 +1128,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp < kWarpCorrection) {
     regs_inc<kRegsSoftmax>();
-    run_softmax<D, BF16, PAGED>(cx, p, warp & 3, lane);
+    run_softmax<D, BF16, PAGED>(cx, p, (warp - kWarpSoftmax) >> 2, warp & 3, lane);
   } else {
-    regs_dec<kRegsCorrection>();
+    regs_inc<kRegsCorrection>();
     run_correction<D, BF16>(cx, p, warp & 3, lane);
   }
   __syncwarp();

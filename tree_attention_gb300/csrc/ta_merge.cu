@@ -154,10 +154,12 @@ __device__ __forceinline__ void merge_row_few(int n, LseOf lse_of, OOf o_of, uin
 }
 
 // Split-KV merge: a unit is 8 packed rows of one (pair, kv head), one row per
-// warp (packed row = q row * g + head in the group, the row order of the
-// attention kernel's tiles).
+// warp.  A pair's partial states hold its two Q tiles' 128 packed rows each
+// (packed row = q row in the tile * g + head in the group, the row order of
+// the attention kernel's tiles), tile A's first.
 constexpr int kMergeRowsPerUnit = kMergeThreads / 32;
-constexpr int kMergeUnitsPerItem = kBlockM / kMergeRowsPerUnit;
+constexpr int kMergeRowsPerItem = kTilesPerUnit * kBlockM;
+constexpr int kMergeUnitsPerItem = kMergeRowsPerItem / kMergeRowsPerUnit;
 static_assert(kMaxChunks <= 32, "one lane per chunk's lse");
 
 template <int D, bool BF16>
@@ -168,7 +170,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeParams 
   const unsigned int np = *(volatile const unsigned int*)&p.hdr->num_pairs;
   const long long n_pairs = (long long)np < p.max_pairs ? (long long)np : p.max_pairs;
   const long long units = n_pairs * p.h_kv * kMergeUnitsPerItem;
-  const int g = p.g;
+  const int g = p.g, R = kBlockM / p.g;
   uint16_t* outp = static_cast<uint16_t*>(p.out);
   for (long long u = blockIdx.x; u < units; u += gridDim.x) {
     const int part8 = (int)(u % kMergeUnitsPerItem);
@@ -178,10 +180,14 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeParams 
     if (mr.z <= 1 || mr.z > kMaxChunks || mr.w < 0 || (long long)mr.w + mr.z > p.max_records)
       continue;
     const int pr = part8 * kMergeRowsPerUnit + warp;
-    if (pr >= mr.y * g) continue;
-    const int qr = pr / g, hh = pr - qr * g;
+    const int tile = pr / kBlockM, local = pr % kBlockM;
+    if (local >= R * g) continue;
+    const int qr = tile * R + local / g, hh = local % g;
+    if (qr >= mr.y) continue;
     const size_t orow = (size_t)(mr.x + qr) * p.h_q + (size_t)kvh * g + hh;
-    auto slot = [&](int c) { return (((size_t)(mr.w + c)) * p.h_kv + kvh) * kBlockM + pr; };
+    auto slot = [&](int c) {
+      return (((size_t)(mr.w + c)) * p.h_kv + kvh) * kMergeRowsPerItem + pr;
+    };
     merge_row_few<D, BF16, kMaxChunks>(
         mr.z, [&](int c) { return __ldg(p.part_lse + slot(c)); },
         [&](int c) { return load_f32<D>(p.part_o + slot(c) * D, lane); }, outp + orow * D,

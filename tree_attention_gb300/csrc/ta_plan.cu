@@ -2,15 +2,17 @@
 // mask export used by tests.
 //
 // One launch of the plan kernel, every CTA:
-//   1. walks the (sequence, q tile) pairs of the ragged batch (the
+//   1. walks the (sequence, unit) pairs of the ragged batch -- a unit is two
+//      consecutive Q tiles of 128 packed rows each (the
 //      ``advance_tile_batch`` walk of the page "_kernel_common.py", done once
 //      up front), validating the index arrays, and places its own pair in the
 //      longest-first (LPT) order of the attention kernel's work queue by an
 //      estimated cost -- no global barrier, no serial tail;
 //   2. (all warps) classifies every kv tile of its pair as EMPTY / PARTIAL /
-//      FULL exactly from the DFS intervals of ``_check_tree_order`` (page
-//      "tree_attn.py") and writes the pair's item record -- with split-KV, one
-//      record per chunk of the pair's kv tiles plus the pair's merge record;
+//      FULL for each of its two Q tiles, exactly, from the DFS intervals of
+//      ``_check_tree_order`` (page "tree_attn.py") and writes the pair's item
+//      record -- with split-KV, one record per chunk of the pair's kv tiles
+//      plus the pair's merge record;
 //   3. for the one-call entry points, (the CTAs without a pair first) the
 //      run's key rotation: every kv token's RoPE cos/sin and rotated keys.
 #include <cuda_runtime.h>
@@ -26,8 +28,8 @@ namespace ta {
 namespace {
 
 constexpr int kPlanThreads = 256;
-constexpr int kGroup = 128;  // threads per warp group
-constexpr int kBarA = 1;
+constexpr int kGroup = 128;  // threads per warp group (one group per Q tile of a unit)
+constexpr int kBarA = 1;     // named barriers kBarA (tile A's group), kBarA + 1 (tile B's)
 constexpr int kPassTiles = 256;  // kv tiles classified per pass
 
 __device__ __forceinline__ void group_sync(int id) {
@@ -113,12 +115,12 @@ __device__ __forceinline__ long long seg_bytes(int kv) {
   return ((kv + kBlockN - 1) / kBlockN + 15) / 16 * 16;
 }
 
-// Estimated cost of q tile t of a sequence, in kv tiles, for the
-// longest-first order: the kv tiles up to the tile's last row's own slot
-// (exact for trees whose nodes come after their parents, as in a causal
+// Estimated cost of unit t of a sequence (units of U q rows), in kv tiles,
+// for the longest-first order: the kv tiles up to the unit's last row's own
+// slot (exact for trees whose nodes come after their parents, as in a causal
 // prefix; only the order and the split of the work depend on it).
-__device__ __forceinline__ int pair_tiles(int qo, int kv, int R, int t) {
-  const long long end = (long long)kv - max(0LL, (long long)qo - (long long)(t + 1) * R);
+__device__ __forceinline__ int pair_tiles(int qo, int kv, int U, int t) {
+  const long long end = (long long)kv - max(0LL, (long long)qo - (long long)(t + 1) * U);
   return (int)((end + kBlockN - 1) / kBlockN);
 }
 
@@ -216,23 +218,23 @@ __device__ __noinline__ void rope_tokens(const uint32_t* k, uint32_t* krot, cons
 
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanParams p) {
   __shared__ long long s_scan_a[9], s_scan_b[9];
-  __shared__ int s_keys[kBlockM];
+  __shared__ int s_keys[kTilesPerUnit * kBlockM];   // sorted enter keys: tile A, tile B
   __shared__ int s_pair_b, s_pair_t, s_pair_cost, s_pair_chunks;
   __shared__ long long s_total_cost;
   __shared__ int s_last;
-  __shared__ int s_ccount[kMaxChunks];
+  __shared__ int s_ccount[kMaxChunks], s_ccount_a[kMaxChunks], s_ccount_b[kMaxChunks];
   __shared__ long long s_pair_off;
   __shared__ int s_bad, s_rank;
-  __shared__ int s_any[kPassTiles], s_notall[kPassTiles];
-  __shared__ uint32_t s_cls2[3];
-  __shared__ int s_count;
+  __shared__ int s_any[kTilesPerUnit][kPassTiles], s_notall[kTilesPerUnit][kPassTiles];
+  __shared__ uint32_t s_cls;
+  __shared__ int s_count, s_count_a, s_count_b;
   __shared__ int s_hist[kCostBuckets];
   __shared__ float4 s_sct[27];
 
   pdl_wait();
   pdl_trigger();
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int B = p.batch, R = p.R;
+  const int B = p.batch, R = p.R, U = kTilesPerUnit * p.R;   // q rows per Q tile / unit
   // ---- 0. constants and counters of this CTA
   for (int i = tid; i < kCostBuckets; i += kPlanThreads) s_hist[i] = 0;
   if (p.rot && tid < 27)
@@ -241,11 +243,17 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanParams p) 
   if (tid == 0) {
     s_bad = 0;
     s_count = 0;
+    s_count_a = 0;
+    s_count_b = 0;
     s_rank = 0;
     s_total_cost = 0;
     s_last = 0;
   }
-  if (tid < kMaxChunks) s_ccount[tid] = 0;
+  if (tid < kMaxChunks) {
+    s_ccount[tid] = 0;
+    s_ccount_a[tid] = 0;
+    s_ccount_b[tid] = 0;
+  }
   __syncthreads();
   // the ends of the index arrays, read by the last thread alongside the
   // sequences' entries below (one round trip for both)
@@ -273,11 +281,11 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanParams p) 
       bad = 1;
       continue;
     }
-    const int tiles = (qo + R - 1) / R;
+    const int tiles = (qo + U - 1) / U;
     my_tiles += tiles;
     my_seg += (long long)tiles * seg_bytes(kv);
     for (int t = 0; t < tiles; ++t) {
-      const int c = pair_tiles(qo, kv, R, t);
+      const int c = pair_tiles(qo, kv, U, t);
       if (split)
         my_cost += c;
       else
@@ -302,9 +310,9 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanParams p) 
       const int kv = seq_kv_len(p, b);
       const int tl = p.mn_indptr[b + 1] - p.mn_indptr[b];
       if (qo < 0 || tl < qo || kv < tl || seq_pages_bad(p, b)) continue;
-      const int tiles = (qo + R - 1) / R;
+      const int tiles = (qo + U - 1) / U;
       for (int t = 0; t < tiles; ++t) {
-        const int c = pair_tiles(qo, kv, R, t);
+        const int c = pair_tiles(qo, kv, U, t);
         const int nch = pair_chunks(c, chunk_tiles, p.max_chunks);
         atomicAdd(&s_hist[record_bucket(c, nch)], nch);
       }
@@ -345,13 +353,13 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanParams p) 
     for (int b = b_lo; b < b_hi; ++b) {
       const int qo = p.q_indptr[b + 1] - p.q_indptr[b];
       const int kv = seq_kv_len(p, b);
-      const long long tiles = (qo + R - 1) / R;
+      const long long tiles = (qo + U - 1) / U;
       if (pair < tcum + tiles) {
         const int t = (int)(pair - tcum);
         s_pair_b = b;
         s_pair_t = t;
         s_pair_off = scum + (long long)t * seg_bytes(kv);
-        const int c = pair_tiles(qo, kv, R, t);
+        const int c = pair_tiles(qo, kv, U, t);
         const int nch = pair_chunks(c, chunk_tiles, p.max_chunks);
         s_pair_chunks = nch;
         s_pair_cost = record_bucket(c, nch);
@@ -364,16 +372,21 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanParams p) 
   __syncthreads();
   const bool has_pair = ok && pair < total_tiles;
   // the pair's q rows' enter indices, loaded now so that the round trip
-  // overlaps the ranking below
-  int key = INT_MAX, nrows = 0;
+  // overlaps the ranking below: threads 0-127 take tile A's rows, threads
+  // 128-255 tile B's
+  int key = INT_MAX, nrows = 0, n_a = 0, n_b = 0;
   if (has_pair) {
     const int b = s_pair_b;
     const int qo = p.q_indptr[b + 1] - p.q_indptr[b];
     const int tree_base = p.mn_indptr[b];
     const int tl = p.mn_indptr[b + 1] - tree_base;
-    const int r0 = s_pair_t * R;
-    nrows = min(R, qo - r0);
-    if (tid < nrows) key = p.tree_order[2 * (tree_base + r0 + tid + tl - qo)];
+    const int r0 = s_pair_t * U;
+    nrows = min(U, qo - r0);
+    n_a = min(R, nrows);
+    n_b = nrows - n_a;
+    const int grp = tid / kGroup, lt = tid % kGroup;
+    if (lt < (grp ? n_b : n_a))
+      key = p.tree_order[2 * (tree_base + r0 + grp * R + lt + tl - qo)];
   }
   if (has_pair) {
     // records of the same bucket that come earlier in (sequence, q tile) order
@@ -382,10 +395,10 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanParams p) 
     for (int b = b_lo; b < min(b_hi, pb + 1); ++b) {
       const int qo = p.q_indptr[b + 1] - p.q_indptr[b];
       const int kv = seq_kv_len(p, b);
-      const int tiles = (qo + R - 1) / R;
+      const int tiles = (qo + U - 1) / U;
       const int t_end = b < pb ? tiles : pt;
       for (int t = 0; t < t_end; ++t) {
-        const int c = pair_tiles(qo, kv, R, t);
+        const int c = pair_tiles(qo, kv, U, t);
         const int nch = pair_chunks(c, chunk_tiles, p.max_chunks);
         cnt += record_bucket(c, nch) == pc ? nch : 0;
       }
@@ -394,8 +407,9 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanParams p) 
   }
   __syncthreads();
 
-  // ---- 4. classify the pair's kv tiles (warps 0-3 sort the rows' keys,
-  // then all warps take the columns) and write its record
+  // ---- 4. classify the pair's kv tiles for both Q tiles (warps 0-3 sort
+  // tile A's keys, warps 4-7 tile B's, then all warps take the columns) and
+  // write its record
   if (has_pair) {
     const int b = s_pair_b, t = s_pair_t;
     const long long off = s_pair_off;
@@ -407,49 +421,56 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanParams p) 
     const int tree_base = p.mn_indptr[b];
     const int tl = p.mn_indptr[b + 1] - tree_base;
     const int ts = kv - tl;
-    const int r0 = t * R;
+    const int r0 = t * U;
     // exact classification from the DFS intervals of ``_check_tree_order``
-    // (page "tree_attn.py"): the rows' enter indices are sorted (bitonic, one
-    // key per thread); a kv column is seen by some row iff the first key not
-    // below its enter index is below its exit index, and by every row iff
-    // its interval holds the smallest and the largest key
-    if (tid >= kGroup) {
-      // warps 4-7 wait for the sorted keys below
-    } else if (nrows <= 32) {
-      // one warp, shuffles only
-      if (tid < 32) {
-        int x = key;
-        for (int k = 2; k <= 32; k <<= 1) {
-          for (int j = k >> 1; j > 0; j >>= 1) {
-            const int y = __shfl_xor_sync(0xffffffffu, x, j);
-            const bool keep_min = ((tid & j) == 0) == ((tid & k) == 0);
-            x = keep_min ? min(x, y) : max(x, y);
-          }
-        }
-        s_keys[tid] = x;
-      }
-      group_sync(kBarA);
-    } else {
-      s_keys[tid] = key;
-      group_sync(kBarA);
-      for (int k = 2; k <= kBlockM; k <<= 1) {
-        for (int j = k >> 1; j > 0; j >>= 1) {
-          const int ixj = tid ^ j;
-          if (ixj > tid) {
-            const int a = s_keys[tid], c = s_keys[ixj];
-            const bool up = (tid & k) == 0;
-            if ((a > c) == up) {
-              s_keys[tid] = c;
-              s_keys[ixj] = a;
+    // (page "tree_attn.py"), for each Q tile of the unit: its rows' enter
+    // indices are sorted (warps 0-3 tile A's, warps 4-7 tile B's: bitonic,
+    // one key per thread); a kv column is seen by some row of a tile iff the
+    // first key not below its enter index is below its exit index, and by
+    // every row iff its interval holds the smallest and the largest key
+    {
+      const int grp = tid / kGroup, lt = tid % kGroup;
+      const int ng = grp ? n_b : n_a;
+      int* keys = s_keys + grp * kBlockM;
+      if (ng <= 32) {
+        // one warp, shuffles only
+        if (lt < 32) {
+          int x = key;
+          for (int k = 2; k <= 32; k <<= 1) {
+            for (int j = k >> 1; j > 0; j >>= 1) {
+              const int y = __shfl_xor_sync(0xffffffffu, x, j);
+              const bool keep_min = ((lt & j) == 0) == ((lt & k) == 0);
+              x = keep_min ? min(x, y) : max(x, y);
             }
           }
-          group_sync(kBarA);
+          keys[lt] = x;
+        }
+        group_sync(kBarA + grp);
+      } else {
+        keys[lt] = key;
+        group_sync(kBarA + grp);
+        for (int k = 2; k <= kBlockM; k <<= 1) {
+          for (int j = k >> 1; j > 0; j >>= 1) {
+            const int ixj = lt ^ j;
+            if (ixj > lt) {
+              const int a = keys[lt], c = keys[ixj];
+              const bool up = (lt & k) == 0;
+              if ((a > c) == up) {
+                keys[lt] = c;
+                keys[ixj] = a;
+              }
+            }
+            group_sync(kBarA + grp);
+          }
         }
       }
     }
-    if (tid < 3) s_cls2[tid] = 0;
+    if (tid == 0) s_cls = 0;
     __syncthreads();
-    const int kmin = s_keys[0], kmax = s_keys[nrows - 1];
+    const int* keys_a = s_keys;
+    const int* keys_b = s_keys + kBlockM;
+    const int kmin_a = keys_a[0], kmax_a = keys_a[n_a - 1];
+    const int kmin_b = n_b > 0 ? keys_b[0] : 0, kmax_b = n_b > 0 ? keys_b[n_b - 1] : 0;
     const int kvt = (kv + kBlockN - 1) / kBlockN;
     // tiles wholly inside the causal prefix are FULL for every row (a pair
     // has at least one row, and such a tile ends at or before the tree
@@ -460,8 +481,10 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanParams p) 
     for (int j0 = 0; j0 < kvt; j0 += kPassTiles) {
       const int nt = min(kPassTiles, kvt - j0);
       for (int i = tid; i < nt; i += kPlanThreads) {
-        s_any[i] = 0;
-        s_notall[i] = 0;
+        s_any[0][i] = 0;
+        s_notall[0][i] = 0;
+        s_any[1][i] = 0;
+        s_notall[1][i] = 0;
       }
       __syncthreads();
       const int c_end = min(kv, (j0 + nt) * kBlockN);
@@ -482,31 +505,44 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanParams p) 
           const int c = c0 + u * kPlanThreads;
           if (c >= c_end) break;
           // prefix columns (of the tile that holds the tree start) are seen by every row
-          bool any = true, all = true;
+          bool any_a = true, all_a = true, any_b = n_b > 0, all_b = true;
           if (c >= ts) {
-            const int lo = lower_bound(s_keys, nrows, iv[u].x);
-            any = lo < nrows && s_keys[lo] < iv[u].y;
-            all = iv[u].x <= kmin && kmax < iv[u].y;
+            const int lo = lower_bound(keys_a, n_a, iv[u].x);
+            any_a = lo < n_a && keys_a[lo] < iv[u].y;
+            all_a = iv[u].x <= kmin_a && kmax_a < iv[u].y;
+            if (n_b > 0) {
+              const int lb = lower_bound(keys_b, n_b, iv[u].x);
+              any_b = lb < n_b && keys_b[lb] < iv[u].y;
+              all_b = iv[u].x <= kmin_b && kmax_b < iv[u].y;
+            }
           }
           const int jt = c / kBlockN - j0;
-          if (any && !s_any[jt]) s_any[jt] = 1;
-          if (!all && !s_notall[jt]) s_notall[jt] = 1;
+          if (any_a && !s_any[0][jt]) s_any[0][jt] = 1;
+          if (!all_a && !s_notall[0][jt]) s_notall[0][jt] = 1;
+          if (any_b && !s_any[1][jt]) s_any[1][jt] = 1;
+          if (!all_b && !s_notall[1][jt]) s_notall[1][jt] = 1;
         }
       }
       __syncthreads();
       for (int i = tid; i < nt; i += kPlanThreads) {
         const int j = j0 + i;
         const bool ragged = (j + 1) * kBlockN > kv;
-        const uint8_t cls =
-            j < prefix_tiles
-                ? kTileFull
-                : (!s_any[i] ? kTileEmpty : ((!s_notall[i] && !ragged) ? kTileFull : kTilePartial));
+        auto tile_cls = [&](int x) -> uint8_t {
+          if (x == 1 && n_b == 0) return kTileEmpty;
+          if (j < prefix_tiles) return kTileFull;
+          if (!s_any[x][i]) return kTileEmpty;
+          return (!s_notall[x][i] && !ragged) ? kTileFull : kTilePartial;
+        };
+        const uint8_t cls_a = tile_cls(0), cls_b = tile_cls(1);
+        const uint8_t cls = (uint8_t)(cls_a | (cls_b << 2));
         p.classes[off + j] = cls;
         if (cls != kTileEmpty) {
           atomicAdd(&s_count, 1);
           if (split) atomicMax(&s_last, j + 1);
         }
-        if (kvt <= kInlineTiles) atomicOr(&s_cls2[j >> 4], (uint32_t)cls << (2 * (j & 15)));
+        if (cls_a != kTileEmpty) atomicAdd(&s_count_a, 1);
+        if (cls_b != kTileEmpty) atomicAdd(&s_count_b, 1);
+        if (kvt <= kInlineTiles) atomicOr(&s_cls, (uint32_t)cls << (4 * j));
       }
       __syncthreads();
     }
@@ -517,17 +553,20 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanParams p) 
     const int last = s_last;
     if (nch > 1) {
       for (int j = tid; j < last; j += kPlanThreads) {
-        if (p.classes[off + j] == kTileEmpty) continue;
+        const int cls = p.classes[off + j];
+        if (cls == kTileEmpty) continue;
         int c = 0;
         while (c + 1 < nch && j >= (int)((long long)last * (c + 1) / nch)) ++c;
         atomicAdd(&s_ccount[c], 1);
+        if (cls & 3) atomicAdd(&s_ccount_a[c], 1);
+        if (cls >> 2) atomicAdd(&s_ccount_b[c], 1);
       }
       __syncthreads();
     }
     if (tid < nch) {
       ItemRec r;
       r.part = nch > 1 ? (int32_t)(pos + tid) : -1;
-      r.t = t;
+      r.r0 = r0;
       r.q_row0 = q0 + r0;
       r.nq = nrows;
       r.qo = qo;
@@ -539,9 +578,9 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanParams p) 
       r.n_tiles = nch > 1 ? s_ccount[tid] : s_count;
       r.class_off = (int32_t)off;
       r.kvt = kvt;
-      r.cls2[0] = s_cls2[0];
-      r.cls2[1] = s_cls2[1];
-      r.cls2[2] = s_cls2[2];
+      r.n_a = nch > 1 ? s_ccount_a[tid] : s_count_a;
+      r.n_b = nch > 1 ? s_ccount_b[tid] : s_count_b;
+      r.cls = s_cls;
       p.sorted[pos + tid] = r;
     }
     if (tid == 0 && p.merge)
