@@ -33,6 +33,7 @@
 #include <cuda_runtime.h>
 
 #include <climits>
+#include <cstddef>
 #include <cstdint>
 #include <type_traits>
 
@@ -73,9 +74,10 @@ enum Bar : int {
   B_K_FULL = B_Q_EMPTY + 2,            // [kStages]
   B_V_FULL = B_K_FULL + kStages,       // [kStages]
   B_EX_FULL = B_V_FULL + kStages,      // [kStages] column intervals of a partial tile
-  B_K_EMPTY = B_EX_FULL + kStages,     // [kStages] both QK^T of the tile in the stage done
-  B_V_EMPTY = B_K_EMPTY + kStages,     // [kStages] both PV of the tile in the stage done
-  B_S_FULL = B_V_EMPTY + kStages,      // [2] score buffer of tile A / B written
+  // one commit per kv tile t on KV_DONE[t & 1], after its QK^Ts: it reports
+  // tile t's QK^Ts (its K stage free) and tile t - 1's PVs (its V stage free)
+  B_KV_DONE = B_EX_FULL + kStages,     // [kStages]
+  B_S_FULL = B_KV_DONE + kStages,      // [2] score buffer of tile A / B written
   B_P_FULL = B_S_FULL + 2,             // [2] P written over it
   B_O_FULL = B_P_FULL + 2,             // [2] the unit's last PV into O_A / O_B done
   B_O_FREE = B_O_FULL + 2,             // [2] correction read O_A / O_B and its (m, l)
@@ -197,6 +199,9 @@ __device__ __forceinline__ int tile_rows(const ItemRec& r, int x, int R) {
   return max(0, min(R, r.nq - x * R));
 }
 __device__ __forceinline__ int tile_count(const ItemRec& r, int x) { return x ? r.n_b : r.n_a; }
+static_assert(offsetof(ItemRec, q_row0) == 8 && offsetof(ItemRec, n_a) == 52 &&
+                  offsetof(ItemRec, n_b) == 56,
+              "record words read by the producer's Q prefetch");
 
 // ---------------------------------------------------------------------------
 // producer warps (lane 0 issues): warp 0 stages the units and loads their Q
@@ -306,8 +311,8 @@ __device__ void run_producer(const Ctx& cx, const CUtensorMap* tm_q, const CUten
         const int stage = kv_it % kStages;
         int ph[kPagesPerTile];
         if constexpr (PAGED) tile_pages(p, r, j, lane, ph);
-        // the K stage is free once both QK^T of the tile two back are done
-        if (!cx.warp_wait(B_K_EMPTY + stage, ((kv_it / kStages) & 1) ^ 1)) { aborted = true; break; }
+        // the K stage is free once the QK^Ts of the tile two back are done
+        if (!cx.warp_wait(B_KV_DONE + stage, ((kv_it / kStages) & 1) ^ 1)) { aborted = true; break; }
         if (lane == 0) {
           mbar_arrive_expect_tx(&cx.bar[B_K_FULL + stage], (uint32_t)C::kKVBytes);
           load_kv_tile<D, PAGED>(sK + stage * C::kKVBytes, tm_k, &cx.bar[B_K_FULL + stage], 0, kvh,
@@ -319,8 +324,24 @@ __device__ void run_producer(const Ctx& cx, const CUtensorMap* tm_q, const CUten
       if (aborted) break;
     }
     idx = __shfl_sync(0xffffffffu, nidx, 0);
-    if (idx < num_items && lane < 4)
-      rec_next = __ldg(reinterpret_cast<const int4*>(p.sorted + idx / p.h_kv) + lane);
+    if (idx < num_items) {
+      if (lane < 4) rec_next = __ldg(reinterpret_cast<const int4*>(p.sorted + idx / p.h_kv) + lane);
+      // warm L2 with the next unit's Q tiles while this unit's last kv tiles
+      // run: their loads wait for this unit's last QK^Ts, then hit L2.
+      // Record words: q_row0 = 2 (lane 0, .z), n_a / n_b = 13 / 14 (lane 3, .y / .z).
+      const int nq_row0 = __shfl_sync(0xffffffffu, rec_next.z, 0);
+      const int nn_a = __shfl_sync(0xffffffffu, rec_next.y, 3);
+      const int nn_b = __shfl_sync(0xffffffffu, rec_next.z, 3);
+      if (lane == 0) {
+        const int nkvh = (int)(idx % (unsigned)p.h_kv);
+#pragma unroll
+        for (int x = 0; x < 2; ++x)
+          if ((x ? nn_b : nn_a) > 0)
+#pragma unroll
+            for (int a = 0; a < C::kAtoms; ++a)
+              tma_prefetch_l2_3d(tm_q, a * 64, nkvh * g, nq_row0 + x * R);
+      }
+    }
     ++it;
   }
   if (aborted && lane == 0) {
@@ -363,8 +384,13 @@ __device__ void run_producer_v(const Ctx& cx, const CUtensorMap* tm_v, const Att
       const int stage = kv_it % kStages;
       int ph[kPagesPerTile];
       if constexpr (PAGED) tile_pages(p, r, j, lane, ph);
-      // the V stage is free once both PV of the tile two back are done
-      if (!cx.warp_wait(B_V_EMPTY + stage, ((kv_it / kStages) & 1) ^ 1)) { aborted = true; break; }
+      // the V stage is free once the PVs of the tile two back are done: the
+      // commit of the tile after it reports them
+      if (kv_it >= kStages &&
+          !cx.warp_wait(B_KV_DONE + ((kv_it - 1) & 1), ((kv_it - 1) >> 1) & 1)) {
+        aborted = true;
+        break;
+      }
       if (lane == 0) {
         mbar_arrive_expect_tx(&cx.bar[B_V_FULL + stage], (uint32_t)C::kKVBytes);
         load_kv_tile<D, PAGED>(sV + stage * C::kKVBytes, tm_v, &cx.bar[B_V_FULL + stage], 1, kvh,
@@ -447,15 +473,11 @@ __device__ void run_mma(const Ctx& cx, const AttnParams& p) {
     ++it;
     if (!valid) break;
     if (r.n_tiles == 0) continue;
-    const bool has0 = r.n_a > 0, has1 = r.n_b > 0;
-    if (has0) {
-      if (!cx.wait(q_bar + 0, qx & 1)) break;
-      qx ^= 1;
-    }
-    if (has1) {
-      if (!cx.wait(q_bar + 1, (qx >> 1) & 1)) break;
-      qx ^= 2;
-    }
+    // QK^Ts still to issue per Q tile in this unit (its Q buffer is released
+    // after the last); a tile's Q is waited for at its first QK^T
+    int left0 = r.n_a, left1 = r.n_b;
+    bool q_ok0 = false, q_ok1 = false;
+    uint32_t v_kc = 0xFFFFFFFFu;   // the kv tile whose V stage was last waited for
     // the PV each Q tile owes for its previous kv tile: valid kv columns
     // (bits 0-7; 0: none), K/V stage (bit 8), that stage's phase (bit 9)
     uint32_t pend0 = 0, pend1 = 0;
@@ -466,7 +488,11 @@ __device__ void run_mma(const Ctx& cx, const AttnParams& p) {
       bool& started = x ? started1 : started0;
       const int nv = (int)(pend & 0xFFu), stage = (int)((pend >> 8) & 1u);
       if (!cx.wait(B_P_FULL + x, (kp >> x) & 1)) return false;
-      if (!cx.wait(B_V_FULL + stage, (pend >> 9) & 1)) return false;
+      const uint32_t tile_kc = kc - 1;   // a pending PV belongs to the previous kv tile
+      if (v_kc != tile_kc) {
+        if (!cx.wait(B_V_FULL + stage, (pend >> 9) & 1)) return false;
+        v_kc = tile_kc;
+      }
       // O is free once the epilogue of the Q tile's previous unit read it
       if (!started && !cx.wait(B_O_FREE + x, ((ox >> x) & 1) ^ 1)) return false;
       tc_fence_after();
@@ -495,6 +521,12 @@ __device__ void run_mma(const Ctx& cx, const AttnParams& p) {
       uint32_t& pend = x ? pend1 : pend0;
       if (pend && !issue_pv(xc)) return false;
       if ((cls >> (2 * x)) & 3) {
+        bool& q_ok = x ? q_ok1 : q_ok0;
+        if (!q_ok) {
+          if (!cx.wait(q_bar + x, (qx >> x) & 1)) return false;
+          qx ^= 1u << x;
+          q_ok = true;
+        }
         if (!k_ready) {
           if (!cx.wait(B_K_FULL + stage, (kc >> 1) & 1)) return false;
           k_ready = true;
@@ -514,6 +546,8 @@ __device__ void run_mma(const Ctx& cx, const AttnParams& p) {
         umma_commit(&cx.bar[B_S_FULL + x]);
         issued_any = true;
         pend = (uint32_t)nvalid | ((uint32_t)stage << 8) | (((kc >> 1) & 1u) << 9);
+        int& left = x ? left1 : left0;
+        if (--left == 0) umma_commit(&cx.bar[B_Q_EMPTY + x]);   // the unit's last QK^T of this tile
       }
       return true;
     };
@@ -527,18 +561,12 @@ __device__ void run_mma(const Ctx& cx, const AttnParams& p) {
         ok = false;
         break;
       }
-      umma_commit(&cx.bar[B_K_EMPTY + stage]);                // the tile's QK^Ts are issued
-      if (n > 0) umma_commit(&cx.bar[B_V_EMPTY + (stage ^ 1)]); // and the previous tile's PVs
-      if (n == r.n_tiles - 1) {                                 // the unit's last QK^Ts
-        if (has0) umma_commit(&cx.bar[B_Q_EMPTY + 0]);
-        if (has1) umma_commit(&cx.bar[B_Q_EMPTY + 1]);
-      }
+      umma_commit(&cx.bar[B_KV_DONE + stage]);   // this tile's QK^Ts, the previous tile's PVs
       ++kc;
     }
     if (!ok) break;
     // the unit's last PVs; then its outputs are complete
     if ((pend0 && !issue_pv(X0{})) || (pend1 && !issue_pv(X1{}))) break;
-    umma_commit(&cx.bar[B_V_EMPTY + ((kc - 1) & 1)]);
     if (started0) umma_commit(&cx.bar[B_O_FULL + 0]);
     if (started1) umma_commit(&cx.bar[B_O_FULL + 1]);
   }
@@ -717,6 +745,25 @@ __device__ void softmax_loop(const Ctx& cx, const AttnParams& p, int x, int wq, 
             if (!((uint32_t)(e_row - e.z) < (uint32_t)e.w)) x[2 * i + 1] = -INFINITY;
           }
         }
+        // a row without a reference yet (its first visible columns, usually
+        // the unit's first tile) takes it from this chunk's max before any
+        // exponential: nothing before carries weight (l, O and this tile's P
+        // are 0), so the factor is 0
+        if (__any_sync(0xffffffffu, m_ref == -INFINITY)) {
+          float m4[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) m4[k] = x[k];
+#pragma unroll
+          for (int i = 4; i < 32; ++i) m4[i & 3] = fmaxf(m4[i & 3], x[i]);
+          const float tmax = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+          if (m_ref == -INFINITY && tmax > -INFINITY) {
+            m_ref = tmax;   // m_use was 0
+            alpha_t = 0.f;
+            lsum = 0.f;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) x[i] -= tmax;
+          }
+        }
         float p[32];
         float2 la = make_float2(0.f, 0.f), lb = make_float2(0.f, 0.f);
 #pragma unroll
@@ -729,24 +776,20 @@ __device__ void softmax_loop(const Ctx& cx, const AttnParams& p, int x, int wq, 
             la = fadd2(la, make_float2(p[2 * i], p[2 * i + 1]));
         }
         float csum = (la.x + la.y) + (lb.x + lb.y);
-        if (__any_sync(0xffffffffu, m_ref == -INFINITY || !(csum <= 256.f))) {
-          // the chunk's max: a row's first visible chunk always sets its
-          // reference (nothing before it carries weight: l, O and this
-          // tile's P are 0, so the factor is 0 rather than 2^-tmax, which
-          // may not be finite); otherwise the reference moves when the max
-          // exceeds it by more than 2^8
+        if (__any_sync(0xffffffffu, !(csum <= 256.f))) {
+          // some t may exceed 8: the chunk's max moves the reference of the
+          // rows whose max outgrew it by more than 2^8
           float m4[4];
 #pragma unroll
           for (int k = 0; k < 4; ++k) m4[k] = x[k];
 #pragma unroll
           for (int i = 4; i < 32; ++i) m4[i & 3] = fmaxf(m4[i & 3], x[i]);
           const float tmax = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
-          const bool first_vis = m_ref == -INFINITY && tmax > -INFINITY;
-          const bool mv = tmax > 8.f || first_vis;
+          const bool mv = tmax > 8.f;
           if (__any_sync(0xffffffffu, mv)) {
-            const float a = mv ? (first_vis ? 0.f : ex2_approx(-tmax)) : 1.f;
+            const float a = mv ? ex2_approx(-tmax) : 1.f;
             const float sh = mv ? tmax : 0.f;
-            if (mv) m_ref = m_use + tmax;
+            if (mv) m_ref += tmax;
             alpha_t *= a;
             lsum *= a;
             csum = 0.f;
@@ -1091,8 +1134,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bar[B_K_FULL + i], 1);
       mbar_init(&bar[B_V_FULL + i], 1);
       mbar_init(&bar[B_EX_FULL + i], 1);
-      mbar_init(&bar[B_K_EMPTY + i], 1);
-      mbar_init(&bar[B_V_EMPTY + i], 1);
+      mbar_init(&bar[B_KV_DONE + i], 1);
     }
     mbar_init(&bar[B_DRAIN], 1);
     mbar_init(&bar[B_STALL], 1);
