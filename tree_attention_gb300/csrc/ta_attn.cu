@@ -722,6 +722,9 @@ __device__ void softmax_loop(const Ctx& cx, const AttnParams& p, int x, int wq, 
       const int2* ivs = sEX + sb * kBlockN;
       float alpha_t = 1.f;   // product of this tile's reference moves
       float lsum = 0.f;
+      // some row of the warp has no reference yet (usually only in the
+      // unit's first tile)
+      bool need_ref = __any_sync(0xffffffffu, m_ref == -INFINITY);
 #pragma unroll 1
       for (int q = 0; q < nch; ++q) {
         float x[32];
@@ -749,7 +752,7 @@ __device__ void softmax_loop(const Ctx& cx, const AttnParams& p, int x, int wq, 
         // the unit's first tile) takes it from this chunk's max before any
         // exponential: nothing before carries weight (l, O and this tile's P
         // are 0), so the factor is 0
-        if (__any_sync(0xffffffffu, m_ref == -INFINITY)) {
+        if (need_ref && __any_sync(0xffffffffu, m_ref == -INFINITY)) {
           float m4[4];
 #pragma unroll
           for (int k = 0; k < 4; ++k) m4[k] = x[k];
@@ -764,16 +767,18 @@ __device__ void softmax_loop(const Ctx& cx, const AttnParams& p, int x, int wq, 
             for (int i = 0; i < 32; ++i) x[i] -= tmax;
           }
         }
-        float p[32];
+        // P, two per 32-bit word, for columns 16q .. 16q + 15 of the score
+        // buffer (read by the PV's k-steps 2q and 2q + 1)
+        uint32_t pk[16];
         float2 la = make_float2(0.f, 0.f), lb = make_float2(0.f, 0.f);
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          p[2 * i] = ex2_approx(x[2 * i]);
-          p[2 * i + 1] = ex2_approx(x[2 * i + 1]);
+          const float p0 = ex2_approx(x[2 * i]), p1 = ex2_approx(x[2 * i + 1]);
           if (i & 1)
-            lb = fadd2(lb, make_float2(p[2 * i], p[2 * i + 1]));
+            lb = fadd2(lb, make_float2(p0, p1));
           else
-            la = fadd2(la, make_float2(p[2 * i], p[2 * i + 1]));
+            la = fadd2(la, make_float2(p0, p1));
+          pk[i] = pack2<BF16>(p0, p1);
         }
         float csum = (la.x + la.y) + (lb.x + lb.y);
         if (__any_sync(0xffffffffu, !(csum <= 256.f))) {
@@ -794,9 +799,10 @@ __device__ void softmax_loop(const Ctx& cx, const AttnParams& p, int x, int wq, 
             lsum *= a;
             csum = 0.f;
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              p[i] = ex2_approx(x[i] - sh);
-              csum += p[i];
+            for (int i = 0; i < 16; ++i) {
+              const float p0 = ex2_approx(x[2 * i] - sh), p1 = ex2_approx(x[2 * i + 1] - sh);
+              csum += p0 + p1;
+              pk[i] = pack2<BF16>(p0, p1);
             }
             if (q > 0) {
               // this tile's P chunks already written: rescale them in TMEM
@@ -816,11 +822,6 @@ __device__ void softmax_loop(const Ctx& cx, const AttnParams& p, int x, int wq, 
           }
         }
         lsum += csum;
-        // P, two per 32-bit word, over columns 16q .. 16q + 15 of the score
-        // buffer (read by the PV's k-steps 2q and 2q + 1)
-        uint32_t pk[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) pk[i] = pack2<BF16>(p[2 * i], p[2 * i + 1]);
         tmem_st16(t_s + 16 * q, pk);
       }
       l = l * alpha_t + lsum;
