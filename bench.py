@@ -283,7 +283,7 @@ def _config_dict(w, l2_note):
     return d
 
 
-PER_CONFIG = ("spec-decode", "prefix+tree", "ragged-large", "degenerate")
+PER_CONFIG = ("spec-decode", "prefix+tree", "ragged-large", "degenerate", "long-prefix")
 
 
 def _roofline(nbytes, flops, seconds, peaks):
@@ -323,6 +323,7 @@ def measure_workload(ta, w, args, dev, stream, world, local, headline=False):
         d["lse"] = torch.empty(d["q"].shape[:2], dtype=torch.float32, device=dev)
         dims = ta.make_dims(d["q"], d["k"], d["q_indptr"], d["tree_order"], w.rotary_mode)
         d["ws"] = torch.zeros(ta.workspace_size(dims), dtype=torch.uint8, device=dev)
+        d["dims"] = dims
         sets.append(d)
 
     def step(d):
@@ -385,17 +386,22 @@ def measure_workload(ta, w, args, dev, stream, world, local, headline=False):
         clk = clocks.stop()
     run_ms = statistics.median(runs)
     ms_step = run_ms / K
-    # per-kernel split for the roofline
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
-    for i in range(K):
-        step_two_launch(sets[i % n_sets], evs[i])
-    torch.cuda.synchronize(dev)
-    attn_ms = statistics.median(e[1].elapsed_time(e[2]) for e in evs)
-    plan_ms = statistics.median(e[0].elapsed_time(e[1]) for e in evs)
+    # per-kernel split for the roofline (the plan / run entry points never
+    # split: when the one-call step splits the kv range by itself, the step
+    # time stands for the kernels)
+    split_cap = ta.auto_split_chunks(sets[0]["dims"])
+    attn_ms = plan_ms = None
+    if split_cap == 1:
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+        for i in range(K):
+            step_two_launch(sets[i % n_sets], evs[i])
+        torch.cuda.synchronize(dev)
+        attn_ms = statistics.median(e[1].elapsed_time(e[2]) for e in evs)
+        plan_ms = statistics.median(e[0].elapsed_time(e[1]) for e in evs)
     check_status("after timing")
 
     peaks, peak_src = measured_peaks()
-    roof = _roofline(nbytes, flops, attn_ms / 1e3, peaks)
+    roof = _roofline(nbytes, flops, (attn_ms if attn_ms is not None else ms_step) / 1e3, peaks)
     roof["traffic"] = recorded_traffic(w.name)
     roof["peak_source"] = peak_src
     step_roof = _roofline(nbytes, flops, ms_step / 1e3, peaks)
@@ -406,8 +412,10 @@ def measure_workload(ta, w, args, dev, stream, world, local, headline=False):
         "tokens_per_s": w.total_q / (ms_step / 1e3),
         "bound": roof["bound"], "frac": roof["frac"], "step_frac": step_roof["frac"],
         "attn_kernel_ms": attn_ms, "plan_kernel_ms": plan_ms, "traffic": roof["traffic"],
+        "auto_split_chunks": split_cap,
         "algorithmic_bytes": nbytes, "algorithmic_flops": flops,
-        "gpu_launches_per_step": 2 + (w.rotary_mode == 1 and not ta.folds_rotation(w.total_kv)),
+        "gpu_launches_per_step": (2 + (w.rotary_mode == 1 and not ta.folds_rotation(w.total_kv))
+                                  + (split_cap > 1)),
         "l2": l2_note,
     }
     if not headline:

@@ -74,9 +74,23 @@ typedef struct {
  * (tile classes, the cost-ordered work queue), a device status word and,
  * with RoPE, the cos/sin table of the kv tokens and the rotated k
  * (total_kv * h_kv * head_dim elements, rotated once per call instead of
- * once per q tile that reads it).  It depends on the dims only, so one
- * allocation serves every call with the same dims. */
+ * once per q tile that reads it), and when tree_attn splits the kv range
+ * (tree_attn_auto_split_chunks > 1) the split-KV partial states, as
+ * tree_attn_split_workspace_size(dims, that cap).  It depends on the dims and
+ * the current device's SM count only, so one allocation serves every call
+ * with the same dims on that kind of GPU. */
 size_t tree_attn_workspace_size(const ta_dims* dims);
+
+/* The split-KV chunk cap tree_attn uses for these dims on the current device
+ * (0 on invalid dims).  1: no split.  tree_attn splits when the work units
+ * (a unit is 2 q tiles of 128 / g rows of one sequence and kv head) number
+ * fewer than the SMs even at their lower bound ceil(total_q / (256 / g)) x
+ * h_kv, while the sequences average at least 2048 kv rows; the cap is then
+ * ceil(4 x SMs / ((ceil(total_q / (256 / g)) + batch_size) x h_kv)) clamped
+ * to 2..16 (about four work records per SM), and the plan picks the chunk
+ * length (chunk_tiles 0 of tree_attn_split).  A split result equals the
+ * unsplit one up to float32 rounding order (merge of base-2 LSE states). */
+int32_t tree_attn_auto_split_chunks(const ta_dims* dims);
 
 /* Batched tree attention.  Layouts (all row-major, contiguous, device):
  *   q               [total_q, h_q, head_dim]   dtype
@@ -110,7 +124,9 @@ size_t tree_attn_workspace_size(const ta_dims* dims);
  *                   next one.  Calls that may overlap on the GPU must use
  *                   distinct workspaces.
  * q, k, v and out must be 16-byte aligned.  Returns TA_OK once the work is
- * enqueued; device-side failures are reported by tree_attn_device_status. */
+ * enqueued; device-side failures are reported by tree_attn_device_status.
+ * When tree_attn_auto_split_chunks(dims) > 1 the call is tree_attn_split with
+ * that cap and chunk_tiles 0 (plan, attention and merge kernels). */
 ta_status tree_attn(const void* q, const int32_t* q_indptr, const void* k, const void* v,
                     const int32_t* kv_indptr, const int32_t* q_rope_position,
                     const int32_t* mn_indptr, const int32_t* tree_order, void* out,
@@ -118,8 +134,9 @@ ta_status tree_attn(const void* q, const int32_t* q_indptr, const void* k, const
                     float sm_scale, const ta_dims* dims, void* workspace,
                     size_t workspace_bytes, void* stream);
 
-/* The two launches of tree_attn, for callers that reuse one tree layout
- * across calls (every layer of a model verifies the same draft tree):
+/* The two launches of unsplit tree_attn (these never split the kv range), for
+ * callers that reuse one tree layout across calls (every layer of a model
+ * verifies the same draft tree):
  *   tree_attn_plan  enumerates the (sequence, q tile) work items, classifies
  *                   every (q tile, kv tile) pair as empty / partial / full
  *                   from the DFS intervals and orders the items
@@ -157,7 +174,9 @@ ta_status tree_attn_run(const void* q, const void* k, const void* v, const int32
  * uses a static device array of 32 MiB (held by every GPU that loads the
  * library until the process exits) as its workspace; it calls no cudaMalloc,
  * cudaFree or other allocating routine.
- *   - Problems whose tree_attn_workspace_size exceeds 32 MiB are rejected
+ *   - It never splits the kv range (tree_attn_split with max_chunks 1).
+ *   - Problems whose unsplit workspace (tree_attn_split_workspace_size(dims,
+ *     1)) exceeds 32 MiB are rejected
  *     with TA_ERR_UNSUPPORTED before anything is enqueued.
  *   - The first call on each device looks up the array's device address
  *     (cudaGetSymbolAddress); make that first call before any stream capture.

@@ -300,3 +300,23 @@ def test_wait_hooks_validate_and_reset(lib):
     assert lib.tree_attn_set_wait_hooks(0, 2) == ta.TA_ERR_INVALID_ARGUMENT
     assert lib.tree_attn_set_wait_hooks(1000, 1) == ta.TA_OK
     assert lib.tree_attn_set_wait_hooks(0, 0) == ta.TA_OK
+
+
+def test_auto_split_chunks(lib):
+    """The one-call entry point's split-KV choice is a host function of the
+    dims (and the device's SM count): invalid dims give 0, a batch with many
+    short work units never splits, and the workspace it asks for is the split
+    workspace at that cap."""
+    assert ta.auto_split_chunks(_dims(h_kv=3)) == 0          # h_q % h_kv != 0
+    small = _dims()
+    assert ta.auto_split_chunks(small) == 1
+    assert ta.workspace_size(small) == ta.split_workspace_size(small, 1)
+    # 4096 sequences of 64 q rows: at least 4096 x h_kv units, never split
+    many = _dims(batch_size=4096, total_q=4096 * 64, total_kv=4096 * 4096,
+                 total_tree=4096 * 64)
+    assert ta.auto_split_chunks(many) == 1
+    # a few long sequences: split on a GPU, unsplit (no device) otherwise
+    few = _dims(batch_size=4, total_q=256, total_kv=4 * 32832, total_tree=256)
+    cap = ta.auto_split_chunks(few)
+    assert 1 <= cap <= ta.MAX_CHUNKS
+    assert ta.workspace_size(few) == ta.split_workspace_size(few, cap)

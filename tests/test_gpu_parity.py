@@ -344,4 +344,10 @@ def test_plan_once_run_per_layer(idx):
                             w1.rope_scale, w1.rope_theta, w1.sm_scale)
     out1, lse1 = attn(**d1)
     assert ta.device_status(attn.workspace) == ta.TA_OK
-    assert torch.equal(out1, outs[0][0]) and torch.equal(lse1, outs[0][1])
+    if ta.auto_split_chunks(dims) == 1:
+        assert torch.equal(out1, outs[0][0]) and torch.equal(lse1, outs[0][1])
+    else:
+        # the one-call path split this batch of few long sequences: the same
+        # states merged, equal up to float32 rounding order
+        assert torch.allclose(lse1, outs[0][1], rtol=0, atol=1e-4)
+        assert torch.allclose(out1.float(), outs[0][0].float(), rtol=0, atol=1e-2)

@@ -71,11 +71,19 @@ def run_split(w, max_chunks, chunk_tiles, ws=None):
 
 
 def run_plain(w):
+    """The unsplit kernel: the plan / run entry points, which never split (the
+    one-call tree_attn may split long sequences by itself)."""
     d = wl.device_inputs(w)
-    attn = ta.TreeAttention(d["q"], d["k"], d["q_indptr"], d["tree_order"], w.rotary_mode,
-                            w.rope_scale, w.rope_theta, w.sm_scale)
-    out, lse = attn(**d)
-    assert ta.device_status(attn.workspace) == ta.TA_OK
+    dims = ta.make_dims(d["q"], d["k"], d["q_indptr"], d["tree_order"], w.rotary_mode)
+    ws = torch.zeros(ta.workspace_size(dims), dtype=torch.uint8, device="cuda")
+    out = torch.empty_like(d["q"])
+    lse = torch.empty(d["q"].shape[:2], dtype=torch.float32, device="cuda")
+    ta.plan(d["q"], d["q_indptr"], d["k"], d["kv_indptr"], d["q_rope_position"],
+            d["mn_indptr"], d["tree_order"], w.rotary_mode, w.rope_scale, w.rope_theta, ws)
+    ta.run(d["q"], d["k"], d["v"], d["q_indptr"], d["kv_indptr"], d["q_rope_position"],
+           d["mn_indptr"], d["tree_order"], out, lse, w.rotary_mode, w.rope_scale,
+           w.rope_theta, w.sm_scale, ws)
+    assert ta.device_status(ws) == ta.TA_OK
     return out, lse
 
 
@@ -154,6 +162,41 @@ def test_split_long_prefix_full_size():
                                 w.rope_theta, w.sm_scale, seqs=seqs)
     rows = np.concatenate([np.arange(w.q_indptr[b], w.q_indptr[b + 1]) for b in seqs])
     assert_parity(w, out, lse, ref, rows=rows)
+
+
+def test_one_call_splits_long_prefix_by_itself():
+    """tree_attn on the long-prefix workload (4 sequences, 32768-token
+    prefixes: 32 units for 8 kv heads, far fewer than the SMs) chooses
+    split-KV itself, matches the oracle on two of its four sequences, and
+    agrees with tree_attn_split at the same cap bit for bit."""
+    w = wl.long_prefix()
+    d = wl.device_inputs(w)
+    dims = ta.make_dims(d["q"], d["k"], d["q_indptr"], d["tree_order"], w.rotary_mode)
+    cap = ta.auto_split_chunks(dims)
+    assert cap > 1
+    assert ta.workspace_size(dims) == ta.split_workspace_size(dims, cap)
+    attn = ta.TreeAttention(d["q"], d["k"], d["q_indptr"], d["tree_order"], w.rotary_mode,
+                            w.rope_scale, w.rope_theta, w.sm_scale)
+    out, lse = attn(**d)
+    assert ta.device_status(attn.workspace) == ta.TA_OK
+    seqs = [1, 2]
+    ref = oracle.tree_attention(w.q, w.q_indptr, w.k, w.v, w.kv_indptr, w.rope_position,
+                                w.mn_indptr, w.tree_order, w.rotary_mode, w.rope_scale,
+                                w.rope_theta, w.sm_scale, seqs=seqs)
+    rows = np.concatenate([np.arange(w.q_indptr[b], w.q_indptr[b + 1]) for b in seqs])
+    assert_parity(w, out, lse, ref, rows=rows)
+    out_s, lse_s, _ = run_split(w, cap, 0)
+    assert torch.equal(out, out_s) and torch.equal(lse, lse_s)
+
+
+def test_one_call_does_not_split_the_benchmark_workloads():
+    """Configs 2-5 give every SM work without a split: tree_attn keeps them
+    in one pass."""
+    for idx in (2, 3, 4, 5):
+        w = wl.config(idx)
+        d = wl.device_inputs(w)
+        dims = ta.make_dims(d["q"], d["k"], d["q_indptr"], d["tree_order"], w.rotary_mode)
+        assert ta.auto_split_chunks(dims) == 1, w.name
 
 
 def test_split_bad_index_arrays_are_reported():

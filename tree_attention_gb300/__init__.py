@@ -27,7 +27,7 @@ __all__ = [
     "tree_attn", "plan", "run", "device_status", "status_string", "mask_dense", "check_inputs",
     "TreeAttention", "PagedDims", "make_paged_dims", "paged_workspace_size", "tree_attn_paged",
     "MAX_CHUNKS", "split_workspace_size", "tree_attn_split", "merge_states", "last_cuda_error",
-    "folds_rotation", "noalloc_device_status", "set_wait_hooks",
+    "folds_rotation", "noalloc_device_status", "set_wait_hooks", "auto_split_chunks",
 ]
 
 TA_OK = 0
@@ -121,6 +121,8 @@ def lib() -> ctypes.CDLL:
     L.tree_attn_paged.restype = ctypes.c_int
     L.tree_attn_split_workspace_size.argtypes = [ctypes.POINTER(Dims), ctypes.c_int32]
     L.tree_attn_split_workspace_size.restype = sz
+    L.tree_attn_auto_split_chunks.argtypes = [ctypes.POINTER(Dims)]
+    L.tree_attn_auto_split_chunks.restype = ctypes.c_int32
     L.tree_attn_split.argtypes = [vp, i32p, vp, vp, i32p, i32p, i32p, i32p, vp, vp,
                                   ctypes.c_int32, ctypes.c_float, ctypes.c_float, ctypes.c_float,
                                   ctypes.c_int32, ctypes.c_int32, ctypes.POINTER(Dims), vp, sz,
@@ -183,6 +185,12 @@ def make_dims(q: torch.Tensor, k: torch.Tensor, q_indptr: torch.Tensor,
 
 def workspace_size(dims: Dims) -> int:
     return int(lib().tree_attn_workspace_size(ctypes.byref(dims)))
+
+
+def auto_split_chunks(dims: Dims) -> int:
+    """The split-KV chunk cap ``tree_attn`` uses for ``dims`` on the current
+    device (1: no split; 0: invalid dims)."""
+    return int(lib().tree_attn_auto_split_chunks(ctypes.byref(dims)))
 
 
 def _check_dev(name: str, t: Optional[torch.Tensor], dtype=None):

@@ -97,6 +97,25 @@ size_t ws_size(const ta_dims* d, int max_chunks) {
   return L.total;
 }
 
+// Split-KV chunk cap of the one-call entry point for dims on a GPU of nsm
+// SMs.  1 (no split) unless the (sequence, unit) pairs times the kv heads
+// leave SMs without work while the sequences are long on average (at least
+// two chunks of the least automatic length each); then enough chunks for
+// about four work records per SM, 2 .. kMaxChunks.  The pair count is taken
+// from its lower bound ceil(total_q / U) and the workspace from its upper
+// bound (one more pair per sequence), so the choice depends on dims alone.
+int auto_max_chunks(const ta_dims* d, int nsm) {
+  if (!dims_valid(d) || nsm <= 0 || d->total_q == 0) return 1;
+  const int64_t U = ta::rows_per_unit(d->h_q / d->h_kv);
+  const int64_t pairs_lo = ta::ceil_div(d->total_q, U);
+  if (pairs_lo * d->h_kv >= nsm) return 1;
+  const int64_t long_kv = (int64_t)d->batch_size * 2 * ta::kMinChunkTiles * ta::kBlockN;
+  if ((int64_t)d->total_kv < long_kv) return 1;
+  const int64_t pairs_hi = pairs_lo + d->batch_size;
+  const int64_t c = ta::ceil_div(4LL * nsm, pairs_hi * d->h_kv);
+  return (int)std::min<int64_t>(ta::kMaxChunks, std::max<int64_t>(2, c));
+}
+
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
 // 3-D tensor map over [rows, heads, d] (d fastest) with a {64, box_heads,
@@ -143,7 +162,14 @@ bool make_pages_map(CUtensorMap* m, const void* base, ta_dtype dt, int num_pages
 
 extern "C" {
 
-size_t tree_attn_workspace_size(const ta_dims* dims) { return ws_size(dims, 1); }
+size_t tree_attn_workspace_size(const ta_dims* dims) {
+  return ws_size(dims, auto_max_chunks(dims, sm_count()));
+}
+
+int32_t tree_attn_auto_split_chunks(const ta_dims* dims) {
+  if (!dims_valid(dims)) return 0;
+  return auto_max_chunks(dims, sm_count());
+}
 
 size_t tree_attn_split_workspace_size(const ta_dims* dims, int32_t max_chunks) {
   return ws_size(dims, max_chunks);
@@ -433,23 +459,11 @@ ta_status tree_attn(const void* q, const int32_t* q_indptr, const void* k, const
                     const int32_t* mn_indptr, const int32_t* tree_order, void* out, float* lse,
                     int32_t rotary_mode, float rope_scale, float rope_theta, float sm_scale,
                     const ta_dims* dims, void* workspace, size_t workspace_bytes, void* stream) {
-  ta_status s = check_common(q_indptr, kv_indptr, mn_indptr, tree_order, rotary_mode, dims,
-                             workspace, workspace_bytes);
-  if (s != TA_OK) return s;
-  s = check_plan_args(q_rope_position, rotary_mode, rope_scale, rope_theta, dims);
-  if (s != TA_OK) return s;
-  s = check_run_args(q, k, v, out, lse, sm_scale, dims);
-  if (s != TA_OK) return s;
-  if (dims->total_q == 0) return TA_OK;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const RopeArgs ra{k, q_rope_position, rope_scale, rope_theta};
-  const bool rot = fold_rotation(dims, sm_count());
-  s = launch_plan_checked(q_indptr, kv_indptr, mn_indptr, tree_order, dims, workspace, st, 1, 0,
-                          rot ? &ra : nullptr);
-  if (s != TA_OK) return s;
-  return launch_run_checked(q, k, v, q_indptr, kv_indptr, q_rope_position, mn_indptr,
-                            tree_order, out, lse, rotary_mode, rope_scale, rope_theta,
-                            sm_scale, dims, workspace, st, 1, rot);
+  // few, long sequences go through split-KV (the plan picks the chunk length)
+  const int max_chunks = dims_valid(dims) ? auto_max_chunks(dims, sm_count()) : 1;
+  return tree_attn_split(q, q_indptr, k, v, kv_indptr, q_rope_position, mn_indptr, tree_order,
+                         out, lse, rotary_mode, rope_scale, rope_theta, sm_scale, max_chunks, 0,
+                         dims, workspace, workspace_bytes, stream);
 }
 
 ta_status tree_attn_split(const void* q, const int32_t* q_indptr, const void* k, const void* v,
@@ -631,7 +645,7 @@ ta_status tree_attn_noalloc(const void* q, const int32_t* q_indptr, const void* 
                             float* lse, int32_t rotary_mode, float rope_scale, float rope_theta,
                             float sm_scale, const ta_dims* dims, void* stream) {
   if (!dims_valid(dims)) return TA_ERR_INVALID_ARGUMENT;
-  const size_t need = tree_attn_workspace_size(dims);
+  const size_t need = ws_size(dims, 1);   // never split: the scratch stays small
   if (need == 0) return dims_supported(dims) != TA_OK ? TA_ERR_UNSUPPORTED : TA_ERR_INVALID_ARGUMENT;
   if (need > kNoAllocScratchBytes) return TA_ERR_UNSUPPORTED;  // problem too large for the scratch
   void* ws = noalloc_scratch_address();
@@ -643,9 +657,9 @@ ta_status tree_attn_noalloc(const void* q, const int32_t* q_indptr, const void* 
   cudaError_t e = cudaMemsetAsync(hdr, 0, 8, st);
   if (e == cudaSuccess) e = cudaMemsetAsync(hdr + 12, 0, sizeof(WsHeader) - 12, st);
   if (e != cudaSuccess) return cuda_status(e);
-  return tree_attn(q, q_indptr, k, v, kv_indptr, q_rope_position, mn_indptr, tree_order, out,
-                   lse, rotary_mode, rope_scale, rope_theta, sm_scale, dims, ws,
-                   kNoAllocScratchBytes, stream);
+  return tree_attn_split(q, q_indptr, k, v, kv_indptr, q_rope_position, mn_indptr, tree_order,
+                         out, lse, rotary_mode, rope_scale, rope_theta, sm_scale, 1, 0, dims, ws,
+                         kNoAllocScratchBytes, stream);
 }
 
 ta_status tree_attn_noalloc_device_status(void* stream) {
@@ -695,7 +709,7 @@ extern "C" {
 size_t tree_attn_paged_workspace_size(const ta_paged_dims* dims) {
   if (!paged_dims_valid(dims)) return 0;
   const ta_dims d = as_dims(dims);
-  return tree_attn_workspace_size(&d);
+  return ws_size(&d, 1);   // the paged kernel does not split
 }
 
 ta_status tree_attn_paged(const void* q, const int32_t* q_indptr, const void* pages,
@@ -714,7 +728,7 @@ ta_status tree_attn_paged(const void* q, const int32_t* q_indptr, const void* pa
   if (dims->nnz_pages > 0 && !page_values) return TA_ERR_INVALID_ARGUMENT;
   if (dims->total_tree > 0 && !tree_order) return TA_ERR_INVALID_ARGUMENT;
   if (!aligned(workspace, 256) || !aligned(pages, 16)) return TA_ERR_INVALID_ARGUMENT;
-  const size_t need = tree_attn_workspace_size(&d);
+  const size_t need = ws_size(&d, 1);
   if (need == 0) return TA_ERR_UNSUPPORTED;
   if (workspace_bytes < need) return TA_ERR_INVALID_ARGUMENT;
   if (dims->total_q > 0 && dims->nnz_pages == 0) return TA_ERR_INVALID_ARGUMENT;

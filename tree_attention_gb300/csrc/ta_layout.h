@@ -81,6 +81,10 @@ inline int rows_per_item(int g) { return kBlockM / g; }
 inline int rows_per_unit(int g) { return kTilesPerUnit * rows_per_item(g); }
 
 constexpr int kMaxChunks = 16;  // split-KV: chunks per (sequence, unit) at most
+// split-KV: the least kv tiles of a chunk when the chunk length is chosen
+// automatically (a chunk's fixed costs -- its Q tiles, its partial state
+// written and read back -- stay small against its kv tiles)
+constexpr int kMinChunkTiles = 8;
 
 struct WsLayout {
   int64_t max_pairs;    // upper bound on (sequence, unit) pairs

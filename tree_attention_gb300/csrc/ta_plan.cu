@@ -136,10 +136,7 @@ __device__ __forceinline__ int record_bucket(int tiles, int chunks) {
 }
 
 // Split-KV chunk size when the caller leaves it to the plan: about a quarter
-// of the per-pipeline share of the batch's work, at least kMinChunkTiles so
-// that a chunk's fixed costs (its Q tile, its partial state written and read
-// back) stay small against its kv tiles.
-constexpr int kMinChunkTiles = 8;
+// of the per-pipeline share of the batch's work, at least kMinChunkTiles.
 __device__ __forceinline__ int auto_chunk_tiles(long long total_tiles, int h_kv, int pipes) {
   const long long per = (total_tiles * h_kv + 4LL * pipes - 1) / (4LL * pipes);
   return (int)max((long long)kMinChunkTiles, min(per, (long long)INT_MAX));
