@@ -374,7 +374,8 @@ def measure_workload(ta, w, args, dev, stream, world, local, headline=False):
 
     repeats = max(1, args.repeats)
     clk = None
-    if headline:
+    sample_clocks = headline and not args.no_clocks
+    if sample_clocks:
         # enough repeats that the timed runs span about a second of clock samples
         probe = timed_run()
         repeats = max(repeats, min(400, math.ceil(1000.0 / max(probe, 1e-3))))
@@ -382,7 +383,7 @@ def measure_workload(ta, w, args, dev, stream, world, local, headline=False):
         clocks.start()
         time.sleep(0.3)
     runs = [timed_run() for _ in range(repeats)]
-    if headline:
+    if sample_clocks:
         clk = clocks.stop()
     run_ms = statistics.median(runs)
     ms_step = run_ms / K
@@ -803,6 +804,10 @@ def main(argv=None):
                     choices=list(WORKLOADS) + list(EXTRA_WORKLOADS))
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--sets", type=int, default=0, help="input/output buffer sets to rotate")
+    ap.add_argument("--no-clocks", action="store_true",
+                    help="no clock sampling (and no stretching of the timed runs to the "
+                         "sampler's second): for runs under a profiler, whose line is not a "
+                         "bench value")
     ap.add_argument("--repeats", type=int, default=5,
                     help="timed runs of --steps steps each; the median run is reported")
     ap.add_argument("--no-per-config", action="store_true",
