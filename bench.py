@@ -468,6 +468,7 @@ def run_gb300(args):
     dev = torch.device("cuda", local)
     ta_build.build()
     ta.lib()
+    ta.set_scheduler(1 if args.sched == "clc" else 0)
     stream = torch.cuda.current_stream(dev)
     w = make_workload(args.workload)
     head, extra = measure_workload(ta, w, args, dev, stream, world, local, headline=True)
@@ -506,7 +507,7 @@ def run_gb300(args):
         "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
         "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
-        "config": _config_dict(w, extra["l2_note"]),
+        "config": dict(_config_dict(w, extra["l2_note"]), scheduler=args.sched),
         "timing": (f"median of {head['runs']} runs of {K} steps (min {head['run_ms_min']:.4f}, "
                    f"max {head['run_ms_max']:.4f} ms per step), CUDA events on the launching "
                    f"stream, max over ranks"),
@@ -545,6 +546,7 @@ def run_gb300_paged(args):
     dev = torch.device("cuda", local)
     ta_build.build()
     ta.lib()
+    ta.set_scheduler(1 if args.sched == "clc" else 0)
     w = dataclasses.replace(make_workload(args.workload), rotary_mode=0)
     flops = wl.algorithmic_flops(w)
     nbytes = wl.algorithmic_bytes(w)
@@ -677,6 +679,7 @@ def run_gb300_split(args):
     dev = torch.device("cuda", local)
     ta_build.build()
     ta.lib()
+    ta.set_scheduler(1 if args.sched == "clc" else 0)
     w = make_workload(args.workload)
     flops = wl.algorithmic_flops(w)
     nbytes = wl.algorithmic_bytes(w)
@@ -804,6 +807,9 @@ def main(argv=None):
                     choices=list(WORKLOADS) + list(EXTRA_WORKLOADS))
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--sets", type=int, default=0, help="input/output buffer sets to rotate")
+    ap.add_argument("--sched", choices=("queue", "clc"), default="clc",
+                    help="attention work scheduling: cluster launch control over one CTA per "
+                         "work unit (default) or the atomic work queue over one CTA per SM")
     ap.add_argument("--no-clocks", action="store_true",
                     help="no clock sampling (and no stretching of the timed runs to the "
                          "sampler's second): for runs under a profiler, whose line is not a "

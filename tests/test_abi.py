@@ -320,3 +320,11 @@ def test_auto_split_chunks(lib):
     cap = ta.auto_split_chunks(few)
     assert 1 <= cap <= ta.MAX_CHUNKS
     assert ta.workspace_size(few) == ta.split_workspace_size(few, cap)
+
+
+def test_scheduler_setting_validates(lib):
+    """The scheduler choice is a host setting of the calling thread."""
+    assert lib.tree_attn_set_scheduler(2) == ta.TA_ERR_INVALID_ARGUMENT
+    assert lib.tree_attn_set_scheduler(-1) == ta.TA_ERR_INVALID_ARGUMENT
+    assert lib.tree_attn_set_scheduler(0) == ta.TA_OK
+    assert lib.tree_attn_set_scheduler(1) == ta.TA_OK   # the default again

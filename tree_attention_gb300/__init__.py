@@ -28,6 +28,7 @@ __all__ = [
     "TreeAttention", "PagedDims", "make_paged_dims", "paged_workspace_size", "tree_attn_paged",
     "MAX_CHUNKS", "split_workspace_size", "tree_attn_split", "merge_states", "last_cuda_error",
     "folds_rotation", "noalloc_device_status", "set_wait_hooks", "auto_split_chunks",
+    "set_scheduler",
 ]
 
 TA_OK = 0
@@ -121,6 +122,8 @@ def lib() -> ctypes.CDLL:
     L.tree_attn_paged.restype = ctypes.c_int
     L.tree_attn_split_workspace_size.argtypes = [ctypes.POINTER(Dims), ctypes.c_int32]
     L.tree_attn_split_workspace_size.restype = sz
+    L.tree_attn_set_scheduler.argtypes = [ctypes.c_int32]
+    L.tree_attn_set_scheduler.restype = ctypes.c_int
     L.tree_attn_auto_split_chunks.argtypes = [ctypes.POINTER(Dims)]
     L.tree_attn_auto_split_chunks.restype = ctypes.c_int32
     L.tree_attn_split.argtypes = [vp, i32p, vp, vp, i32p, i32p, i32p, i32p, vp, vp,
@@ -384,6 +387,14 @@ def set_wait_hooks(wait_limit_ns: int = 0, stall: bool = False) -> None:
     st = lib().tree_attn_set_wait_hooks(int(wait_limit_ns), 1 if stall else 0)
     if st != TA_OK:
         raise TreeAttnError(st, "tree_attn_set_wait_hooks")
+
+
+def set_scheduler(mode: int) -> None:
+    """Work scheduling of later calls' attention kernels on this thread: 0
+    the atomic work queue, 1 cluster launch control (default)."""
+    st = lib().tree_attn_set_scheduler(int(mode))
+    if st != TA_OK:
+        raise TreeAttnError(st, "tree_attn_set_scheduler")
 
 
 def mask_dense(q_indptr, kv_indptr, mn_indptr, tree_order, total_q: int, max_kv: int,

@@ -33,6 +33,19 @@ thread_local int g_stall = 0;
 
 unsigned long long wait_limit_ns() { return g_wait_limit_ns ? g_wait_limit_ns : kDeviceWaitLimitNs; }
 
+// Work scheduling of the attention kernels the calling thread launches
+// (tree_attn_set_scheduler): 0 the atomic work queue over one CTA per SM,
+// 1 (default) cluster launch control over one CTA per work unit.
+thread_local int g_sched = 1;
+
+// Attention grid: one CTA per SM (atomic queue), or one per possible work
+// unit (cluster launch control: the CTAs that run take the units of those
+// that have not started yet).
+int attn_grid(int64_t max_items, int nsm) {
+  if (g_sched == 1) return (int)max_items;
+  return (int)(max_items < nsm ? max_items : nsm);
+}
+
 // TA_ERR_CUDA for a failed CUDA call, remembering its error; TA_OK otherwise.
 ta_status cuda_status(cudaError_t e) {
   if (e == cudaSuccess) return TA_OK;
@@ -380,10 +393,11 @@ ta_status launch_run_checked(const void* q, const void* k, const void* v, const 
   ap.scale_log2 = sm_scale * 1.4426950408889634f;
   ap.timeout_ns = wait_limit_ns();
   ap.debug_stall = g_stall;
+  ap.sched_clc = g_sched;
   ap.part_o = w.part_o;
   ap.part_lse = w.part_lse;
   const int64_t max_items = L.max_records * dims->h_kv;
-  const int grid = (int)(max_items < nsm ? max_items : nsm);
+  const int grid = attn_grid(max_items, nsm);
   cudaError_t e;
   const bool bf16 = dims->dtype == TA_BF16;
   if (D == 64)
@@ -537,6 +551,12 @@ ta_status tree_attn_set_wait_hooks(uint64_t wait_limit_ns, int32_t stall) {
   if (stall != 0 && stall != 1) return TA_ERR_INVALID_ARGUMENT;
   g_wait_limit_ns = wait_limit_ns;
   g_stall = stall;
+  return TA_OK;
+}
+
+ta_status tree_attn_set_scheduler(int32_t mode) {
+  if (mode != 0 && mode != 1) return TA_ERR_INVALID_ARGUMENT;
+  g_sched = mode;
   return TA_OK;
 }
 
@@ -794,10 +814,11 @@ ta_status tree_attn_paged(const void* q, const int32_t* q_indptr, const void* pa
   ap.scale_log2 = sm_scale * 1.4426950408889634f;
   ap.timeout_ns = wait_limit_ns();
   ap.debug_stall = g_stall;
+  ap.sched_clc = g_sched;
   ap.part_o = nullptr;
   ap.part_lse = nullptr;
   const int64_t max_items = L.max_records * d.h_kv;
-  const int grid = (int)(max_items < nsm ? max_items : nsm);
+  const int grid = attn_grid(max_items, nsm);
   const bool bf16 = d.dtype == TA_BF16;
   cudaError_t e;
   if (d.head_dim == 64)

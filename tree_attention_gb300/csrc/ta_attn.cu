@@ -84,6 +84,7 @@ enum Bar : int {
   B_ML_FULL = B_O_FREE + 2,            // [2] softmax wrote the rows' (m, l)
   B_DRAIN = B_ML_FULL + 2,
   B_STALL,                             // test hook: nothing ever arrives on it
+  B_CLC,                               // launch-cancel response landed
   B_COUNT
 };
 constexpr int kBarSlots = 48;
@@ -111,7 +112,8 @@ struct Cfg {
   static constexpr int kOffItems = kOffOst + 4 * kOstBytes;
   static constexpr int kOffBar = kOffItems + kSlots * (int)sizeof(Item);
   static constexpr int kOffCta = kOffBar + kBarSlots * 8;
-  static constexpr int kUsed = kOffCta + 64;
+  static constexpr int kOffClc = kOffCta + 64;    // 16-byte launch-cancel response
+  static constexpr int kUsed = kOffClc + 16;
   static constexpr int kSmemAlloc = kUsed + 1024;   // room to align the base to 1024
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kTmemS = 0;      // S of tile x at 128 * x (P over its first half)
@@ -125,6 +127,7 @@ struct CtaShared {
 
 struct Ctx {
   uint8_t* smem;
+  void* clc_resp;
   uint64_t* bar;
   Item* items;
   volatile int* abort;
@@ -254,10 +257,15 @@ __device__ void run_producer(const Ctx& cx, const CUtensorMap* tm_q, const CUten
   const int g = p.g, R = p.R;
   uint32_t it = 0, kv_it = 0, q_it[2] = {0, 0};
   uint32_t issued_k = 0;   // loads issued (stage = count % kStages)
+  // cluster launch control: requests stop at the first that finds no launch
+  // left; at most one is in flight (lane 0's copies count)
+  bool clc_live = p.sched_clc != 0, clc_pending = false;
+  uint32_t clc_phase = 0;
   bool aborted = false;
   // the first unit of every CTA is fixed (CTA b takes item b, the items being
-  // in longest-first order already), the rest come from the queue, which
-  // starts after those grid items
+  // in longest-first order already); the rest come from the queue, which
+  // starts after those grid items, or with cluster launch control from the
+  // CTAs whose launches this one cancels
   const unsigned int n_static = gridDim.x;
   unsigned int idx = blockIdx.x;
   // lanes 0-3 hold the next record (16 bytes each), fetched one item ahead
@@ -280,7 +288,15 @@ __device__ void run_producer(const Ctx& cx, const CUtensorMap* tm_q, const CUten
     // pop the next index now; its round trip overlaps this unit's issue
     unsigned int nidx = 0;
     if (lane == 0) {
-      nidx = n_static + atomicAdd(&p.hdr->queue_head, 1u);
+      if (!p.sched_clc) {
+        nidx = n_static + atomicAdd(&p.hdr->queue_head, 1u);
+      } else if (clc_live) {
+        // ask for the unit of a CTA that has not started (read after this
+        // unit's loads are issued)
+        mbar_arrive_expect_tx(&cx.bar[B_CLC], 16);
+        clc_try_cancel(cx.clc_resp, &cx.bar[B_CLC]);
+        clc_pending = true;
+      }
       s.valid = 1;
       s.kvh = kvh;
     }
@@ -323,6 +339,39 @@ __device__ void run_producer(const Ctx& cx, const CUtensorMap* tm_q, const CUten
       }
       if (aborted) break;
     }
+    if (p.sched_clc) {
+      // the cancelled CTA's index is this CTA's next unit; a CTA past the
+      // last unit is cancelled as well (and the next one asked for), so that
+      // none of them launches only to find no work
+      int stop = 0;
+      nidx = num_items;
+      if (lane == 0 && clc_live) {
+        for (;;) {
+          if (!cx.wait(B_CLC, clc_phase)) {
+            stop = 1;
+            break;
+          }
+          clc_pending = false;
+          clc_phase ^= 1u;
+          uint32_t x = 0;
+          if (!clc_query(cx.clc_resp, &x)) {
+            clc_live = false;   // every launch has started: no further requests
+            break;
+          }
+          if (x < num_items) {
+            nidx = x;
+            break;
+          }
+          mbar_arrive_expect_tx(&cx.bar[B_CLC], 16);
+          clc_try_cancel(cx.clc_resp, &cx.bar[B_CLC]);
+          clc_pending = true;
+        }
+      }
+      if (__shfl_sync(0xffffffffu, stop, 0)) {
+        aborted = true;
+        break;
+      }
+    }
     idx = __shfl_sync(0xffffffffu, nidx, 0);
     if (idx < num_items) {
       if (lane < 4) rec_next = __ldg(reinterpret_cast<const int4*>(p.sorted + idx / p.h_kv) + lane);
@@ -345,6 +394,8 @@ __device__ void run_producer(const Ctx& cx, const CUtensorMap* tm_q, const CUten
     ++it;
   }
   if (aborted && lane == 0) {
+    // a launch-cancel request still in flight writes shared memory too
+    if (clc_pending) cx.drain_wait(B_CLC, clc_phase);
     // let every copy already in flight land before the CTA's memory goes away:
     // the last load issued into each Q buffer and each K stage (load i of a
     // stage went to stage i % 2 and completes that stage's phase i / 2)
@@ -1108,6 +1159,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   Ctx cx;
   cx.smem = smem;
+  cx.clc_resp = smem + C::kOffClc;
   cx.bar = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
   cx.items = reinterpret_cast<Item*>(smem + C::kOffItems);
   cx.abort = &cta->abort;
@@ -1139,6 +1191,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(&bar[B_DRAIN], 1);
     mbar_init(&bar[B_STALL], 1);
+    mbar_init(&bar[B_CLC], 1);
     cta->abort = 0;
     mbar_fence_init();
     tma_prefetch_desc(&tm_q);
@@ -1184,7 +1237,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(cta->tmem_base, C::kTmemCols);
   }
-  if (threadIdx.x == 0) {
+  if (threadIdx.x == 0 && !p.sched_clc) {
     // the last CTA re-arms the work queue so the plan can be reused
     __threadfence();
     const unsigned int done = atomicAdd(&p.hdr->queue_done, 1u);

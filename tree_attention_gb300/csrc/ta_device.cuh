@@ -213,6 +213,34 @@ __device__ __forceinline__ void umma_f16_tmem_a(uint32_t d_tmem, uint32_t a_tmem
       : "memory");
 }
 
+// Cluster launch control: asks the hardware to cancel the launch of a CTA of
+// this grid that has not started yet.  The 16-byte response lands in
+// ``resp`` (16-byte aligned shared memory) and completes 16 bytes of
+// transaction on ``bar`` (the caller arms it with expect_tx).
+__device__ __forceinline__ void clc_try_cancel(void* resp, uint64_t* bar) {
+  asm volatile(
+      "clusterlaunchcontrol.try_cancel.async.shared::cta.mbarrier::complete_tx::bytes.b128 "
+      "[%0], [%1];" ::"r"(smem_u32(resp)),
+      "r"(smem_u32(bar))
+      : "memory");
+}
+// Reads a completed response: whether a launch was cancelled, and if so the
+// x index of that CTA.
+__device__ __forceinline__ bool clc_query(const void* resp, uint32_t* ctaid_x) {
+  uint32_t ok, x;
+  asm volatile(
+      "{\n\t.reg .b128 r;\n\t.reg .pred p;\n\t"
+      "ld.shared.b128 r, [%2];\n\t"
+      "clusterlaunchcontrol.query_cancel.is_canceled.pred.b128 p, r;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t"
+      "clusterlaunchcontrol.query_cancel.get_first_ctaid::x.b32.b128 %1, r;\n\t}"
+      : "=r"(ok), "=r"(x)
+      : "r"(smem_u32(resp))
+      : "memory");
+  *ctaid_x = x;
+  return ok != 0;
+}
+
 // Arrive on ``bar`` once every tcgen05 operation this thread issued so far
 // has completed.
 __device__ __forceinline__ void umma_commit(uint64_t* bar) {

@@ -91,6 +91,11 @@ struct AttnParams {
   // test hook: the MMA threads first wait on a barrier that nothing arrives
   // on, so that the bounded wait runs out and the abort path runs
   int debug_stall;
+  // 0: one CTA per SM takes its first unit by CTA index and the rest from the
+  // atomic work queue; 1: one CTA per possible unit, and a CTA that finishes
+  // takes the unit of a CTA not yet started by cancelling its launch
+  // (cluster launch control)
+  int sched_clc;
   // split-KV partial states of the records with part >= 0: O / l in float32
   // [record][h_kv][128 packed rows][d] and the base-2 lse [record][h_kv][128]
   float* part_o;
