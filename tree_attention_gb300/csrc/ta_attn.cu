@@ -580,6 +580,12 @@ __device__ void run_mma(const Ctx& cx, const AttnParams& p) {
         }
         if (!k_ready) {
           if (!cx.wait(B_K_FULL + stage, (kc >> 1) & 1)) return false;
+          // the tile's column intervals too: a softmax warpgroup whose Q tile
+          // skips kv tiles could otherwise reach this tile while the V
+          // producer is two tiles behind, and its own wait on the two-stage
+          // EX_FULL barrier would then match the older phase of the same
+          // parity.  Waiting here keeps every phase in order.
+          if (!cx.wait(B_EX_FULL + stage, (kc >> 1) & 1)) return false;
           k_ready = true;
         }
         // S = Q K^T of this Q tile (K from TMA, Q from TMA or the correction
