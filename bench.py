@@ -422,8 +422,8 @@ def measure_workload(ta, w, args, dev, stream, world, local, headline=False):
     if not headline:
         return res, None
 
-    # end to end through the public call with host buffers: this step's inputs
-    # in from pinned host memory, out and lse back, every step
+    # end to end through the public call with host buffers: every step's
+    # inputs in from pinned host memory and its out and lse back
     keys_in = ["q", "k", "v", "q_indptr", "kv_indptr", "mn_indptr", "tree_order",
                "q_rope_position"]
     host = {k: (base[k].cpu().pin_memory() if base[k] is not None else None) for k in keys_in}
@@ -432,26 +432,51 @@ def measure_workload(ta, w, args, dev, stream, world, local, headline=False):
     h2d = sum(host[k].numel() * host[k].element_size() for k in keys_in if host[k] is not None)
     d2h = host_out.numel() * host_out.element_size() + host_lse.numel() * 4
 
-    def e2e_step(d):
-        for k in keys_in:
-            if host[k] is not None:
-                d[k].copy_(host[k], non_blocking=True)
+    # two device sets in flight: while step i computes on one, step i+1's
+    # inputs are copied into the other and step i-1's results copied out
+    # (copy-in and copy-out streams of their own, ordered by events)
+    e2e_sets = sets[:2] if len(sets) >= 2 else sets + [
+        {k: (v.clone() if isinstance(v, torch.Tensor) else v) for k, v in sets[0].items()}]
+    cin = torch.cuda.Stream(dev)
+    cout = torch.cuda.Stream(dev)
+    ev = [{n: torch.cuda.Event() for n in ("in", "done", "read")} for _ in e2e_sets]
+    started = [False] * len(e2e_sets)
+
+    def e2e_step(i):
+        j = i % len(e2e_sets)
+        d, e = e2e_sets[j], ev[j]
+        if started[j]:
+            cin.wait_event(e["done"])      # the set's previous step has read its inputs
+        with torch.cuda.stream(cin):
+            for k in keys_in:
+                if host[k] is not None:
+                    d[k].copy_(host[k], non_blocking=True)
+            e["in"].record(cin)
+        stream.wait_event(e["in"])
+        if started[j]:
+            stream.wait_event(e["read"])   # its previous results are out
         step(d)
-        host_out.copy_(d["out"], non_blocking=True)
-        host_lse.copy_(d["lse"], non_blocking=True)
+        e["done"].record(stream)
+        cout.wait_event(e["done"])
+        with torch.cuda.stream(cout):
+            host_out.copy_(d["out"], non_blocking=True)
+            host_lse.copy_(d["lse"], non_blocking=True)
+            e["read"].record(cout)
+        started[j] = True
 
     for i in range(min(args.warmup, 3)):
-        e2e_step(sets[i % n_sets])
+        e2e_step(i)
     torch.cuda.synchronize(dev)
     barrier(world)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
+    e0.record(cin)
     for i in range(K):
-        e2e_step(sets[i % n_sets])
-    e1.record(stream)
+        e2e_step(i)
+    e1.record(cout)
     torch.cuda.synchronize(dev)
     barrier(world)
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
+    sets.extend(x for x in e2e_sets if all(x is not y for y in sets))
     check_status("after the end-to-end pass")
     extra = {"roofline": roof, "clocks": clk, "e2e_ms": e2e_ms, "h2d": h2d, "d2h": d2h,
              "l2_note": l2_note, "flops": flops}
