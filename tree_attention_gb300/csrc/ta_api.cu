@@ -290,7 +290,7 @@ bool fold_rotation(const ta_dims* dims, int nsm) {
 
 // The plan kernel (work records, tile classes, longest-first order).  With
 // ``rope`` it also does the run's key rotation on its idle warps, over a
-// grid of at least 4 CTAs per SM.
+// grid of at least 2 CTAs per SM (measured against 1 and 4 on spec-decode).
 ta_status launch_plan_checked(const int32_t* q_indptr, const int32_t* kv_indptr,
                               const int32_t* mn_indptr, const int32_t* tree_order,
                               const ta_dims* dims, void* workspace, cudaStream_t st,
@@ -330,7 +330,7 @@ ta_status launch_plan_checked(const int32_t* q_indptr, const int32_t* kv_indptr,
     pp.rot_pos = rope->pos;
     pp.rot_cs = reinterpret_cast<float4*>(w.rope_cs);
     pp.kp = krot_params(dims, *rope);
-    if (grid < 4 * nsm) grid = 4 * nsm;
+    if (grid < 2 * nsm) grid = 2 * nsm;
   }
   return cuda_status(ta::launch_plan(pp, grid, st));
 }
