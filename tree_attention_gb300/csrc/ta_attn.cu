@@ -731,7 +731,7 @@ __device__ void rope_q_rows(uint8_t* tile, const float2* __restrict__ cs, long l
 // ---------------------------------------------------------------------------
 // softmax warps (warpgroup x: rows of Q tile x)
 // ---------------------------------------------------------------------------
-template <int D, bool BF16, bool PAGED>
+template <int D, bool BF16, bool PAGED, int GL>
 __device__ void softmax_loop(const Ctx& cx, const AttnParams& p, int x, int wq, int lane) {
   using C = Cfg<D>;
   const int row = wq * 32 + lane;             // packed row = TMEM lane
@@ -798,11 +798,30 @@ __device__ void softmax_loop(const Ctx& cx, const AttnParams& p, int x, int wq, 
         if (partial) {
           // column c is visible iff e_row lies in its interval, stored by
           // the V producer as (start, length): (e_row - start) < length unsigned
+          if constexpr (GL > 0) {
+            // g a multiple of GL (4 or 8): lanes GL*k .. GL*k + GL - 1 hold
+            // heads of one q row.  Lane s of those tests columns s, s + GL,
+            // s + 2 GL, ... of the chunk, and 32 / GL ballots give the row's
+            // 32 visibility bits (bit i: column i)
+            const int base = lane & ~(GL - 1), sl = lane & (GL - 1);
+            uint32_t w = 0;
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const int4 e = reinterpret_cast<const int4*>(ivs + 32 * q)[i];
-            if (!((uint32_t)(e_row - e.x) < (uint32_t)e.y)) x[2 * i] = -INFINITY;
-            if (!((uint32_t)(e_row - e.z) < (uint32_t)e.w)) x[2 * i + 1] = -INFINITY;
+            for (int k = 0; k < 32 / GL; ++k) {
+              const int2 e = ivs[32 * q + GL * k + sl];
+              const uint32_t b =
+                  __ballot_sync(0xffffffffu, (uint32_t)(e_row - e.x) < (uint32_t)e.y);
+              w |= ((b >> base) & ((1u << GL) - 1u)) << (GL * k);
+            }
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (!((w >> i) & 1u)) x[i] = -INFINITY;
+          } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const int4 e = reinterpret_cast<const int4*>(ivs + 32 * q)[i];
+              if (!((uint32_t)(e_row - e.x) < (uint32_t)e.y)) x[2 * i] = -INFINITY;
+              if (!((uint32_t)(e_row - e.z) < (uint32_t)e.w)) x[2 * i + 1] = -INFINITY;
+            }
           }
         }
         // a row without a reference yet (its first visible columns, usually
@@ -939,9 +958,9 @@ __device__ void softmax_loop(const Ctx& cx, const AttnParams& p, int x, int wq, 
 // The softmax warps' loop; on every way out (the work is done, or a bounded
 // wait gave up) the warp waits for its own TMEM loads and stores to finish
 // before the CTA frees the TMEM.
-template <int D, bool BF16, bool PAGED>
+template <int D, bool BF16, bool PAGED, int GL>
 __device__ void run_softmax(const Ctx& cx, const AttnParams& p, int x, int wq, int lane) {
-  softmax_loop<D, BF16, PAGED>(cx, p, x, wq, lane);
+  softmax_loop<D, BF16, PAGED, GL>(cx, p, x, wq, lane);
   tmem_wait_ld();
   tmem_wait_st();
 }
@@ -1153,7 +1172,9 @@ __device__ void run_correction(const Ctx& cx, const AttnParams& p, int wq, int l
 }
 
 // ---------------------------------------------------------------------------
-template <int D, bool BF16, bool PAGED>
+// GL: the softmax's mask test shared by groups of GL lanes of one q row (g a
+// multiple of GL), or per lane (GL = 0)
+template <int D, bool BF16, bool PAGED, int GL>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const AttnParams p) {
@@ -1230,7 +1251,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp < kWarpCorrection) {
     regs_inc<kRegsSoftmax>();
-    run_softmax<D, BF16, PAGED>(cx, p, (warp - kWarpSoftmax) >> 2, warp & 3, lane);
+    run_softmax<D, BF16, PAGED, GL>(cx, p, (warp - kWarpSoftmax) >> 2, warp & 3, lane);
   } else {
     regs_inc<kRegsCorrection>();
     run_correction<D, BF16>(cx, p, warp & 3, lane);
@@ -1263,7 +1284,9 @@ cudaError_t launch_attn(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const 
   using C = Cfg<D>;
   static_assert(C::kSmemAlloc <= 227 * 1024, "shared memory budget");
   static_assert(B_COUNT <= kBarSlots, "barrier area");
-  auto kern = attn_kernel<D, BF16, PAGED>;
+  // groups of 8 lanes pay (ragged-large, g = 8: -3.6 %); groups of 4 measured
+  // slower than the per-lane test on prefix+tree (g = 4), so g = 4 stays per lane
+  auto kern = (p.g % 8 == 0) ? attn_kernel<D, BF16, PAGED, 8> : attn_kernel<D, BF16, PAGED, 0>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemAlloc);
   if (e != cudaSuccess) return e;
