@@ -80,9 +80,8 @@ enum Bar : int {
   B_S_FULL = B_KV_DONE + kStages,      // [2] score buffer of tile A / B written
   B_P_FULL = B_S_FULL + 2,             // [2] P written over it
   B_O_FULL = B_P_FULL + 2,             // [2] the unit's last PV into O_A / O_B done
-  B_O_FREE = B_O_FULL + 2,             // [2] correction read O_A / O_B and its (m, l)
-  B_ML_FULL = B_O_FREE + 2,            // [2] softmax wrote the rows' (m, l)
-  B_DRAIN = B_ML_FULL + 2,
+  B_O_FREE = B_O_FULL + 2,             // [2] the tile's epilogue read O_A / O_B
+  B_DRAIN = B_O_FREE + 2,
   B_STALL,                             // test hook: nothing ever arrives on it
   B_CLC,                               // launch-cancel response landed
   B_COUNT
@@ -102,14 +101,13 @@ struct Cfg {
   static constexpr int kKVAtomBytes = kBlockN * 128;   // 128 rows x 128 bytes
   static constexpr int kQBytes = kAtoms * kQAtomBytes;
   static constexpr int kKVBytes = kAtoms * kKVAtomBytes;
-  static constexpr int kOstBytes = 32 * 64;            // per correction warp: 32 rows x 64 bytes
+  static constexpr int kOstBytes = 32 * 64;            // per softmax warp: 32 rows x 64 bytes
   static constexpr int kOffQ = 0;                                   // [2] tile A, tile B
   static constexpr int kOffK = kOffQ + 2 * kQBytes;                 // [kStages]
   static constexpr int kOffV = kOffK + kStages * kKVBytes;          // [kStages]
   static constexpr int kOffEX = kOffV + kStages * kKVBytes;         // int2 [kStages][kBlockN]
-  static constexpr int kOffML = kOffEX + kStages * kBlockN * 8;     // float2 [2][kBlockM]
-  static constexpr int kOffOst = kOffML + 2 * kBlockM * 8;          // [4 warps]
-  static constexpr int kOffItems = kOffOst + 4 * kOstBytes;
+  static constexpr int kOffOst = kOffEX + kStages * kBlockN * 8;    // [2 tiles][4 warps]
+  static constexpr int kOffItems = kOffOst + 8 * kOstBytes;
   static constexpr int kOffBar = kOffItems + kSlots * (int)sizeof(Item);
   static constexpr int kOffCta = kOffBar + kBarSlots * 8;
   static constexpr int kOffClc = kOffCta + 64;    // 16-byte launch-cancel response
@@ -723,21 +721,125 @@ __device__ void rope_q_rows(uint8_t* tile, const float2* __restrict__ cs, long l
   }
 }
 
+// ---------------------------------------------------------------------------
+// softmax warps (warpgroup x: rows of Q tile x, their scores and epilogue)
+// ---------------------------------------------------------------------------
+// Writes Q tile x's rows of a unit: O / l in the storage dtype and
+// lse = m + log2(l) (or, for a split-KV chunk, float32 O / l and lse into its
+// partial state).  With ``has_o`` the tile's O is read from TMEM (and the
+// buffer released); without, the tile attended nothing: out = 0, lse = -inf.
+template <int D, bool BF16>
+__device__ void store_tile(const Ctx& cx, const AttnParams& p, const ItemRec& r, int x, int kvh,
+                           int wq, int lane, bool has_o, float m_ref, float l) {
+  using C = Cfg<D>;
+  const int row = wq * 32 + lane;
+  const uint32_t t_o = cx.tmem + ((uint32_t)(wq * 32) << 16) + C::kTmemO + 128 * x;
+  uint8_t* ost = cx.smem + C::kOffOst + (x * 4 + wq) * C::kOstBytes;
+  const int g = p.g, R = p.R;
+  const bool in_pack = row < g * R;
+  const int qr = in_pack ? row / g : 0;
+  const int hh = in_pack ? row - qr * g : 0;
+  const bool valid = in_pack && qr < tile_rows(r, x, R);
+  const int head = kvh * g + hh;
+  const size_t orow = (size_t)(r.q_row0 + x * R + qr) * p.h_q + head;
+  const float inv = l > 0.f ? 1.f / l : 0.f;
+  const float lse_v = l > 0.f ? m_ref + log2f(l) : -INFINITY;
+  if (r.part >= 0) {
+    // split-KV chunk: O / l and lse in float32 into the record's partial
+    // state (tile x's 128 packed rows, packed row = TMEM lane), merged with
+    // the pair's other chunks by the merge kernel
+    const size_t prow = (((size_t)r.part * p.h_kv + kvh) * kTilesPerUnit + x) * kBlockM + row;
+    if (valid) p.part_lse[prow] = lse_v;
+    float4* po = reinterpret_cast<float4*>(p.part_o + prow * D);
+#pragma unroll
+    for (int oc = 0; oc < D / 32; ++oc) {
+      float o[32];
+      if (has_o) {
+        tmem_ld32(t_o + oc * 32, o);
+        tmem_wait_ld(o);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) o[i] = 0.f;
+      }
+      if (oc == D / 32 - 1) {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0 && has_o) mbar_arrive(&cx.bar[B_O_FREE + x]);
+      }
+      if (valid) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          po[oc * 8 + i] = make_float4(o[4 * i] * inv, o[4 * i + 1] * inv, o[4 * i + 2] * inv,
+                                       o[4 * i + 3] * inv);
+      }
+    }
+    return;
+  }
+  if (valid) p.lse[orow] = lse_v;
+  // O / l in the storage dtype: 64 columns per TMEM round trip, written 32
+  // columns (64 bytes per row) at a time through the warp's staging buffer,
+  // then as whole-warp 16-byte stores of 8 rows x 64 bytes
+  uint16_t* outp = reinterpret_cast<uint16_t*>(p.out);
+  long long ro[4];
+  int ok[4];
+#pragma unroll
+  for (int st = 0; st < 4; ++st) {
+    const int src = st * 8 + (lane >> 2);   // row within the quadrant
+    ro[st] = __shfl_sync(0xffffffffu, (long long)orow, src);
+    ok[st] = __shfl_sync(0xffffffffu, valid ? 1 : 0, src);
+  }
+#pragma unroll
+  for (int oc2 = 0; oc2 < D / 64; ++oc2) {
+    float oa[32], ob2[32];
+    if (has_o) {
+      tmem_ld32(t_o + oc2 * 64, oa);
+      tmem_ld32(t_o + oc2 * 64 + 32, ob2);
+      tmem_wait_ld(oa);
+      tmem_wait_ld(ob2);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) oa[i] = ob2[i] = 0.f;
+    }
+    if (oc2 == D / 64 - 1) {
+      // O is out of TMEM: the Q tile's next unit may accumulate into it
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0 && has_o) mbar_arrive(&cx.bar[B_O_FREE + x]);
+    }
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf) {
+      const int oc = oc2 * 2 + hf;
+      uint32_t pk[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const float x0 = hf ? ob2[2 * i] : oa[2 * i];
+        const float x1 = hf ? ob2[2 * i + 1] : oa[2 * i + 1];
+        pk[i] = pack2<BF16>(x0 * inv, x1 * inv);
+      }
+      __syncwarp();   // the previous chunk's readers are done with the buffer
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc)
+        *reinterpret_cast<uint4*>(ost + lane * 64 + ((cc ^ ((lane >> 1) & 3)) * 16)) =
+            make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
+      __syncwarp();
+#pragma unroll
+      for (int st = 0; st < 4; ++st) {
+        const int src = st * 8 + (lane >> 2);
+        const int cc = lane & 3;
+        const uint4 val =
+            *reinterpret_cast<const uint4*>(ost + src * 64 + ((cc ^ ((src >> 1) & 3)) * 16));
+        if (ok[st]) *reinterpret_cast<uint4*>(outp + ro[st] * D + oc * 32 + cc * 8) = val;
+      }
+    }
+  }
+}
 
-// ---------------------------------------------------------------------------
-// softmax warps
-// ---------------------------------------------------------------------------
-
-// ---------------------------------------------------------------------------
-// softmax warps (warpgroup x: rows of Q tile x)
-// ---------------------------------------------------------------------------
 template <int D, bool BF16, bool PAGED, int GL>
 __device__ void softmax_loop(const Ctx& cx, const AttnParams& p, int x, int wq, int lane) {
   using C = Cfg<D>;
   const int row = wq * 32 + lane;             // packed row = TMEM lane
   const uint32_t t_row = cx.tmem + ((uint32_t)(wq * 32) << 16);
   const int2* sEX = reinterpret_cast<const int2*>(cx.smem + C::kOffEX);
-  float2* sML = reinterpret_cast<float2*>(cx.smem + C::kOffML);
   const float c2 = p.scale_log2;
   const int g = p.g, R = p.R;
   const bool in_pack = row < g * R;
@@ -750,6 +852,7 @@ __device__ void softmax_loop(const Ctx& cx, const AttnParams& p, int x, int wq, 
     const Item& s = cx.items[slot];
     if (!s.valid) return;
     const ItemRec r = s.r;
+    const int kvh = s.kvh;
     const bool valid = in_pack && qr < tile_rows(r, x, R);
     int e_row = INT_MIN;
     if (valid && tile_count(r, x) > 0)
@@ -940,15 +1043,16 @@ __device__ void softmax_loop(const Ctx& cx, const AttnParams& p, int x, int wq, 
       ++kx;
       first = false;
     }
-    if (tile_count(r, x) > 0) {
-      // the rows' (m, l) for the epilogue; the buffer is free once the
-      // epilogue of this Q tile's previous unit has read it
-      if (!cx.warp_wait(B_O_FREE + x, (sx & 1) ^ 1)) return;
-      sML[x * kBlockM + row] = make_float2(m_ref, l);
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&cx.bar[B_ML_FULL + x]);
+    // the tile's epilogue, as soon as its last PV is done (while the next
+    // unit's Q tiles land and rotate); a tile that attended nothing is
+    // written as out = 0, lse = -inf
+    const bool has_o = tile_count(r, x) > 0;
+    if (has_o) {
+      if (!cx.warp_wait(B_O_FULL + x, sx & 1)) return;
+      tc_fence_after();
       ++sx;
     }
+    store_tile<D, BF16>(cx, p, r, x, kvh, wq, lane, has_o, m_ref, l);
     __syncwarp();
     if (lane == 0) mbar_arrive(&cx.bar[B_ITEM_EMPTY + slot]);
     ++it;
@@ -966,202 +1070,46 @@ __device__ void run_softmax(const Ctx& cx, const AttnParams& p, int x, int wq, i
 }
 
 // ---------------------------------------------------------------------------
-// correction warps: RoPE of Q, epilogues
+// correction warps: RoPE of Q
 // ---------------------------------------------------------------------------
-// Writes Q tile x's rows of a unit: O / l in the storage dtype and
-// lse = m + log2(l) (or, for a split-KV chunk, float32 O / l and lse into its
-// partial state).  With ``has_o`` the tile's O is read from TMEM (and the
-// buffer released); without, the tile attended nothing: out = 0, lse = -inf.
-template <int D, bool BF16>
-__device__ void store_tile(const Ctx& cx, const AttnParams& p, const ItemRec& r, int x, int kvh,
-                           int wq, int lane, bool has_o, float m_ref, float l) {
-  using C = Cfg<D>;
-  const int row = wq * 32 + lane;
-  const uint32_t t_o = cx.tmem + ((uint32_t)(wq * 32) << 16) + C::kTmemO + 128 * x;
-  uint8_t* ost = cx.smem + C::kOffOst + wq * C::kOstBytes;
-  const int g = p.g, R = p.R;
-  const bool in_pack = row < g * R;
-  const int qr = in_pack ? row / g : 0;
-  const int hh = in_pack ? row - qr * g : 0;
-  const bool valid = in_pack && qr < tile_rows(r, x, R);
-  const int head = kvh * g + hh;
-  const size_t orow = (size_t)(r.q_row0 + x * R + qr) * p.h_q + head;
-  const float inv = l > 0.f ? 1.f / l : 0.f;
-  const float lse_v = l > 0.f ? m_ref + log2f(l) : -INFINITY;
-  if (r.part >= 0) {
-    // split-KV chunk: O / l and lse in float32 into the record's partial
-    // state (tile x's 128 packed rows, packed row = TMEM lane), merged with
-    // the pair's other chunks by the merge kernel
-    const size_t prow = (((size_t)r.part * p.h_kv + kvh) * kTilesPerUnit + x) * kBlockM + row;
-    if (valid) p.part_lse[prow] = lse_v;
-    float4* po = reinterpret_cast<float4*>(p.part_o + prow * D);
-#pragma unroll
-    for (int oc = 0; oc < D / 32; ++oc) {
-      float o[32];
-      if (has_o) {
-        tmem_ld32(t_o + oc * 32, o);
-        tmem_wait_ld(o);
-      } else {
-#pragma unroll
-        for (int i = 0; i < 32; ++i) o[i] = 0.f;
-      }
-      if (oc == D / 32 - 1) {
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0 && has_o) mbar_arrive(&cx.bar[B_O_FREE + x]);
-      }
-      if (valid) {
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-          po[oc * 8 + i] = make_float4(o[4 * i] * inv, o[4 * i + 1] * inv, o[4 * i + 2] * inv,
-                                       o[4 * i + 3] * inv);
-      }
-    }
-    return;
-  }
-  if (valid) p.lse[orow] = lse_v;
-  // O / l in the storage dtype: 64 columns per TMEM round trip, written 32
-  // columns (64 bytes per row) at a time through the warp's staging buffer,
-  // then as whole-warp 16-byte stores of 8 rows x 64 bytes
-  uint16_t* outp = reinterpret_cast<uint16_t*>(p.out);
-  long long ro[4];
-  int ok[4];
-#pragma unroll
-  for (int st = 0; st < 4; ++st) {
-    const int src = st * 8 + (lane >> 2);   // row within the quadrant
-    ro[st] = __shfl_sync(0xffffffffu, (long long)orow, src);
-    ok[st] = __shfl_sync(0xffffffffu, valid ? 1 : 0, src);
-  }
-#pragma unroll
-  for (int oc2 = 0; oc2 < D / 64; ++oc2) {
-    float oa[32], ob2[32];
-    if (has_o) {
-      tmem_ld32(t_o + oc2 * 64, oa);
-      tmem_ld32(t_o + oc2 * 64 + 32, ob2);
-      tmem_wait_ld(oa);
-      tmem_wait_ld(ob2);
-    } else {
-#pragma unroll
-      for (int i = 0; i < 32; ++i) oa[i] = ob2[i] = 0.f;
-    }
-    if (oc2 == D / 64 - 1) {
-      // O is out of TMEM: the Q tile's next unit may accumulate into it
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0 && has_o) mbar_arrive(&cx.bar[B_O_FREE + x]);
-    }
-#pragma unroll
-    for (int hf = 0; hf < 2; ++hf) {
-      const int oc = oc2 * 2 + hf;
-      uint32_t pk[16];
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const float x0 = hf ? ob2[2 * i] : oa[2 * i];
-        const float x1 = hf ? ob2[2 * i + 1] : oa[2 * i + 1];
-        pk[i] = pack2<BF16>(x0 * inv, x1 * inv);
-      }
-      __syncwarp();   // the previous chunk's readers are done with the buffer
-#pragma unroll
-      for (int cc = 0; cc < 4; ++cc)
-        *reinterpret_cast<uint4*>(ost + lane * 64 + ((cc ^ ((lane >> 1) & 3)) * 16)) =
-            make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
-      __syncwarp();
-#pragma unroll
-      for (int st = 0; st < 4; ++st) {
-        const int src = st * 8 + (lane >> 2);
-        const int cc = lane & 3;
-        const uint4 val =
-            *reinterpret_cast<const uint4*>(ost + src * 64 + ((cc ^ ((src >> 1) & 3)) * 16));
-        if (ok[st]) *reinterpret_cast<uint4*>(outp + ro[st] * D + oc * 32 + cc * 8) = val;
-      }
-    }
-  }
-}
-
-// The correction warps walk the units one behind the softmax: for each unit
-// with tiles, the RoPE of its Q tiles (rotary calls), then the epilogue of
-// the unit before it -- so a unit's first QK^T never waits for an epilogue,
-// and an epilogue never waits for the next unit's RoPE.
+// The correction warps rotate each unit's Q tiles under RoPE (a tile's first
+// QK^T waits for its rotation); the softmax warpgroups write the epilogues.
 template <int D, bool BF16>
 __device__ void correction_loop(const Ctx& cx, const AttnParams& p, int wq, int lane) {
   using C = Cfg<D>;
-  const int row = wq * 32 + lane;
-  const float2* sML = reinterpret_cast<const float2*>(cx.smem + C::kOffML);
   const int g = p.g, R = p.R;
-  // slots; per Q tile x (bit x): parity of its units with tiles (Q phases,
-  // O / ML phases)
-  uint32_t it = 0, qi = 0, oi = 0;
-  bool pend = false;   // a unit waits for its epilogue
-  int pend_slot = 0, pend_kvh = 0;
-  uint32_t pend_has = 0, pend_par = 0;   // bit x: tile x attends; its O / ML phase
-  ItemRec pend_r;
-  auto finish_pending = [&]() -> bool {
-#pragma unroll 1
-    for (int x = 0; x < 2; ++x) {
-      if ((pend_has >> x) & 1) {
-        const uint32_t par = (pend_par >> x) & 1;
-        if (!cx.warp_wait(B_ML_FULL + x, par)) return false;
-        const float2 ml = sML[x * kBlockM + row];
-        if (!cx.warp_wait(B_O_FULL + x, par)) return false;
-        tc_fence_after();
-        store_tile<D, BF16>(cx, p, pend_r, x, pend_kvh, wq, lane, true, ml.x, ml.y);
-      } else {
-        store_tile<D, BF16>(cx, p, pend_r, x, pend_kvh, wq, lane, false, -INFINITY, 0.f);
-      }
-    }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&cx.bar[B_ITEM_EMPTY + pend_slot]);
-    pend = false;
-    return true;
-  };
+  // slots; per Q tile x (bit x): parity of its units with tiles
+  uint32_t it = 0, qi = 0;
   for (;;) {
     const int slot = it % kSlots;
     if (!cx.warp_wait(B_ITEM_FULL + slot, (it / kSlots) & 1)) return;
     const Item& s = cx.items[slot];
     if (!s.valid) break;
     const ItemRec r = s.r;
-    const int kvh = s.kvh;
-    if (r.n_tiles > 0) {
+    if (p.rotary && r.n_tiles > 0) {
 #pragma unroll 1
       for (int x = 0; x < 2; ++x) {
         if (tile_count(r, x) == 0) continue;
-        if (p.rotary) {
-          // q row r of the tile takes the position of its own tree node's kv
-          // slot (the first cos/sin batch is fetched while the Q tile lands)
-          const long long qtok0 =
-              (long long)r.kv_base + (r.kv - r.qo) + (long long)r.r0 + (long long)x * R;
-          const RopeRange rr = rope_range<D>(tile_rows(r, x, R), g, wq);
-          float4 cv[2][4];
-          rope_load<D>(cv, p.rope_cs, qtok0, rr, 0, lane);
-          if (!cx.warp_wait(B_Q_FULL + x, (qi >> x) & 1)) return;
-          rope_q_rows<D, BF16>(cx.smem + C::kOffQ + x * C::kQBytes, p.rope_cs, qtok0, rr, g,
-                               lane, cv);
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&cx.bar[B_Q_READY + x]);
-        }
+        // q row r of the tile takes the position of its own tree node's kv
+        // slot (the first cos/sin batch is fetched while the Q tile lands)
+        const long long qtok0 =
+            (long long)r.kv_base + (r.kv - r.qo) + (long long)r.r0 + (long long)x * R;
+        const RopeRange rr = rope_range<D>(tile_rows(r, x, R), g, wq);
+        float4 cv[2][4];
+        rope_load<D>(cv, p.rope_cs, qtok0, rr, 0, lane);
+        if (!cx.warp_wait(B_Q_FULL + x, (qi >> x) & 1)) return;
+        rope_q_rows<D, BF16>(cx.smem + C::kOffQ + x * C::kQBytes, p.rope_cs, qtok0, rr, g, lane,
+                             cv);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&cx.bar[B_Q_READY + x]);
         qi ^= 1u << x;
       }
     }
-    if (pend && !finish_pending()) return;
-    if (r.n_tiles == 0) {
-#pragma unroll 1
-      for (int x = 0; x < 2; ++x)
-        store_tile<D, BF16>(cx, p, r, x, kvh, wq, lane, false, -INFINITY, 0.f);
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&cx.bar[B_ITEM_EMPTY + slot]);
-    } else {
-      pend = true;
-      pend_slot = slot;
-      pend_r = r;
-      pend_kvh = kvh;
-      pend_has = (r.n_a > 0 ? 1u : 0u) | (r.n_b > 0 ? 2u : 0u);
-      pend_par = oi;
-      oi ^= pend_has;
-    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&cx.bar[B_ITEM_EMPTY + slot]);
     ++it;
   }
-  if (pend) finish_pending();
 }
 
 template <int D, bool BF16>
@@ -1208,7 +1156,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bar[B_P_FULL + i], 4);
       mbar_init(&bar[B_O_FULL + i], 1);
       mbar_init(&bar[B_O_FREE + i], 4);
-      mbar_init(&bar[B_ML_FULL + i], 4);
     }
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&bar[B_K_FULL + i], 1);
