@@ -620,9 +620,11 @@ __device__ void run_mma(const Ctx& cx, const AttnParams& p) {
       ++kc;
     }
     if (!ok) break;
-    // the unit's last PVs; then its outputs are complete
-    if ((pend0 && !issue_pv(X0{})) || (pend1 && !issue_pv(X1{}))) break;
+    // the unit's last PVs; each tile's output is complete after its own
+    // (tile A's epilogue does not wait for tile B's last P)
+    if (pend0 && !issue_pv(X0{})) break;
     if (started0) umma_commit(&cx.bar[B_O_FULL + 0]);
+    if (pend1 && !issue_pv(X1{})) break;
     if (started1) umma_commit(&cx.bar[B_O_FULL + 1]);
   }
   if (*cx.abort && issued_any) {
