@@ -728,11 +728,13 @@ __device__ void rope_q_rows(uint8_t* tile, const float2* __restrict__ cs, long l
 // ---------------------------------------------------------------------------
 // Writes Q tile x's rows of a unit: O / l in the storage dtype and
 // lse = m + log2(l) (or, for a split-KV chunk, float32 O / l and lse into its
-// partial state).  With ``has_o`` the tile's O is read from TMEM (and the
-// buffer released); without, the tile attended nothing: out = 0, lse = -inf.
+// partial state).  With ``has_o`` the tile's O is read from TMEM once the
+// unit's last PV is done (O_FULL phase ``o_par``; lse, 1 / l and the row
+// addresses are prepared before that wait) and the buffer released; without,
+// the tile attended nothing: out = 0, lse = -inf.  False if the wait gave up.
 template <int D, bool BF16>
-__device__ void store_tile(const Ctx& cx, const AttnParams& p, const ItemRec& r, int x, int kvh,
-                           int wq, int lane, bool has_o, float m_ref, float l) {
+__device__ bool store_tile(const Ctx& cx, const AttnParams& p, const ItemRec& r, int x, int kvh,
+                           int wq, int lane, bool has_o, uint32_t o_par, float m_ref, float l) {
   using C = Cfg<D>;
   const int row = wq * 32 + lane;
   const uint32_t t_o = cx.tmem + ((uint32_t)(wq * 32) << 16) + C::kTmemO + 128 * x;
@@ -752,6 +754,10 @@ __device__ void store_tile(const Ctx& cx, const AttnParams& p, const ItemRec& r,
     // the pair's other chunks by the merge kernel
     const size_t prow = (((size_t)r.part * p.h_kv + kvh) * kTilesPerUnit + x) * kBlockM + row;
     if (valid) p.part_lse[prow] = lse_v;
+    if (has_o) {
+      if (!cx.warp_wait(B_O_FULL + x, o_par)) return false;
+      tc_fence_after();
+    }
     float4* po = reinterpret_cast<float4*>(p.part_o + prow * D);
 #pragma unroll
     for (int oc = 0; oc < D / 32; ++oc) {
@@ -775,7 +781,7 @@ __device__ void store_tile(const Ctx& cx, const AttnParams& p, const ItemRec& r,
                                        o[4 * i + 3] * inv);
       }
     }
-    return;
+    return true;
   }
   if (valid) p.lse[orow] = lse_v;
   // O / l in the storage dtype: 64 columns per TMEM round trip, written 32
@@ -789,6 +795,10 @@ __device__ void store_tile(const Ctx& cx, const AttnParams& p, const ItemRec& r,
     const int src = st * 8 + (lane >> 2);   // row within the quadrant
     ro[st] = __shfl_sync(0xffffffffu, (long long)orow, src);
     ok[st] = __shfl_sync(0xffffffffu, valid ? 1 : 0, src);
+  }
+  if (has_o) {
+    if (!cx.warp_wait(B_O_FULL + x, o_par)) return false;
+    tc_fence_after();
   }
 #pragma unroll
   for (int oc2 = 0; oc2 < D / 64; ++oc2) {
@@ -834,6 +844,7 @@ __device__ void store_tile(const Ctx& cx, const AttnParams& p, const ItemRec& r,
       }
     }
   }
+  return true;
 }
 
 template <int D, bool BF16, bool PAGED, int GL>
@@ -1049,12 +1060,8 @@ __device__ void softmax_loop(const Ctx& cx, const AttnParams& p, int x, int wq, 
     // unit's Q tiles land and rotate); a tile that attended nothing is
     // written as out = 0, lse = -inf
     const bool has_o = tile_count(r, x) > 0;
-    if (has_o) {
-      if (!cx.warp_wait(B_O_FULL + x, sx & 1)) return;
-      tc_fence_after();
-      ++sx;
-    }
-    store_tile<D, BF16>(cx, p, r, x, kvh, wq, lane, has_o, m_ref, l);
+    if (!store_tile<D, BF16>(cx, p, r, x, kvh, wq, lane, has_o, sx & 1, m_ref, l)) return;
+    if (has_o) ++sx;
     __syncwarp();
     if (lane == 0) mbar_arrive(&cx.bar[B_ITEM_EMPTY + slot]);
     ++it;
