@@ -107,7 +107,8 @@ struct Cfg {
   static constexpr int kOffV = kOffK + kStages * kKVBytes;          // [kStages]
   static constexpr int kOffEX = kOffV + kStages * kKVBytes;         // int2 [kStages][kBlockN]
   static constexpr int kOffOst = kOffEX + kStages * kBlockN * 8;    // [2 tiles][4 warps]
-  static constexpr int kOffItems = kOffOst + 8 * kOstBytes;
+  static constexpr int kOffEq = kOffOst + 8 * kOstBytes;           // int [kSlots][2][kBlockM]
+  static constexpr int kOffItems = kOffEq + kSlots * 2 * kBlockM * 4;
   static constexpr int kOffBar = kOffItems + kSlots * (int)sizeof(Item);
   static constexpr int kOffCta = kOffBar + kBarSlots * 8;
   static constexpr int kOffClc = kOffCta + 64;    // 16-byte launch-cancel response
@@ -300,6 +301,23 @@ __device__ void run_producer(const Ctx& cx, const CUtensorMap* tm_q, const CUten
     }
     __syncwarp();
     const ItemRec r = s.r;
+    {
+      // the DFS enter index of each q row of the unit's two tiles (INT_MIN
+      // past a tile's rows or for a tile that attends nothing), read by the
+      // softmax warps' interval tests from the slot
+      int* eq = reinterpret_cast<int*>(cx.smem + C::kOffEq) + slot * 2 * kBlockM;
+      int v[2 * kBlockM / 32];
+#pragma unroll
+      for (int k = 0; k < 2 * kBlockM / 32; ++k) {
+        const int x = k / (kBlockM / 32), i = (k % (kBlockM / 32)) * 32 + lane;
+        v[k] = INT_MIN;
+        if (tile_count(r, x) > 0 && i < tile_rows(r, x, R))
+          v[k] = __ldg(&p.tree_order[2 * (r.tree_base + r.r0 + x * R + i + r.tl - r.qo)]);
+      }
+#pragma unroll
+      for (int k = 0; k < 2 * kBlockM / 32; ++k) eq[k * 32 + lane] = v[k];
+      __syncwarp();
+    }
     if (lane == 0) mbar_arrive(&cx.bar[B_ITEM_FULL + slot]);
     if (r.n_tiles > 0) {
       // the Q tiles that attend anything (each into its own buffer)
@@ -867,9 +885,10 @@ __device__ void softmax_loop(const Ctx& cx, const AttnParams& p, int x, int wq, 
     const ItemRec r = s.r;
     const int kvh = s.kvh;
     const bool valid = in_pack && qr < tile_rows(r, x, R);
-    int e_row = INT_MIN;
-    if (valid && tile_count(r, x) > 0)
-      e_row = __ldg(&p.tree_order[2 * (r.tree_base + r.r0 + x * R + qr + r.tl - r.qo)]);
+    // the row's DFS enter index, staged with the record by the producer
+    const int e_row =
+        valid ? reinterpret_cast<const int*>(cx.smem + C::kOffEq)[(slot * 2 + x) * kBlockM + qr]
+              : INT_MIN;
     float m_ref = -INFINITY, l = 0.f;
     bool first = true;
     TileIter ti(r, p.classes);
