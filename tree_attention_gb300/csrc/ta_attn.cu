@@ -301,10 +301,11 @@ __device__ void run_producer(const Ctx& cx, const CUtensorMap* tm_q, const CUten
     }
     __syncwarp();
     const ItemRec r = s.r;
-    {
+    if constexpr (!PAGED) {
       // the DFS enter index of each q row of the unit's two tiles (INT_MIN
       // past a tile's rows or for a tile that attends nothing), read by the
-      // softmax warps' interval tests from the slot
+      // softmax warps' interval tests from the slot (the paged producer,
+      // busy with page look-ups, leaves them to the softmax warps)
       int* eq = reinterpret_cast<int*>(cx.smem + C::kOffEq) + slot * 2 * kBlockM;
       int v[2 * kBlockM / 32];
 #pragma unroll
@@ -885,10 +886,15 @@ __device__ void softmax_loop(const Ctx& cx, const AttnParams& p, int x, int wq, 
     const ItemRec r = s.r;
     const int kvh = s.kvh;
     const bool valid = in_pack && qr < tile_rows(r, x, R);
-    // the row's DFS enter index, staged with the record by the producer
-    const int e_row =
-        valid ? reinterpret_cast<const int*>(cx.smem + C::kOffEq)[(slot * 2 + x) * kBlockM + qr]
-              : INT_MIN;
+    // the row's DFS enter index (staged with the record by the producer on
+    // the contiguous path)
+    int e_row = INT_MIN;
+    if constexpr (PAGED) {
+      if (valid && tile_count(r, x) > 0)
+        e_row = __ldg(&p.tree_order[2 * (r.tree_base + r.r0 + x * R + qr + r.tl - r.qo)]);
+    } else {
+      if (valid) e_row = reinterpret_cast<const int*>(cx.smem + C::kOffEq)[(slot * 2 + x) * kBlockM + qr];
+    }
     float m_ref = -INFINITY, l = 0.f;
     bool first = true;
     TileIter ti(r, p.classes);
