@@ -10,7 +10,8 @@
 // loaded into shared memory serves two Q tiles.  Tensor memory holds one
 // score buffer and one output accumulator per Q tile (S_A, S_B, O_A, O_B:
 // 128 columns each).  Warp roles:
-//   warp 0      producer: stages each unit's record, TMA-loads its Q tiles
+//   warp 0      producer: stages each unit's record (and, on the contiguous
+//               path, its q rows' DFS enter indices), TMA-loads its Q tiles
 //               (one buffer each) and its K tiles (two stages)
 //   warp 1      MMA issuer (one thread): for kv tile t, PV_A(t-1) then
 //               QK_A(t), PV_B(t-1) then QK_B(t) (tcgen05.mma, M = 128,
@@ -22,10 +23,10 @@
 //               lane = packed row per thread): tree mask, online softmax
 //               against a lazily moved reference, P (fp16/bf16) written over
 //               the first half of the tile's score buffer, the rare rescale
-//               of O
+//               of O, and the tile's epilogue once its last PV is done (O / l
+//               and lse from tensor memory to global memory)
 //   warps 12-15 correction: RoPE of each unit's Q tiles (before their first
-//               QK^T) and the epilogue of the unit before it (O / l and lse
-//               from tensor memory to global memory)
+//               QK^T)
 // A kv tile that is empty for one Q tile (the plan classifies each tile for
 // A and B) is skipped by that tile's QK^T, softmax and PV.  Keys arrive
 // rotated (the run rotates them once per call).  Every cross-warp hand-off
