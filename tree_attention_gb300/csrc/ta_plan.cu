@@ -372,17 +372,24 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanParams p) 
   // overlaps the ranking below: threads 0-127 take tile A's rows, threads
   // 128-255 tile B's
   int key = INT_MAX, nrows = 0, n_a = 0, n_b = 0;
+  // a pair whose only kv tile holds its own tree (no causal prefix) needs no
+  // look-up: each of its Q tiles with rows sees at least its rows' own nodes
+  // there, so the tile is PARTIAL for it (the softmax's per-column test
+  // decides the rest; a FULL tile taken as PARTIAL gives the same result)
+  bool one_tile = false;
   if (has_pair) {
     const int b = s_pair_b;
     const int qo = p.q_indptr[b + 1] - p.q_indptr[b];
     const int tree_base = p.mn_indptr[b];
     const int tl = p.mn_indptr[b + 1] - tree_base;
+    const int kv = seq_kv_len(p, b);
+    one_tile = kv <= kBlockN && kv == tl && s_pair_chunks == 1;
     const int r0 = s_pair_t * U;
     nrows = min(U, qo - r0);
     n_a = min(R, nrows);
     n_b = nrows - n_a;
     const int grp = tid / kGroup, lt = tid % kGroup;
-    if (lt < (grp ? n_b : n_a))
+    if (!one_tile && lt < (grp ? n_b : n_a))
       key = p.tree_order[2 * (tree_base + r0 + grp * R + lt + tl - qo)];
   }
   if (has_pair) {
@@ -419,6 +426,31 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanParams p) 
     const int tl = p.mn_indptr[b + 1] - tree_base;
     const int ts = kv - tl;
     const int r0 = t * U;
+    if (one_tile) {
+      const uint8_t cls = (uint8_t)(kTilePartial | ((n_b > 0 ? kTilePartial : kTileEmpty) << 2));
+      if (tid == 0) {
+        p.classes[off] = cls;
+        ItemRec r;
+        r.part = -1;
+        r.r0 = r0;
+        r.q_row0 = q0 + r0;
+        r.nq = nrows;
+        r.qo = qo;
+        r.kv = kv;
+        r.tl = tl;
+        r.tile_lo = 0;
+        r.kv_base = kv_base;
+        r.tree_base = tree_base;
+        r.n_tiles = 1;
+        r.class_off = (int32_t)off;
+        r.kvt = 1;
+        r.n_a = 1;
+        r.n_b = n_b > 0 ? 1 : 0;
+        r.cls = cls;
+        p.sorted[pos] = r;
+        if (p.merge) p.merge[pair] = make_int4(q0 + r0, nrows, 1, (int)pos);
+      }
+    } else {
     // exact classification from the DFS intervals of ``_check_tree_order``
     // (page "tree_attn.py"), for each Q tile of the unit: its rows' enter
     // indices are sorted (warps 0-3 tile A's, warps 4-7 tile B's: bitonic,
@@ -582,6 +614,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanParams p) 
     }
     if (tid == 0 && p.merge)
       p.merge[pair] = make_int4(q0 + r0, nrows, nch, (int)pos);
+    }
   }
 
   // ---- 5. (one-call entry points) the run's key rotation: every kv token's
