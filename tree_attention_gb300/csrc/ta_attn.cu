@@ -752,7 +752,7 @@ __device__ void rope_q_rows(uint8_t* tile, const float2* __restrict__ cs, long l
 // unit's last PV is done (O_FULL phase ``o_par``; lse, 1 / l and the row
 // addresses are prepared before that wait) and the buffer released; without,
 // the tile attended nothing: out = 0, lse = -inf.  False if the wait gave up.
-template <int D, bool BF16>
+template <int D, bool BF16, bool SPLIT>
 __device__ bool store_tile(const Ctx& cx, const AttnParams& p, const ItemRec& r, int x, int kvh,
                            int wq, int lane, bool has_o, uint32_t o_par, float m_ref, float l) {
   using C = Cfg<D>;
@@ -768,7 +768,7 @@ __device__ bool store_tile(const Ctx& cx, const AttnParams& p, const ItemRec& r,
   const size_t orow = (size_t)(r.q_row0 + x * R + qr) * p.h_q + head;
   const float inv = l > 0.f ? 1.f / l : 0.f;
   const float lse_v = l > 0.f ? m_ref + log2f(l) : -INFINITY;
-  if (r.part >= 0) {
+  if (SPLIT && r.part >= 0) {
     // split-KV chunk: O / l and lse in float32 into the record's partial
     // state (tile x's 128 packed rows, packed row = TMEM lane), merged with
     // the pair's other chunks by the merge kernel
@@ -867,7 +867,7 @@ __device__ bool store_tile(const Ctx& cx, const AttnParams& p, const ItemRec& r,
   return true;
 }
 
-template <int D, bool BF16, bool PAGED, int GL>
+template <int D, bool BF16, bool PAGED, int GL, bool SPLIT>
 __device__ void softmax_loop(const Ctx& cx, const AttnParams& p, int x, int wq, int lane) {
   using C = Cfg<D>;
   const int row = wq * 32 + lane;             // packed row = TMEM lane
@@ -1086,7 +1086,7 @@ __device__ void softmax_loop(const Ctx& cx, const AttnParams& p, int x, int wq, 
     // unit's Q tiles land and rotate); a tile that attended nothing is
     // written as out = 0, lse = -inf
     const bool has_o = tile_count(r, x) > 0;
-    if (!store_tile<D, BF16>(cx, p, r, x, kvh, wq, lane, has_o, sx & 1, m_ref, l)) return;
+    if (!store_tile<D, BF16, SPLIT>(cx, p, r, x, kvh, wq, lane, has_o, sx & 1, m_ref, l)) return;
     if (has_o) ++sx;
     __syncwarp();
     if (lane == 0) mbar_arrive(&cx.bar[B_ITEM_EMPTY + slot]);
@@ -1097,9 +1097,9 @@ __device__ void softmax_loop(const Ctx& cx, const AttnParams& p, int x, int wq, 
 // The softmax warps' loop; on every way out (the work is done, or a bounded
 // wait gave up) the warp waits for its own TMEM loads and stores to finish
 // before the CTA frees the TMEM.
-template <int D, bool BF16, bool PAGED, int GL>
+template <int D, bool BF16, bool PAGED, int GL, bool SPLIT>
 __device__ void run_softmax(const Ctx& cx, const AttnParams& p, int x, int wq, int lane) {
-  softmax_loop<D, BF16, PAGED, GL>(cx, p, x, wq, lane);
+  softmax_loop<D, BF16, PAGED, GL, SPLIT>(cx, p, x, wq, lane);
   tmem_wait_ld();
   tmem_wait_st();
 }
@@ -1157,7 +1157,7 @@ __device__ void run_correction(const Ctx& cx, const AttnParams& p, int wq, int l
 // ---------------------------------------------------------------------------
 // GL: the softmax's mask test shared by groups of GL lanes of one q row (g a
 // multiple of GL), or per lane (GL = 0)
-template <int D, bool BF16, bool PAGED, int GL>
+template <int D, bool BF16, bool PAGED, int GL, bool SPLIT>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const AttnParams p) {
@@ -1233,7 +1233,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp < kWarpCorrection) {
     regs_inc<kRegsSoftmax>();
-    run_softmax<D, BF16, PAGED, GL>(cx, p, (warp - kWarpSoftmax) >> 2, warp & 3, lane);
+    run_softmax<D, BF16, PAGED, GL, SPLIT>(cx, p, (warp - kWarpSoftmax) >> 2, warp & 3, lane);
   } else {
     regs_inc<kRegsCorrection>();
     run_correction<D, BF16>(cx, p, warp & 3, lane);
@@ -1268,7 +1268,16 @@ cudaError_t launch_attn(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const 
   static_assert(B_COUNT <= kBarSlots, "barrier area");
   // groups of 8 lanes pay (ragged-large, g = 8: -3.6 %); groups of 4 measured
   // slower than the per-lane test on prefix+tree (g = 4), so g = 4 stays per lane
-  auto kern = (p.g % 8 == 0) ? attn_kernel<D, BF16, PAGED, 8> : attn_kernel<D, BF16, PAGED, 0>;
+  // calls whose records may be split-KV chunks (a workspace with partial
+  // states) take the kernel with the float32 partial-state epilogue; the
+  // others leave that code out
+  auto kern = (p.g % 8 == 0) ? attn_kernel<D, BF16, PAGED, 8, false>
+                             : attn_kernel<D, BF16, PAGED, 0, false>;
+  if constexpr (!PAGED) {
+    if (p.part_o != nullptr)
+      kern = (p.g % 8 == 0) ? attn_kernel<D, BF16, PAGED, 8, true>
+                            : attn_kernel<D, BF16, PAGED, 0, true>;
+  }
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemAlloc);
   if (e != cudaSuccess) return e;
