@@ -204,6 +204,30 @@ def test_edge_case(name):
     assert_parity(w, out, lse)
 
 
+@pytest.mark.parametrize("g,tree", [(1, "chain"), (1, "random"), (8, "chain"), (8, "random")])
+def test_reference_moves_across_chunks(g, tree):
+    """Scores that grow along the kv columns: every row's running reference
+    (the lazy max of the online softmax) has to move several times within and
+    across kv tiles, so the rare path that moves it -- re-forming the chunk's
+    P and rescaling the tile's P chunks already written -- runs, and the
+    result still matches the oracle."""
+    rng = np.random.default_rng(91 + g)
+    n = 700
+    parents = [wl.chain_tree(n) if tree == "chain" else wl.random_tree(n, rng)]
+    w = wl.build_workload(f"ref_moves_{tree}_g{g}", parents, h_q=g, h_kv=1, head_dim=64,
+                          dtype="fp16", tensor_seed=5 + g, sm_scale=1.0)
+    d = w.head_dim
+    # q . k_j = 0.06 j (+ noise): log2-scaled scores rise ~11 per 128 columns
+    q = torch.full((w.total_q, w.h_q, d), 1.0 / d ** 0.5)
+    ramp = torch.arange(w.total_kv, dtype=torch.float32) * (0.06 / d ** 0.5)
+    k = ramp[:, None, None].expand(w.total_kv, 1, d).clone()
+    k += 0.05 * torch.randn(w.total_kv, 1, d, generator=torch.Generator().manual_seed(3))
+    w.q = q.to(torch.float16)
+    w.k = k.to(torch.float16)
+    out, lse = run_gpu(w)
+    assert_parity(w, out, lse)
+
+
 def test_repeated_calls_are_bitwise_identical():
     w = wl.config(2, batch_scale=0.5)
     d = wl.device_inputs(w)

@@ -867,6 +867,104 @@ __device__ bool store_tile(const Ctx& cx, const AttnParams& p, const ItemRec& r,
   return true;
 }
 
+// The rare reference move of one 32-column chunk (some row's P sum above
+// 256), kept out of the softmax's chunk loop so that its code is fetched
+// only when it runs.  The chunk's scores are read again from tensor memory
+// (its P is not yet written over them) and formed exactly as the loop formed
+// them (the loop's m_use; the mask from its visibility word ``w`` or the
+// column intervals; a row that took its reference m_ref in this chunk
+// subtracts it); then, as in the loop, the chunk's max moves the reference of
+// the rows whose max outgrew it by more than 2^8 (rescaling this tile's P
+// chunks already written) and the chunk's P is written.  Returns the row's
+// (m_ref, alpha_t, lsum, chunk sum).
+template <bool BF16, int GL>
+__device__ __noinline__ float4 chunk_ref_move(uint32_t t_s, int q, float c2, float m_use, bool fr,
+                                              float m_ref, float alpha_t, float lsum,
+                                              bool partial, uint32_t w, const int2* ivs,
+                                              int e_row) {
+  float x[32];
+  tmem_ld32(t_s + 32 * q, x);
+  tmem_wait_ld(x);
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const float2 t = ffma2(make_float2(x[2 * i], x[2 * i + 1]), make_float2(c2, c2),
+                           make_float2(-m_use, -m_use));
+    x[2 * i] = t.x;
+    x[2 * i + 1] = t.y;
+  }
+  if (partial) {
+    if constexpr (GL > 0) {
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        if (!((w >> i) & 1u)) x[i] = -INFINITY;
+    } else {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const int4 e = reinterpret_cast<const int4*>(ivs + 32 * q)[i];
+        if (!((uint32_t)(e_row - e.x) < (uint32_t)e.y)) x[2 * i] = -INFINITY;
+        if (!((uint32_t)(e_row - e.z) < (uint32_t)e.w)) x[2 * i + 1] = -INFINITY;
+      }
+    }
+  }
+  if (fr) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) x[i] -= m_ref;
+  }
+  float m4[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) m4[k] = x[k];
+#pragma unroll
+  for (int i = 4; i < 32; ++i) m4[i & 3] = fmaxf(m4[i & 3], x[i]);
+  const float tmax = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+  const bool mv = tmax > 8.f;
+  uint32_t pk[16];
+  float csum;
+  if (__any_sync(0xffffffffu, mv)) {
+    const float a = mv ? ex2_approx(-tmax) : 1.f;
+    const float sh = mv ? tmax : 0.f;
+    if (mv) m_ref += tmax;
+    alpha_t *= a;
+    lsum *= a;
+    csum = 0.f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const float p0 = ex2_approx(x[2 * i] - sh), p1 = ex2_approx(x[2 * i + 1] - sh);
+      csum += p0 + p1;
+      pk[i] = pack2<BF16>(p0, p1);
+    }
+    if (q > 0) {
+      // this tile's P chunks already written: rescale them in TMEM
+      tmem_wait_st();
+      for (int j = 0; j < q; ++j) {
+        uint32_t v[16];
+        tmem_ld16(t_s + 16 * j, v);
+        tmem_wait_ld(v);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float2 f = unpack2<BF16>(v[i]);
+          v[i] = pack2<BF16>(f.x * a, f.y * a);
+        }
+        tmem_st16(t_s + 16 * j, v);
+      }
+    }
+  } else {
+    // no row moved: the chunk's P and sum as the loop formed them
+    float2 la = make_float2(0.f, 0.f), lb = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const float p0 = ex2_approx(x[2 * i]), p1 = ex2_approx(x[2 * i + 1]);
+      if (i & 1)
+        lb = fadd2(lb, make_float2(p0, p1));
+      else
+        la = fadd2(la, make_float2(p0, p1));
+      pk[i] = pack2<BF16>(p0, p1);
+    }
+    csum = (la.x + la.y) + (lb.x + lb.y);
+  }
+  tmem_st16(t_s + 16 * q, pk);
+  return make_float4(m_ref, alpha_t, lsum, csum);
+}
+
 template <int D, bool BF16, bool PAGED, int GL, bool SPLIT>
 __device__ void softmax_loop(const Ctx& cx, const AttnParams& p, int x, int wq, int lane) {
   using C = Cfg<D>;
@@ -929,6 +1027,8 @@ __device__ void softmax_loop(const Ctx& cx, const AttnParams& p, int x, int wq, 
         float x[32];
         tmem_ld32(t_s + 32 * q, x);
         const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
+        uint32_t wv = 0xffffffffu;   // the chunk's visibility word (GL > 0, PARTIAL)
+        bool fr = false;             // the row took its reference from this chunk
         tmem_wait_ld(x);
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
@@ -946,7 +1046,8 @@ __device__ void softmax_loop(const Ctx& cx, const AttnParams& p, int x, int wq, 
             // s + 2 GL, ... of the chunk, and 32 / GL ballots give the row's
             // 32 visibility bits (bit i: column i)
             const int base = lane & ~(GL - 1), sl = lane & (GL - 1);
-            uint32_t w = 0;
+            uint32_t& w = wv;
+            w = 0;
 #pragma unroll
             for (int k = 0; k < 32 / GL; ++k) {
               const int2 e = ivs[32 * q + GL * k + sl];
@@ -979,6 +1080,7 @@ __device__ void softmax_loop(const Ctx& cx, const AttnParams& p, int x, int wq, 
           const float tmax = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
           if (m_ref == -INFINITY && tmax > -INFINITY) {
             m_ref = tmax;   // m_use was 0
+            fr = true;
             alpha_t = 0.f;
             lsum = 0.f;
 #pragma unroll
@@ -1000,47 +1102,17 @@ __device__ void softmax_loop(const Ctx& cx, const AttnParams& p, int x, int wq, 
         }
         float csum = (la.x + la.y) + (lb.x + lb.y);
         if (__any_sync(0xffffffffu, !(csum <= 256.f))) {
-          // some t may exceed 8: the chunk's max moves the reference of the
-          // rows whose max outgrew it by more than 2^8
-          float m4[4];
-#pragma unroll
-          for (int k = 0; k < 4; ++k) m4[k] = x[k];
-#pragma unroll
-          for (int i = 4; i < 32; ++i) m4[i & 3] = fmaxf(m4[i & 3], x[i]);
-          const float tmax = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
-          const bool mv = tmax > 8.f;
-          if (__any_sync(0xffffffffu, mv)) {
-            const float a = mv ? ex2_approx(-tmax) : 1.f;
-            const float sh = mv ? tmax : 0.f;
-            if (mv) m_ref += tmax;
-            alpha_t *= a;
-            lsum *= a;
-            csum = 0.f;
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              const float p0 = ex2_approx(x[2 * i] - sh), p1 = ex2_approx(x[2 * i + 1] - sh);
-              csum += p0 + p1;
-              pk[i] = pack2<BF16>(p0, p1);
-            }
-            if (q > 0) {
-              // this tile's P chunks already written: rescale them in TMEM
-              tmem_wait_st();
-              for (int j = 0; j < q; ++j) {
-                uint32_t w[16];
-                tmem_ld16(t_s + 16 * j, w);
-                tmem_wait_ld(w);
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                  const float2 f = unpack2<BF16>(w[i]);
-                  w[i] = pack2<BF16>(f.x * a, f.y * a);
-                }
-                tmem_st16(t_s + 16 * j, w);
-              }
-            }
-          }
+          // some t may exceed 8: the reference-move path, out of line; it
+          // writes the chunk's P itself
+          const float4 mr = chunk_ref_move<BF16, GL>(t_s, q, c2, m_use, fr, m_ref, alpha_t, lsum,
+                                                     partial, wv, ivs, e_row);
+          m_ref = mr.x;
+          alpha_t = mr.y;
+          lsum = mr.z + mr.w;
+        } else {
+          lsum += csum;
+          tmem_st16(t_s + 16 * q, pk);
         }
-        lsum += csum;
-        tmem_st16(t_s + 16 * q, pk);
       }
       l = l * alpha_t + lsum;
       // rescale the running O when the reference moved: the PV of this Q
