@@ -877,6 +877,22 @@ __device__ bool store_tile(const Ctx& cx, const AttnParams& p, const ItemRec& r,
 // the rows whose max outgrew it by more than 2^8 (rescaling this tile's P
 // chunks already written) and the chunk's P is written.  Returns the row's
 // (m_ref, alpha_t, lsum, chunk sum).
+// The rare rescale of a Q tile's running O (D columns of this warp's rows
+// in tensor memory) by the product of the tile's reference moves, out of the
+// tile loop.
+template <int D>
+__device__ __noinline__ void rescale_o(uint32_t t_o, float alpha_t) {
+#pragma unroll 1
+  for (int oc = 0; oc < D / 32; ++oc) {
+    float o[32];
+    tmem_ld32(t_o + oc * 32, o);
+    tmem_wait_ld(o);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) o[i] *= alpha_t;
+    tmem_st32(t_o + oc * 32, o);
+  }
+}
+
 template <bool BF16, int GL>
 __device__ __noinline__ float4 chunk_ref_move(uint32_t t_s, int q, float c2, float m_use, bool fr,
                                               float m_ref, float alpha_t, float lsum,
@@ -1118,17 +1134,8 @@ __device__ void softmax_loop(const Ctx& cx, const AttnParams& p, int x, int wq, 
       // rescale the running O when the reference moved: the PV of this Q
       // tile's previous kv tile, the last one that wrote O, was issued
       // before the QK^T whose completion S_FULL reported, so it is done
-      if (!first && __any_sync(0xffffffffu, alpha_t != 1.f)) {
-#pragma unroll 1
-        for (int oc = 0; oc < D / 32; ++oc) {
-          float o[32];
-          tmem_ld32(t_row + C::kTmemO + 128 * x + oc * 32, o);
-          tmem_wait_ld(o);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] *= alpha_t;
-          tmem_st32(t_row + C::kTmemO + 128 * x + oc * 32, o);
-        }
-      }
+      if (!first && __any_sync(0xffffffffu, alpha_t != 1.f))
+        rescale_o<D>(t_row + C::kTmemO + 128 * x, alpha_t);
       if constexpr (PAGED) {
         // the last page of a sequence may be partly filled: its remaining
         // slots hold whatever the cache holds (not necessarily finite), so
