@@ -142,12 +142,47 @@ struct Ctx {
     const bool ok = mbar_wait(&bar[b], parity, abort, dev_error, limit_ns);
     return __all_sync(0xffffffffu, ok);
   }
+  // waits whose bounded retry loop is one out-of-line function per register
+  // budget instead of a copy at every wait site, which keeps the roles' loops
+  // small: warp_wait_sm for the softmax and correction warpgroups (136
+  // registers each), wait_is / warp_wait_is for the producer, V producer and
+  // MMA warps (104).  (A function called from regions of different
+  // setmaxnreg budgets cannot be register-allocated.)
+  __device__ bool warp_wait_sm(int b, uint32_t parity) const;
+  __device__ bool wait_is(int b, uint32_t parity) const;
+  __device__ bool warp_wait_is(int b, uint32_t parity) const;
   // wait used while draining after an abort: ignores the abort flag
   __device__ bool drain_wait(int b, uint32_t parity) const {
     int no_abort = 0;
     return mbar_wait(&bar[b], parity, &no_abort, dev_error, 200000000ull);
   }
 };
+
+__device__ __noinline__ bool softmax_wait_slow(uint64_t* bar, uint32_t parity,
+                                               volatile int* abort, unsigned int* dev_error,
+                                               uint64_t limit_ns) {
+  return mbar_wait(bar, parity, abort, dev_error, limit_ns);
+}
+__device__ bool Ctx::warp_wait_sm(int b, uint32_t parity) const {
+  const bool ok = mbar_try_wait(&bar[b], parity) ||
+                  softmax_wait_slow(&bar[b], parity, abort, dev_error, limit_ns);
+  return __all_sync(0xffffffffu, ok);
+}
+
+__device__ __noinline__ bool issue_wait_slow(uint64_t* bar, uint32_t parity,
+                                             volatile int* abort, unsigned int* dev_error,
+                                             uint64_t limit_ns) {
+  return mbar_wait(bar, parity, abort, dev_error, limit_ns);
+}
+__device__ bool Ctx::wait_is(int b, uint32_t parity) const {
+  return mbar_try_wait(&bar[b], parity) ||
+         issue_wait_slow(&bar[b], parity, abort, dev_error, limit_ns);
+}
+__device__ bool Ctx::warp_wait_is(int b, uint32_t parity) const {
+  const bool ok = mbar_try_wait(&bar[b], parity) ||
+                  issue_wait_slow(&bar[b], parity, abort, dev_error, limit_ns);
+  return __all_sync(0xffffffffu, ok);
+}
 
 // Iterates the kv tiles of a work unit that are non-empty for tile A or B
 // from its first tile (tile_lo, past 0 for a split-KV chunk): from the
@@ -435,7 +470,7 @@ __device__ void run_producer_v(const Ctx& cx, const CUtensorMap* tm_v, const Att
   bool aborted = false;
   for (;;) {
     const int slot = it % kSlots;
-    if (!cx.warp_wait(B_ITEM_FULL + slot, (it / kSlots) & 1)) { aborted = true; break; }
+    if (!cx.warp_wait_is(B_ITEM_FULL + slot, (it / kSlots) & 1)) { aborted = true; break; }
     const Item& s = cx.items[slot];
     const int valid = s.valid;
     const ItemRec r = s.r;
@@ -456,7 +491,7 @@ __device__ void run_producer_v(const Ctx& cx, const CUtensorMap* tm_v, const Att
       // the V stage is free once the PVs of the tile two back are done: the
       // commit of the tile after it reports them
       if (kv_it >= kStages &&
-          !cx.warp_wait(B_KV_DONE + ((kv_it - 1) & 1), ((kv_it - 1) >> 1) & 1)) {
+          !cx.warp_wait_is(B_KV_DONE + ((kv_it - 1) & 1), ((kv_it - 1) >> 1) & 1)) {
         aborted = true;
         break;
       }
@@ -526,14 +561,14 @@ __device__ void run_mma(const Ctx& cx, const AttnParams& p) {
   // test hook: a wait that runs out before any MMA is issued (the other warps
   // then find the abort flag in their own waits)
   if (p.debug_stall) {
-    cx.wait(B_STALL, 0);
+    cx.wait_is(B_STALL, 0);
     ok = false;
   }
   using X0 = std::integral_constant<int, 0>;
   using X1 = std::integral_constant<int, 1>;
   while (ok) {
     const int slot = it % kSlots;
-    if (!cx.wait(B_ITEM_FULL + slot, (it / kSlots) & 1)) break;
+    if (!cx.wait_is(B_ITEM_FULL + slot, (it / kSlots) & 1)) break;
     const Item& s = cx.items[slot];
     const int valid = s.valid;
     const ItemRec r = s.r;
@@ -556,14 +591,14 @@ __device__ void run_mma(const Ctx& cx, const AttnParams& p) {
       uint32_t& pend = x ? pend1 : pend0;
       bool& started = x ? started1 : started0;
       const int nv = (int)(pend & 0xFFu), stage = (int)((pend >> 8) & 1u);
-      if (!cx.wait(B_P_FULL + x, (kp >> x) & 1)) return false;
+      if (!cx.wait_is(B_P_FULL + x, (kp >> x) & 1)) return false;
       const uint32_t tile_kc = kc - 1;   // a pending PV belongs to the previous kv tile
       if (v_kc != tile_kc) {
-        if (!cx.wait(B_V_FULL + stage, (pend >> 9) & 1)) return false;
+        if (!cx.wait_is(B_V_FULL + stage, (pend >> 9) & 1)) return false;
         v_kc = tile_kc;
       }
       // O is free once the epilogue of the Q tile's previous unit read it
-      if (!started && !cx.wait(B_O_FREE + x, ((ox >> x) & 1) ^ 1)) return false;
+      if (!started && !cx.wait_is(B_O_FREE + x, ((ox >> x) & 1) ^ 1)) return false;
       tc_fence_after();
       const int nk = (nv + 15) >> 4;   // 16-row k-steps holding valid kv rows
       const uint64_t dv = stage ? dv1 : dv0;
@@ -592,18 +627,18 @@ __device__ void run_mma(const Ctx& cx, const AttnParams& p) {
       if ((cls >> (2 * x)) & 3) {
         bool& q_ok = x ? q_ok1 : q_ok0;
         if (!q_ok) {
-          if (!cx.wait(q_bar + x, (qx >> x) & 1)) return false;
+          if (!cx.wait_is(q_bar + x, (qx >> x) & 1)) return false;
           qx ^= 1u << x;
           q_ok = true;
         }
         if (!k_ready) {
-          if (!cx.wait(B_K_FULL + stage, (kc >> 1) & 1)) return false;
+          if (!cx.wait_is(B_K_FULL + stage, (kc >> 1) & 1)) return false;
           // the tile's column intervals too: a softmax warpgroup whose Q tile
           // skips kv tiles could otherwise reach this tile while the V
           // producer is two tiles behind, and its own wait on the two-stage
           // EX_FULL barrier would then match the older phase of the same
           // parity.  Waiting here keeps every phase in order.
-          if (!cx.wait(B_EX_FULL + stage, (kc >> 1) & 1)) return false;
+          if (!cx.wait_is(B_EX_FULL + stage, (kc >> 1) & 1)) return false;
           k_ready = true;
         }
         // S = Q K^T of this Q tile (K from TMA, Q from TMA or the correction
@@ -775,7 +810,7 @@ __device__ bool store_tile(const Ctx& cx, const AttnParams& p, const ItemRec& r,
     const size_t prow = (((size_t)r.part * p.h_kv + kvh) * kTilesPerUnit + x) * kBlockM + row;
     if (valid) p.part_lse[prow] = lse_v;
     if (has_o) {
-      if (!cx.warp_wait(B_O_FULL + x, o_par)) return false;
+      if (!cx.warp_wait_sm(B_O_FULL + x, o_par)) return false;
       tc_fence_after();
     }
     float4* po = reinterpret_cast<float4*>(p.part_o + prow * D);
@@ -817,7 +852,7 @@ __device__ bool store_tile(const Ctx& cx, const AttnParams& p, const ItemRec& r,
     ok[st] = __shfl_sync(0xffffffffu, valid ? 1 : 0, src);
   }
   if (has_o) {
-    if (!cx.warp_wait(B_O_FULL + x, o_par)) return false;
+    if (!cx.warp_wait_sm(B_O_FULL + x, o_par)) return false;
     tc_fence_after();
   }
 #pragma unroll
@@ -995,7 +1030,7 @@ __device__ void softmax_loop(const Ctx& cx, const AttnParams& p, int x, int wq, 
   uint32_t it = 0, c = 0, kx = 0, sx = 0;
   for (;;) {
     const int slot = it % kSlots;
-    if (!cx.warp_wait(B_ITEM_FULL + slot, (it / kSlots) & 1)) return;
+    if (!cx.warp_wait_sm(B_ITEM_FULL + slot, (it / kSlots) & 1)) return;
     const Item& s = cx.items[slot];
     if (!s.valid) return;
     const ItemRec r = s.r;
@@ -1019,8 +1054,8 @@ __device__ void softmax_loop(const Ctx& cx, const AttnParams& p, int x, int wq, 
       const int nvalid = min(kBlockN, r.kv - ti.j * kBlockN);
       const int sb = c & 1;   // the kv tile's K / V stage (its column intervals)
       const bool partial = cls == kTilePartial;
-      if (partial && !cx.warp_wait(B_EX_FULL + sb, (c >> 1) & 1)) return;
-      if (!cx.warp_wait(B_S_FULL + x, kx & 1)) return;
+      if (partial && !cx.warp_wait_sm(B_EX_FULL + sb, (c >> 1) & 1)) return;
+      if (!cx.warp_wait_sm(B_S_FULL + x, kx & 1)) return;
       tc_fence_after();
       const uint32_t t_s = t_row + C::kTmemS + 128 * x;
       // One pass over the tile's 32-column chunks (a rolled loop: the code
@@ -1143,7 +1178,7 @@ __device__ void softmax_loop(const Ctx& cx, const AttnParams& p, int x, int wq, 
         // PV are zeroed before the PV reads them (P is 0 there); both Q
         // tiles' softmax warps may write the same zeros
         if (nvalid < kBlockN && (nvalid & 15)) {
-          if (!cx.warp_wait(B_V_FULL + sb, (c >> 1) & 1)) return;
+          if (!cx.warp_wait_sm(B_V_FULL + sb, (c >> 1) & 1)) return;
           const int r0 = nvalid, nr = ((nvalid + 15) & ~15) - nvalid;
           uint8_t* vt = cx.smem + C::kOffV + sb * C::kKVBytes;
           for (int i = wq * 32 + lane; i < nr * 8 * C::kAtoms; i += 128) {
@@ -1196,7 +1231,7 @@ __device__ void correction_loop(const Ctx& cx, const AttnParams& p, int wq, int 
   uint32_t it = 0, qi = 0;
   for (;;) {
     const int slot = it % kSlots;
-    if (!cx.warp_wait(B_ITEM_FULL + slot, (it / kSlots) & 1)) return;
+    if (!cx.warp_wait_sm(B_ITEM_FULL + slot, (it / kSlots) & 1)) return;
     const Item& s = cx.items[slot];
     if (!s.valid) break;
     const ItemRec r = s.r;
@@ -1211,7 +1246,7 @@ __device__ void correction_loop(const Ctx& cx, const AttnParams& p, int wq, int 
         const RopeRange rr = rope_range<D>(tile_rows(r, x, R), g, wq);
         float4 cv[2][4];
         rope_load<D>(cv, p.rope_cs, qtok0, rr, 0, lane);
-        if (!cx.warp_wait(B_Q_FULL + x, (qi >> x) & 1)) return;
+        if (!cx.warp_wait_sm(B_Q_FULL + x, (qi >> x) & 1)) return;
         rope_q_rows<D, BF16>(cx.smem + C::kOffQ + x * C::kQBytes, p.rope_cs, qtok0, rr, g, lane,
                              cv);
         fence_proxy_async_smem();
