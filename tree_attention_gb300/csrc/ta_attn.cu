@@ -55,11 +55,11 @@ constexpr int kWarpCorrection = 12;  // warps 12..15
 
 // Register split (setmaxnreg) of the 512 threads' launch allocation of 128
 // each (65,536 in all): the producer / MMA warpgroup gives registers up, the
-// softmax and correction warpgroups take them.
+// softmax warpgroups take them, the correction warps (RoPE only) keep theirs.
 constexpr uint32_t kRegsLaunch = 128;
-constexpr uint32_t kRegsIssue = 104;       // warps 0-3
+constexpr uint32_t kRegsIssue = 112;       // warps 0-3
 constexpr uint32_t kRegsSoftmax = 136;     // warps 4-11
-constexpr uint32_t kRegsCorrection = 136;  // warps 12-15
+constexpr uint32_t kRegsCorrection = 128;  // warps 12-15
 static_assert(128 * (kRegsIssue + 2 * kRegsSoftmax + kRegsCorrection) <= kThreads * kRegsLaunch,
               "register split exceeds the launch allocation");
 static_assert(kRegsIssue <= kRegsLaunch && kRegsSoftmax >= kRegsLaunch &&
@@ -144,11 +144,12 @@ struct Ctx {
   }
   // waits whose bounded retry loop is one out-of-line function per register
   // budget instead of a copy at every wait site, which keeps the roles' loops
-  // small: warp_wait_sm for the softmax and correction warpgroups (136
-  // registers each), wait_is / warp_wait_is for the producer, V producer and
-  // MMA warps (104).  (A function called from regions of different
-  // setmaxnreg budgets cannot be register-allocated.)
+  // small: warp_wait_sm for the softmax warpgroups, warp_wait_cr for the
+  // correction warps, wait_is / warp_wait_is for the producer, V producer and
+  // MMA warps.  (A function called from regions of different setmaxnreg
+  // budgets cannot be register-allocated.)
   __device__ bool warp_wait_sm(int b, uint32_t parity) const;
+  __device__ bool warp_wait_cr(int b, uint32_t parity) const;
   __device__ bool wait_is(int b, uint32_t parity) const;
   __device__ bool warp_wait_is(int b, uint32_t parity) const;
   // wait used while draining after an abort: ignores the abort flag
@@ -162,6 +163,16 @@ __device__ __noinline__ bool softmax_wait_slow(uint64_t* bar, uint32_t parity,
                                                volatile int* abort, unsigned int* dev_error,
                                                uint64_t limit_ns) {
   return mbar_wait(bar, parity, abort, dev_error, limit_ns);
+}
+__device__ __noinline__ bool correction_wait_slow(uint64_t* bar, uint32_t parity,
+                                                  volatile int* abort, unsigned int* dev_error,
+                                                  uint64_t limit_ns) {
+  return mbar_wait(bar, parity, abort, dev_error, limit_ns);
+}
+__device__ bool Ctx::warp_wait_cr(int b, uint32_t parity) const {
+  const bool ok = mbar_try_wait(&bar[b], parity) ||
+                  correction_wait_slow(&bar[b], parity, abort, dev_error, limit_ns);
+  return __all_sync(0xffffffffu, ok);
 }
 __device__ bool Ctx::warp_wait_sm(int b, uint32_t parity) const {
   const bool ok = mbar_try_wait(&bar[b], parity) ||
@@ -1231,7 +1242,7 @@ __device__ void correction_loop(const Ctx& cx, const AttnParams& p, int wq, int 
   uint32_t it = 0, qi = 0;
   for (;;) {
     const int slot = it % kSlots;
-    if (!cx.warp_wait_sm(B_ITEM_FULL + slot, (it / kSlots) & 1)) return;
+    if (!cx.warp_wait_cr(B_ITEM_FULL + slot, (it / kSlots) & 1)) return;
     const Item& s = cx.items[slot];
     if (!s.valid) break;
     const ItemRec r = s.r;
@@ -1246,7 +1257,7 @@ __device__ void correction_loop(const Ctx& cx, const AttnParams& p, int wq, int 
         const RopeRange rr = rope_range<D>(tile_rows(r, x, R), g, wq);
         float4 cv[2][4];
         rope_load<D>(cv, p.rope_cs, qtok0, rr, 0, lane);
-        if (!cx.warp_wait_sm(B_Q_FULL + x, (qi >> x) & 1)) return;
+        if (!cx.warp_wait_cr(B_Q_FULL + x, (qi >> x) & 1)) return;
         rope_q_rows<D, BF16>(cx.smem + C::kOffQ + x * C::kQBytes, p.rope_cs, qtok0, rr, g, lane,
                              cv);
         fence_proxy_async_smem();
